@@ -1,0 +1,536 @@
+"""Benchmark of the K-quant x Q8_K path on GB300.
+
+Headline workload: the Qwen3-4B-shaped decode layer at M = 1 (hidden 2560;
+Q4_K Wq 2560->4096, Wk/Wv 2560->1024, Wo 4096->2560, gate/up 2560->9728;
+Q6_K down 9728->2560).  One step = one pass of the hot path over one layer:
+Q8_K quantization of the layer's four GEMV inputs, then the seven GEMVs.
+Steps rotate over L distinct copies of the layer's weights (8 by default,
+505 MB, about 4x the 126 MB L2) so that every step streams its weights from
+HBM, as consecutive layers of a model do.  `value` = weight bytes streamed
+per second (GB/s), timed on the device with CUDA events around K steps
+replayed from CUDA graphs.
+
+Also reported: the same metric end to end (activations copied in from pinned
+host memory and outputs copied back every step), the roofline of the GEMV
+kernels, the M = 512 GEMM throughput (TOPS, 2*M*N*K ops) on the 27B-shaped
+FFN and the Qwen3-4B prefill layers and the MoE grouped GEMM, and the CPU
+oracle's throughput on the same workload.
+
+`--impl reference` times the CPU oracle instead (the only reference this
+method has), with the same metric, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_gemv_gemm_gb300 import synth  # noqa: E402
+
+METRIC = "kq GEMV weight GB/s at M=1 and GEMM int8 TOPS at M=512, % of GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        p["source"] = "measured"
+        return p
+    p = dict(FALLBACK_PEAKS)
+    p["source"] = "fallback"
+    return p
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# the decode-layer workload on the GPU
+
+LAYER_INPUTS = [("x_attn", 2560), ("x_o", 4096), ("x_ffn", 2560), ("x_down", 9728)]
+# matrix -> index of its input
+LAYER_USES = {"wq": 0, "wk": 0, "wv": 0, "wo": 1, "gate": 2, "up": 2, "down": 3}
+
+
+class DecodeLayers:
+    """L copies of the Qwen3-4B-shaped layer, packed on the device."""
+
+    def __init__(self, kq, torch, n_copies: int, seed_cfg: int = 1):
+        cfg = synth.configs()[1]
+        self.kq, self.torch = kq, torch
+        self.mats = cfg.matrices
+        self.copies = []
+        for l in range(n_copies):
+            packed = []
+            for i, m in enumerate(self.mats):
+                disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(seed_cfg, 1000 * l + i))
+                dd = torch.from_numpy(disk.reshape(-1)).cuda()
+                packed.append(kq.kq_repack(m.fmt, dd, m.N, m.K))
+                del dd
+            xs = [torch.from_numpy(synth.activations(1, k, synth.rng_for(seed_cfg, 1000 * l + 100 + j))).cuda()
+                  for j, (_, k) in enumerate(LAYER_INPUTS)]
+            self.copies.append({"packed": packed, "x": xs})
+        torch.cuda.synchronize()
+        self.q8 = [kq.q8k_empty(1, k) for _, k in LAYER_INPUTS]
+        self.y_total = sum(m.N for m in self.mats)
+        self.y = torch.empty(self.y_total, dtype=torch.float32, device="cuda")
+        offs = np.cumsum([0] + [m.N for m in self.mats])
+        self.y_views = [self.y[offs[i]:offs[i + 1]] for i in range(len(self.mats))]
+        self.weight_bytes = sum(m.weight_bytes for m in self.mats)
+        self.x_total = sum(k for _, k in LAYER_INPUTS)
+
+    def step(self, l, events=None, x_override=None):
+        kq = self.kq
+        c = self.copies[l]
+        xs = c["x"] if x_override is None else x_override
+        for j in range(len(LAYER_INPUTS)):
+            kq.kq_quantize_q8k(xs[j], out=self.q8[j])
+            for i, m in enumerate(self.mats):
+                if LAYER_USES[m.name] != j:
+                    continue
+                if events is not None:
+                    events[i][0].record()
+                kq.kq_gemv(m.fmt, c["packed"][i], m.N, m.K, self.q8[j], y=self.y_views[i])
+                if events is not None:
+                    events[i][1].record()
+
+    @property
+    def launches_per_step(self):
+        return len(LAYER_INPUTS) + len(self.mats)
+
+    def algorithmic_gemv_bytes(self):
+        """Per launch: packed weight bytes + Q8_K activation bytes (292 B per
+        256) + 4 B per output."""
+        return [m.weight_bytes + (m.K // 256) * 292 + 4 * m.N for m in self.mats]
+
+
+def graph_of(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # warm the path outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    torch.cuda.set_device(local)
+    from quantized_gemv_gemm_gb300 import build as kq_build
+    if rank == 0 or world == 1:
+        kq_build.build()
+    if world > 1:
+        torch.distributed.barrier()
+        kq_build.build()
+    from quantized_gemv_gemm_gb300 import kq
+
+    peaks = load_peaks()
+    L = args.layers
+    layers = DecodeLayers(kq, torch, L)
+    rot = lambda: [layers.step(l) for l in range(L)]  # noqa: E731
+    g_plain = graph_of(torch, rot)
+
+    # events around every GEMV of every step of one rotation
+    def timing_event():
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:  # torch without graph event-record nodes
+            return None
+
+    ev = [[[timing_event(), timing_event()] for _ in layers.mats] for _ in range(L)]
+    graph_events = ev[0][0][0] is not None
+    if graph_events:
+        g_timed = graph_of(torch, lambda: [layers.step(l, events=ev[l]) for l in range(L)])
+    else:
+        ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+               for _ in layers.mats] for _ in range(L)]
+
+    reps = max(1, args.steps // L)
+    steps = reps * L
+    warm_reps = max(1, -(-args.warmup // L))
+    for _ in range(warm_reps):
+        g_plain.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        t0.record()
+        for _ in range(reps):
+            g_plain.replay()
+        t1.record()
+        torch.cuda.synchronize()
+        barrier()
+        ms = t0.elapsed_time(t1)
+        # kernel-timing pass: same graphs with event nodes; per-launch times of
+        # the last rotation are read after each of a few replays
+        kt = {i: [] for i in range(len(layers.mats))}
+        for _ in range(max(3, min(50, reps // 4))):
+            if graph_events:
+                g_timed.replay()
+            else:
+                for l in range(L):
+                    layers.step(l, events=ev[l])
+            torch.cuda.synchronize()
+            for l in range(L):
+                for i in range(len(layers.mats)):
+                    kt[i].append(ev[l][i][0].elapsed_time(ev[l][i][1]))
+    clocks = clk.summary()
+
+    ms_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    bytes_per_step = layers.weight_bytes
+    value = bytes_per_step * steps * world / (ms_max * 1e-3) / 1e9
+
+    # roofline of the GEMV kernels (all seven launches of a step)
+    alg = layers.algorithmic_gemv_bytes()
+    mean_ms = [float(np.mean(kt[i])) for i in range(len(layers.mats))]
+    achieved = sum(alg) / (sum(mean_ms) * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    per_matrix = [{"name": m.name, "fmt": synth.FORMAT_NAMES[m.fmt], "N": m.N, "K": m.K,
+                   "us": round(t * 1e3, 3), "gbs": round(b / (t * 1e-3) / 1e9, 1)}
+                  for m, t, b in zip(layers.mats, mean_ms, alg)]
+
+    # end to end through the public API: H2D of the step's activations from
+    # pinned host memory, the step, D2H of all outputs, replayed from a graph
+    x_host = torch.from_numpy(np.concatenate(
+        [synth.activations(1, k, synth.rng_for(1, 7000 + j))[0] for j, (_, k) in enumerate(LAYER_INPUTS)])).pin_memory()
+    y_host = torch.empty(layers.y_total, dtype=torch.float32).pin_memory()
+    x_dev = torch.empty(layers.x_total, dtype=torch.float32, device="cuda")
+    xo = np.cumsum([0] + [k for _, k in LAYER_INPUTS])
+    x_views = [x_dev[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))]
+
+    def e2e_rot():
+        for l in range(L):
+            x_dev.copy_(x_host, non_blocking=True)
+            layers.step(l, x_override=x_views)
+            y_host.copy_(layers.y, non_blocking=True)
+
+    g_e2e = graph_of(torch, e2e_rot)
+    for _ in range(warm_reps):
+        g_e2e.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_reps = max(1, reps // 2)
+    barrier()
+    e0.record()
+    for _ in range(e_reps):
+        g_e2e.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e_ms], device="cuda")
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e_ms = float(tt.item())
+    e2e_value = bytes_per_step * e_reps * L * world / (e_ms * 1e-3) / 1e9
+    y_check = y_host.numpy()
+    assert np.isfinite(y_check).all()
+
+    gemm = None if args.no_gemm else bench_gemm(kq, torch, peaks, args)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": steps, "warmup": warm_reps * L, "ms_per_step": round(ms_max / steps, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded random K-quant superblocks and N(0,1) activations)",
+            "config": {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
+                       "M": 1, "hidden": 2560,
+                       "matrices": [f"{m.name} {synth.FORMAT_NAMES[m.fmt]} {m.N}x{m.K}" for m in layers.mats],
+                       "weight_bytes_per_step": bytes_per_step, "layer_copies": L,
+                       "l2": f"inputs larger than L2: {L} rotating layer copies, "
+                             f"{bytes_per_step * L / 1e6:.1f} MB of weights",
+                       "timing": "CUDA events around graph replays of K steps",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "kernel": "kq mv_kernel (GEMV, 7 launches per step)",
+                         "timing": "event nodes in graph replays" if graph_events else "eager launches with events",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_source": peaks["source"],
+                         "traffic": None, "per_matrix": per_matrix},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": 4 * layers.x_total, "d2h_bytes_per_step": 4 * layers.y_total,
+                    "how": "graph replay of: H2D of the 4 fp32 inputs from pinned memory, 4 quantize + 7 GEMV "
+                           "launches, D2H of all 7 outputs"},
+            "gpu_launches": layers.launches_per_step * steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "gemm": gemm,
+        }
+        print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# M = 512 GEMMs (secondary metric)
+
+def bench_gemm(kq, torch, peaks, args):
+    out = []
+    tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+
+    def time_it(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def dense(name, cfg_index, mats, outliers):
+        M = 512
+        items = []
+        for i, m in enumerate(mats):
+            disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(cfg_index, 2 * i))
+            packed = kq.kq_repack(m.fmt, torch.from_numpy(disk.reshape(-1)).cuda(), m.N, m.K)
+            x = torch.from_numpy(synth.activations(M, m.K, synth.rng_for(cfg_index, 2 * i + 1), outliers)).cuda()
+            a = kq.q8k_empty(M, m.K)
+            y = torch.empty((M, m.N), dtype=torch.float32, device="cuda")
+            ws_n = kq.kq_gemm_workspace_bytes(m.fmt, M, m.N, m.K)
+            ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda") if ws_n else None
+            items.append((m, packed, x, a, y, ws))
+        torch.cuda.synchronize()
+
+        def step():
+            for m, packed, x, a, y, ws in items:
+                kq.kq_quantize_q8k(x, out=a)
+                kq.kq_gemm(m.fmt, packed, m.N, m.K, a, y=y, workspace=ws)
+
+        ms = time_it(step, args.gemm_reps)
+        ops = sum(2 * M * m.N * m.K for m in mats)
+        tops = ops / (ms * 1e-3) / 1e12
+        out.append({"workload": name, "M": M, "ms": round(ms, 4), "tops": round(tops, 2),
+                    "frac_of_fp16_tensor_peak": round(tops / tc_peak, 4),
+                    "weight_gbs": round(sum(m.weight_bytes for m in mats) / (ms * 1e-3) / 1e9, 1)})
+        del items
+        torch.cuda.empty_cache()
+
+    cfgs = synth.configs()
+    dense("27B-shaped dense FFN Q4_K, M=512", 3, cfgs[3].matrices, True)
+    dense("Qwen3-4B prefill pp512 all-Q5_K", 2, cfgs[2].matrices[:7], False)
+    dense("Qwen3-4B prefill pp512 all-Q6_K", 2, cfgs[2].matrices[7:], False)
+
+    # MoE grouped
+    cfg = cfgs[4]
+    T, E = cfg.M, cfg.experts
+    row_token, _, offsets = synth.moe_routing(T, E, cfg.topk, synth.rng_for(4, 0))
+    off_d = torch.from_numpy(offsets).cuda()
+    x_tok = synth.activations(T, 2048, synth.rng_for(4, 1))
+    items = []
+    for i, m in enumerate(cfg.matrices):
+        per = kq.kq_repack_bytes(m.fmt, m.N, m.K)
+        packed = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(4, 10 + 1000 * i + e))
+            kq.kq_repack(m.fmt, torch.from_numpy(disk.reshape(-1)).cuda(), m.N, m.K, packed=packed[e * per:(e + 1) * per])
+        x = x_tok[row_token] if m.name != "down" else synth.activations(len(row_token), m.K, synth.rng_for(4, 2))
+        xd = torch.from_numpy(np.ascontiguousarray(x)).cuda()
+        a = kq.q8k_empty(len(row_token), m.K)
+        y = torch.empty((len(row_token), m.N), dtype=torch.float32, device="cuda")
+        ws_n = kq.kq_gemm_workspace_bytes(m.fmt, len(row_token), m.N, m.K)
+        ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda") if ws_n else None
+        items.append((m, packed, xd, a, y, ws))
+    torch.cuda.synchronize()
+
+    def moe_step():
+        for m, packed, x, a, y, ws in items:
+            kq.kq_quantize_q8k(x, out=a)
+            kq.kq_gemm_grouped(m.fmt, packed, E, off_d, m.N, m.K, a, y=y, workspace=ws)
+
+    ms = time_it(moe_step, args.gemm_reps)
+    rows = len(row_token)
+    ops = sum(2 * rows * m.N * m.K for m in cfg.matrices)
+    wbytes = sum(m.weight_bytes for m in cfg.matrices) * E
+    out.append({"workload": "30B-A3B-shaped MoE grouped GEMM (128 experts, top-8, 512 tokens)", "rows": rows,
+                "ms": round(ms, 4), "tops": round(ops / (ms * 1e-3) / 1e12, 2),
+                "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+                "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / float(peaks["hbm_gbs"]), 4)})
+    del items
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+
+def cpu_oracle_layer_rate(seconds: float, threads: int | None = None):
+    """GB/s of the oracle on the decode layer: repeat the full 7-matrix layer
+    (every output) until `seconds` of wall time have passed."""
+    import oracle
+    if threads:
+        oracle.set_num_threads(threads)
+    cfg = synth.configs()[1]
+    mats = []
+    for i, m in enumerate(cfg.matrices):
+        disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(1, i))
+        x = synth.activations(1, m.K, synth.rng_for(1, 100 + i))
+        mats.append((m, disk, x))
+    layer_bytes = sum(m.weight_bytes for m in cfg.matrices)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        for m, disk, x in mats:
+            d8, q8, bs = oracle.quantize_q8k(x)
+            oracle.gemm(m.fmt, disk, d8, q8, bs)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return layer_bytes * passes / el / 1e9, passes, el
+
+
+def cpu_baseline(seconds):
+    import oracle
+    v, passes, el = cpu_oracle_layer_rate(seconds)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "host_cpus": os.cpu_count(),
+            "sample": f"{passes} full passes of the Qwen3-4B-shaped decode layer (7 matrices, every output), "
+                      f"{el:.1f} s wall, OpenMP over weight rows"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    import oracle
+    per_step = max(0.5, min(5.0, 60.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_layer_rate(per_step)
+    vals, passes_total, el_total = [], 0, 0.0
+    for _ in range(args.steps):
+        v, p, el = cpu_oracle_layer_rate(per_step)
+        vals.append(v)
+        passes_total += p
+        el_total += el
+    value = sum(synth.configs()[1].matrices[i].weight_bytes for i in range(7)) * passes_total / el_total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el_total / max(1, passes_total) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+            "data": "synthetic (seeded random K-quant superblocks and N(0,1) activations)",
+            "config": {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
+                       "M": 1, "hidden": 2560, "step": "full layer passes of the CPU oracle for ~%.1f s" % per_step},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{passes_total} full layer passes over {args.steps} steps"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=80000)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layers", type=int, default=8, help="rotating layer copies (weights > L2)")
+    ap.add_argument("--gemm-reps", type=int, default=20)
+    ap.add_argument("--no-gemm", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * kq.h - C ABI of libkq: K-quant (Q4_K / Q5_K / Q6_K) x Q8_K matrix products
+ * on GB300 (sm_103a).
+ *
+ * Method source ("kq-arc" below): the page "dasLLAMA: K-quant kernel arc -
+ * kq v2 integer folds, kq v3 panel-scratch tiles, chain regrain, parity
+ * gates" (daScript pull request #3450): section "The pieces" (kq v2 integer
+ * folds, kq v3 panel scratch), the k4 kq-v2 commit message ("Adopts
+ * llama.cpp's proven K-quant kernel design for the k4 family") and the k5/k6
+ * kq-v2 commit message ("Finishes what the k4 rework proved").
+ *
+ * Conventions for every entry point
+ *   - Pointers named as device pointers must be device (or managed) memory
+ *     of the current CUDA device; the library never allocates, frees or
+ *     synchronises.  All work is enqueued on the caller's stream `s`
+ *     (0 = legacy default stream) and the call returns before it finishes.
+ *   - The caller owns every buffer.  Inputs are read-only.
+ *   - Sizes are int64_t; K must be a positive multiple of 256.
+ *   - Return value: KQ_OK (0) or a negative kq_status.  Argument errors are
+ *     detected on the host before anything is enqueued; KQ_ERR_LAUNCH
+ *     reports a CUDA launch failure (cudaGetLastError after the launch).
+ *     kq_strerror() names a code.
+ *   - Nothing here reads the status of earlier launches except
+ *     kq_device_status(), which synchronises the given stream.
+ *
+ * Block formats (256 weights per superblock, GGUF byte order, little
+ * endian; the pages name the fields, the bit layout is the public GGUF one):
+ *   Q4_K, 144 B: d f16 | dmin f16 | scales[12] (8 six-bit sub-scales and 8
+ *                six-bit sub-mins, one per 32 weights) | qs[128] (4-bit)
+ *   Q5_K, 176 B: d f16 | dmin f16 | scales[12] | qh[32] (5th bits) | qs[128]
+ *   Q6_K, 210 B: ql[128] (low 4 bits) | qh[64] (high 2 bits) |
+ *                scales[16] (signed int8, one per 16 weights) | d f16
+ *   Q8_K activations (kq-arc, k4 kq-v2 commit: "ONE fp32 scale per
+ *   256-superblock + per-16 bsums") are held as three row-major planes:
+ *     d     float  [M][K/256]   block scale d8
+ *     qs    int8   [M][K]       quants in -127..127
+ *     bsums int16  [M][K/16]    sum of each 16 consecutive quants
+ *
+ * Output of every product: y float32 row-major [M][N] (M tokens, N weight
+ * rows), y[m][n] = sum over superblocks sb of
+ *     Q4_K/Q5_K: d*d8*isum - dmin*d8*msum
+ *                isum = sum_j sc_j * dot32_j(q, a8), msum = sum_j m_j*(bs_2j + bs_2j+1)
+ *     Q6_K:      d*d8*(iacc - 32*bacc)
+ *                iacc = sum_i sc_i * dot16_i(q, a8), bacc = sum_i sc_i * bs_i
+ * with isum, msum, iacc, bacc formed exactly in int32 and one float fold per
+ * superblock (kq-arc, "The pieces", kq v2).
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3 } kq_format;
+
+typedef enum {
+    KQ_OK = 0,
+    KQ_ERR_ARG = -1,       /* null pointer, K % 256 != 0, negative size, ... */
+    KQ_ERR_ALIGN = -2,     /* a pointer is not 16-byte aligned (256 for packed) */
+    KQ_ERR_FORMAT = -3,    /* unknown kq_format */
+    KQ_ERR_LAUNCH = -4,    /* CUDA reported an error at launch */
+    KQ_ERR_TIMEOUT = -5,   /* a device-side bounded wait gave up (see kq_device_status) */
+    KQ_ERR_WORKSPACE = -6, /* workspace missing or smaller than required */
+    KQ_ERR_DEVICE = -7     /* the current device is not sm_103 / cannot run the kernel */
+} kq_status;
+
+/* Q8_K planes (device pointers), see the format note above. */
+typedef struct { const float *d; const int8_t *qs; const int16_t *bsums; } kq_q8k_const;
+typedef struct { float *d; int8_t *qs; int16_t *bsums; } kq_q8k;
+
+/* Human-readable name of a kq_status. */
+const char *kq_strerror(int code);
+
+/* Bytes of one disk superblock of format f (144 / 176 / 210), 0 if unknown. */
+size_t kq_block_bytes(kq_format f);
+
+/*
+ * Activation quantization to Q8_K (kq-arc, k4 kq-v2 commit: quantize_q8_k_into,
+ * "ONE fp32 scale per 256-superblock + per-16 bsums").  Per 256-block of each
+ * row of x: amax = max|x|; if amax == 0 then d8 = 0 and q = 0; otherwise
+ * iscale = 127/amax and q = clamp(round_half_even(x*iscale), -127, 127), both
+ * steps in IEEE fp32, and d8 = amax/127.  bsums[i] sums q over 16i..16i+15.
+ *   x   device float32 [M][K] row-major, 16-byte aligned, finite values
+ *   out device planes as described above (qs 16-byte aligned)
+ * Errors: KQ_ERR_ARG (null, M < 0, K % 256), KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ * M == 0 is a no-op.
+ */
+int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream_t s);
+
+/*
+ * Size in bytes of the repacked (device) image of an [N][K] weight matrix.
+ * Always a multiple of 256, so experts stacked back to back stay aligned.
+ * Returns 0 for an unknown format, N < 0 or K not a positive multiple of 256.
+ *
+ * Packed image (kq-arc, k4 kq-v2 commit: scale planes kept "verbatim-disk";
+ * kq v3 commit: "DRAM planes keep the packed ... form"), planes back to back,
+ * each starting on a 256-byte boundary, every plane row-major over
+ * (row n, superblock sb):
+ *   Q4_K: qs  [N][K/256][128] | hdr [N][K/256][16] (d, dmin, scales[12] verbatim)
+ *   Q5_K: qs  [N][K/256][128] | qh [N][K/256][32] | hdr [N][K/256][16]
+ *   Q6_K: ql  [N][K/256][128] | qh [N][K/256][64] | sc [N][K/256][16] | d [N][K/256] f16
+ * Every byte of the disk superblock is kept once, so the image is the disk
+ * size plus at most 3 x 255 bytes of plane padding.
+ */
+size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
+
+/*
+ * One-time repack of disk superblocks into the packed image (kq-arc, k4
+ * kq-v2 commit: "transcode" and repack at load; the image dequantizes
+ * bit-identically to the file).
+ *   disk   device uint8 [N][K/256][block_bytes] (GGUF order), 16-byte aligned
+ *   packed device, kq_repack_bytes(f, N, K) bytes, 256-byte aligned
+ * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ */
+int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s);
+
+/*
+ * Decode GEMV, M = 1 (kq-arc, "The pieces", kq v2 GEMV: in-kernel unpack of
+ * the packed planes; kq v3 commit: "decode is model-level DRAM-bound, so
+ * plane bytes are decode time").  y[n] for n < N, as in the header note.
+ *   packed device image from kq_repack (256-byte aligned)
+ *   a      device Q8_K planes of one row of K
+ *   y      device float32 [N]
+ * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ */
+int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
+            float *y, cudaStream_t s);
+
+/*
+ * Size of the device workspace kq_gemm / kq_gemm_grouped need for M token
+ * rows of K (an fp16 image of the activation quants and bsums, plus tile
+ * bookkeeping).  0 means no workspace is needed for this shape.
+ */
+size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K);
+
+/*
+ * Prefill GEMM (kq-arc, "The pieces", kq v3: each weight panel unpacked once
+ * per token block, "amortized xTB"): y [M][N] = the fold above for every
+ * token row m of a.
+ *   a          device Q8_K planes of M rows
+ *   y          device float32 [M][N]
+ *   workspace  device, >= kq_gemm_workspace_bytes(f, M, N, K) bytes,
+ *              256-byte aligned (may be NULL when that size is 0)
+ * Calls that share a workspace must not overlap on the GPU.
+ * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_WORKSPACE,
+ * KQ_ERR_LAUNCH.  M == 0 is a no-op.
+ */
+int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
+            int64_t M, float *y, void *workspace, size_t workspace_bytes, cudaStream_t s);
+
+/*
+ * Grouped (MoE) GEMM (kq-arc, k5/k6 kq-v2 commit: MoE prefill gathers off a
+ * K-form batch image, ffn_moe_prefill_grouped): rows of a are grouped by
+ * expert; rows row_offsets[e] .. row_offsets[e+1]-1 use expert e's weights.
+ *   packed       device, E expert images back to back, each
+ *                kq_repack_bytes(f, N, K) bytes (expert e at
+ *                packed + e * kq_repack_bytes(f, N, K))
+ *   row_offsets  device int32 [E+1], non-decreasing, row_offsets[0] = 0,
+ *                row_offsets[E] = M_total (not checked on the host: the
+ *                kernels clamp every range to [0, M_total])
+ *   a            device Q8_K planes of M_total rows
+ *   y            device float32 [M_total][N]
+ *   workspace    as for kq_gemm with M = M_total
+ * Errors as kq_gemm.
+ */
+int kq_gemm_grouped(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets,
+                    int64_t N, int64_t K, kq_q8k_const a, int64_t M_total, float *y,
+                    void *workspace, size_t workspace_bytes, cudaStream_t s);
+
+/*
+ * Test hook: the int32 partials of the fold, per (token, row, superblock),
+ * computed by the same device code the GEMV runs.
+ *   isum, msum  device int32 [M][N][K/256]; for Q6_K isum = iacc - 32*bacc
+ *               and msum = 0 (kq-arc, k5/k6 kq-v2 commit).
+ */
+int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
+                      int64_t M, int32_t *isum, int32_t *msum, cudaStream_t s);
+
+/*
+ * Test hook: decode the packed image back to stored quants and scales with
+ * the device unpack helpers, to check the repack round trip.
+ *   q     device int32 [N][K]        stored quant (Q6_K: 0..63, before -32)
+ *   sc    device int32 [N][K/256][16] sub-scales (8 used for Q4_K/Q5_K)
+ *   mn    device int32 [N][K/256][8]  sub-mins (0 for Q6_K)
+ *   d     device float [N][K/256], dmin device float [N][K/256] (0 for Q6_K)
+ */
+int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32_t *q,
+                    int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
+
+/*
+ * Synchronise stream s and return the device status word of the library's
+ * bounded waits on the current device (KQ_OK, or KQ_ERR_TIMEOUT if a kernel
+ * gave up waiting), then clear it.  Returns KQ_ERR_LAUNCH if the
+ * synchronisation itself failed.
+ */
+int kq_device_status(cudaStream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KQ_H */

@@ -1,0 +1,155 @@
+// kq_api.cu - the C ABI of libkq (declared in include/kq.h): argument
+// checks on the host, then the launchers.  Nothing here allocates memory or
+// synchronises, except kq_device_status().
+#include "../../include/kq.h"
+#include "kq_internal.h"
+
+using namespace kq;
+
+namespace {
+
+bool fmt_ok(int f) { return f == KQ_Q4_K || f == KQ_Q5_K || f == KQ_Q6_K; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_shape(int64_t N, int64_t K) {
+    if (N < 0 || K <= 0 || K % QK != 0) return KQ_ERR_ARG;
+    return KQ_OK;
+}
+
+int check_q8k(const float *d, const int8_t *qs, const int16_t *bs) {
+    if (!d || !qs || !bs) return KQ_ERR_ARG;
+    if (!aligned(d, 4) || !aligned(qs, 16) || !aligned(bs, 16)) return KQ_ERR_ALIGN;
+    return KQ_OK;
+}
+
+int launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return KQ_OK;
+    cudaGetLastError();  // clear a non-sticky launch error
+    return KQ_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kq_strerror(int code) {
+    switch (code) {
+    case KQ_OK: return "ok";
+    case KQ_ERR_ARG: return "invalid argument (null pointer, negative size or K not a multiple of 256)";
+    case KQ_ERR_ALIGN: return "misaligned pointer (16 bytes; 256 bytes for packed images and workspaces)";
+    case KQ_ERR_FORMAT: return "unknown K-quant format";
+    case KQ_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case KQ_ERR_TIMEOUT: return "a device-side bounded wait timed out";
+    case KQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KQ_ERR_DEVICE: return "unsupported device";
+    default: return "unknown kq status";
+    }
+}
+
+size_t kq_block_bytes(kq_format f) { return fmt_ok(f) ? (size_t)block_bytes(f) : 0; }
+
+int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream_t s) {
+    if (M < 0 || K <= 0 || K % QK != 0) return KQ_ERR_ARG;
+    if (M == 0) return KQ_OK;
+    if (!x) return KQ_ERR_ARG;
+    if (int r = check_q8k(out.d, out.qs, out.bsums)) return r;
+    if (!aligned(x, 16)) return KQ_ERR_ALIGN;
+    return launch_status(launch_quantize(x, M, K, out.d, out.qs, out.bsums, s));
+}
+
+size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K) {
+    if (!fmt_ok(f) || check_shape(N, K)) return 0;
+    uint64_t off[5];
+    plane_offsets(f, N, K / QK, off);
+    return (size_t)off[4];
+}
+
+int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (N == 0) return KQ_OK;
+    if (!disk || !packed) return KQ_ERR_ARG;
+    if (!aligned(disk, 16) || !aligned(packed, 256)) return KQ_ERR_ALIGN;
+    return launch_status(launch_repack(f, static_cast<const uint8_t *>(disk), N, K, static_cast<uint8_t *>(packed), s));
+}
+
+int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, float *y, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (N == 0) return KQ_OK;
+    if (!packed || !y) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_mv(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, 1, nullptr, 1, 0, y, s));
+}
+
+size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
+    if (!fmt_ok(f) || M < 0 || check_shape(N, K)) return 0;
+    return gemm_workspace_bytes(f, M, N, K);
+}
+
+static int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offsets, int64_t N, int64_t K,
+                       kq_q8k_const a, int64_t M, float *y, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (M < 0 || E < 1) return KQ_ERR_ARG;
+    if (M == 0 || N == 0) return KQ_OK;
+    if (!packed || !y) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    const size_t need = gemm_workspace_bytes(f, M, N, K);
+    if (need && (!ws || ws_bytes < need)) return KQ_ERR_WORKSPACE;
+    if (ws && !aligned(ws, 256)) return KQ_ERR_ALIGN;
+    const Q8K q{a.d, a.qs, a.bsums};
+    const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
+    cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        e = launch_mv(f, packed, N, K, q, M, offsets, E, expert_bytes, y, s);
+    }
+    return launch_status(e);
+}
+
+int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M, float *y,
+            void *workspace, size_t workspace_bytes, cudaStream_t s) {
+    return gemm_common(f, packed, 1, nullptr, N, K, a, M, y, workspace, workspace_bytes, s);
+}
+
+int kq_gemm_grouped(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets, int64_t N, int64_t K,
+                    kq_q8k_const a, int64_t M_total, float *y, void *workspace, size_t workspace_bytes,
+                    cudaStream_t s) {
+    if (!row_offsets && M_total > 0) return KQ_ERR_ARG;
+    if (row_offsets && !aligned(row_offsets, 4)) return KQ_ERR_ALIGN;
+    return gemm_common(f, packed, E, row_offsets, N, K, a, M_total, y, workspace, workspace_bytes, s);
+}
+
+int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M,
+                      int32_t *isum, int32_t *msum, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (M < 0) return KQ_ERR_ARG;
+    if (M == 0 || N == 0) return KQ_OK;
+    if (!packed || !isum || !msum) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(isum, 4) || !aligned(msum, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_partials(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, M, isum, msum, s));
+}
+
+int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32_t *q, int32_t *sc, int32_t *mn,
+                    float *d, float *dmin, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (N == 0) return KQ_OK;
+    if (!packed || !q || !sc || !mn || !d || !dmin) return KQ_ERR_ARG;
+    if (!aligned(packed, 256)) return KQ_ERR_ALIGN;
+    return launch_status(launch_debug_decode(f, packed, N, K, q, sc, mn, d, dmin, s));
+}
+
+int kq_device_status(cudaStream_t s) {
+    int st = 0;
+    if (read_and_clear_status(s, &st)) return KQ_ERR_LAUNCH;
+    return st ? KQ_ERR_TIMEOUT : KQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,299 @@
+// kq_device.cuh - device-side building blocks shared by the libkq kernels:
+// the packed-image layout, streaming loads, and the per-lane unpack + integer
+// fold of one 256-weight superblock for each K-quant format.
+//
+// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
+//
+// Lane geometry (GEMV, small-M and partials kernels).  Four consecutive lanes
+// ("a quad") own one weight row; lane c = lane & 3 of the quad owns 64 of the
+// superblock's 256 weights, so one warp covers 8 rows of one superblock:
+//   Q4_K/Q5_K: lane c reads qs bytes [16c, 16c+16) and [64+16c, 64+16c+16).
+//     Byte b of qs holds element 64*(b/32) + b%32 (low nibble, sub-block
+//     2*(b/32)) and element 64*(b/32) + 32 + b%32 (high nibble, sub-block
+//     2*(b/32)+1), so lane c owns sub-blocks {2k, 2k+1, 2k+4, 2k+5}, k = c/2,
+//     at element offsets 16*(c&1) .. +15 inside each.
+//   Q6_K: lane c = (half h = c/2, p = c&1) reads ql[64h+16p ..+16],
+//     ql[64h+32+16p ..+16] and qh[32h+16p ..+16]; it owns the four 16-wide
+//     sub-blocks 8h + 2t + p, t = 0..3.
+// Each warp-wide load instruction covers whole 32-byte sectors.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace kq {
+
+constexpr int QK = 256;
+constexpr int FMT_Q4_K = 1, FMT_Q5_K = 2, FMT_Q6_K = 3;
+
+__host__ __device__ inline int block_bytes(int f) {
+    return f == FMT_Q4_K ? 144 : f == FMT_Q5_K ? 176 : f == FMT_Q6_K ? 210 : 0;
+}
+
+__host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+// Bytes per superblock of each plane of the packed image.
+__host__ __device__ inline void plane_unit_bytes(int f, int u[4]) {
+    u[0] = 128; u[1] = 0; u[2] = 0; u[3] = 0;
+    if (f == FMT_Q4_K) { u[1] = 16; }
+    else if (f == FMT_Q5_K) { u[1] = 32; u[2] = 16; }
+    else if (f == FMT_Q6_K) { u[1] = 64; u[2] = 16; u[3] = 2; }
+}
+
+// Offsets of the planes of an [N][K] image; off[4] = total bytes.
+__host__ __device__ inline void plane_offsets(int f, int64_t N, int64_t nsb, uint64_t off[5]) {
+    int u[4];
+    plane_unit_bytes(f, u);
+    const uint64_t units = (uint64_t)N * (uint64_t)nsb;
+    off[0] = 0;
+    for (int i = 0; i < 4; ++i) off[i + 1] = off[i] + align256(units * (uint64_t)u[i]);
+}
+
+// Plane base pointers of one packed matrix.
+struct Planes {
+    const uint8_t *p0, *p1, *p2, *p3;
+};
+
+__host__ __device__ inline Planes make_planes(int f, const void *base, int64_t N, int64_t nsb) {
+    uint64_t off[5];
+    plane_offsets(f, N, nsb, off);
+    const uint8_t *b = static_cast<const uint8_t *>(base);
+    return Planes{b + off[0], b + off[1], b + off[2], b + off[3]};
+}
+
+// ---------------------------------------------------------------------------
+// loads
+
+// Weight bytes are read exactly once per kernel: do not allocate them in L1.
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// Small data shared by the lanes of a quad (scale headers) and activations,
+// which every warp of the block re-reads: keep them in L1.
+__device__ __forceinline__ uint4 ld_keep(const void *p) {
+    return __ldg(static_cast<const uint4 *>(p));
+}
+__device__ __forceinline__ int4 ld_act16(const int8_t *p) {
+    return __ldg(reinterpret_cast<const int4 *>(p));
+}
+
+__device__ __forceinline__ int dp4a(uint32_t a, int b, int c) {
+    return __dp4a(static_cast<int>(a), b, c);
+}
+
+__device__ __forceinline__ int dot16(uint4 q, int4 a) {
+    int s = dp4a(q.x, a.x, 0);
+    s = dp4a(q.y, a.y, s);
+    s = dp4a(q.z, a.z, s);
+    return dp4a(q.w, a.w, s);
+}
+
+__device__ __forceinline__ uint4 and4(uint4 v, uint32_t m) {
+    return make_uint4(v.x & m, v.y & m, v.z & m, v.w & m);
+}
+__device__ __forceinline__ uint4 shr4(uint4 v, int s) {
+    return make_uint4(v.x >> s, v.y >> s, v.z >> s, v.w >> s);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float half_hi(uint32_t w) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+
+// ---------------------------------------------------------------------------
+// The 12-byte six-bit scale/min block of Q4_K and Q5_K (kq-arc, k4 kq-v2
+// commit: "f16 d/dmin + 12B 6-bit packing"; k5/k6 commit: the Q5_K scale
+// block is the Q4_K one).  With y, z, w = scale bytes 0..3, 4..7, 8..11
+// (little-endian words), byte j of the results is:
+//   sc_lo: sub-scale j   (j < 4) = low 6 bits of scale byte j
+//   m_lo : sub-min j     (j < 4) = low 6 bits of scale byte 4+j
+//   sc_hi: sub-scale 4+j = low nibble of byte 8+j | top 2 bits of byte j  << 4
+//   m_hi : sub-min   4+j = high nibble of byte 8+j | top 2 bits of byte 4+j << 4
+struct ScaleMin {
+    uint32_t sc_lo, sc_hi, m_lo, m_hi;
+};
+
+__device__ __forceinline__ ScaleMin unpack_scale_min(uint4 hdr) {
+    ScaleMin r;
+    r.sc_lo = hdr.y & 0x3F3F3F3Fu;
+    r.m_lo = hdr.z & 0x3F3F3F3Fu;
+    r.sc_hi = (hdr.w & 0x0F0F0F0Fu) | ((hdr.y >> 2) & 0x30303030u);
+    r.m_hi = ((hdr.w >> 4) & 0x0F0F0F0Fu) | ((hdr.z >> 2) & 0x30303030u);
+    return r;
+}
+
+__device__ __forceinline__ int byte_of(uint32_t w, int i) { return (w >> (8 * i)) & 0xFF; }
+
+// ---------------------------------------------------------------------------
+// Per-lane weight registers of one superblock, and their loads.
+
+struct WQ4 { uint4 qa, qb, hdr; };
+struct WQ5 { uint4 qa, qb, qh, hdr; };
+struct WQ6 { uint4 la, lb, qh, sc; uint32_t d; };
+
+template <int F> struct WRegs;
+template <> struct WRegs<FMT_Q4_K> { using T = WQ4; };
+template <> struct WRegs<FMT_Q5_K> { using T = WQ5; };
+template <> struct WRegs<FMT_Q6_K> { using T = WQ6; };
+
+// u = n * nsb + sb, the superblock's index in the row-major planes.
+__device__ __forceinline__ void load_w(WQ4 &w, const Planes &P, uint64_t u, int c) {
+    const uint8_t *qs = P.p0 + u * 128;
+    w.qa = ld_stream(qs + 16 * c);
+    w.qb = ld_stream(qs + 64 + 16 * c);
+    w.hdr = ld_keep(P.p1 + u * 16);
+}
+__device__ __forceinline__ void load_w(WQ5 &w, const Planes &P, uint64_t u, int c) {
+    const uint8_t *qs = P.p0 + u * 128;
+    w.qa = ld_stream(qs + 16 * c);
+    w.qb = ld_stream(qs + 64 + 16 * c);
+    w.qh = ld_stream(P.p1 + u * 32 + 16 * (c & 1));
+    w.hdr = ld_keep(P.p2 + u * 16);
+}
+__device__ __forceinline__ void load_w(WQ6 &w, const Planes &P, uint64_t u, int c) {
+    const int h = c >> 1, p = c & 1;
+    const uint8_t *ql = P.p0 + u * 128 + 64 * h + 16 * p;
+    w.la = ld_stream(ql);
+    w.lb = ld_stream(ql + 32);
+    w.qh = ld_stream(P.p1 + u * 64 + 32 * h + 16 * p);
+    w.sc = ld_keep(P.p2 + u * 16);
+    w.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3) + u);
+}
+
+// ---------------------------------------------------------------------------
+// Decoded per-lane quants: four groups of 16 stored quant bytes (one uint4
+// each, bytes 0..63) with their sub-scales, plus the lane's share of the
+// min term.  Decoding is done once per superblock and reused for every token.
+
+struct LaneQ {
+    uint4 g[4];     // stored quants of the lane's four 16-element groups
+    int sc[4];      // sub-scale of each group
+    int aoff[4];    // element offset of each group inside the superblock
+    // Q4_K/Q5_K: lane c's mins m_{2c}, m_{2c+1} (bsums 4c..4c+3)
+    // Q6_K: unused (the -32 offset goes through sc and the group's bsum)
+    int m0, m1;
+    float d, dmin;  // super-scales
+};
+
+__device__ __forceinline__ void decode_lane(const WQ4 &w, int c, LaneQ &L) {
+    const int k = c >> 1, o = 16 * (c & 1);
+    const ScaleMin s = unpack_scale_min(w.hdr);
+    L.g[0] = and4(w.qa, 0x0F0F0F0Fu);            // sub-block 2k
+    L.g[1] = and4(shr4(w.qa, 4), 0x0F0F0F0Fu);   // sub-block 2k+1
+    L.g[2] = and4(w.qb, 0x0F0F0F0Fu);            // sub-block 2k+4
+    L.g[3] = and4(shr4(w.qb, 4), 0x0F0F0F0Fu);   // sub-block 2k+5
+    L.sc[0] = byte_of(s.sc_lo, 2 * k);
+    L.sc[1] = byte_of(s.sc_lo, 2 * k + 1);
+    L.sc[2] = byte_of(s.sc_hi, 2 * k);
+    L.sc[3] = byte_of(s.sc_hi, 2 * k + 1);
+    L.aoff[0] = 64 * k + o;
+    L.aoff[1] = 64 * k + 32 + o;
+    L.aoff[2] = 64 * (k + 2) + o;
+    L.aoff[3] = 64 * (k + 2) + 32 + o;
+    const uint32_t mw = (c < 2) ? s.m_lo : s.m_hi;
+    L.m0 = byte_of(mw, 2 * (c & 1));
+    L.m1 = byte_of(mw, 2 * (c & 1) + 1);
+    L.d = half_lo(w.hdr.x);
+    L.dmin = half_hi(w.hdr.x);
+}
+
+// Q5_K: the Q4_K walk plus the fifth bit (kq-arc, k5/k6 commit: "only the
+// high-bit OR in the quant walk differs").  Element 64k+l takes bit 2k of
+// qh[l], element 64k+32+l bit 2k+1; this lane's qh bytes are l in [o, o+16).
+__device__ __forceinline__ uint4 q5_bit(uint4 qh, int bit) {
+    // move bit `bit` of every byte to bit 4
+    uint4 r;
+    if (bit <= 4) {
+        const int sh = 4 - bit;
+        r = make_uint4(qh.x << sh, qh.y << sh, qh.z << sh, qh.w << sh);
+    } else {
+        r = shr4(qh, bit - 4);
+    }
+    return and4(r, 0x10101010u);
+}
+
+__device__ __forceinline__ uint4 or4(uint4 a, uint4 b) {
+    return make_uint4(a.x | b.x, a.y | b.y, a.z | b.z, a.w | b.w);
+}
+
+__device__ __forceinline__ void decode_lane(const WQ5 &w, int c, LaneQ &L) {
+    const int k = c >> 1;
+    WQ4 w4{w.qa, w.qb, w.hdr};
+    decode_lane(w4, c, L);
+    L.g[0] = or4(L.g[0], q5_bit(w.qh, 2 * k));
+    L.g[1] = or4(L.g[1], q5_bit(w.qh, 2 * k + 1));
+    L.g[2] = or4(L.g[2], q5_bit(w.qh, 2 * k + 4));
+    L.g[3] = or4(L.g[3], q5_bit(w.qh, 2 * k + 5));
+}
+
+// Q6_K (kq-arc, k5/k6 commit: "SIGNED per-16 sub-scales"): group t of lane
+// (h, p) holds elements 128h + 32t + 16p .. +15 of sub-block 8h + 2t + p.
+__device__ __forceinline__ void decode_lane(const WQ6 &w, int c, LaneQ &L) {
+    const int h = c >> 1, p = c & 1;
+    L.g[0] = or4(and4(w.la, 0x0F0F0F0Fu), make_uint4((w.qh.x << 4) & 0x30303030u, (w.qh.y << 4) & 0x30303030u,
+                                                      (w.qh.z << 4) & 0x30303030u, (w.qh.w << 4) & 0x30303030u));
+    L.g[1] = or4(and4(w.lb, 0x0F0F0F0Fu), make_uint4((w.qh.x << 2) & 0x30303030u, (w.qh.y << 2) & 0x30303030u,
+                                                      (w.qh.z << 2) & 0x30303030u, (w.qh.w << 2) & 0x30303030u));
+    L.g[2] = or4(and4(shr4(w.la, 4), 0x0F0F0F0Fu), and4(w.qh, 0x30303030u));
+    L.g[3] = or4(and4(shr4(w.lb, 4), 0x0F0F0F0Fu), and4(shr4(w.qh, 2), 0x30303030u));
+    // sub-block i = 8h + 2t + p sits in scale word 2h + t/2, byte 2(t&1) + p
+    const uint32_t w01 = h ? w.sc.z : w.sc.x, w23 = h ? w.sc.w : w.sc.y;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint32_t word = (t < 2) ? w01 : w23;
+        L.sc[t] = static_cast<int>(static_cast<int8_t>((word >> (8 * (2 * (t & 1) + p))) & 0xFF));
+        L.aoff[t] = 128 * h + 32 * t + 16 * p;
+    }
+    L.m0 = L.m1 = 0;
+    L.d = half_lo(w.d);
+    L.dmin = 0.0f;
+}
+
+// ---------------------------------------------------------------------------
+// The lane's integer partials against one token's Q8_K superblock.
+//   a8: the token's 256 quants of this superblock, bs: its 16 bsums.
+// Q4_K/Q5_K: isum_lane = sum_g sc_g * dot16_g, msum_lane = m0*(bs_4c+bs_4c+1)
+//            + m1*(bs_4c+2 + bs_4c+3)   (kq-arc, k4 kq-v2 commit)
+// Q6_K     : isum_lane = sum_t sc_t * dot16_t - 32 * sum_t sc_t * bs_(8h+2t+p),
+//            msum_lane = 0                (kq-arc, k5/k6 commit)
+template <int F>
+__device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, const int16_t *bs, int c,
+                                              int &isum, int &msum) {
+    int acc = 0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) acc += L.sc[g] * dot16(L.g[g], ld_act16(a8 + L.aoff[g]));
+    if constexpr (F == FMT_Q6_K) {
+        const int4 b = __ldg(reinterpret_cast<const int4 *>(bs + 8 * (c >> 1)));  // bs[8h .. 8h+7]
+        const int p = c & 1;
+        const uint32_t bw[4] = {(uint32_t)b.x, (uint32_t)b.y, (uint32_t)b.z, (uint32_t)b.w};
+        int bacc = 0;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int v = static_cast<int16_t>((bw[t] >> (16 * p)) & 0xFFFF);
+            bacc += L.sc[t] * v;
+        }
+        isum = acc - 32 * bacc;
+        msum = 0;
+    } else {
+        const int2 b = __ldg(reinterpret_cast<const int2 *>(bs + 4 * c));  // bs[4c .. 4c+3]
+        const int b0 = static_cast<int16_t>(b.x & 0xFFFF), b1 = static_cast<int16_t>(b.x >> 16);
+        const int b2 = static_cast<int16_t>(b.y & 0xFFFF), b3 = static_cast<int16_t>(b.y >> 16);
+        isum = acc;
+        msum = L.m0 * (b0 + b1) + L.m1 * (b2 + b3);
+    }
+}
+
+__device__ __forceinline__ int quad_sum(int v) {
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+    return v;
+}
+
+}  // namespace kq

@@ -1,0 +1,50 @@
+// kq_internal.h - host-side launchers shared between the translation units of
+// libkq.  Arguments are validated by the C-ABI layer (kq_api.cu) before any
+// of these run; they only shape grids and enqueue kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kq_device.cuh"
+
+namespace kq {
+
+struct Q8K {
+    const float *d;
+    const int8_t *qs;
+    const int16_t *bsums;
+};
+
+// Q8_K quantization of x [M][K].
+cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8_t *qs,
+                            int16_t *bsums, cudaStream_t s);
+
+// Disk superblocks -> packed image.
+cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,
+                          cudaStream_t s);
+
+// CUDA-core matrix-vector family: M tokens (grouped by expert when
+// row_offsets != nullptr), each weight superblock unpacked once per pass
+// over a group of up to 8 tokens.
+cudaError_t launch_mv(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
+                      const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
+                      cudaStream_t s);
+
+cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
+                            int32_t *isum, int32_t *msum, cudaStream_t s);
+
+cudaError_t launch_debug_decode(int f, const void *packed, int64_t N, int64_t K, int32_t *q,
+                                int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
+
+// Tensor-core GEMM (tcgen05).  Returns cudaErrorNotSupported when the shape
+// or device is not handled, so the caller can fall back to launch_mv.
+size_t gemm_workspace_bytes(int f, int64_t M, int64_t N, int64_t K);
+cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
+                           const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
+                           void *workspace, size_t workspace_bytes, cudaStream_t s);
+
+// Device status word of the bounded waits.
+int read_and_clear_status(cudaStream_t s, int *status);
+
+}  // namespace kq

@@ -1,0 +1,124 @@
+// kq_quant.cu - Q8_K activation quantization and the one-time weight repack.
+//
+// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
+#include "kq_internal.h"
+
+namespace kq {
+
+// ---------------------------------------------------------------------------
+// Q8_K quantization (kq-arc, k4 kq-v2 commit: quantize_q8_k_into, "ONE fp32
+// scale per 256-superblock + per-16 bsums").  One warp per 256-block; lane l
+// owns elements 8l .. 8l+7.  Per block: amax = max|x| (a max over the bit
+// patterns of |x|, which order like the values for finite floats);
+// iscale = 127/amax and q = round_half_even(x*iscale), clamped to +-127,
+// both single IEEE fp32 operations; d8 = amax/127; bsum i = sum of q over
+// 16i .. 16i+15 (lanes 2i and 2i+1).
+__global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restrict__ x, int64_t K,
+                                                           int64_t nblocks, float *__restrict__ d,
+                                                           int8_t *__restrict__ qs,
+                                                           int16_t *__restrict__ bsums) {
+    const int lane = threadIdx.x & 31;
+    const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (blk >= nblocks) return;
+    const int64_t nsb = K / QK;
+    const int64_t m = blk / nsb, sb = blk % nsb;
+    const float *xb = x + m * K + sb * QK + 8 * lane;
+    const float4 v0 = __ldg(reinterpret_cast<const float4 *>(xb));
+    const float4 v1 = __ldg(reinterpret_cast<const float4 *>(xb + 4));
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float ax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ax = fmaxf(ax, fabsf(v[i]));
+    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(ax)));
+
+    int q[8];
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+    } else {
+        const float iscale = __fdiv_rn(127.0f, amax);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int t = __float2int_rn(__fmul_rn(v[i], iscale));
+            q[i] = max(-127, min(127, t));
+        }
+    }
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        lo |= (static_cast<uint32_t>(q[i]) & 0xFFu) << (8 * i);
+        hi |= (static_cast<uint32_t>(q[i + 4]) & 0xFFu) << (8 * i);
+    }
+    *reinterpret_cast<uint2 *>(qs + m * K + sb * QK + 8 * lane) = make_uint2(lo, hi);
+
+    int part = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+    if ((lane & 1) == 0) bsums[blk * 16 + (lane >> 1)] = static_cast<int16_t>(part);
+    if (lane == 0) d[blk] = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+}
+
+cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8_t *qs,
+                            int16_t *bsums, cudaStream_t s) {
+    const int64_t nblocks = M * (K / QK);
+    if (nblocks == 0) return cudaSuccess;
+    const int64_t grid = (nblocks + 7) / 8;
+    quantize_q8k_kernel<<<(unsigned)grid, 256, 0, s>>>(x, K, nblocks, d, qs, bsums);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Repack (kq-arc, k4 kq-v2 commit: the transcode keeps the disk scale block
+// verbatim and the plane dequant is bit-identical to the disk dequant).
+// One thread per superblock moves each field of the GGUF-order block into
+// its plane; no value is changed.  The disk block is read as 16-bit words
+// (210-byte Q6_K blocks are only 2-byte aligned).
+
+__device__ __forceinline__ void copy16s(uint8_t *dst, const uint16_t *src, int n16) {
+    // dst 16-byte aligned, n16 = bytes / 16
+    for (int i = 0; i < n16; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = static_cast<uint32_t>(src[8 * i + 2 * j]) | (static_cast<uint32_t>(src[8 * i + 2 * j + 1]) << 16);
+        *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <int F>
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ disk, int64_t units,
+                                                     Planes P) {
+    const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (u >= units) return;
+    const uint16_t *b = reinterpret_cast<const uint16_t *>(disk + u * (int64_t)block_bytes(F));
+    uint8_t *p0 = const_cast<uint8_t *>(P.p0), *p1 = const_cast<uint8_t *>(P.p1);
+    uint8_t *p2 = const_cast<uint8_t *>(P.p2), *p3 = const_cast<uint8_t *>(P.p3);
+    if constexpr (F == FMT_Q4_K) {
+        copy16s(p1 + u * 16, b, 1);            // d, dmin, scales[12]
+        copy16s(p0 + u * 128, b + 8, 8);       // qs
+    } else if constexpr (F == FMT_Q5_K) {
+        copy16s(p2 + u * 16, b, 1);            // d, dmin, scales[12]
+        copy16s(p1 + u * 32, b + 8, 2);        // qh
+        copy16s(p0 + u * 128, b + 24, 8);      // qs
+    } else {
+        copy16s(p0 + u * 128, b, 8);           // ql
+        copy16s(p1 + u * 64, b + 64, 4);       // qh
+        copy16s(p2 + u * 16, b + 96, 1);       // scales (int8)
+        reinterpret_cast<uint16_t *>(p3)[u] = b[104];  // d
+    }
+}
+
+cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,
+                          cudaStream_t s) {
+    const int64_t nsb = K / QK;
+    const int64_t units = N * nsb;
+    if (units == 0) return cudaSuccess;
+    const Planes P = make_planes(f, packed, N, nsb);
+    const unsigned grid = (unsigned)((units + 255) / 256);
+    if (f == FMT_Q4_K) repack_kernel<FMT_Q4_K><<<grid, 256, 0, s>>>(disk, units, P);
+    else if (f == FMT_Q5_K) repack_kernel<FMT_Q5_K><<<grid, 256, 0, s>>>(disk, units, P);
+    else repack_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(disk, units, P);
+    return cudaGetLastError();
+}
+
+}  // namespace kq

@@ -1,0 +1,222 @@
+"""Thin ctypes binding of libkq.so (include/kq.h), with the same names.
+
+Argument marshalling only: torch tensors provide device memory and the
+current CUDA stream; every step of the computation runs in libkq's CUDA
+kernels.  Importing this module raises if libkq.so has not been built
+(``python -m quantized_gemv_gemm_gb300.build``): there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+import torch
+
+Q4_K, Q5_K, Q6_K = 1, 2, 3
+QK = 256
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkq.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"libkq.so is missing at {_LIB_PATH}: build it with "
+                      "`python -m quantized_gemv_gemm_gb300.build` (no CPU fallback exists)")
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+_INT = ctypes.c_int
+
+
+class _Q8KConst(ctypes.Structure):
+    _fields_ = [("d", _P), ("qs", _P), ("bsums", _P)]
+
+
+_lib.kq_strerror.argtypes = [_INT]
+_lib.kq_strerror.restype = ctypes.c_char_p
+_lib.kq_block_bytes.argtypes = [_INT]
+_lib.kq_block_bytes.restype = _SZ
+_lib.kq_quantize_q8k.argtypes = [_P, _I64, _I64, _Q8KConst, _P]
+_lib.kq_repack_bytes.argtypes = [_INT, _I64, _I64]
+_lib.kq_repack_bytes.restype = _SZ
+_lib.kq_repack.argtypes = [_INT, _P, _I64, _I64, _P, _P]
+_lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P]
+_lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
+_lib.kq_gemm_workspace_bytes.restype = _SZ
+_lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
+_lib.kq_gemm_grouped.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
+_lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
+_lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
+_lib.kq_device_status.argtypes = [_P]
+for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemm", "kq_gemm_grouped",
+           "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
+    getattr(_lib, _f).restype = _INT
+
+LIB_PATH = _LIB_PATH
+
+
+class KQError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {kq_strerror(code)} ({code})")
+
+
+class Q8K(NamedTuple):
+    """Q8_K activation planes on the device."""
+    d: torch.Tensor        # float32 [M, K/256]
+    qs: torch.Tensor       # int8    [M, K]
+    bsums: torch.Tensor    # int16   [M, K/16]
+
+
+def kq_strerror(code: int) -> str:
+    return _lib.kq_strerror(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise KQError(rc, where)
+
+
+def _q8k_struct(a: Q8K) -> _Q8KConst:
+    return _Q8KConst(a.d.data_ptr(), a.qs.data_ptr(), a.bsums.data_ptr())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("libkq takes contiguous CUDA tensors")
+
+
+def kq_block_bytes(fmt: int) -> int:
+    return int(_lib.kq_block_bytes(int(fmt)))
+
+
+def q8k_empty(M: int, K: int, device="cuda") -> Q8K:
+    return Q8K(torch.empty((M, K // QK), dtype=torch.float32, device=device),
+               torch.empty((M, K), dtype=torch.int8, device=device),
+               torch.empty((M, K // 16), dtype=torch.int16, device=device))
+
+
+def kq_quantize_q8k(x: torch.Tensor, out: Optional[Q8K] = None, stream=None) -> Q8K:
+    """Q8_K planes of float32 x [M, K] (or [K])."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    _need_cuda(x)
+    if x.dtype != torch.float32:
+        raise ValueError("x must be float32")
+    M, K = x.shape
+    if out is None:
+        out = q8k_empty(M, K, x.device)
+    _need_cuda(*out)
+    _check(_lib.kq_quantize_q8k(_ptr(x), M, K, _q8k_struct(out), _stream(stream)), "kq_quantize_q8k")
+    return out
+
+
+def kq_repack_bytes(fmt: int, N: int, K: int) -> int:
+    return int(_lib.kq_repack_bytes(int(fmt), int(N), int(K)))
+
+
+def kq_repack(fmt: int, disk: torch.Tensor, N: int, K: int, packed: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """Repack disk superblocks (uint8 device tensor, N*K/256*block_bytes bytes)."""
+    _need_cuda(disk)
+    nbytes = kq_repack_bytes(fmt, N, K)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=disk.device)
+    _need_cuda(packed)
+    if packed.numel() < nbytes:
+        raise ValueError("packed buffer too small")
+    _check(_lib.kq_repack(int(fmt), _ptr(disk), N, K, _ptr(packed), _stream(stream)), "kq_repack")
+    return packed
+
+
+def kq_gemv(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, y: Optional[torch.Tensor] = None,
+            stream=None) -> torch.Tensor:
+    _need_cuda(packed, *a)
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=packed.device)
+    _need_cuda(y)
+    _check(_lib.kq_gemv(int(fmt), _ptr(packed), N, K, _q8k_struct(a), _ptr(y), _stream(stream)), "kq_gemv")
+    return y
+
+
+def kq_gemm_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
+    return int(_lib.kq_gemm_workspace_bytes(int(fmt), int(M), int(N), int(K)))
+
+
+def _workspace(fmt, M, N, K, workspace, device):
+    need = kq_gemm_workspace_bytes(fmt, M, N, K)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    return workspace, (0 if workspace is None else workspace.numel())
+
+
+def kq_gemm(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, y: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    _need_cuda(packed, *a)
+    M = a.qs.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=packed.device)
+    _need_cuda(y, workspace)
+    workspace, ws_bytes = _workspace(fmt, M, N, K, workspace, packed.device)
+    _check(_lib.kq_gemm(int(fmt), _ptr(packed), N, K, _q8k_struct(a), M, _ptr(y), _ptr(workspace), ws_bytes,
+                        _stream(stream)), "kq_gemm")
+    return y
+
+
+def kq_gemm_grouped(fmt: int, packed: torch.Tensor, E: int, row_offsets: torch.Tensor, N: int, K: int,
+                    a: Q8K, y: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    _need_cuda(packed, row_offsets, *a)
+    if row_offsets.dtype != torch.int32:
+        raise ValueError("row_offsets must be int32")
+    M = a.qs.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=packed.device)
+    _need_cuda(y, workspace)
+    workspace, ws_bytes = _workspace(fmt, M, N, K, workspace, packed.device)
+    _check(_lib.kq_gemm_grouped(int(fmt), _ptr(packed), E, _ptr(row_offsets), N, K, _q8k_struct(a), M, _ptr(y),
+                                _ptr(workspace), ws_bytes, _stream(stream)), "kq_gemm_grouped")
+    return y
+
+
+def kq_debug_partials(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, stream=None):
+    _need_cuda(packed, *a)
+    M = a.qs.shape[0]
+    isum = torch.zeros((M, N, K // QK), dtype=torch.int32, device=packed.device)
+    msum = torch.zeros_like(isum)
+    _check(_lib.kq_debug_partials(int(fmt), _ptr(packed), N, K, _q8k_struct(a), M, _ptr(isum), _ptr(msum),
+                                  _stream(stream)), "kq_debug_partials")
+    return isum, msum
+
+
+def kq_debug_decode(fmt: int, packed: torch.Tensor, N: int, K: int, stream=None) -> dict:
+    _need_cuda(packed)
+    nsb = K // QK
+    dev = packed.device
+    q = torch.zeros((N, K), dtype=torch.int32, device=dev)
+    sc = torch.zeros((N, nsb, 16), dtype=torch.int32, device=dev)
+    mn = torch.zeros((N, nsb, 8), dtype=torch.int32, device=dev)
+    d = torch.zeros((N, nsb), dtype=torch.float32, device=dev)
+    dmin = torch.zeros((N, nsb), dtype=torch.float32, device=dev)
+    _check(_lib.kq_debug_decode(int(fmt), _ptr(packed), N, K, _ptr(q), _ptr(sc), _ptr(mn), _ptr(d), _ptr(dmin),
+                                _stream(stream)), "kq_debug_decode")
+    return {"q": q, "sc": sc, "m": mn, "d": d, "dmin": dmin}
+
+
+def kq_device_status(stream=None) -> int:
+    return int(_lib.kq_device_status(_stream(stream)))
+
+
+def raw():
+    """The ctypes handle of libkq.so, for callers that pass raw pointers."""
+    return _lib

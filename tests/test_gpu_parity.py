@@ -1,0 +1,298 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Bit-exact: Q8_K quantization (d8, q8, bsums), the repacked image's decode,
+and the int32 partials of the fold.  Floating point: every output within
+1e-3 x max|row output| of the oracle's fp64 value, per token row.
+Full-size workloads are checked on sampled outputs computed one by one by
+the oracle, in the launch configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_gemv_gemm_gb300 import synth
+
+from gpu_util import (assert_row_tol, check_guard, kq, oracle_q8k, pack, poisoned, q8k_to_dev, to_dev)
+
+pytestmark = pytest.mark.gpu
+FMTS = [synth.Q4_K, synth.Q5_K, synth.Q6_K]
+
+
+@pytest.fixture(scope="module")
+def K():
+    assert torch.cuda.is_available()
+    return kq()
+
+
+# ---------------------------------------------------------------- Q8_K
+@pytest.mark.parametrize("M,Kdim,outliers", [(1, 1024, False), (3, 2560, False), (512, 5120, True),
+                                             (4096, 2048, False), (7, 256, False)])
+def test_quantize_bit_exact(K, M, Kdim, outliers):
+    rng = synth.rng_for(100, M * 7 + Kdim)
+    x = synth.activations(M, Kdim, rng, outliers=outliers)
+    if M >= 3:
+        x[0, :256] = 0.0                           # zero block
+        x[1, 256 * (Kdim // 512):] *= np.float32(1e-30)
+        x[2, 5] = np.float32(3e4)
+        x[2, :256] = np.float32(2.5)               # ties: x*iscale lands on .5
+        x[2, 0] = np.float32(127.0)
+    ref = oracle_q8k(x)
+    got = K.kq_quantize_q8k(to_dev(x))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got.d.cpu().numpy(), ref[0])
+    np.testing.assert_array_equal(got.qs.cpu().numpy(), ref[1])
+    np.testing.assert_array_equal(got.bsums.cpu().numpy(), ref[2])
+
+
+# ---------------------------------------------------------------- repack
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,Kdim", [(1, 256), (200, 768), (37, 2560)])
+def test_repack_round_trip(K, fmt, N, Kdim):
+    disk = synth.disk_weights(fmt, N, Kdim, synth.rng_for(101, fmt * 1000 + N))
+    packed = pack(K, fmt, disk)
+    dec = K.kq_debug_decode(fmt, packed, N, Kdim)
+    torch.cuda.synchronize()
+    nsb = Kdim // 256
+    nsub = 16 if fmt == synth.Q6_K else 8
+    q = dec["q"].cpu().numpy().reshape(N, nsb, 256)
+    sc = dec["sc"].cpu().numpy()
+    mn = dec["m"].cpu().numpy()
+    d = dec["d"].cpu().numpy()
+    dmin = dec["dmin"].cpu().numpy()
+    for n in range(N):
+        for s in range(nsb):
+            ref = oracle.decode(fmt, disk[n, s])
+            np.testing.assert_array_equal(q[n, s], ref["q"])
+            np.testing.assert_array_equal(sc[n, s, :nsub], ref["sc"])
+            np.testing.assert_array_equal(mn[n, s], ref["m"])
+            assert d[n, s] == np.float32(ref["d"]) and dmin[n, s] == np.float32(ref["dmin"])
+
+
+# ---------------------------------------------------------------- partials
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,Kdim,M", [(1, 256, 1), (8, 768, 3), (200, 2560, 2)])
+def test_partials_bit_exact(K, fmt, N, Kdim, M):
+    rng = synth.rng_for(102, fmt * 100 + N)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    x = synth.activations(M, Kdim, rng)
+    planes = oracle_q8k(x)
+    ref_i, ref_m = oracle.partials(fmt, disk, planes[1], planes[2])
+    got_i, got_m = K.kq_debug_partials(fmt, pack(K, fmt, disk), N, Kdim, q8k_to_dev(K, planes))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got_i.cpu().numpy(), ref_i)
+    np.testing.assert_array_equal(got_m.cpu().numpy(), ref_m)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_partials_worst_case_fields(K, fmt):
+    """Every stored field at its extreme (q max, sub-scales max / -128, q8 = -127):
+    the int32 partials still match exactly (the page's |iacc| < 2^28 bound)."""
+    blk = np.full((2, 1, synth.BLOCK_BYTES[fmt]), 255, np.uint8)
+    if fmt == synth.Q6_K:
+        blk[0, 0, 192:208] = np.array([-128] * 16, np.int8).view(np.uint8)
+        blk[1, 0, 192:208] = np.array([127] * 16, np.int8).view(np.uint8)
+        blk[:, 0, 208:210] = [0x00, 0x3C]
+    else:
+        blk[:, 0, 0:4] = [0x00, 0x3C, 0x00, 0x3C]
+    planes = (np.ones((2, 1), np.float32), np.array([[-127] * 256, [127] * 256], np.int8),
+              np.array([[-127 * 16] * 16, [127 * 16] * 16], np.int16))
+    ref_i, ref_m = oracle.partials(fmt, blk, planes[1], planes[2])
+    got_i, got_m = K.kq_debug_partials(fmt, pack(K, fmt, blk), 2, 256, q8k_to_dev(K, planes))
+    np.testing.assert_array_equal(got_i.cpu().numpy(), ref_i)
+    np.testing.assert_array_equal(got_m.cpu().numpy(), ref_m)
+
+
+# ---------------------------------------------------------------- GEMV
+def run_gemv(K, fmt, disk, x):
+    N, nsb, _ = disk.shape
+    Kdim = nsb * 256
+    planes = oracle_q8k(x)
+    full, y = poisoned((N,))
+    K.kq_gemv(fmt, pack(K, fmt, disk), N, Kdim, q8k_to_dev(K, planes), y=y)
+    torch.cuda.synchronize()
+    check_guard(full, N)
+    return y.cpu().numpy(), planes
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("N,Kdim", [(1, 256), (8, 1024), (200, 768), (1000, 2560), (77, 4096)])
+def test_gemv_small_shapes(K, fmt, N, Kdim):
+    rng = synth.rng_for(103, fmt * 10000 + N)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    x = synth.activations(1, Kdim, rng)
+    y, planes = run_gemv(K, fmt, disk, x)
+    ref = oracle.gemm(fmt, disk, *planes)[0]
+    assert_row_tol(y, ref)
+
+
+def test_gemv_tiny_config(K):
+    """The tiny Q4_K GEMV workload: N=256, K=1024, seed 0."""
+    cfg = synth.configs()[0]
+    m = cfg.matrices[0]
+    disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(0, 0))
+    x = synth.activations(1, m.K, synth.rng_for(0, 1))
+    y, planes = run_gemv(K, m.fmt, disk, x)
+    assert_row_tol(y, oracle.gemm(m.fmt, disk, *planes)[0])
+
+
+@pytest.mark.parametrize("cfg_index", [1, 3])
+def test_gemv_full_size_layers(K, cfg_index):
+    """Decode layers at full size (Qwen3-4B-shaped layer; 27B-shaped FFN at M=1),
+    every output compared."""
+    cfg = synth.configs()[cfg_index]
+    for i, m in enumerate(cfg.matrices):
+        disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(cfg_index, 2 * i))
+        x = synth.activations(1, m.K, synth.rng_for(cfg_index, 2 * i + 1), outliers=cfg.outliers)
+        y, planes = run_gemv(K, m.fmt, disk, x)
+        assert_row_tol(y, oracle.gemm(m.fmt, disk, *planes)[0])
+
+
+def test_gemv_row_stride(K):
+    """8 rows, each perturbed differently: each output equals its own row's
+    dot (the page's multi-row stride gate)."""
+    fmt, N, Kdim = synth.Q4_K, 8, 2560
+    rng = synth.rng_for(104, 0)
+    base = synth.disk_weights(fmt, 1, Kdim, rng)
+    disk = np.repeat(base, N, axis=0)
+    for n in range(N):
+        disk[n, :, 20 + n] ^= np.uint8(0x5A)
+    x = synth.activations(1, Kdim, rng)
+    y, planes = run_gemv(K, fmt, disk, x)
+    for n in range(N):
+        assert_row_tol(y[n:n + 1], oracle.gemm(fmt, disk[n:n + 1], *planes)[0], row_max=np.abs(y).max())
+
+
+# ---------------------------------------------------------------- GEMM
+def run_gemm(K, fmt, disk, planes, M):
+    N, nsb, _ = disk.shape
+    full, y = poisoned((M, N))
+    K.kq_gemm(fmt, pack(K, fmt, disk), N, nsb * 256, q8k_to_dev(K, planes), y=y)
+    torch.cuda.synchronize()
+    check_guard(full, M * N)
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N,Kdim", [(2, 200, 768), (3, 64, 256), (17, 130, 1024), (100, 200, 768),
+                                      (129, 136, 512), (300, 250, 1280)])
+def test_gemm_small_shapes(K, fmt, M, N, Kdim):
+    rng = synth.rng_for(105, fmt * 100000 + M * 100 + N)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    planes = oracle_q8k(synth.activations(M, Kdim, rng))
+    y = run_gemm(K, fmt, disk, planes, M)
+    assert_row_tol(y, oracle.gemm(fmt, disk, *planes))
+
+
+def sample_check(y, fmt, disk, planes, rng, n_rows=48, n_toks=6):
+    """Oracle on all tokens x sampled rows, and sampled tokens x all rows."""
+    M, N = y.shape
+    rows = np.sort(rng.choice(N, size=min(n_rows, N), replace=False))
+    rows[0], rows[-1] = 0, N - 1
+    ref = oracle.gemm(fmt, disk, *planes, n_idx=rows)
+    toks = np.unique(np.concatenate([[0, M - 1], rng.choice(M, size=min(n_toks, M), replace=False)]))
+    ref_t = oracle.gemm(fmt, disk, *planes, tok_idx=toks)
+    assert_row_tol(y[toks], ref_t)
+    # sampled rows of every token: scale by the largest |output| among them
+    # (never larger than the full row's, so no looser than the bound)
+    assert_row_tol(y[:, rows], ref)
+
+
+@pytest.mark.parametrize("half", [0, 1])
+def test_gemm_prefill_qwen3_4b(K, half):
+    """Qwen3-4B-shaped prefill pp512: all-Q5_K layer, then all-Q6_K layer."""
+    cfg = synth.configs()[2]
+    M = cfg.M
+    for i, m in enumerate(cfg.matrices[7 * half:7 * half + 7]):
+        j = 7 * half + i
+        disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(2, 2 * j))
+        planes = oracle_q8k(synth.activations(M, m.K, synth.rng_for(2, 2 * j + 1)))
+        y = run_gemm(K, m.fmt, disk, planes, M)
+        sample_check(y, m.fmt, disk, planes, synth.rng_for(902, j))
+
+
+def test_gemm_prefill_27b_ffn(K):
+    cfg = synth.configs()[3]
+    M = cfg.M
+    for i, m in enumerate(cfg.matrices):
+        disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(3, 2 * i))
+        planes = oracle_q8k(synth.activations(M, m.K, synth.rng_for(3, 2 * i + 1), outliers=True))
+        y = run_gemm(K, m.fmt, disk, planes, M)
+        sample_check(y, m.fmt, disk, planes, synth.rng_for(903, i))
+
+
+def test_gemm_row_equals_gemv(K):
+    """Row m of the GEMM equals the GEMV of token m (within the tolerance; the
+    int32 partials themselves are checked bit-exact above)."""
+    fmt, N, Kdim, M = synth.Q6_K, 300, 2560, 40
+    rng = synth.rng_for(106, 0)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    planes = oracle_q8k(synth.activations(M, Kdim, rng))
+    y = run_gemm(K, fmt, disk, planes, M)
+    packed = pack(K, fmt, disk)
+    for m in (0, 17, M - 1):
+        one = tuple(p[m:m + 1] for p in planes)
+        g = K.kq_gemv(fmt, packed, N, Kdim, q8k_to_dev(K, one)).cpu().numpy()
+        assert_row_tol(y[m], g)
+
+
+# ---------------------------------------------------------------- grouped
+def run_grouped(K, fmt, disks, planes, offsets):
+    E = len(disks)
+    N, nsb, _ = disks[0].shape
+    Kdim = nsb * 256
+    per = K.kq_repack_bytes(fmt, N, Kdim)
+    packed = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        K.kq_repack(fmt, to_dev(disks[e].reshape(-1)), N, Kdim, packed=packed[e * per:(e + 1) * per])
+    M = int(offsets[-1])
+    full, y = poisoned((M, N))
+    K.kq_gemm_grouped(fmt, packed, E, to_dev(offsets.astype(np.int32)), N, Kdim, q8k_to_dev(K, planes), y=y)
+    torch.cuda.synchronize()
+    check_guard(full, M * N)
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_grouped_uneven_and_empty_experts(K, fmt):
+    rng = synth.rng_for(107, fmt)
+    E, N, Kdim = 6, 72, 512
+    counts = np.array([5, 0, 17, 1, 0, 40])
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    planes = oracle_q8k(synth.activations(int(offsets[-1]), Kdim, rng))
+    y = run_grouped(K, fmt, disks, planes, offsets)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        sl = tuple(p[a:b] for p in planes)
+        assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
+
+
+def test_grouped_moe_30b_a3b(K):
+    """The MoE workload: 128 experts, top-8 of 512 tokens (4096 rows grouped by
+    expert); gate/up Q4_K [768 x 2048], down Q6_K [2048 x 768]."""
+    cfg = synth.configs()[4]
+    T, E = cfg.M, cfg.experts
+    row_token, row_expert, offsets = synth.moe_routing(T, E, cfg.topk, synth.rng_for(4, 0))
+    x_tok = synth.activations(T, 2048, synth.rng_for(4, 1))
+    check_rng = synth.rng_for(904, 0)
+    for i, m in enumerate(cfg.matrices):
+        disks = [synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(4, 10 + 1000 * i + e)) for e in range(E)]
+        if m.name == "down":
+            x = synth.activations(len(row_token), m.K, synth.rng_for(4, 2))
+        else:
+            x = x_tok[row_token]
+        planes = oracle_q8k(x)
+        y = run_grouped(K, m.fmt, disks, planes, offsets)
+        # every expert's first and last row, plus a few random rows, all N
+        rows = set()
+        for e in range(E):
+            if offsets[e] < offsets[e + 1]:
+                rows.update({int(offsets[e]), int(offsets[e + 1]) - 1})
+        rows.update(check_rng.choice(len(row_token), 32, replace=False).tolist())
+        for r in sorted(rows):
+            e = int(row_expert[r])
+            one = tuple(p[r:r + 1] for p in planes)
+            assert_row_tol(y[r:r + 1], oracle.gemm(m.fmt, disks[e], *one))

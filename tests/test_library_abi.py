@@ -1,0 +1,86 @@
+"""libkq.so loads, exports every entry point of include/kq.h, and rejects bad
+arguments on the host (no GPU needed: argument checks run before any CUDA
+call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kq.h")
+
+
+@pytest.fixture(scope="module")
+def kq():
+    from quantized_gemv_gemm_gb300 import build
+    build.build()
+    from quantized_gemv_gemm_gb300 import kq as mod
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(kq):
+    lib = ctypes.CDLL(kq.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in kq.h but not exported"
+
+
+def test_sizes_and_names(kq):
+    assert [kq.kq_block_bytes(f) for f in (1, 2, 3)] == [144, 176, 210]
+    assert kq.kq_block_bytes(7) == 0
+    for f, per_sb in ((1, 144), (2, 176), (3, 210)):
+        for N, K in ((4096, 2560), (1, 256), (5, 17408)):
+            nb = kq.kq_repack_bytes(f, N, K)
+            assert nb % 256 == 0
+            disk = N * (K // 256) * per_sb
+            assert disk <= nb <= disk + 4 * 255
+    assert kq.kq_repack_bytes(1, 10, 100) == 0
+    assert kq.kq_repack_bytes(1, -1, 256) == 0
+    assert kq.kq_repack_bytes(4, 10, 256) == 0
+    assert "invalid" in kq.kq_strerror(-1)
+    assert kq.kq_strerror(12345) == "unknown kq status"
+
+
+def test_host_argument_checks(kq):
+    lib = kq.raw()
+    Q = kq._Q8KConst
+    nullq = Q(0, 0, 0)
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: checks fail first
+    odd = ctypes.c_void_p(0x10004)
+    goodq = Q(0x10000, 0x10000, 0x10000)
+    ARG, ALIGN, FMT, WS = -1, -2, -3, -6
+    # format
+    assert lib.kq_gemv(9, fake, 8, 256, goodq, fake, None) == FMT
+    assert lib.kq_repack(0, fake, 8, 256, fake, None) == FMT
+    # shapes
+    assert lib.kq_gemv(1, fake, 8, 100, goodq, fake, None) == ARG
+    assert lib.kq_gemv(1, fake, -1, 256, goodq, fake, None) == ARG
+    assert lib.kq_quantize_q8k(fake, -1, 256, goodq, None) == ARG
+    assert lib.kq_quantize_q8k(fake, 2, 300, goodq, None) == ARG
+    # null pointers
+    assert lib.kq_gemv(1, None, 8, 256, goodq, fake, None) == ARG
+    assert lib.kq_gemv(1, fake, 8, 256, nullq, fake, None) == ARG
+    assert lib.kq_gemm(1, fake, 8, 256, goodq, 4, None, None, 0, None) == ARG
+    assert lib.kq_gemm_grouped(1, fake, 4, None, 8, 256, goodq, 4, fake, None, 0, None) == ARG
+    assert lib.kq_quantize_q8k(None, 2, 256, goodq, None) == ARG
+    # alignment
+    assert lib.kq_gemv(1, odd, 8, 256, goodq, fake, None) == ALIGN
+    assert lib.kq_gemv(1, fake, 8, 256, Q(0x10000, 0x10004, 0x10000), fake, None) == ALIGN
+    assert lib.kq_quantize_q8k(odd, 2, 256, goodq, None) == ALIGN
+    assert lib.kq_repack(1, odd, 8, 256, fake, None) == ALIGN
+    # empty problems are no-ops that touch nothing
+    assert lib.kq_gemv(1, None, 0, 256, nullq, None, None) == 0
+    assert lib.kq_gemm(2, None, 16, 512, nullq, 0, None, None, 0, None) == 0
+    assert lib.kq_quantize_q8k(None, 0, 256, nullq, None) == 0
+    # workspace: required size must be provided when non-zero
+    need = kq.kq_gemm_workspace_bytes(1, 512, 4096, 2560)
+    if need:
+        assert lib.kq_gemm(1, fake, 4096, 2560, goodq, 512, fake, None, 0, None) == WS
