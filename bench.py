@@ -201,6 +201,8 @@ def run_ours(args, world, rank, local):
     from quantized_gemv_gemm_gb300 import kq
 
     peaks = load_peaks()
+    if not args.no_pdl:
+        kq.kq_set_launch_flags(kq.KQ_LAUNCH_PDL)
     L = args.layers
     layers = DecodeLayers(kq, torch, L)
     rot = lambda: [layers.step(l) for l in range(L)]  # noqa: E731
@@ -330,6 +332,7 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs larger than L2: {L} rotating layer copies, "
                              f"{bytes_per_step * L / 1e6:.1f} MB of weights",
                        "timing": "CUDA events around graph replays of K steps",
+                       "pdl": not args.no_pdl,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "kq mv_kernel (GEMV, 7 launches per step)",
                          "timing": "event nodes in graph replays" if graph_events else "eager launches with events",
@@ -514,6 +517,7 @@ def main():
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_env()

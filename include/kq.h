@@ -193,6 +193,25 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
                     int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
 
 /*
+ * Launch options, process-wide (a plain atomic word; the new value applies
+ * to launches enqueued after the call).  Returns the previous flags.
+ *
+ * KQ_LAUNCH_PDL: launch kq_quantize_q8k and kq_gemv with programmatic
+ *   dependent launch, so that each may start while the previous kernel in
+ *   the stream is still running.  Both wait (griddepcontrol.wait) for the
+ *   previous kernels to complete before reading activations or writing any
+ *   output, except that kq_gemv reads the packed weight image BEFORE that
+ *   wait, to overlap its weight stream with the previous kernel.  With the
+ *   flag set, a packed image must not be written by work that may still be
+ *   running on the stream when kq_gemv is enqueued (synchronise, or wait on
+ *   an event recorded after kq_repack, before the first kq_gemv).
+ *   Default: off.
+ */
+#define KQ_LAUNCH_PDL 1u
+unsigned kq_set_launch_flags(unsigned flags);
+unsigned kq_get_launch_flags(void);
+
+/*
  * Synchronise stream s and return the device status word of the library's
  * bounded waits on the current device (KQ_OK, or KQ_ERR_TIMEOUT if a kernel
  * gave up waiting), then clear it.  Returns KQ_ERR_LAUNCH if the

@@ -4,7 +4,14 @@
 #include "../../include/kq.h"
 #include "kq_internal.h"
 
+#include <atomic>
+
 using namespace kq;
+
+namespace kq {
+static std::atomic<unsigned> g_launch_flags{0};
+unsigned launch_flags() { return g_launch_flags.load(std::memory_order_relaxed); }
+}  // namespace kq
 
 namespace {
 
@@ -145,6 +152,12 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
     if (!aligned(packed, 256)) return KQ_ERR_ALIGN;
     return launch_status(launch_debug_decode(f, packed, N, K, q, sc, mn, d, dmin, s));
 }
+
+unsigned kq_set_launch_flags(unsigned flags) {
+    return g_launch_flags.exchange(flags & KQ_LAUNCH_PDL, std::memory_order_relaxed);
+}
+
+unsigned kq_get_launch_flags(void) { return launch_flags(); }
 
 int kq_device_status(cudaStream_t s) {
     int st = 0;

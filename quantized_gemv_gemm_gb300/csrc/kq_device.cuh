@@ -263,14 +263,20 @@ __device__ __forceinline__ void decode_lane(const WQ6 &w, int c, LaneQ &L) {
 //            + m1*(bs_4c+2 + bs_4c+3)   (kq-arc, k4 kq-v2 commit)
 // Q6_K     : isum_lane = sum_t sc_t * dot16_t - 32 * sum_t sc_t * bs_(8h+2t+p),
 //            msum_lane = 0                (kq-arc, k5/k6 commit)
-template <int F>
+template <int F, bool SMEM = false>
 __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, const int16_t *bs, int c,
                                               int &isum, int &msum) {
+    // SMEM: a8 / bs point into shared memory (plain loads); otherwise global
+    // memory read through the read-only path.
+    auto ld16 = [](const void *q) -> int4 {
+        if constexpr (SMEM) return *reinterpret_cast<const int4 *>(q);
+        else return __ldg(reinterpret_cast<const int4 *>(q));
+    };
     int acc = 0;
 #pragma unroll
-    for (int g = 0; g < 4; ++g) acc += L.sc[g] * dot16(L.g[g], ld_act16(a8 + L.aoff[g]));
+    for (int g = 0; g < 4; ++g) acc += L.sc[g] * dot16(L.g[g], ld16(a8 + L.aoff[g]));
     if constexpr (F == FMT_Q6_K) {
-        const int4 b = __ldg(reinterpret_cast<const int4 *>(bs + 8 * (c >> 1)));  // bs[8h .. 8h+7]
+        const int4 b = ld16(bs + 8 * (c >> 1));  // bs[8h .. 8h+7]
         const int p = c & 1;
         const uint32_t bw[4] = {(uint32_t)b.x, (uint32_t)b.y, (uint32_t)b.z, (uint32_t)b.w};
         int bacc = 0;
@@ -282,12 +288,23 @@ __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, 
         isum = acc - 32 * bacc;
         msum = 0;
     } else {
-        const int2 b = __ldg(reinterpret_cast<const int2 *>(bs + 4 * c));  // bs[4c .. 4c+3]
+        int2 b;
+        if constexpr (SMEM) b = *reinterpret_cast<const int2 *>(bs + 4 * c);  // bs[4c .. 4c+3]
+        else b = __ldg(reinterpret_cast<const int2 *>(bs + 4 * c));
         const int b0 = static_cast<int16_t>(b.x & 0xFFFF), b1 = static_cast<int16_t>(b.x >> 16);
         const int b2 = static_cast<int16_t>(b.y & 0xFFFF), b3 = static_cast<int16_t>(b.y >> 16);
         isum = acc;
         msum = L.m0 * (b0 + b1) + L.m1 * (b2 + b3);
     }
+}
+
+// Programmatic dependent launch.  griddep_wait() blocks until the grids this
+// one depends on have completed and their memory is visible (a no-op when
+// the kernel was launched without the programmatic attribute);
+// griddep_launch_dependents() lets the next kernel in the stream start.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ int quad_sum(int v) {

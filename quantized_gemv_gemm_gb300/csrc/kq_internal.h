@@ -10,6 +10,10 @@
 
 namespace kq {
 
+// Library-wide launch options (kq_set_launch_flags).
+constexpr unsigned LAUNCH_PDL = 1u;
+unsigned launch_flags();
+
 struct Q8K {
     const float *d;
     const int8_t *qs;

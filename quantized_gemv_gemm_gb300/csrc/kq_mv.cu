@@ -116,6 +116,92 @@ __global__ void __launch_bounds__(256) mv_kernel(const MvParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------
+// Decode GEMV (M = 1).  Same lane geometry and fold as mv_kernel, plus:
+//  - a D-deep ring of weight registers per lane: loads for the next D
+//    superblocks are in flight while the current one is folded;
+//  - the weight prefetch of the first D superblocks is issued before
+//    griddep_wait(), so with programmatic dependent launch it overlaps the
+//    tail of the previous kernel (weights are never written by the path);
+//  - the Q8_K row (quants, bsums, scales) is staged once per block in shared
+//    memory, where the eight quads of a warp read the same superblock.
+template <int F> constexpr int gemv_depth() { return F == FMT_Q4_K ? 4 : 3; }
+constexpr int64_t GEMV_SMEM_MAX_K = 40960;  // keeps the staged row under 48 KB
+
+__host__ __device__ inline size_t gemv_smem_bytes(int64_t K) { return (size_t)(K + K / 8 + K / 64); }
+
+template <int F, int D>
+__global__ void __launch_bounds__(256, 2) gemv_kernel(const MvParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float red[8][8];
+    const int64_t K = p.K;
+    int8_t *s_qs = reinterpret_cast<int8_t *>(smem);
+    int16_t *s_bs = reinterpret_cast<int16_t *>(smem + K);
+    float *s_d8 = reinterpret_cast<float *>(smem + K + K / 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wk = p.wk;
+    const int kw = warp % wk, rg = warp / wk;
+    const int rows_per_block = 8 * (8 / wk);
+    const int r8 = lane >> 2, c = lane & 3;
+    const int64_t n = (int64_t)blockIdx.x * rows_per_block + rg * 8 + r8;
+    const int64_t nc = n < p.N ? n : p.N - 1;
+    const Planes P = make_planes(F, p.packed, p.N, p.nsb);
+    const int64_t s_begin = kw * p.nsb / wk, s_end = (kw + 1) * p.nsb / wk;
+    const uint64_t row_u = (uint64_t)nc * p.nsb;
+
+    using W = typename WRegs<F>::T;
+    W buf[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i)
+        if (s_begin + i < s_end) load_w(buf[i], P, row_u + s_begin + i, c);
+
+    griddep_wait();
+    {
+        const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs);
+        const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs);
+        for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(s_qs)[i] = gq[i];
+        for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(s_bs)[i] = gb[i];
+        for (int64_t i = threadIdx.x; i < K / 256; i += 256) s_d8[i] = p.d8[i];
+    }
+    __syncthreads();
+    griddep_launch_dependents();
+
+    float acc = 0.0f;
+    for (int64_t base = s_begin; base < s_end; base += D) {
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            const int64_t sb = base + i;
+            if (sb < s_end) {
+                LaneQ L;
+                decode_lane(buf[i], c, L);
+                if (sb + D < s_end) load_w(buf[i], P, row_u + sb + D, c);
+                int isum, msum;
+                lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
+                isum = quad_sum(isum);
+                const float d8 = s_d8[sb];
+                acc = fmaf(L.d * d8, static_cast<float>(isum), acc);
+                if constexpr (F != FMT_Q6_K) {
+                    msum = quad_sum(msum);
+                    acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
+                }
+            }
+        }
+    }
+
+    if (wk == 1) {
+        if (c == 0 && n < p.N) p.y[n] = acc;
+    } else {
+        if (c == 0) red[warp][r8] = acc;
+        __syncthreads();
+        if (kw == 0 && c == 0 && n < p.N) {
+            float v = red[warp][r8];
+            for (int k = 1; k < wk; ++k) v += red[warp + k][r8];
+            p.y[n] = v;
+        }
+    }
+}
+
 static int pick_wk(int64_t N, int64_t nsb, int64_t token_groups) {
     // enough warps in flight for HBM (about 13 per SM on 152 SMs), without
     // slicing a row finer than one superblock per warp
@@ -140,8 +226,29 @@ static cudaError_t launch_mv_s(const MvParams &p0, int64_t E, int64_t tg, cudaSt
 }
 
 template <int F>
+static cudaError_t launch_gemv(const MvParams &p0, cudaStream_t s) {
+    MvParams p = p0;
+    p.wk = pick_wk(p.N, p.nsb, 1);
+    const int rows_per_block = 8 * (8 / p.wk);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.N + rows_per_block - 1) / rows_per_block));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = gemv_smem_bytes(p.K);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, gemv_depth<F>()>, p);
+}
+
+template <int F>
 static cudaError_t launch_mv_f(const MvParams &p, int64_t E, cudaStream_t s) {
-    if (!p.offsets && p.M == 1) return launch_mv_s<F, 1>(p, 1, 1, s);
+    if (!p.offsets && p.M == 1) {
+        if (p.K <= GEMV_SMEM_MAX_K) return launch_gemv<F>(p, s);
+        return launch_mv_s<F, 1>(p, 1, 1, s);
+    }
     // token groups of 8; enough groups in parallel to fill the GPU, each
     // block walking further groups with the same weights hot in L1/L2
     const int64_t per_expert = p.offsets ? (p.M + E - 1) / E : p.M;

@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restri
                                                            int16_t *__restrict__ bsums) {
     const int lane = threadIdx.x & 31;
     const int64_t blk = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    // x may be produced, and the Q8_K planes still read, by the previous
+    // kernels in the stream
+    griddep_wait();
+    griddep_launch_dependents();
     if (blk >= nblocks) return;
     const int64_t nsb = K / QK;
     const int64_t m = blk / nsb, sb = blk % nsb;
@@ -63,8 +67,16 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8
     const int64_t nblocks = M * (K / QK);
     if (nblocks == 0) return cudaSuccess;
     const int64_t grid = (nblocks + 7) / 8;
-    quantize_q8k_kernel<<<(unsigned)grid, 256, 0, s>>>(x, K, nblocks, d, qs, bsums);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, quantize_q8k_kernel, x, K, nblocks, d, qs, bsums);
 }
 
 // ---------------------------------------------------------------------------

@@ -48,6 +48,10 @@ _lib.kq_gemm_grouped.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64
 _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
+_lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
+_lib.kq_set_launch_flags.restype = ctypes.c_uint
+_lib.kq_get_launch_flags.argtypes = []
+_lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemm", "kq_gemm_grouped",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
     getattr(_lib, _f).restype = _INT
@@ -215,6 +219,18 @@ def kq_debug_decode(fmt: int, packed: torch.Tensor, N: int, K: int, stream=None)
 
 def kq_device_status(stream=None) -> int:
     return int(_lib.kq_device_status(_stream(stream)))
+
+
+KQ_LAUNCH_PDL = 1
+
+
+def kq_set_launch_flags(flags: int) -> int:
+    """Set the process-wide launch flags (KQ_LAUNCH_PDL); returns the old ones."""
+    return int(_lib.kq_set_launch_flags(int(flags)))
+
+
+def kq_get_launch_flags() -> int:
+    return int(_lib.kq_get_launch_flags())
 
 
 def raw():

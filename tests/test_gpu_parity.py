@@ -296,3 +296,39 @@ def test_grouped_moe_30b_a3b(K):
             e = int(row_expert[r])
             one = tuple(p[r:r + 1] for p in planes)
             assert_row_tol(y[r:r + 1], oracle.gemm(m.fmt, disks[e], *one))
+
+
+# ---------------------------------------------------------------- PDL chains
+def test_pdl_chain_matches_plain_launches(K):
+    """With programmatic dependent launch on, a chain of producer kernel ->
+    quantize -> GEMV -> consumer gives the same bits as plain launches: each
+    kernel waits for the previous ones before touching their data."""
+    fmt, N, Kdim = synth.Q4_K, 4096, 2560
+    rng = synth.rng_for(108, 0)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    packed = pack(K, fmt, disk)
+    x0 = to_dev(synth.activations(1, Kdim, rng))
+    torch.cuda.synchronize()
+
+    def chain():
+        outs = []
+        a = K.q8k_empty(1, Kdim)
+        for i in range(6):
+            x = x0 * (1.0 + 0.25 * i)          # produced by the kernel right before
+            K.kq_quantize_q8k(x, out=a)
+            y = K.kq_gemv(fmt, packed, N, Kdim, a)
+            outs.append(y * 2.0)               # consumed right after
+        torch.cuda.synchronize()
+        return torch.stack(outs).cpu().numpy()
+
+    old = K.kq_set_launch_flags(0)
+    try:
+        plain = chain()
+        K.kq_set_launch_flags(K.KQ_LAUNCH_PDL)
+        assert K.kq_get_launch_flags() == K.KQ_LAUNCH_PDL
+        pdl = chain()
+    finally:
+        K.kq_set_launch_flags(old)
+    np.testing.assert_array_equal(pdl, plain)
+    planes = oracle_q8k((x0 * 2.25).cpu().numpy())
+    assert_row_tol(pdl[5] / 2.0, oracle.gemm(fmt, disk, *planes)[0])
