@@ -150,29 +150,44 @@ class DecodeLayers:
         self.weight_bytes = sum(m.weight_bytes for m in self.mats)
         self.x_total = sum(k for _, k in LAYER_INPUTS)
 
-    def step(self, l, events=None, x_override=None):
+    # fused path: one launch per group of matrices sharing an input
+    GROUPS = [["wq", "wk", "wv"], ["wo"], ["gate", "up"], ["down"]]
+
+    def step(self, l, events=None, x_override=None, fused=True):
+        """One layer: fused -> 4 launches of kq_gemv_fused (q/k/v, o, gate/up,
+        down); separate -> 4 kq_quantize_q8k + 7 kq_gemv launches."""
         kq = self.kq
         c = self.copies[l]
         xs = c["x"] if x_override is None else x_override
-        for j in range(len(LAYER_INPUTS)):
-            kq.kq_quantize_q8k(xs[j], out=self.q8[j])
-            for i, m in enumerate(self.mats):
-                if LAYER_USES[m.name] != j:
-                    continue
+        idx = {m.name: i for i, m in enumerate(self.mats)}
+        for j, names in enumerate(self.GROUPS):
+            ii = [idx[n] for n in names]
+            m0 = self.mats[ii[0]]
+            if fused:
                 if events is not None:
-                    events[i][0].record()
-                kq.kq_gemv(m.fmt, c["packed"][i], m.N, m.K, self.q8[j], y=self.y_views[i])
+                    events[j][0].record()
+                kq.kq_gemv_fused(m0.fmt, [c["packed"][i] for i in ii], [self.mats[i].N for i in ii], m0.K,
+                                 xs[j], [self.y_views[i] for i in ii])
                 if events is not None:
-                    events[i][1].record()
+                    events[j][1].record()
+            else:
+                kq.kq_quantize_q8k(xs[j], out=self.q8[j])
+                for i in ii:
+                    kq.kq_gemv(self.mats[i].fmt, c["packed"][i], self.mats[i].N, self.mats[i].K, self.q8[j],
+                               y=self.y_views[i])
 
-    @property
-    def launches_per_step(self):
-        return len(LAYER_INPUTS) + len(self.mats)
+    def launches_per_step(self, fused=True):
+        return len(self.GROUPS) if fused else len(LAYER_INPUTS) + len(self.mats)
 
-    def algorithmic_gemv_bytes(self):
-        """Per launch: packed weight bytes + Q8_K activation bytes (292 B per
-        256) + 4 B per output."""
-        return [m.weight_bytes + (m.K // 256) * 292 + 4 * m.N for m in self.mats]
+    def algorithmic_launch_bytes(self):
+        """Per fused launch: packed weight bytes of its matrices + the fp32
+        input row (4 B per element, read once) + 4 B per output."""
+        idx = {m.name: i for i, m in enumerate(self.mats)}
+        out = []
+        for j, names in enumerate(self.GROUPS):
+            ms = [self.mats[idx[n]] for n in names]
+            out.append(sum(m.weight_bytes + 4 * m.N for m in ms) + 4 * ms[0].K)
+        return out
 
 
 def graph_of(torch, fn):
@@ -205,49 +220,55 @@ def run_ours(args, world, rank, local):
         kq.kq_set_launch_flags(kq.KQ_LAUNCH_PDL)
     L = args.layers
     layers = DecodeLayers(kq, torch, L)
-    rot = lambda: [layers.step(l) for l in range(L)]  # noqa: E731
-    g_plain = graph_of(torch, rot)
+    NG = len(layers.GROUPS)
+    g_plain = graph_of(torch, lambda: [layers.step(l) for l in range(L)])
+    g_sep = graph_of(torch, lambda: [layers.step(l, fused=False) for l in range(L)])
 
-    # events around every GEMV of every step of one rotation
+    # events around every launch of every step of one rotation
     def timing_event():
         try:
             return torch.cuda.Event(enable_timing=True, external=True)
         except TypeError:  # torch without graph event-record nodes
             return None
 
-    ev = [[[timing_event(), timing_event()] for _ in layers.mats] for _ in range(L)]
+    ev = [[[timing_event(), timing_event()] for _ in range(NG)] for _ in range(L)]
     graph_events = ev[0][0][0] is not None
     if graph_events:
         g_timed = graph_of(torch, lambda: [layers.step(l, events=ev[l]) for l in range(L)])
     else:
         ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-               for _ in layers.mats] for _ in range(L)]
+               for _ in range(NG)] for _ in range(L)]
 
     reps = max(1, args.steps // L)
     steps = reps * L
     warm_reps = max(1, -(-args.warmup // L))
     for _ in range(warm_reps):
         g_plain.replay()
+        g_sep.replay()
     torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    def timed(graph, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(n):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        barrier()
+        return a.elapsed_time(b)
+
     with ClockSampler(local) as clk:
-        barrier()
-        torch.cuda.synchronize()
-        t0.record()
-        for _ in range(reps):
-            g_plain.replay()
-        t1.record()
-        torch.cuda.synchronize()
-        barrier()
-        ms = t0.elapsed_time(t1)
-        # kernel-timing pass: same graphs with event nodes; per-launch times of
-        # the last rotation are read after each of a few replays
-        kt = {i: [] for i in range(len(layers.mats))}
+        ms = timed(g_plain, reps)
+        ms_sep = timed(g_sep, max(1, reps // 2))
+        # kernel-timing pass: event nodes around each launch; the times of the
+        # last rotation are read after each of a few replays
+        kt = {j: [] for j in range(NG)}
         for _ in range(max(3, min(50, reps // 4))):
             if graph_events:
                 g_timed.replay()
@@ -256,26 +277,32 @@ def run_ours(args, world, rank, local):
                     layers.step(l, events=ev[l])
             torch.cuda.synchronize()
             for l in range(L):
-                for i in range(len(layers.mats)):
-                    kt[i].append(ev[l][i][0].elapsed_time(ev[l][i][1]))
+                for j in range(NG):
+                    kt[j].append(ev[l][j][0].elapsed_time(ev[l][j][1]))
     clocks = clk.summary()
 
-    ms_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        tt = torch.tensor([v], device="cuda")
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
+        return float(tt.item())
+
+    ms_max = max_over_ranks(ms)
+    ms_sep = max_over_ranks(ms_sep)
     bytes_per_step = layers.weight_bytes
     value = bytes_per_step * steps * world / (ms_max * 1e-3) / 1e9
+    value_sep = bytes_per_step * max(1, reps // 2) * L * world / (ms_sep * 1e-3) / 1e9
 
-    # roofline of the GEMV kernels (all seven launches of a step)
-    alg = layers.algorithmic_gemv_bytes()
-    mean_ms = [float(np.mean(kt[i])) for i in range(len(layers.mats))]
+    # roofline of the GEMV kernel over its launches (algorithmic bytes summed
+    # over the 4 launches of a step / their summed mean durations)
+    alg = layers.algorithmic_launch_bytes()
+    mean_ms = [float(np.mean(kt[j])) for j in range(NG)]
     achieved = sum(alg) / (sum(mean_ms) * 1e-3) / 1e9
     hbm = float(peaks["hbm_gbs"])
-    per_matrix = [{"name": m.name, "fmt": synth.FORMAT_NAMES[m.fmt], "N": m.N, "K": m.K,
-                   "us": round(t * 1e3, 3), "gbs": round(b / (t * 1e-3) / 1e9, 1)}
-                  for m, t, b in zip(layers.mats, mean_ms, alg)]
+    per_launch = [{"matrices": "+".join(names), "us": round(t * 1e3, 3), "bytes": b,
+                   "gbs": round(b / (t * 1e-3) / 1e9, 1)}
+                  for names, t, b in zip(layers.GROUPS, mean_ms, alg)]
 
     # end to end through the public API: H2D of the step's activations from
     # pinned host memory, the step, D2H of all outputs, replayed from a graph
@@ -334,16 +361,18 @@ def run_ours(args, world, rank, local):
                        "timing": "CUDA events around graph replays of K steps",
                        "pdl": not args.no_pdl,
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "hbm", "kernel": "kq mv_kernel (GEMV, 7 launches per step)",
+            "roofline": {"bound": "hbm", "kernel": "kq gemv_kernel (fused quantize + GEMV, 4 launches per step)",
                          "timing": "event nodes in graph replays" if graph_events else "eager launches with events",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peaks["source"],
-                         "traffic": None, "per_matrix": per_matrix},
+                         "traffic": None, "per_launch": per_launch},
+            "separate_path": {"value": round(value_sep, 2), "unit": "GB/s",
+                              "how": "4 kq_quantize_q8k + 7 kq_gemv launches per step"},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": 4 * layers.x_total, "d2h_bytes_per_step": 4 * layers.y_total,
-                    "how": "graph replay of: H2D of the 4 fp32 inputs from pinned memory, 4 quantize + 7 GEMV "
+                    "how": "graph replay of: H2D of the 4 fp32 inputs from pinned memory, 4 kq_gemv_fused "
                            "launches, D2H of all 7 outputs"},
-            "gpu_launches": layers.launches_per_step * steps,
+            "gpu_launches": layers.launches_per_step() * steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
             "gemm": gemm,

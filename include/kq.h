@@ -132,6 +132,28 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
             float *y, cudaStream_t s);
 
 /*
+ * Fused decode GEMV: quantize + GEMV in one launch, over up to four matrices
+ * that share one input row (q/k/v projections, gate/up).  The fp32 row x is
+ * quantized to Q8_K inside the kernel, bit-identically to kq_quantize_q8k,
+ * and y_m = W_m x for each matrix m, as kq_gemv computes it.  This is the
+ * kernel-level form of the page's "chain regrain" (kq-arc, "The pieces":
+ * the decode chains quantize the activation image where it is consumed, in
+ * whole superblocks).
+ *   n_mats  1..4
+ *   packed  host array of n_mats device pointers to packed images of format
+ *           f (256-byte aligned); N host array of their row counts (>= 0;
+ *           a matrix with N = 0 is skipped)
+ *   K       shared inner dimension: a multiple of 256, at most 40960
+ *   x       device float32 [K], 16-byte aligned, finite values
+ *   y       host array of n_mats device pointers, y[m] float32 [N[m]]
+ * The host arrays are read during the call only.
+ * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (n_mats out of range, null, K), KQ_ERR_ALIGN,
+ * KQ_ERR_LAUNCH.
+ */
+int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K,
+                  const float *x, float *const *y, cudaStream_t s);
+
+/*
  * Size of the device workspace kq_gemm / kq_gemm_grouped need for M token
  * rows of K (an fp16 image of the activation quants and bsums, plus tile
  * bookkeeping).  0 means no workspace is needed for this shape.

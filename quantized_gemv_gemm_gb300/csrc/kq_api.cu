@@ -88,7 +88,35 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
     if (!packed || !y) return KQ_ERR_ARG;
     if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
     if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
-    return launch_status(launch_mv(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, 1, nullptr, 1, 0, y, s));
+    const Q8K q{a.d, a.qs, a.bsums};
+    if (K <= GEMV_MAX_K) return launch_status(launch_gemv(f, 1, &packed, &N, K, nullptr, q, &y, s));
+    return launch_status(launch_mv(f, packed, N, K, q, 1, nullptr, 1, 0, y, s));
+}
+
+int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K, const float *x,
+                  float *const *y, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (n_mats < 1 || n_mats > GEMV_MAX_MATRICES || !packed || !N || !y) return KQ_ERR_ARG;
+    if (K <= 0 || K % QK != 0 || K > GEMV_MAX_K) return KQ_ERR_ARG;
+    int64_t total = 0;
+    for (int m = 0; m < n_mats; ++m) {
+        if (N[m] < 0) return KQ_ERR_ARG;
+        total += N[m];
+        if (N[m] == 0) continue;
+        if (!packed[m] || !y[m]) return KQ_ERR_ARG;
+        if (!aligned(packed[m], 256) || !aligned(y[m], 4)) return KQ_ERR_ALIGN;
+    }
+    if (total == 0) return KQ_OK;
+    if (!x) return KQ_ERR_ARG;
+    if (!aligned(x, 16)) return KQ_ERR_ALIGN;
+    // matrices with N = 0 are dropped
+    const void *pk[GEMV_MAX_MATRICES];
+    int64_t nn[GEMV_MAX_MATRICES];
+    float *yy[GEMV_MAX_MATRICES];
+    int k = 0;
+    for (int m = 0; m < n_mats; ++m)
+        if (N[m] > 0) { pk[k] = packed[m]; nn[k] = N[m]; yy[k] = y[m]; ++k; }
+    return launch_status(launch_gemv(f, k, pk, nn, K, x, Q8K{nullptr, nullptr, nullptr}, yy, s));
 }
 
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {

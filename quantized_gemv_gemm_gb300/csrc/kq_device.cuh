@@ -298,6 +298,48 @@ __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, 
     }
 }
 
+// Q8_K quantization of one 256-block by one warp (kq-arc, k4 kq-v2 commit:
+// quantize_q8_k_into, "ONE fp32 scale per 256-superblock + per-16 bsums").
+// Lane l owns elements 8l .. 8l+7.  amax = max|x| (a max over the bit
+// patterns of |x|, which order like the values for finite floats);
+// iscale = 127/amax and q = round_half_even(x*iscale), clamped to +-127,
+// both single IEEE fp32 operations; d8 = amax/127 (0 when amax = 0, with
+// every q = 0); bsum i = sum of q over 16i .. 16i+15 (lanes 2i and 2i+1).
+// xb: the block's 256 floats (16-byte aligned); qb / bb / db: its 256
+// quants, 16 bsums and scale, in global or shared memory.
+__device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, int8_t *qb, int16_t *bb, float *db) {
+    const float4 v0 = *reinterpret_cast<const float4 *>(xb + 8 * lane);
+    const float4 v1 = *reinterpret_cast<const float4 *>(xb + 8 * lane + 4);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float ax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ax = fmaxf(ax, fabsf(v[i]));
+    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(ax)));
+    int q[8];
+    if (amax == 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = 0;
+    } else {
+        const float iscale = __fdiv_rn(127.0f, amax);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int t = __float2int_rn(__fmul_rn(v[i], iscale));
+            q[i] = max(-127, min(127, t));
+        }
+    }
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        lo |= (static_cast<uint32_t>(q[i]) & 0xFFu) << (8 * i);
+        hi |= (static_cast<uint32_t>(q[i + 4]) & 0xFFu) << (8 * i);
+    }
+    *reinterpret_cast<uint2 *>(qb + 8 * lane) = make_uint2(lo, hi);
+    int part = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
+    if ((lane & 1) == 0) bb[lane >> 1] = static_cast<int16_t>(part);
+    if (lane == 0) *db = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+}
+
 // Programmatic dependent launch.  griddep_wait() blocks until the grids this
 // one depends on have completed and their memory is visible (a no-op when
 // the kernel was launched without the programmatic attribute);

@@ -35,6 +35,13 @@ cudaError_t launch_mv(int f, const void *packed, int64_t N, int64_t K, Q8K a, in
                       const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
                       cudaStream_t s);
 
+// Decode GEMV over nmat (<= 4) matrices sharing one input row: either the
+// fp32 row x (quantized inside the kernel) or, when x is null, Q8_K planes a.
+constexpr int GEMV_MAX_MATRICES = 4;
+constexpr int64_t GEMV_MAX_K = 40960;
+cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
+                        Q8K a, float *const *y, cudaStream_t s);
+
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);
 

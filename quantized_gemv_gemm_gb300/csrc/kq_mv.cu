@@ -17,6 +17,8 @@
 // superblock").  Slices of one row are summed through shared memory.
 #include "kq_internal.h"
 
+#include <algorithm>
+
 namespace kq {
 
 struct MvParams {
@@ -117,65 +119,119 @@ __global__ void __launch_bounds__(256) mv_kernel(const MvParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Decode GEMV (M = 1).  Same lane geometry and fold as mv_kernel, plus:
-//  - a D-deep ring of weight registers per lane: loads for the next D
-//    superblocks are in flight while the current one is folded;
-//  - the weight prefetch of the first D superblocks is issued before
-//    griddep_wait(), so with programmatic dependent launch it overlaps the
-//    tail of the previous kernel (weights are never written by the path);
-//  - the Q8_K row (quants, bsums, scales) is staged once per block in shared
-//    memory, where the eight quads of a warp read the same superblock.
+// Decode GEMV (M = 1), over up to four matrices of one format that share one
+// input row, optionally quantizing that row itself (fp32 in).
+//
+// Grid: at most one 256-thread block per SM (persistent).  Work is a list of
+// row groups of 8 rows (one per quad) across the matrices; warp w of the grid
+// owns row groups w, w + W, w + 2W, ... (W warps in the grid) and walks the
+// flattened sequence (row group, superblock) of all of them with a D-deep
+// ring of weight registers: the loads of item i + D are issued as soon as
+// item i is decoded, across row-group boundaries, so a warp keeps D
+// superblocks in flight from its first load to its last.
+// Ordering: the first D items are loaded before griddep_wait() (weights are
+// read-only on this path), so under programmatic dependent launch they
+// overlap the previous kernel; the block then stages the Q8_K row in shared
+// memory (copying it, or quantizing the fp32 row with quantize_block_warp,
+// bit-identical to kq_quantize_q8k) and lets the next kernel launch.  One
+// block per SM leaves room for a block of the next kernel to start early.
+
+struct GemvParams {
+    int nmat;
+    const uint8_t *packed[GEMV_MAX_MATRICES];
+    int64_t N[GEMV_MAX_MATRICES];
+    float *y[GEMV_MAX_MATRICES];
+    int64_t gpre[GEMV_MAX_MATRICES + 1];  // prefix sums of row groups
+    int64_t K, nsb;
+    const float *x;                    // fp32 row (fused quantize), or nullptr
+    const float *d8;                   // else: the Q8_K planes of the row
+    const int8_t *qs;
+    const int16_t *bs;
+};
+
 template <int F> constexpr int gemv_depth() { return F == FMT_Q4_K ? 4 : 3; }
-constexpr int64_t GEMV_SMEM_MAX_K = 40960;  // keeps the staged row under 48 KB
 
 __host__ __device__ inline size_t gemv_smem_bytes(int64_t K) { return (size_t)(K + K / 8 + K / 64); }
 
+struct GemvItem {
+    int64_t g;   // row group
+    int64_t sb;  // superblock
+};
+
 template <int F, int D>
-__global__ void __launch_bounds__(256, 2) gemv_kernel(const MvParams p) {
+__global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
-    __shared__ float red[8][8];
-    const int64_t K = p.K;
+    __shared__ Planes s_planes[GEMV_MAX_MATRICES];
+    const int64_t K = p.K, nsb = p.nsb;
     int8_t *s_qs = reinterpret_cast<int8_t *>(smem);
     int16_t *s_bs = reinterpret_cast<int16_t *>(smem + K);
     float *s_d8 = reinterpret_cast<float *>(smem + K + K / 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wk = p.wk;
-    const int kw = warp % wk, rg = warp / wk;
-    const int rows_per_block = 8 * (8 / wk);
     const int r8 = lane >> 2, c = lane & 3;
-    const int64_t n = (int64_t)blockIdx.x * rows_per_block + rg * 8 + r8;
-    const int64_t nc = n < p.N ? n : p.N - 1;
-    const Planes P = make_planes(F, p.packed, p.N, p.nsb);
-    const int64_t s_begin = kw * p.nsb / wk, s_end = (kw + 1) * p.nsb / wk;
-    const uint64_t row_u = (uint64_t)nc * p.nsb;
+    if (threadIdx.x < p.nmat) s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
+    __syncthreads();
+
+    const int64_t TW = (int64_t)gridDim.x * 8;
+    const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
+    const int64_t G = p.gpre[p.nmat];
+    const int64_t ngroups = G > gw ? (G - gw + TW - 1) / TW : 0;
+    const int64_t n_items = ngroups * nsb;
+
+    // matrix / row / packed superblock index of an item
+    auto locate = [&](const GemvItem &it, int &m, int64_t &n, uint64_t &u) {
+        m = 0;
+        while (m + 1 < p.nmat && it.g >= p.gpre[m + 1]) ++m;
+        n = (it.g - p.gpre[m]) * 8 + r8;
+        const int64_t nc = n < p.N[m] ? n : p.N[m] - 1;
+        u = (uint64_t)nc * nsb + it.sb;
+    };
+    auto advance = [&](GemvItem &it) {
+        if (++it.sb == nsb) { it.sb = 0; it.g += TW; }
+    };
 
     using W = typename WRegs<F>::T;
     W buf[D];
+    GemvItem pre{gw, 0};  // next item to prefetch
 #pragma unroll
-    for (int i = 0; i < D; ++i)
-        if (s_begin + i < s_end) load_w(buf[i], P, row_u + s_begin + i, c);
+    for (int i = 0; i < D; ++i) {
+        if (i < n_items) {
+            int m; int64_t n; uint64_t u;
+            locate(pre, m, n, u);
+            load_w(buf[i], s_planes[m], u, c);
+            advance(pre);
+        }
+    }
 
     griddep_wait();
-    {
+    if (p.x) {
+        for (int64_t b = warp; b < nsb; b += 8)
+            quantize_block_warp(p.x + b * QK, lane, s_qs + b * QK, s_bs + b * 16, s_d8 + b);
+    } else {
         const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs);
         const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs);
         for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(s_qs)[i] = gq[i];
         for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(s_bs)[i] = gb[i];
-        for (int64_t i = threadIdx.x; i < K / 256; i += 256) s_d8[i] = p.d8[i];
+        for (int64_t i = threadIdx.x; i < nsb; i += 256) s_d8[i] = p.d8[i];
     }
     __syncthreads();
     griddep_launch_dependents();
 
+    GemvItem cur{gw, 0};
     float acc = 0.0f;
-    for (int64_t base = s_begin; base < s_end; base += D) {
+    for (int64_t base = 0; base < n_items; base += D) {
 #pragma unroll
         for (int i = 0; i < D; ++i) {
-            const int64_t sb = base + i;
-            if (sb < s_end) {
+            if (base + i < n_items) {
                 LaneQ L;
                 decode_lane(buf[i], c, L);
-                if (sb + D < s_end) load_w(buf[i], P, row_u + sb + D, c);
+                if (base + i + D < n_items) {
+                    int m; int64_t n; uint64_t u;
+                    locate(pre, m, n, u);
+                    load_w(buf[i], s_planes[m], u, c);
+                    advance(pre);
+                }
+                const int64_t sb = cur.sb;
                 int isum, msum;
                 lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
                 isum = quad_sum(isum);
@@ -185,21 +241,68 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const MvParams p) {
                     msum = quad_sum(msum);
                     acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
                 }
+                if (sb == nsb - 1) {
+                    int m; int64_t n; uint64_t u;
+                    locate(cur, m, n, u);
+                    if (c == 0 && n < p.N[m]) p.y[m][n] = acc;
+                    acc = 0.0f;
+                }
+                advance(cur);
             }
         }
     }
+}
 
-    if (wk == 1) {
-        if (c == 0 && n < p.N) p.y[n] = acc;
-    } else {
-        if (c == 0) red[warp][r8] = acc;
-        __syncthreads();
-        if (kw == 0 && c == 0 && n < p.N) {
-            float v = red[warp][r8];
-            for (int k = 1; k < wk; ++k) v += red[warp + k][r8];
-            p.y[n] = v;
-        }
+static int sm_count() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (!cached[dev]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+        cached[dev] = v;
     }
+    return cached[dev];
+}
+
+template <int F>
+static cudaError_t launch_gemv_t(GemvParams p, cudaStream_t s) {
+    p.gpre[0] = 0;
+    for (int m = 0; m < p.nmat; ++m) p.gpre[m + 1] = p.gpre[m] + (p.N[m] + 7) / 8;
+    const int64_t G = p.gpre[p.nmat];
+    if (G == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((G + 7) / 8, sm_count());
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = gemv_smem_bytes(p.K);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, gemv_depth<F>()>, p);
+}
+
+cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
+                        Q8K a, float *const *y, cudaStream_t s) {
+    GemvParams p{};
+    p.nmat = nmat;
+    for (int m = 0; m < nmat; ++m) {
+        p.packed[m] = static_cast<const uint8_t *>(packed[m]);
+        p.N[m] = N[m];
+        p.y[m] = y[m];
+    }
+    p.K = K;
+    p.nsb = K / QK;
+    p.x = x;
+    p.d8 = a.d;
+    p.qs = a.qs;
+    p.bs = a.bsums;
+    if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K>(p, s);
+    if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K>(p, s);
+    return launch_gemv_t<FMT_Q6_K>(p, s);
 }
 
 static int pick_wk(int64_t N, int64_t nsb, int64_t token_groups) {
@@ -226,29 +329,8 @@ static cudaError_t launch_mv_s(const MvParams &p0, int64_t E, int64_t tg, cudaSt
 }
 
 template <int F>
-static cudaError_t launch_gemv(const MvParams &p0, cudaStream_t s) {
-    MvParams p = p0;
-    p.wk = pick_wk(p.N, p.nsb, 1);
-    const int rows_per_block = 8 * (8 / p.wk);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.N + rows_per_block - 1) / rows_per_block));
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = gemv_smem_bytes(p.K);
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, gemv_depth<F>()>, p);
-}
-
-template <int F>
 static cudaError_t launch_mv_f(const MvParams &p, int64_t E, cudaStream_t s) {
-    if (!p.offsets && p.M == 1) {
-        if (p.K <= GEMV_SMEM_MAX_K) return launch_gemv<F>(p, s);
-        return launch_mv_s<F, 1>(p, 1, 1, s);
-    }
+    if (!p.offsets && p.M == 1) return launch_mv_s<F, 1>(p, 1, 1, s);
     // token groups of 8; enough groups in parallel to fill the GPU, each
     // block walking further groups with the same weights hot in L1/L2
     const int64_t per_expert = p.offsets ? (p.M + E - 1) / E : p.M;

@@ -7,13 +7,8 @@
 namespace kq {
 
 // ---------------------------------------------------------------------------
-// Q8_K quantization (kq-arc, k4 kq-v2 commit: quantize_q8_k_into, "ONE fp32
-// scale per 256-superblock + per-16 bsums").  One warp per 256-block; lane l
-// owns elements 8l .. 8l+7.  Per block: amax = max|x| (a max over the bit
-// patterns of |x|, which order like the values for finite floats);
-// iscale = 127/amax and q = round_half_even(x*iscale), clamped to +-127,
-// both single IEEE fp32 operations; d8 = amax/127; bsum i = sum of q over
-// 16i .. 16i+15 (lanes 2i and 2i+1).
+// Q8_K quantization of M rows: one warp per 256-block (quantize_block_warp
+// in kq_device.cuh holds the arithmetic).
 __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restrict__ x, int64_t K,
                                                            int64_t nblocks, float *__restrict__ d,
                                                            int8_t *__restrict__ qs,
@@ -27,39 +22,7 @@ __global__ void __launch_bounds__(256) quantize_q8k_kernel(const float *__restri
     if (blk >= nblocks) return;
     const int64_t nsb = K / QK;
     const int64_t m = blk / nsb, sb = blk % nsb;
-    const float *xb = x + m * K + sb * QK + 8 * lane;
-    const float4 v0 = __ldg(reinterpret_cast<const float4 *>(xb));
-    const float4 v1 = __ldg(reinterpret_cast<const float4 *>(xb + 4));
-    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float ax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) ax = fmaxf(ax, fabsf(v[i]));
-    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(ax)));
-
-    int q[8];
-    if (amax == 0.0f) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = 0;
-    } else {
-        const float iscale = __fdiv_rn(127.0f, amax);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int t = __float2int_rn(__fmul_rn(v[i], iscale));
-            q[i] = max(-127, min(127, t));
-        }
-    }
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        lo |= (static_cast<uint32_t>(q[i]) & 0xFFu) << (8 * i);
-        hi |= (static_cast<uint32_t>(q[i + 4]) & 0xFFu) << (8 * i);
-    }
-    *reinterpret_cast<uint2 *>(qs + m * K + sb * QK + 8 * lane) = make_uint2(lo, hi);
-
-    int part = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
-    if ((lane & 1) == 0) bsums[blk * 16 + (lane >> 1)] = static_cast<int16_t>(part);
-    if (lane == 0) d[blk] = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+    quantize_block_warp(x + m * K + sb * QK, lane, qs + m * K + sb * QK, bsums + blk * 16, d + blk);
 }
 
 cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8_t *qs,

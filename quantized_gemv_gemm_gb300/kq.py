@@ -41,6 +41,7 @@ _lib.kq_repack_bytes.argtypes = [_INT, _I64, _I64]
 _lib.kq_repack_bytes.restype = _SZ
 _lib.kq_repack.argtypes = [_INT, _P, _I64, _I64, _P, _P]
 _lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P]
+_lib.kq_gemv_fused.argtypes = [_INT, _INT, _P, _P, _I64, _P, _P, _P]
 _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
@@ -52,7 +53,7 @@ _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
-for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemm", "kq_gemm_grouped",
+for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemm", "kq_gemm_grouped",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
     getattr(_lib, _f).restype = _INT
 
@@ -151,6 +152,22 @@ def kq_gemv(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, y: Optional[
     _need_cuda(y)
     _check(_lib.kq_gemv(int(fmt), _ptr(packed), N, K, _q8k_struct(a), _ptr(y), _stream(stream)), "kq_gemv")
     return y
+
+
+def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list=None, stream=None):
+    """Quantize the fp32 row x and multiply it by up to 4 matrices in one launch."""
+    n = len(packed_list)
+    _need_cuda(x, *packed_list)
+    if x.dtype != torch.float32:
+        raise ValueError("x must be float32")
+    if y_list is None:
+        y_list = [torch.empty(int(N), dtype=torch.float32, device=x.device) for N in N_list]
+    _need_cuda(*y_list)
+    pk = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in packed_list])
+    nn = (ctypes.c_int64 * max(n, 1))(*[int(v) for v in N_list])
+    yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
+    _check(_lib.kq_gemv_fused(int(fmt), n, pk, nn, int(K), _ptr(x), yy, _stream(stream)), "kq_gemv_fused")
+    return y_list
 
 
 def kq_gemm_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:

@@ -332,3 +332,50 @@ def test_pdl_chain_matches_plain_launches(K):
     np.testing.assert_array_equal(pdl, plain)
     planes = oracle_q8k((x0 * 2.25).cpu().numpy())
     assert_row_tol(pdl[5] / 2.0, oracle.gemm(fmt, disk, *planes)[0])
+
+
+# ---------------------------------------------------------------- fused GEMV
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_fused_multi_matrix_bit_identical(K, fmt):
+    """kq_gemv_fused over several matrices sharing x equals kq_quantize_q8k +
+    kq_gemv per matrix, bit for bit, and the oracle within tolerance."""
+    rng = synth.rng_for(109, fmt)
+    Kdim = 2560
+    Ns = [4096, 1000, 8, 333]
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for N in Ns]
+    packs = [pack(K, fmt, d) for d in disks]
+    x = synth.activations(1, Kdim, rng, outliers=True)
+    xd = to_dev(x[0])
+    ys = K.kq_gemv_fused(fmt, packs, Ns, Kdim, xd)
+    a = K.kq_quantize_q8k(xd)
+    planes = oracle_q8k(x)
+    for N, pk, y, disk in zip(Ns, packs, ys, disks):
+        y_sep = K.kq_gemv(fmt, pk, N, Kdim, a)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(y.cpu().numpy(), y_sep.cpu().numpy())
+        assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes)[0])
+
+
+def test_gemv_fused_layer_groups_and_edges(K):
+    """The decode layer's launch groups (q/k/v; gate/up), a single-superblock
+    K, N = 1, a skipped empty matrix, and the host-side argument checks."""
+    fmt = synth.Q4_K
+    rng = synth.rng_for(110, 0)
+    for Kdim, Ns in ((2560, [4096, 1024, 1024]), (2560, [9728, 9728]), (256, [1, 7, 0, 9])):
+        disks = [synth.disk_weights(fmt, max(N, 1), Kdim, rng) for N in Ns]
+        packs = [pack(K, fmt, d) for d in disks]
+        x = synth.activations(1, Kdim, rng)
+        fulls = [poisoned((max(N, 1),)) for N in Ns]
+        K.kq_gemv_fused(fmt, packs, Ns, Kdim, to_dev(x[0]), [f[1] for f in fulls])
+        torch.cuda.synchronize()
+        planes = oracle_q8k(x)
+        for N, disk, (full, y) in zip(Ns, disks, fulls):
+            if N == 0:
+                assert np.isnan(full.cpu().numpy()).all()
+                continue
+            check_guard(full, N)
+            assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk[:N], *planes)[0])
+    with pytest.raises(K.KQError):
+        K.kq_gemv_fused(fmt, packs * 2, [1] * 8, 256, to_dev(x[0]))       # more than 4 matrices
+    with pytest.raises(K.KQError):
+        K.kq_gemv_fused(fmt, packs[:1], [1], 40960 + 256, to_dev(np.zeros(41216, np.float32)))
