@@ -122,19 +122,22 @@ __global__ void __launch_bounds__(256) mv_kernel(const MvParams p) {
 // Decode GEMV (M = 1), over up to four matrices of one format that share one
 // input row, optionally quantizing that row itself (fp32 in).
 //
-// Grid: at most one 256-thread block per SM (persistent).  Work is a list of
-// row groups of 8 rows (one per quad) across the matrices; warp w of the grid
-// owns row groups w, w + W, w + 2W, ... (W warps in the grid) and walks the
-// flattened sequence (row group, superblock) of all of them with a D-deep
-// ring of weight registers: the loads of item i + D are issued as soon as
-// item i is decoded, across row-group boundaries, so a warp keeps D
-// superblocks in flight from its first load to its last.
-// Ordering: the first D items are loaded before griddep_wait() (weights are
-// read-only on this path), so under programmatic dependent launch they
-// overlap the previous kernel; the block then stages the Q8_K row in shared
-// memory (copying it, or quantizing the fp32 row with quantize_block_warp,
-// bit-identical to kq_quantize_q8k) and lets the next kernel launch.  One
-// block per SM leaves room for a block of the next kernel to start early.
+// Work split.  Rows are taken in groups of 8 (one per quad of a warp) across
+// all the matrices; G groups in total.  A task is R = 8/S row groups x S
+// superblock slices, one (group, slice) per warp of a 256-thread block; the
+// S partial sums of a row are added in shared memory in a fixed order (the
+// result does not depend on timing).  S is the smallest of 1, 2, 4, 8 that
+// gives at least one task per block slot; every block gets the same number
+// of consecutive tasks (tpc), so there is no partial second wave.
+// Pipelining.  Each warp walks the flattened sequence (task, superblock of
+// its slice) with a D-deep ring of weight registers: the loads for item i+D
+// are issued as soon as item i is decoded, across task boundaries.  Slices
+// are padded to a common length so every warp reaches each task's
+// reduction barrier at the same item.  The first D items are loaded before
+// griddep_wait() (weights are read-only on this path), overlapping the
+// previous kernel under programmatic dependent launch; then the block stages
+// the Q8_K row in shared memory (copied, or quantized from the fp32 row by
+// quantize_block_warp, bit-identical to kq_quantize_q8k).
 
 struct GemvParams {
     int nmat;
@@ -143,25 +146,23 @@ struct GemvParams {
     float *y[GEMV_MAX_MATRICES];
     int64_t gpre[GEMV_MAX_MATRICES + 1];  // prefix sums of row groups
     int64_t K, nsb;
-    const float *x;                    // fp32 row (fused quantize), or nullptr
-    const float *d8;                   // else: the Q8_K planes of the row
+    int S;                                 // slices per row group (1, 2, 4, 8)
+    int64_t tasks, tpc;                    // task count, tasks per block
+    const float *x;                        // fp32 row (fused quantize), or nullptr
+    const float *d8;                       // else: the Q8_K planes of the row
     const int8_t *qs;
     const int16_t *bs;
 };
 
-template <int F> constexpr int gemv_depth() { return F == FMT_Q4_K ? 4 : 3; }
+template <int F> constexpr int gemv_depth() { return 3; }
 
 __host__ __device__ inline size_t gemv_smem_bytes(int64_t K) { return (size_t)(K + K / 8 + K / 64); }
-
-struct GemvItem {
-    int64_t g;   // row group
-    int64_t sb;  // superblock
-};
 
 template <int F, int D>
 __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     __shared__ Planes s_planes[GEMV_MAX_MATRICES];
+    __shared__ float red[2][8][8];
     const int64_t K = p.K, nsb = p.nsb;
     int8_t *s_qs = reinterpret_cast<int8_t *>(smem);
     int16_t *s_bs = reinterpret_cast<int16_t *>(smem + K);
@@ -169,38 +170,46 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r8 = lane >> 2, c = lane & 3;
+    const int S = p.S, R = 8 / S;
+    const int rg = warp / S, slice = warp % S;
+    const int64_t slen = (nsb + S - 1) / S;                 // padded slice length
+    const int64_t s0 = slice * nsb / S, s1 = (slice + 1) * nsb / S;
+    const int64_t t_begin = (int64_t)blockIdx.x * p.tpc;
+    const int64_t left = p.tasks - t_begin;
+    const int64_t ntask = left <= 0 ? 0 : (left < p.tpc ? left : p.tpc);
+    const int64_t n_items = ntask * slen;
+    const int64_t G = p.gpre[p.nmat];
     if (threadIdx.x < p.nmat) s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
     __syncthreads();
 
-    const int64_t TW = (int64_t)gridDim.x * 8;
-    const int64_t gw = (int64_t)blockIdx.x * 8 + warp;
-    const int64_t G = p.gpre[p.nmat];
-    const int64_t ngroups = G > gw ? (G - gw + TW - 1) / TW : 0;
-    const int64_t n_items = ngroups * nsb;
-
-    // matrix / row / packed superblock index of an item
-    auto locate = [&](const GemvItem &it, int &m, int64_t &n, uint64_t &u) {
+    // item (task tl, offset k) -> row group, superblock, validity
+    struct Item { int64_t tl, k; };
+    auto where = [&](const Item &it, int &m, int64_t &n, int64_t &sb, bool &valid) {
+        const int64_t g = (t_begin + it.tl) * R + rg;
+        sb = s0 + it.k;
+        valid = (g < G) && (sb < s1);
         m = 0;
-        while (m + 1 < p.nmat && it.g >= p.gpre[m + 1]) ++m;
-        n = (it.g - p.gpre[m]) * 8 + r8;
-        const int64_t nc = n < p.N[m] ? n : p.N[m] - 1;
-        u = (uint64_t)nc * nsb + it.sb;
+        while (m + 1 < p.nmat && g >= p.gpre[m + 1]) ++m;
+        n = (g - p.gpre[m]) * 8 + r8;
     };
-    auto advance = [&](GemvItem &it) {
-        if (++it.sb == nsb) { it.sb = 0; it.g += TW; }
+    auto advance = [&](Item &it) {
+        if (++it.k == slen) { it.k = 0; ++it.tl; }
+    };
+    auto issue = [&](typename WRegs<F>::T &w, const Item &it) {
+        int m; int64_t n, sb; bool valid;
+        where(it, m, n, sb, valid);
+        if (valid) {
+            const int64_t nc = n < p.N[m] ? n : p.N[m] - 1;
+            load_w(w, s_planes[m], (uint64_t)nc * nsb + sb, c);
+        }
     };
 
     using W = typename WRegs<F>::T;
     W buf[D];
-    GemvItem pre{gw, 0};  // next item to prefetch
+    Item pre{0, 0};
 #pragma unroll
     for (int i = 0; i < D; ++i) {
-        if (i < n_items) {
-            int m; int64_t n; uint64_t u;
-            locate(pre, m, n, u);
-            load_w(buf[i], s_planes[m], u, c);
-            advance(pre);
-        }
+        if (i < n_items) { issue(buf[i], pre); advance(pre); }
     }
 
     griddep_wait();
@@ -217,35 +226,43 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     __syncthreads();
     griddep_launch_dependents();
 
-    GemvItem cur{gw, 0};
+    Item cur{0, 0};
     float acc = 0.0f;
     for (int64_t base = 0; base < n_items; base += D) {
 #pragma unroll
         for (int i = 0; i < D; ++i) {
             if (base + i < n_items) {
-                LaneQ L;
-                decode_lane(buf[i], c, L);
-                if (base + i + D < n_items) {
-                    int m; int64_t n; uint64_t u;
-                    locate(pre, m, n, u);
-                    load_w(buf[i], s_planes[m], u, c);
-                    advance(pre);
+                int m; int64_t n, sb; bool valid;
+                where(cur, m, n, sb, valid);
+                if (valid) {
+                    LaneQ L;
+                    decode_lane(buf[i], c, L);
+                    if (base + i + D < n_items) issue(buf[i], pre);
+                    int isum, msum;
+                    lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
+                    isum = quad_sum(isum);
+                    const float d8 = s_d8[sb];
+                    acc = fmaf(L.d * d8, static_cast<float>(isum), acc);
+                    if constexpr (F != FMT_Q6_K) {
+                        msum = quad_sum(msum);
+                        acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
+                    }
+                } else if (base + i + D < n_items) {
+                    issue(buf[i], pre);
                 }
-                const int64_t sb = cur.sb;
-                int isum, msum;
-                lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
-                isum = quad_sum(isum);
-                const float d8 = s_d8[sb];
-                acc = fmaf(L.d * d8, static_cast<float>(isum), acc);
-                if constexpr (F != FMT_Q6_K) {
-                    msum = quad_sum(msum);
-                    acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
-                }
-                if (sb == nsb - 1) {
-                    int m; int64_t n; uint64_t u;
-                    locate(cur, m, n, u);
-                    if (c == 0 && n < p.N[m]) p.y[m][n] = acc;
+                if (base + i + D < n_items) advance(pre);
+                if (cur.k == slen - 1) {
+                    // end of this task: add the S slices of each row
+                    float *r = red[cur.tl & 1][warp];
+                    if (c == 0) r[r8] = acc;
                     acc = 0.0f;
+                    __syncthreads();
+                    const int64_t g = (t_begin + cur.tl) * R + rg;
+                    if (slice == 0 && c == 0 && g < G && n < p.N[m]) {
+                        float v = 0.0f;
+                        for (int j = 0; j < S; ++j) v += red[cur.tl & 1][rg * S + j][r8];
+                        p.y[m][n] = v;
+                    }
                 }
                 advance(cur);
             }
@@ -271,7 +288,14 @@ static cudaError_t launch_gemv_t(GemvParams p, cudaStream_t s) {
     for (int m = 0; m < p.nmat; ++m) p.gpre[m + 1] = p.gpre[m] + (p.N[m] + 7) / 8;
     const int64_t G = p.gpre[p.nmat];
     if (G == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((G + 7) / 8, sm_count());
+    const int64_t slots = 2 * (int64_t)sm_count();  // two resident blocks per SM
+    int S = 1;
+    while (S < 8 && 2 * S <= p.nsb && (G * S + 7) / 8 < slots) S *= 2;
+    p.S = S;
+    const int64_t R = 8 / S;
+    p.tasks = (G + R - 1) / R;
+    p.tpc = (p.tasks + slots - 1) / slots;
+    const int64_t blocks = (p.tasks + p.tpc - 1) / p.tpc;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
