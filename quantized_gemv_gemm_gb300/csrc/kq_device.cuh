@@ -340,6 +340,21 @@ __device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, i
     if (lane == 0) *db = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
 }
 
+// Bulk prefetch of [p, p + bytes) from HBM into L2 by the TMA engine
+// (cp.async.bulk.prefetch.L2, a hint: nothing is written, nothing waits).
+// p must be 16-byte aligned; the size is rounded down to 16 bytes and split
+// into 32 KB requests.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint64_t bytes) {
+    const uint8_t *b = static_cast<const uint8_t *>(p);
+    bytes &= ~uint64_t(15);
+    while (bytes) {
+        const uint32_t n = bytes > 32768 ? 32768u : static_cast<uint32_t>(bytes);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(b), "r"(n) : "memory");
+        b += n;
+        bytes -= n;
+    }
+}
+
 // Programmatic dependent launch.  griddep_wait() blocks until the grids this
 // one depends on have completed and their memory is visible (a no-op when
 // the kernel was launched without the programmatic attribute);

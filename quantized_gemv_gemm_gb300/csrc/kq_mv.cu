@@ -155,6 +155,7 @@ struct GemvParams {
 };
 
 template <int F> constexpr int gemv_depth() { return 3; }
+constexpr int64_t GEMV_PREFETCH_TASKS = 3;
 
 __host__ __device__ inline size_t gemv_smem_bytes(int64_t K) { return (size_t)(K + K / 8 + K / 64); }
 
@@ -203,6 +204,25 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
             load_w(w, s_planes[m], (uint64_t)nc * nsb + sb, c);
         }
     };
+
+    // L2 prefetch of whole tasks (their rows are contiguous in every plane),
+    // GEMV_PREFETCH_TASKS ahead of the task being folded
+    auto prefetch_task = [&](int64_t tl) {
+        if (tl >= ntask) return;
+        const int64_t g0 = (t_begin + tl) * R, g1 = g0 + R < G ? g0 + R : G;
+        int u[4];
+        plane_unit_bytes(F, u);
+        for (int m = 0; m < p.nmat; ++m) {
+            const int64_t a = g0 > p.gpre[m] ? g0 : p.gpre[m], b = g1 < p.gpre[m + 1] ? g1 : p.gpre[m + 1];
+            if (a >= b) continue;
+            const int64_t r0 = (a - p.gpre[m]) * 8, r1e = (b - p.gpre[m]) * 8, r1 = r1e < p.N[m] ? r1e : p.N[m];
+            const uint8_t *base[4] = {s_planes[m].p0, s_planes[m].p1, s_planes[m].p2, s_planes[m].p3};
+            for (int q = 0; q < 4; ++q)
+                if (u[q]) prefetch_l2_bulk(base[q] + (uint64_t)r0 * nsb * u[q], (uint64_t)(r1 - r0) * nsb * u[q]);
+        }
+    };
+    if (threadIdx.x == 0)
+        for (int64_t tl = 0; tl < GEMV_PREFETCH_TASKS; ++tl) prefetch_task(tl);
 
     using W = typename WRegs<F>::T;
     W buf[D];
@@ -253,6 +273,7 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                 if (base + i + D < n_items) advance(pre);
                 if (cur.k == slen - 1) {
                     // end of this task: add the S slices of each row
+                    if (threadIdx.x == 0) prefetch_task(cur.tl + GEMV_PREFETCH_TASKS);
                     float *r = red[cur.tl & 1][warp];
                     if (c == 0) r[r8] = acc;
                     acc = 0.0f;

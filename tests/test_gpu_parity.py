@@ -337,8 +337,9 @@ def test_pdl_chain_matches_plain_launches(K):
 # ---------------------------------------------------------------- fused GEMV
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemv_fused_multi_matrix_bit_identical(K, fmt):
-    """kq_gemv_fused over several matrices sharing x equals kq_quantize_q8k +
-    kq_gemv per matrix, bit for bit, and the oracle within tolerance."""
+    """kq_gemv_fused over several matrices sharing x agrees with kq_quantize_q8k
+    + kq_gemv per matrix (the quantization is bit-identical; the fp32 sums
+    may be split differently across warps) and with the oracle."""
     rng = synth.rng_for(109, fmt)
     Kdim = 2560
     Ns = [4096, 1000, 8, 333]
@@ -352,7 +353,7 @@ def test_gemv_fused_multi_matrix_bit_identical(K, fmt):
     for N, pk, y, disk in zip(Ns, packs, ys, disks):
         y_sep = K.kq_gemv(fmt, pk, N, Kdim, a)
         torch.cuda.synchronize()
-        np.testing.assert_array_equal(y.cpu().numpy(), y_sep.cpu().numpy())
+        assert_row_tol(y.cpu().numpy(), y_sep.cpu().numpy().astype(np.float64), rel=1e-5)
         assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes)[0])
 
 
