@@ -167,6 +167,54 @@ __device__ __forceinline__ void load_w(WQ6 &w, const Planes &P, uint64_t u, int 
     w.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3) + u);
 }
 
+// Per-lane plane pointers at one superblock of a row; the row's next
+// superblocks follow at fixed strides (128 / 16 / 32 / 64 / 2 bytes), so a
+// lane walks a row by adding i * stride (load_at).
+struct LanePtr {
+    const uint8_t *p0, *p1, *p2, *p3;
+};
+
+template <int F>
+__device__ __forceinline__ LanePtr lane_ptr(const Planes &P, uint64_t u, int c) {
+    LanePtr r;
+    if constexpr (F == FMT_Q4_K) {
+        r.p0 = P.p0 + u * 128 + 16 * c;
+        r.p1 = P.p1 + u * 16;
+        r.p2 = r.p3 = nullptr;
+    } else if constexpr (F == FMT_Q5_K) {
+        r.p0 = P.p0 + u * 128 + 16 * c;
+        r.p1 = P.p1 + u * 32 + 16 * (c & 1);
+        r.p2 = P.p2 + u * 16;
+        r.p3 = nullptr;
+    } else {
+        const int h = c >> 1, q = c & 1;
+        r.p0 = P.p0 + u * 128 + 64 * h + 16 * q;
+        r.p1 = P.p1 + u * 64 + 32 * h + 16 * q;
+        r.p2 = P.p2 + u * 16;
+        r.p3 = P.p3 + u * 2;
+    }
+    return r;
+}
+
+__device__ __forceinline__ void load_at(WQ4 &w, const LanePtr &lp, int64_t i) {
+    w.qa = ld_stream(lp.p0 + i * 128);
+    w.qb = ld_stream(lp.p0 + i * 128 + 64);
+    w.hdr = ld_keep(lp.p1 + i * 16);
+}
+__device__ __forceinline__ void load_at(WQ5 &w, const LanePtr &lp, int64_t i) {
+    w.qa = ld_stream(lp.p0 + i * 128);
+    w.qb = ld_stream(lp.p0 + i * 128 + 64);
+    w.qh = ld_stream(lp.p1 + i * 32);
+    w.hdr = ld_keep(lp.p2 + i * 16);
+}
+__device__ __forceinline__ void load_at(WQ6 &w, const LanePtr &lp, int64_t i) {
+    w.la = ld_stream(lp.p0 + i * 128);
+    w.lb = ld_stream(lp.p0 + i * 128 + 32);
+    w.qh = ld_stream(lp.p1 + i * 64);
+    w.sc = ld_keep(lp.p2 + i * 16);
+    w.d = __ldg(reinterpret_cast<const unsigned short *>(lp.p3) + i);
+}
+
 // ---------------------------------------------------------------------------
 // Decoded per-lane quants: four groups of 16 stored quant bytes (one uint4
 // each, bytes 0..63) with their sub-scales, plus the lane's share of the

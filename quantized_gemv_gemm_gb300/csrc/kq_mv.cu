@@ -154,7 +154,7 @@ struct GemvParams {
     const int16_t *bs;
 };
 
-template <int F> constexpr int gemv_depth() { return 3; }
+template <int F> constexpr int gemv_depth() { return F == FMT_Q4_K ? 4 : 3; }
 constexpr int64_t GEMV_PREFETCH_TASKS = 3;
 
 __host__ __device__ inline size_t gemv_smem_bytes(int64_t K) { return (size_t)(K + K / 8 + K / 64); }
@@ -173,40 +173,25 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     const int r8 = lane >> 2, c = lane & 3;
     const int S = p.S, R = 8 / S;
     const int rg = warp / S, slice = warp % S;
-    const int64_t slen = (nsb + S - 1) / S;                 // padded slice length
-    const int64_t s0 = slice * nsb / S, s1 = (slice + 1) * nsb / S;
+    const int64_t s0 = slice * nsb / S, s1 = (slice + 1) * nsb / S, len = s1 - s0;
     const int64_t t_begin = (int64_t)blockIdx.x * p.tpc;
     const int64_t left = p.tasks - t_begin;
     const int64_t ntask = left <= 0 ? 0 : (left < p.tpc ? left : p.tpc);
-    const int64_t n_items = ntask * slen;
     const int64_t G = p.gpre[p.nmat];
     if (threadIdx.x < p.nmat) s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
     __syncthreads();
 
-    // item (task tl, offset k) -> row group, superblock, validity
-    struct Item { int64_t tl, k; };
-    auto where = [&](const Item &it, int &m, int64_t &n, int64_t &sb, bool &valid) {
-        const int64_t g = (t_begin + it.tl) * R + rg;
-        sb = s0 + it.k;
-        valid = (g < G) && (sb < s1);
+    // task tl of this block -> this lane's matrix, row and plane pointers
+    auto task_ptr = [&](int64_t tl, int &m, int64_t &n, bool &valid) {
+        const int64_t g = (t_begin + tl) * R + rg;
+        valid = g < G;
         m = 0;
         while (m + 1 < p.nmat && g >= p.gpre[m + 1]) ++m;
         n = (g - p.gpre[m]) * 8 + r8;
+        const int64_t nc = n < p.N[m] ? n : p.N[m] - 1;
+        return lane_ptr<F>(s_planes[m], (uint64_t)nc * nsb + s0, c);
     };
-    auto advance = [&](Item &it) {
-        if (++it.k == slen) { it.k = 0; ++it.tl; }
-    };
-    auto issue = [&](typename WRegs<F>::T &w, const Item &it) {
-        int m; int64_t n, sb; bool valid;
-        where(it, m, n, sb, valid);
-        if (valid) {
-            const int64_t nc = n < p.N[m] ? n : p.N[m] - 1;
-            load_w(w, s_planes[m], (uint64_t)nc * nsb + sb, c);
-        }
-    };
-
-    // L2 prefetch of whole tasks (their rows are contiguous in every plane),
-    // GEMV_PREFETCH_TASKS ahead of the task being folded
+    // L2 prefetch of whole tasks (their rows are contiguous in every plane)
     auto prefetch_task = [&](int64_t tl) {
         if (tl >= ntask) return;
         const int64_t g0 = (t_begin + tl) * R, g1 = g0 + R < G ? g0 + R : G;
@@ -226,10 +211,17 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
 
     using W = typename WRegs<F>::T;
     W buf[D];
-    Item pre{0, 0};
+    int m = 0;
+    int64_t n = 0;
+    bool valid = false;
+    LanePtr lp{};
+    if (ntask > 0) {
+        lp = task_ptr(0, m, n, valid);
+        if (valid) {
 #pragma unroll
-    for (int i = 0; i < D; ++i) {
-        if (i < n_items) { issue(buf[i], pre); advance(pre); }
+            for (int i = 0; i < D; ++i)
+                if (i < len) load_at(buf[i], lp, i);
+        }
     }
 
     griddep_wait();
@@ -246,48 +238,55 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     __syncthreads();
     griddep_launch_dependents();
 
-    Item cur{0, 0};
-    float acc = 0.0f;
-    for (int64_t base = 0; base < n_items; base += D) {
+    for (int64_t tl = 0; tl < ntask; ++tl) {
+        // fold this task's slice: every lane folds its own int32 partials
+        // once per superblock; the quad's four lanes are added at the end
+        float acc = 0.0f;
+        if (valid) {
+            for (int64_t j = 0; j < len; j += D) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) {
-            if (base + i < n_items) {
-                int m; int64_t n, sb; bool valid;
-                where(cur, m, n, sb, valid);
-                if (valid) {
-                    LaneQ L;
-                    decode_lane(buf[i], c, L);
-                    if (base + i + D < n_items) issue(buf[i], pre);
-                    int isum, msum;
-                    lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
-                    isum = quad_sum(isum);
-                    const float d8 = s_d8[sb];
-                    acc = fmaf(L.d * d8, static_cast<float>(isum), acc);
-                    if constexpr (F != FMT_Q6_K) {
-                        msum = quad_sum(msum);
-                        acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
-                    }
-                } else if (base + i + D < n_items) {
-                    issue(buf[i], pre);
-                }
-                if (base + i + D < n_items) advance(pre);
-                if (cur.k == slen - 1) {
-                    // end of this task: add the S slices of each row
-                    if (threadIdx.x == 0) prefetch_task(cur.tl + GEMV_PREFETCH_TASKS);
-                    float *r = red[cur.tl & 1][warp];
-                    if (c == 0) r[r8] = acc;
-                    acc = 0.0f;
-                    __syncthreads();
-                    const int64_t g = (t_begin + cur.tl) * R + rg;
-                    if (slice == 0 && c == 0 && g < G && n < p.N[m]) {
-                        float v = 0.0f;
-                        for (int j = 0; j < S; ++j) v += red[cur.tl & 1][rg * S + j][r8];
-                        p.y[m][n] = v;
+                for (int i = 0; i < D; ++i) {
+                    if (j + i < len) {
+                        const int64_t sb = s0 + j + i;
+                        LaneQ L;
+                        decode_lane(buf[i], c, L);
+                        if (j + i + D < len) load_at(buf[i], lp, j + i + D);
+                        int isum, msum;
+                        lane_partials<F, true>(L, s_qs + sb * QK, s_bs + sb * 16, c, isum, msum);
+                        const float d8 = s_d8[sb];
+                        acc = fmaf(L.d * d8, static_cast<float>(isum), acc);
+                        if constexpr (F != FMT_Q6_K) acc = fmaf(-(L.dmin * d8), static_cast<float>(msum), acc);
                     }
                 }
-                advance(cur);
             }
         }
+        // the next task's first loads go out before the reduction barrier
+        int m2 = 0;
+        int64_t n2 = 0;
+        bool valid2 = false;
+        LanePtr lp2{};
+        if (tl + 1 < ntask) {
+            lp2 = task_ptr(tl + 1, m2, n2, valid2);
+            if (valid2) {
+#pragma unroll
+                for (int i = 0; i < D; ++i)
+                    if (i < len) load_at(buf[i], lp2, i);
+            }
+        }
+        if (threadIdx.x == 0) prefetch_task(tl + GEMV_PREFETCH_TASKS);
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+        acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+        if (c == 0) red[tl & 1][warp][r8] = acc;
+        __syncthreads();
+        if (slice == 0 && c == 0 && valid && n < p.N[m]) {
+            float v = 0.0f;
+            for (int j = 0; j < S; ++j) v += red[tl & 1][rg * S + j][r8];
+            p.y[m][n] = v;
+        }
+        m = m2;
+        n = n2;
+        valid = valid2;
+        lp = lp2;
     }
 }
 
