@@ -1,27 +1,748 @@
-// kq_gemm.cu - tensor-core prefill GEMM (tcgen05).  Placeholder until the
-// tcgen05 kernel lands: every shape reports cudaErrorNotSupported and the
-// C-ABI layer runs the CUDA-core token-group kernel instead.
+// kq_gemm.cu - tensor-core prefill GEMM (tcgen05) and its MoE grouped form.
+//
+// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
+//
+// The contraction the page folds in int32 runs on the fp16 tensor pipe with
+// exact small integers (sm_103a has no integer tcgen05.mma):
+//   - a pre-pass turns the Q8_K activations of the M token rows into an fp16
+//     image of q8 (exact, |q8| <= 127), of the per-16 bsums (exact, <= 2032)
+//     and a transposed copy of d8, in the caller's workspace;
+//   - each block owns 128 weight rows x up to 128 tokens; per superblock its
+//     unpack warps expand the packed weights once into shared memory as fp16
+//     w' = sc*q with the sub-scale folded in (Q4_K <= 945, Q5_K <= 1953:
+//     exact), the kq v3 "panel scratch" unpacked once per token block;
+//     Q6_K's w' = sc*(q-32) is exact for |sc| <= 64, and when a tile holds a
+//     larger sub-scale the weight is split into two exact planes,
+//     sc*(v - (v&1)) (even, |.| <= 4096) and sc*(v&1), both multiplied into
+//     the same accumulator;
+//   - tcgen05.mma kind::f16 accumulates I = sum w'*q8 (the page's isum, or
+//     iacc - 32*bacc for Q6_K) in fp32 TMEM; for Q4_K/Q5_K a second K=16 MMA
+//     of the sub-mins (duplicated per 16) against the bsums gives msum;
+//   - the epilogue folds once per superblock, y += d8*(d*I - dmin*msum), in
+//     fp32 registers (kq-arc, "The pieces": one float fold per superblock).
+// The fp32 accumulator is exact while every partial sum stays below 2^24 in
+// magnitude (true for realistic activations; at adversarial extremes the
+// sum is rounded like the fold's own float(isum)).
+//
+// Warp roles (14 warps): 0 TMA producer of the activation tiles, 1 MMA issuer
+// (and TMEM owner), 2..5 weight unpack (thread = weight row), 6..13 epilogue
+// (thread = row x 64 token columns; TMEM lane quadrant = warp % 4).  Stages are half superblocks (K = 128): an A ring of 2 slots,
+// a B ring of 3 (Q6_K: 2); accumulators I and msum double-buffered by
+// superblock parity.  Every mbarrier wait is bounded; on timeout the block
+// records KQ_ERR_TIMEOUT in the device status word and winds down.
 #include "kq_internal.h"
+#include "kq_sm100.cuh"
+
+#include <cuda_fp16.h>
+#include <cudaTypedefs.h>
+#include <mutex>
 
 namespace kq {
 
 __device__ int g_status = 0;
 
-size_t gemm_workspace_bytes(int, int64_t, int64_t, int64_t) { return 0; }
+using namespace sm100;
 
-cudaError_t launch_gemm_tc(int, const void *, int64_t, int64_t, Q8K, int64_t, const int32_t *, int64_t,
-                           uint64_t, float *, void *, size_t, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int BM = 128;      // weight rows per tile (MMA M)
+constexpr int BT = 128;      // tokens per tile (MMA N, at most)
+constexpr int NTHREADS = 448;
+constexpr int W_TMA = 0, W_MMA = 1, W_UNPACK = 2, W_EPI = 6;
+
+template <int F>
+struct Cfg {
+    static constexpr bool kMins = F != FMT_Q6_K;
+    static constexpr int NB = F == FMT_Q6_K ? 2 : 3;              // B ring slots
+    static constexpr int A_SLOT = F == FMT_Q6_K ? 65536 : 32768;  // 2 sub-tiles (x2 planes for Q6_K)
+    static constexpr int B_SUB = BT * 128;                         // one 64-wide K sub-tile of tokens
+    static constexpr int B_SLOT = 2 * B_SUB + (kMins ? BT * 32 : 0);
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_AMIN = 2 * A_SLOT;
+    static constexpr int OFF_B = OFF_AMIN + (kMins ? BM * 32 : 0);
+    static constexpr int OFF_SD = OFF_B + NB * B_SLOT;            // s_d, s_dmin [2][BM]
+    static constexpr int OFF_D8 = OFF_SD + 2 * 2 * BM * 4;        // per epilogue warp [64] floats
+    static constexpr int OFF_BAR = OFF_D8 + 8 * 64 * 4;
+    static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
+    static constexpr int SMEM = OFF_MISC + 128 + 1024;            // + alignment slack
+    static_assert(OFF_B % 1024 == 0, "B tiles need 1024-byte alignment");
+    static_assert(B_SLOT % 1024 == 0, "B slots need 1024-byte alignment");
+};
+
+// barrier indices
+enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_ACC_FULL = 10, BAR_ACC_EMPTY = 12,
+       BAR_SD_FULL = 14, BAR_MMA_DONE = 16 };
+
+struct GemmParams {
+    const uint8_t *packed;
+    uint64_t expert_bytes;
+    int64_t N, K, nsb, M;
+    const int32_t *offsets;  // grouped: [E+1]; dense: nullptr
+    int64_t E;
+    const float *d8t;        // workspace: d8 transposed [nsb][Mp]
+    int64_t Mp;
+    float *y;
+};
+
+__device__ __forceinline__ void set_timeout() { atomicExch(&g_status, 1); }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_mul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_splat(float v) {
+    const unsigned short h = __half_as_ushort(__float2half_rn(v));
+    return static_cast<uint32_t>(h) | (static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// byte pairs (0,1), (2,3) of a word, each as the low byte of one fp16 lane
+// whose high byte is 0x64 (the fp16 1024 + byte)
+constexpr uint32_t SEL_01 = 0x4140, SEL_23 = 0x4342;
+constexpr uint32_t MAGIC = 0x64646464u;
+
+// ---------------------------------------------------------------------------
+// Unpack of one weight row x one 64-wide K sub-tile of a half superblock into
+// the A operand (128-byte swizzled K-major fp16 rows).  `a_row` is the shared
+// address of the sub-tile base; the row's 8 chunks of 8 fp16 are written at
+// sw128_offset(r, 8q).
+
+// Q4_K/Q5_K: sub-tile = chunk c of the superblock (64 elements): elements
+// 64c + l (low nibbles of qs[32c + l], sub-scale sc_2c) at K 0..31 and
+// 64c + 32 + l (high nibbles, sc_2c+1) at K 32..63; Q5_K ORs bit 2c / 2c+1 of
+// qh[l] in as value 16.  w' = q*sc is built exactly in fp16 as
+// (1024 + q)*sc - 1024*sc (low) and (1024 + 16q)*(sc/16) - 64*sc (high).
+template <int F>
+__device__ __forceinline__ void unpack_q45(uint32_t a_tile, int r, const uint32_t (&qs)[8], const uint32_t (&qh)[8],
+                                           int c, int sc_lo, int sc_hi) {
+    const uint32_t s_lo = h2_splat((float)sc_lo), o_lo = h2_splat(-1024.0f * sc_lo);
+    const uint32_t s_hi = h2_splat(sc_hi * 0.0625f), o_hi = h2_splat(-64.0f * sc_hi);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {  // K 8q .. 8q+7: bytes 8q .. 8q+7 of the chunk
+        uint32_t lo[4], hi[4];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const uint32_t word = qs[2 * q + w];
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+                const uint32_t sel = pr ? SEL_23 : SEL_01;
+                const uint32_t x = prmt(word, MAGIC, sel);
+                uint32_t l = x & 0xFF0FFF0Fu, h = x & 0xFFF0FFF0u;
+                if constexpr (F == FMT_Q5_K) {
+                    const uint32_t hb = prmt(qh[2 * q + w], 0u, pr ? 0x4342u : 0x4140u) & 0x00FF00FFu;
+                    const int b = 2 * c;  // low nibble's fifth bit
+                    l |= (b <= 4 ? (hb << (4 - b)) : (hb >> (b - 4))) & 0x00100010u;
+                    // high nibble's fifth bit (2c+1) lands on bit 8: value 256 = 16 * 16
+                    h |= (hb << (7 - b)) & 0x01000100u;
+                }
+                lo[2 * w + pr] = h2_fma(l, s_lo, o_lo);
+                hi[2 * w + pr] = h2_fma(h, s_hi, o_hi);
+            }
+        }
+        sts128(a_tile + sw128_offset(r, 8 * q), lo[0], lo[1], lo[2], lo[3]);
+        sts128(a_tile + sw128_offset(r, 32 + 8 * q), hi[0], hi[1], hi[2], hi[3]);
+    }
+}
+
+// Q6_K: sub-tile j of half h holds groups t = 2j (K 0..31) and 2j+1 (K 32..63)
+// of the half: element 128h + 32t + l is the low (t < 2) or high (t >= 2)
+// nibble of ql[64h + 32(t&1) + l] with bits 2t..2t+1 of qh[32h + l] on top,
+// sub-scale sc[8h + 2t + l/16] (byte 2(t - 2j) + l/16 of `scw`).  v = q - 32:
+// P1 = v*sc is exact for |sc| <= 64; with `split`, P1 = (v - (v&1))*sc and
+// P2 = (v&1)*sc.  `zero2` writes zeros to this thread's P2 rows instead.
+__device__ __forceinline__ void unpack_q6(uint32_t a_tile, uint32_t a2_tile, int r, const uint32_t (&ql)[16],
+                                          const uint32_t (&qh)[8], uint32_t scw, int j, bool split, bool zero2) {
+    const uint32_t off1056 = h2_splat(1056.0f);
+#pragma unroll
+    for (int tt = 0; tt < 2; ++tt) {
+        const int t = 2 * j + tt;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // K 32tt + 8q .. +7: l = 8q .. 8q+7
+            const int scv = (int)(int8_t)((scw >> (8 * (2 * tt + (q >> 1)))) & 0xFF);
+            const uint32_t s2 = h2_splat((float)scv);
+            uint32_t p1[4], p2[4];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const uint32_t lword = ql[8 * (t & 1) + 2 * q + w];
+                const uint32_t nib = (t >= 2) ? (lword >> 4) : lword;
+                const uint32_t hword = qh[2 * q + w] >> (2 * t);
+#pragma unroll
+                for (int pr = 0; pr < 2; ++pr) {
+                    const uint32_t sel = pr ? SEL_23 : SEL_01;
+                    uint32_t x = prmt(nib, MAGIC, sel) & 0xFF0FFF0Fu;
+                    x |= (prmt(hword, 0u, sel) << 4) & 0x00300030u;   // fp16 1024 + q, q = 0..63
+                    if (split) {
+                        const uint32_t odd = x & 0x00010001u;
+                        p1[2 * w + pr] = h2_mul(h2_sub(x ^ odd, off1056), s2);
+                        p2[2 * w + pr] = h2_mul(odd * 0x3C00u, s2);     // fp16 1.0 in each odd lane
+                    } else {
+                        p1[2 * w + pr] = h2_mul(h2_sub(x, off1056), s2);
+                        p2[2 * w + pr] = 0u;
+                    }
+                }
+            }
+            sts128(a_tile + sw128_offset(r, 32 * tt + 8 * q), p1[0], p1[1], p1[2], p1[3]);
+            if (split || zero2) sts128(a2_tile + sw128_offset(r, 32 * tt + 8 * q), p2[0], p2[1], p2[2], p2[3]);
+        }
+    }
+}
+
+// Raw packed bytes one unpack thread (one weight row) converts for one half
+// superblock (K 128h .. 128h + 127).
+struct RawQ4 { uint32_t qs[16]; uint4 hdr; };              // qs[64h .. 64h+64)
+struct RawQ5 { uint32_t qs[16]; uint32_t qh[8]; uint4 hdr; };
+struct RawQ6 { uint32_t ql[16]; uint32_t qh[8]; uint32_t sc[2]; uint32_t d; };  // ql/qh/sc of half h
+template <int F> struct RawOf;
+template <> struct RawOf<FMT_Q4_K> { using T = RawQ4; };
+template <> struct RawOf<FMT_Q5_K> { using T = RawQ5; };
+template <> struct RawOf<FMT_Q6_K> { using T = RawQ6; };
+
+__device__ __forceinline__ void ld16w(uint32_t *dst, const uint8_t *src) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
+    dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+}
+// u = packed superblock index, h = half
+__device__ __forceinline__ void load_raw(RawQ4 &r, const Planes &P, uint64_t u, int h) {
+    const uint8_t *q = P.p0 + u * 128 + 64 * h;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 16 * i);
+    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p1 + u * 16));
+}
+__device__ __forceinline__ void load_raw(RawQ5 &r, const Planes &P, uint64_t u, int h) {
+    const uint8_t *q = P.p0 + u * 128 + 64 * h;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 16 * i);
+    ld16w(r.qh, P.p1 + u * 32);
+    ld16w(r.qh + 4, P.p1 + u * 32 + 16);
+    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p2 + u * 16));
+}
+__device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, uint64_t u, int h) {
+    const uint8_t *l = P.p0 + u * 128 + 64 * h;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ld16w(r.ql + 4 * i, l + 16 * i);
+    ld16w(r.qh, P.p1 + u * 64 + 32 * h);
+    ld16w(r.qh + 4, P.p1 + u * 64 + 32 * h + 16);
+    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(P.p2 + u * 16 + 8 * h));
+    r.sc[0] = sc.x;
+    r.sc[1] = sc.y;
+    r.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3) + u);
+}
+
+// ---------------------------------------------------------------------------
+template <int F>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap map_a16, const __grid_constant__ CUtensorMap map_b16,
+                const GemmParams p) {
+    using C = Cfg<F>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    float *s_d = reinterpret_cast<float *>(smem + C::OFF_SD);
+    float *s_dmin = s_d + 2 * BM;
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);  // [0] tmem base, [1..] tile info
+    int *s_flag = reinterpret_cast<int *>(misc + 8);                     // Q6_K split flags [2 halves][8 warps]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nsb = p.nsb;
+
+    // ---- tile of this block
+    int64_t t0 = 0, t_end = p.M, w_tile = blockIdx.y;
+    int e = 0;
+    if (p.offsets) {
+        // grouped: blockIdx.x enumerates the experts' token tiles in order
+        if (warp == 0) {
+            int64_t base = 0;
+            int found = -1;
+            int64_t tb = 0, te = 0;
+            for (int64_t e0 = 0; e0 < p.E && found < 0; e0 += 32) {
+                const int64_t ee = e0 + lane;
+                int64_t a = 0, b = 0, tiles = 0;
+                if (ee < p.E) {
+                    a = p.offsets[ee];
+                    b = p.offsets[ee + 1];
+                    a = a < 0 ? 0 : (a > p.M ? p.M : a);
+                    b = b < a ? a : (b > p.M ? p.M : b);
+                    tiles = (b - a + BT - 1) / BT;
+                }
+                int64_t incl = tiles;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                const int64_t excl = base + incl - tiles;
+                const bool mine = tiles > 0 && (int64_t)blockIdx.x >= excl && (int64_t)blockIdx.x < excl + tiles;
+                const unsigned mask = __ballot_sync(0xFFFFFFFFu, mine);
+                if (mask) {
+                    const int src = __ffs(mask) - 1;
+                    found = (int)(e0 + src);
+                    const int64_t jt = (int64_t)blockIdx.x - __shfl_sync(0xFFFFFFFFu, excl, src);
+                    tb = __shfl_sync(0xFFFFFFFFu, a, src) + jt * BT;
+                    te = __shfl_sync(0xFFFFFFFFu, b, src);
+                }
+                base += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            if (lane == 0) {
+                misc[1] = (uint32_t)found;
+                misc[2] = (uint32_t)tb;
+                misc[3] = (uint32_t)te;
+            }
+        }
+        __syncthreads();
+        if ((int)misc[1] < 0) return;  // no token tile for this block
+        e = (int)misc[1];
+        t0 = misc[2];
+        t_end = misc[3];
+    } else {
+        t0 = (int64_t)blockIdx.x * BT;
+    }
+    const int ntok = (int)((t_end - t0) < BT ? (t_end - t0) : BT);
+    const int n_mma = (ntok + 15) & ~15;
+    const int64_t n0 = w_tile * BM;
+    const Planes P = make_planes(F, p.packed + (uint64_t)e * p.expert_bytes, p.N, nsb);
+
+    // ---- setup
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[BAR_FULL_A + 0], 4);
+        mbar_init(&bar[BAR_FULL_A + 1], 4);
+        mbar_init(&bar[BAR_EMPTY_A + 0], 1);
+        mbar_init(&bar[BAR_EMPTY_A + 1], 1);
+        for (int i = 0; i < C::NB; ++i) {
+            mbar_init(&bar[BAR_FULL_B + i], 1);
+            mbar_init(&bar[BAR_EMPTY_B + i], 1);
+        }
+        mbar_init(&bar[BAR_ACC_FULL + 0], 1);
+        mbar_init(&bar[BAR_ACC_FULL + 1], 1);
+        mbar_init(&bar[BAR_ACC_EMPTY + 0], 8);
+        mbar_init(&bar[BAR_ACC_EMPTY + 1], 8);
+        mbar_init(&bar[BAR_SD_FULL + 0], 4);
+        mbar_init(&bar[BAR_SD_FULL + 1], 4);
+        mbar_init(&bar[BAR_MMA_DONE], 1);
+        mbar_fence_init();
+    }
+    if (warp == W_MMA) {
+        tmem_alloc(&misc[0], 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    // TMEM columns: I[b] at 256b, msum[b] at 256b + 128
+    bool ok = true;
+
+    if (warp == W_TMA) {
+        // ------------------------------------------------ activation tiles
+        if (lane == 0) {
+            tma_prefetch_desc(&map_a16);
+            if (C::kMins) tma_prefetch_desc(&map_b16);
+            // the block's weight rows are contiguous in every plane: start
+            // streaming them into L2 for the unpack warps
+            int u[4];
+            plane_unit_bytes(F, u);
+            const int64_t r1 = (n0 + BM < p.N ? n0 + BM : p.N);
+            const uint8_t *base[4] = {P.p0, P.p1, P.p2, P.p3};
+            for (int q = 0; q < 4; ++q)
+                if (u[q] && r1 > n0)
+                    prefetch_l2_bulk(base[q] + (uint64_t)n0 * nsb * u[q], (uint64_t)(r1 - n0) * nsb * u[q]);
+            int64_t use = 0;
+            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+                for (int h = 0; h < 2 && ok; ++h, ++use) {
+                    const int slot = (int)(use % C::NB);
+                    const uint32_t par = (uint32_t)((use / C::NB) & 1);
+                    if (!mbar_wait(&bar[BAR_EMPTY_B + slot], par ^ 1)) { ok = false; break; }
+                    uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
+                    const bool mins = C::kMins && h == 0;
+                    mbar_arrive_expect_tx(&bar[BAR_FULL_B + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
+                    const int k0 = (int)(sb * QK + 128 * h);
+                    tma_load_2d(bs, &map_a16, k0, (int)t0, &bar[BAR_FULL_B + slot]);
+                    tma_load_2d(bs + C::B_SUB, &map_a16, k0 + 64, (int)t0, &bar[BAR_FULL_B + slot]);
+                    if (mins) tma_load_2d(bs + 2 * C::B_SUB, &map_b16, (int)(sb * 16), (int)t0, &bar[BAR_FULL_B + slot]);
+                }
+            }
+            if (!ok) {
+                set_timeout();
+                // let the copies already issued land before the block exits
+                for (int s = 0; s < C::NB; ++s)
+                    if (use > s) mbar_wait(&bar[BAR_FULL_B + ((use - 1 - s) % C::NB)], (uint32_t)(((use - 1 - s) / C::NB) & 1));
+            }
+        }
+    } else if (warp == W_MMA) {
+        // ------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t idesc = idesc_f16_f32(BM, n_mma);
+            const uint32_t a_base = smem_u32(smem + C::OFF_A);
+            const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+            const uint32_t b_base = smem_u32(smem + C::OFF_B);
+            int64_t use = 0;
+            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+                const int b = (int)(sb & 1);
+                const uint32_t acc_i = tmem + 256 * b, acc_m = tmem + 256 * b + 128;
+                if (!mbar_wait(&bar[BAR_ACC_EMPTY + b], (uint32_t)(((sb >> 1) & 1) ^ 1))) { ok = false; break; }
+                tc_fence_after();
+                for (int h = 0; h < 2; ++h, ++use) {
+                    const int slot = (int)(use % C::NB);
+                    if (!mbar_wait(&bar[BAR_FULL_A + h], (uint32_t)(sb & 1)) ||
+                        !mbar_wait(&bar[BAR_FULL_B + slot], (uint32_t)((use / C::NB) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_slot = a_base + h * C::A_SLOT;
+                    const uint32_t b_slot = b_base + slot * C::B_SLOT;
+                    int planes = 1;
+                    if constexpr (F == FMT_Q6_K) {
+                        int any = 0;
+                        for (int w = 0; w < 4; ++w) any |= s_flag[8 * h + w];
+                        planes = any ? 2 : 1;
+                    }
+                    for (int pl = 0; pl < planes; ++pl) {
+                        for (int j = 0; j < 2; ++j) {
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t ad =
+                                    smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * k, 16, 1024, SWZ_128B);
+                                const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * k, 16, 1024, SWZ_128B);
+                                umma_f16(acc_i, ad, bd, idesc, (h | j | k | pl) != 0);
+                            }
+                        }
+                    }
+                    if (C::kMins && h == 0) {
+                        const uint64_t ad = smem_desc(amin, 16, 256, SWZ_32B);
+                        const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
+                        umma_f16(acc_m, ad, bd, idesc, 0);
+                    }
+                    umma_commit(&bar[BAR_EMPTY_A + h]);
+                    umma_commit(&bar[BAR_EMPTY_B + slot]);
+                }
+                if (!ok) break;
+                umma_commit(&bar[BAR_ACC_FULL + b]);
+            }
+            // all MMAs issued by this thread complete before TMEM is released
+            umma_commit(&bar[BAR_MMA_DONE]);
+            if (!mbar_wait(&bar[BAR_MMA_DONE], 0)) ok = false;
+            if (!ok) set_timeout();
+        }
+    } else if (warp < W_EPI) {
+        // ------------------------------------------------ weight unpack
+        const int uw = warp - W_UNPACK;          // 0..3
+        const int r = 32 * uw + lane;            // tile row
+        const int64_t n = n0 + r;
+        const int64_t nc = n < p.N ? n : p.N - 1;
+        const uint32_t a_base = smem_u32(smem + C::OFF_A);
+        using Raw = typename RawOf<F>::T;
+        Raw cur, nxt;
+        bool p2_dirty[2][2] = {{true, true}, {true, true}};  // Q6_K: this row's P2 may be non-zero
+        const int64_t nstage = 2 * nsb;
+        if (nstage > 0) load_raw(cur, P, (uint64_t)nc * nsb, 0);
+        for (int64_t hs = 0; hs < nstage && ok; ++hs) {
+            const int64_t sb = hs >> 1;
+            const int h = (int)(hs & 1);
+            // the next half's bytes are in flight while this one is converted
+            if (hs + 1 < nstage) load_raw(nxt, P, (uint64_t)nc * nsb + ((hs + 1) >> 1), (int)((hs + 1) & 1));
+            if (!mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((sb & 1) ^ 1))) { ok = false; break; }
+            if (h == 0 && !mbar_wait(&bar[BAR_ACC_EMPTY + (sb & 1)], (uint32_t)(((sb >> 1) & 1) ^ 1))) {
+                ok = false;
+                break;
+            }
+            const uint32_t a_slot = a_base + h * C::A_SLOT;
+            float d = 0.0f, dmin = 0.0f;
+            if constexpr (F == FMT_Q6_K) {
+                bool big[2] = {false, false};
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int v = (int)(int8_t)((cur.sc[jj] >> (8 * i)) & 0xFF);
+                        big[jj] |= (v > 64 || v < -64);
+                    }
+                const unsigned any = __ballot_sync(0xFFFFFFFFu, big[0] || big[1]);
+                if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const uint32_t a_tile = a_slot + jj * 16384;
+                    unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, cur.sc[jj], jj, big[jj],
+                              !big[jj] && p2_dirty[h][jj]);
+                    p2_dirty[h][jj] = big[jj];
+                }
+                d = __half2float(__ushort_as_half((unsigned short)cur.d));
+            } else {
+                const ScaleMin sm = unpack_scale_min(cur.hdr);
+                uint32_t qh0[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if constexpr (F == FMT_Q5_K) qh0[i] = cur.qh[i];
+                    else qh0[i] = 0u;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int cch = 2 * h + jj;  // chunk of the superblock; sub-blocks 2c, 2c+1
+                    const uint32_t scw = cch < 2 ? sm.sc_lo : sm.sc_hi;
+                    const int sc_lo = byte_of(scw, 2 * (cch & 1)), sc_hi = byte_of(scw, 2 * (cch & 1) + 1);
+                    uint32_t qsc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) qsc[i] = cur.qs[8 * jj + i];
+                    unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                }
+                if (h == 0) {
+                    // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
+                    const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+                    uint32_t mw[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
+                    sts128(amin + sw32_offset(r, 0), mw[0], mw[1], mw[2], mw[3]);
+                    sts128(amin + sw32_offset(r, 8), mw[4], mw[5], mw[6], mw[7]);
+                }
+                d = half_lo(cur.hdr.x);
+                dmin = half_hi(cur.hdr.x);
+            }
+            if (h == 0) {
+                s_d[(sb & 1) * BM + r] = d;
+                s_dmin[(sb & 1) * BM + r] = dmin;
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&bar[BAR_FULL_A + h]);
+                if (h == 0) mbar_arrive(&bar[BAR_SD_FULL + (sb & 1)]);
+            }
+            cur = nxt;
+        }
+        if (!ok && lane == 0) set_timeout();
+    } else {
+        // ------------------------------------------------ epilogue
+        const int ew = warp - W_EPI;         // 0..7
+        const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
+        const int ch = ew >> 2;              // token columns 64*ch .. +63
+        const int r = 32 * quad + lane;
+        const int64_t n = n0 + r;
+        float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 64 * ew;
+        float y[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) y[i] = 0.0f;
+        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+            const int b = (int)(sb & 1);
+            // this warp's 64 token scales d8 for the superblock
+            {
+                const int64_t tc = t0 + 64 * ch + lane;
+                s_d8[lane] = tc < t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
+                s_d8[lane + 32] = (tc + 32) < t_end ? __ldg(p.d8t + sb * p.Mp + tc + 32) : 0.0f;
+                __syncwarp();
+            }
+            if (!mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((sb >> 1) & 1)) ||
+                !mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((sb >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float dd = s_d[b * BM + r], dm = s_dmin[b * BM + r];
+            const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
+            if (64 * ch < n_mma) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t vi[16], vm[16];
+                    tmem_ld16(lane_addr + 256 * b + 64 * ch + 16 * cc, vi);
+                    if (C::kMins) tmem_ld16(lane_addr + 256 * b + 128 + 64 * ch + 16 * cc, vm);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float iv = __uint_as_float(vi[i]);
+                        float t = dd * iv;
+                        if (C::kMins) t = fmaf(-dm, __uint_as_float(vm[i]), t);
+                        y[16 * cc + i] = fmaf(s_d8[16 * cc + i], t, y[16 * cc + i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+        }
+        if (ok && n < p.N) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) {
+                const int64_t t = t0 + 64 * ch + i;
+                if (t < t_end) p.y[t * p.N + n] = y[i];
+            }
+        }
+        if (!ok && lane == 0) set_timeout();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == W_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Workspace pre-pass: Q8_K planes -> fp16 q8 image [M][K], fp16 bsums
+// [M][K/16] and d8 transposed [K/256][Mp].  One thread per 8 quants.
+__global__ void __launch_bounds__(256) act_image_kernel(const int8_t *__restrict__ qs, const int16_t *__restrict__ bs,
+                                                        const float *__restrict__ d8, int64_t M, int64_t K,
+                                                        int64_t Mp, __half *__restrict__ a16,
+                                                        __half *__restrict__ b16, float *__restrict__ d8t) {
+    griddep_wait();
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 quants
+    const int64_t groups = M * K / 8;
+    if (i < groups) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2 *>(qs) + i);
+        uint32_t o[4];
+        const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int8_t a = (int8_t)((w[k >> 1] >> (16 * (k & 1))) & 0xFF);
+            const int8_t b = (int8_t)((w[k >> 1] >> (16 * (k & 1) + 8)) & 0xFF);
+            const __half2 h = __halves2half2(__int2half_rn(a), __int2half_rn(b));
+            o[k] = *reinterpret_cast<const uint32_t *>(&h);
+        }
+        reinterpret_cast<uint4 *>(a16)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        if ((i & 1) == 0) {  // one bsum per 16 quants
+            const int64_t bi = i >> 1;
+            b16[bi] = __int2half_rn((int)bs[bi]);
+        }
+        const int64_t nsb = K / QK;
+        if ((i & 31) == 0) {  // one d8 per 256 quants
+            const int64_t blk = i >> 5;
+            const int64_t m = blk / nsb, s = blk % nsb;
+            d8t[s * Mp + m] = d8[blk];
+        }
+    }
+    griddep_launch_dependents();
+}
+
+// ---------------------------------------------------------------------------
+// host side
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+static bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct WsLayout {
+    uint64_t a16, b16, d8t, total;
+    int64_t Mp;
+};
+
+static WsLayout ws_layout(int64_t M, int64_t K) {
+    WsLayout w;
+    w.Mp = (M + 3) & ~int64_t(3);
+    w.a16 = 0;
+    w.b16 = align256((uint64_t)M * K * 2);
+    w.d8t = w.b16 + align256((uint64_t)M * (K / 16) * 2);
+    w.total = w.d8t + align256((uint64_t)(K / QK) * w.Mp * 4);
+    return w;
+}
+
+// M below which the CUDA-core token-group kernel is used instead
+constexpr int64_t GEMM_TC_MIN_M = 16;
+
+size_t gemm_workspace_bytes(int, int64_t M, int64_t, int64_t K) {
+    if (M < GEMM_TC_MIN_M) return 0;
+    return (size_t)ws_layout(M, K).total;
+}
+
+template <int F>
+static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
+                                 int64_t E, uint64_t expert_bytes, float *y, uint8_t *ws, cudaStream_t s) {
+    using Cf = Cfg<F>;
+    const WsLayout L = ws_layout(M, K);
+    __half *a16 = reinterpret_cast<__half *>(ws + L.a16);
+    __half *b16 = reinterpret_cast<__half *>(ws + L.b16);
+    float *d8t = reinterpret_cast<float *>(ws + L.d8t);
+    {
+        const int64_t groups = M * K / 8;
+        act_image_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(a.qs, a.bsums, a.d, M, K, L.Mp, a16, b16, d8t);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap ma, mb;
+    if (!make_map_2d(&ma, a16, (uint64_t)K, (uint64_t)M, (uint64_t)K * 2, 64, BT, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (!make_map_2d(&mb, b16, (uint64_t)(K / 16), (uint64_t)M, (uint64_t)(K / 16) * 2, 16, BT,
+                     CU_TENSOR_MAP_SWIZZLE_32B))
+        return cudaErrorInvalidValue;
+    static bool attr_set[4] = {false, false, false, false};
+    if (!attr_set[F]) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[F] = true;
+    }
+    GemmParams p{};
+    p.packed = static_cast<const uint8_t *>(packed);
+    p.expert_bytes = expert_bytes;
+    p.N = N;
+    p.K = K;
+    p.nsb = K / QK;
+    p.M = M;
+    p.offsets = offsets;
+    p.E = E;
+    p.d8t = d8t;
+    p.Mp = L.Mp;
+    p.y = y;
+    const int64_t w_tiles = (N + BM - 1) / BM;
+    const int64_t t_tiles = offsets ? (M + BT - 1) / BT + E : (M + BT - 1) / BT;
+    dim3 grid((unsigned)t_tiles, (unsigned)w_tiles);
+    gemm_kernel<F><<<grid, NTHREADS, Cf::SMEM, s>>>(ma, mb, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
+                           int64_t E, uint64_t expert_bytes, float *y, void *workspace, size_t workspace_bytes,
+                           cudaStream_t s) {
+    if (M < GEMM_TC_MIN_M || !workspace) return cudaErrorNotSupported;
+    if (workspace_bytes < ws_layout(M, K).total) return cudaErrorInvalidValue;
+    if (M > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX / 2) return cudaErrorNotSupported;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (f == FMT_Q4_K) return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
+    if (f == FMT_Q5_K) return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
+    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
 }
 
 int read_and_clear_status(cudaStream_t s, int *status) {
     int v = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-        return -1;
+    if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return -1;
     if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
     const int zero = 0;
-    if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
-        return -1;
+    if (cudaMemcpyToSymbolAsync(g_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s) != cudaSuccess) return -1;
     if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
     *status = v;
     return 0;

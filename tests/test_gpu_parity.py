@@ -380,3 +380,28 @@ def test_gemv_fused_layer_groups_and_edges(K):
         K.kq_gemv_fused(fmt, packs * 2, [1] * 8, 256, to_dev(x[0]))       # more than 4 matrices
     with pytest.raises(K.KQError):
         K.kq_gemv_fused(fmt, packs[:1], [1], 40960 + 256, to_dev(np.zeros(41216, np.float32)))
+
+
+# ---------------------------------------------------------------- Q6_K sub-scale range
+@pytest.mark.parametrize("sc_range", [(-128, 128), (-64, 65), (60, 70)])
+def test_gemm_q6k_full_subscale_range(K, sc_range):
+    """Real Q6_K files use signed sub-scales over the whole int8 range, beyond
+    what one exact fp16 plane holds (|sc| <= 64); the tensor-core path splits
+    those superblocks into two exact planes.  Checked against the oracle."""
+    fmt, M, N, Kdim = synth.Q6_K, 64, 256, 1024
+    rng = synth.rng_for(111, sc_range[0] + 1000)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    lo, hi = sc_range
+    disk[..., 192:208] = rng.integers(lo, hi, size=(N, Kdim // 256, 16)).astype(np.int8).view(np.uint8)
+    planes = oracle_q8k(synth.activations(M, Kdim, rng))
+    y = run_gemm(K, fmt, disk, planes, M)
+    assert_row_tol(y, oracle.gemm(fmt, disk, *planes))
+    # the GEMV on the same weights agrees too
+    one = tuple(p[:1] for p in planes)
+    g = K.kq_gemv(fmt, pack(K, fmt, disk), N, Kdim, q8k_to_dev(K, one)).cpu().numpy()
+    assert_row_tol(g, oracle.gemm(fmt, disk, *one)[0])
+
+
+def test_gemm_device_status_clean(K):
+    """After the tensor-core launches above, no bounded wait has timed out."""
+    assert K.kq_device_status() == 0
