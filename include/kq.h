@@ -2,12 +2,12 @@
  * kq.h - C ABI of libkq: K-quant (Q4_K / Q5_K / Q6_K) x Q8_K matrix products
  * on GB300 (sm_103a).
  *
- * Method source ("kq-arc" below): the page "dasLLAMA: K-quant kernel arc -
- * kq v2 integer folds, kq v3 panel-scratch tiles, chain regrain, parity
- * gates" (daScript pull request #3450): section "The pieces" (kq v2 integer
- * folds, kq v3 panel scratch), the k4 kq-v2 commit message ("Adopts
- * llama.cpp's proven K-quant kernel design for the k4 family") and the k5/k6
- * kq-v2 commit message ("Finishes what the k4 rework proved").
+ * Method source, cited as [kq-arc] below: the page "dasLLAMA: K-quant
+ * kernel arc - kq v2 integer folds, kq v3 panel-scratch tiles, chain
+ * regrain, parity gates" (daScript pull request #3450), its section
+ * "The pieces" (the kq v2 and kq v3 bullets) and two of its commit
+ * messages: the k4 kq-v2 commit (Q8_K activations and integer folds for
+ * Q4_K) and the k5/k6 kq-v2 commit (the same scheme for Q5_K and Q6_K).
  *
  * Conventions for every entry point
  *   - Pointers named as device pointers must be device (or managed) memory
@@ -30,8 +30,9 @@
  *   Q5_K, 176 B: d f16 | dmin f16 | scales[12] | qh[32] (5th bits) | qs[128]
  *   Q6_K, 210 B: ql[128] (low 4 bits) | qh[64] (high 2 bits) |
  *                scales[16] (signed int8, one per 16 weights) | d f16
- *   Q8_K activations (kq-arc, k4 kq-v2 commit: "ONE fp32 scale per
- *   256-superblock + per-16 bsums") are held as three row-major planes:
+ *   Q8_K activations ([kq-arc], k4 kq-v2 commit: a single fp32 scale for
+ *   each 256-element block and a sum for each 16 elements) are held as
+ *   three row-major planes:
  *     d     float  [M][K/256]   block scale d8
  *     qs    int8   [M][K]       quants in -127..127
  *     bsums int16  [M][K/16]    sum of each 16 consecutive quants
@@ -43,7 +44,7 @@
  *     Q6_K:      d*d8*(iacc - 32*bacc)
  *                iacc = sum_i sc_i * dot16_i(q, a8), bacc = sum_i sc_i * bs_i
  * with isum, msum, iacc, bacc formed exactly in int32 and one float fold per
- * superblock (kq-arc, "The pieces", kq v2).
+ * superblock ([kq-arc], "The pieces", kq v2 bullet).
  */
 #ifndef KQ_H
 #define KQ_H
@@ -80,8 +81,9 @@ const char *kq_strerror(int code);
 size_t kq_block_bytes(kq_format f);
 
 /*
- * Activation quantization to Q8_K (kq-arc, k4 kq-v2 commit: quantize_q8_k_into,
- * "ONE fp32 scale per 256-superblock + per-16 bsums").  Per 256-block of each
+ * Activation quantization to Q8_K ([kq-arc], k4 kq-v2 commit, which names
+ * quantize_q8_k_into: one fp32 scale per 256 activations plus per-16 sums).
+ * Per 256-block of each
  * row of x: amax = max|x|; if amax == 0 then d8 = 0 and q = 0; otherwise
  * iscale = 127/amax and q = clamp(round_half_even(x*iscale), -127, 127), both
  * steps in IEEE fp32, and d8 = amax/127.  bsums[i] sums q over 16i..16i+15.
@@ -97,8 +99,9 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
  * Always a multiple of 256, so experts stacked back to back stay aligned.
  * Returns 0 for an unknown format, N < 0 or K not a positive multiple of 256.
  *
- * Packed image (kq-arc, k4 kq-v2 commit: scale planes kept "verbatim-disk";
- * kq v3 commit: "DRAM planes keep the packed ... form"), planes back to back,
+ * Packed image ([kq-arc], k4 kq-v2 commit: the scale block is stored as it
+ * is on disk; kq v3 commit: the planes in DRAM stay bit-packed, never byte-
+ * expanded), planes back to back,
  * each starting on a 256-byte boundary, every plane row-major over
  * (row n, superblock sb):
  *   Q4_K: qs  [N][K/256][128] | hdr [N][K/256][16] (d, dmin, scales[12] verbatim)
@@ -110,9 +113,9 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
 
 /*
- * One-time repack of disk superblocks into the packed image (kq-arc, k4
- * kq-v2 commit: "transcode" and repack at load; the image dequantizes
- * bit-identically to the file).
+ * One-time repack of disk superblocks into the packed image ([kq-arc], k4
+ * kq-v2 commit: the weights are transcoded and repacked once at load, and
+ * the repacked planes dequantize bit-identically to the file).
  *   disk   device uint8 [N][K/256][block_bytes] (GGUF order), 16-byte aligned
  *   packed device, kq_repack_bytes(f, N, K) bytes, 256-byte aligned
  * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
@@ -120,9 +123,10 @@ size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
 int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s);
 
 /*
- * Decode GEMV, M = 1 (kq-arc, "The pieces", kq v2 GEMV: in-kernel unpack of
- * the packed planes; kq v3 commit: "decode is model-level DRAM-bound, so
- * plane bytes are decode time").  y[n] for n < N, as in the header note.
+ * Decode GEMV, M = 1 ([kq-arc], "The pieces", kq v2: the GEMV unpacks the
+ * packed planes in the kernel; kq v3 bullet: decode is bound by DRAM
+ * traffic, so every byte of the weight planes costs decode time).  y[n]
+ * for n < N, as in the header note.
  *   packed device image from kq_repack (256-byte aligned)
  *   a      device Q8_K planes of one row of K
  *   y      device float32 [N]
@@ -136,7 +140,7 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
  * that share one input row (q/k/v projections, gate/up).  The fp32 row x is
  * quantized to Q8_K inside the kernel, bit-identically to kq_quantize_q8k,
  * and y_m = W_m x for each matrix m, as kq_gemv computes it.  This is the
- * kernel-level form of the page's "chain regrain" (kq-arc, "The pieces":
+ * kernel-level form of the page's chain regrain ([kq-arc], "The pieces":
  * the decode chains quantize the activation image where it is consumed, in
  * whole superblocks).
  *   n_mats  1..4
@@ -161,8 +165,9 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K);
 
 /*
- * Prefill GEMM (kq-arc, "The pieces", kq v3: each weight panel unpacked once
- * per token block, "amortized xTB"): y [M][N] = the fold above for every
+ * Prefill GEMM ([kq-arc], "The pieces", kq v3: each weight panel is unpacked
+ * once per block of tokens, so the unpack cost is shared by the whole token
+ * block): y [M][N] = the fold above for every
  * token row m of a.
  *   a          device Q8_K planes of M rows
  *   y          device float32 [M][N]
@@ -176,8 +181,9 @@ int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
             int64_t M, float *y, void *workspace, size_t workspace_bytes, cudaStream_t s);
 
 /*
- * Grouped (MoE) GEMM (kq-arc, k5/k6 kq-v2 commit: MoE prefill gathers off a
- * K-form batch image, ffn_moe_prefill_grouped): rows of a are grouped by
+ * Grouped (MoE) GEMM ([kq-arc], k4 and k5/k6 kq-v2 commits: the grouped MoE
+ * prefill, ffn_moe_prefill_grouped, reads its expert rows from one Q8_K
+ * image of the token batch): rows of a are grouped by
  * expert; rows row_offsets[e] .. row_offsets[e+1]-1 use expert e's weights.
  *   packed       device, E expert images back to back, each
  *                kq_repack_bytes(f, N, K) bytes (expert e at
@@ -198,7 +204,7 @@ int kq_gemm_grouped(kq_format f, const void *packed, int64_t E, const int32_t *r
  * Test hook: the int32 partials of the fold, per (token, row, superblock),
  * computed by the same device code the GEMV runs.
  *   isum, msum  device int32 [M][N][K/256]; for Q6_K isum = iacc - 32*bacc
- *               and msum = 0 (kq-arc, k5/k6 kq-v2 commit).
+ *               and msum = 0 ([kq-arc], k5/k6 kq-v2 commit).
  */
 int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
                       int64_t M, int32_t *isum, int32_t *msum, cudaStream_t s);

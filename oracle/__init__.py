@@ -8,8 +8,8 @@ The arithmetic lives in ``kq_oracle.c`` (plain C, built with gcc,
 ``-ffp-contract=off``, no fast-math).  This module compiles it on first use
 and marshals numpy arrays through ctypes; it holds none of the method.
 
-Method source ("kq-arc"): the page "dasLLAMA: K-quant kernel arc - kq v2
-integer folds, kq v3 panel-scratch tiles, chain regrain, parity gates"
+Method source, cited as [kq-arc]: the page "dasLLAMA: K-quant kernel arc -
+kq v2 integer folds, kq v3 panel-scratch tiles, chain regrain, parity gates"
 (daScript #3450), section "The pieces" and the kq-v2 commit messages.
 """
 from __future__ import annotations

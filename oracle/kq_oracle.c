@@ -4,7 +4,7 @@
  * TEST INFRASTRUCTURE ONLY (see kq_oracle.h): loaded by the tests, the smoke
  * check and the benchmark's CPU-baseline leg, never by the product path.
  *
- * "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+ * [kq-arc] = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
  * kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
  *
  * Written for the reader, not for speed: one superblock at a time, every
@@ -52,9 +52,9 @@ static double half_bits_to_double(uint16_t h) {
 
 static uint16_t le16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
 
-/* The 12-byte 6-bit scale/min packing of Q4_K and Q5_K (kq-arc, k4 kq-v2
- * commit: "f16 d/dmin + 12B 6-bit packing"; k5/k6 commit: "the Q5_K scale
- * block IS the Q4_K scale block").  Reading (GGUF): bytes 0..3 hold the low
+/* The 12-byte 6-bit scale/min packing of Q4_K and Q5_K ([kq-arc], k4 kq-v2
+ * commit: fp16 d and dmin, then 12 bytes of 6-bit fields; the k5/k6 commit
+ * says Q5_K uses the very same scale block).  Reading (GGUF): bytes 0..3 hold the low
  * 6 bits of scales 0..3, bytes 4..7 the low 6 bits of mins 0..3; bytes 8..11
  * hold scales 4..7 (low nibble) and mins 4..7 (high nibble) as their low 4
  * bits, whose top 2 bits sit in bits 6..7 of bytes 0..3 (scales) and 4..7
@@ -78,7 +78,8 @@ int ko_decode(int fmt, const uint8_t *b, double *d, double *dmin,
          * Element 64c+l (c < 4, l < 32) is the low nibble of qs[32c+l] and
          * belongs to sub-block 2c; element 64c+32+l is its high nibble, in
          * sub-block 2c+1.  Q5_K adds bit 2c (resp. 2c+1) of qh[l] as value 16
-         * ("only the high-bit OR in the quant walk differs", k5/k6 commit). */
+         * (k5/k6 commit: Q5_K differs from Q4_K only by OR-ing in that high
+         * bit while walking the quants). */
         *d = half_bits_to_double(le16(b));
         *dmin = half_bits_to_double(le16(b + 2));
         unpack_scale_min_12(b + 4, sc, mn);
@@ -107,7 +108,8 @@ int ko_decode(int fmt, const uint8_t *b, double *d, double *dmin,
          *   128h+64+l : high nibble of ql[l]   | bits 4..5 of qh[l] << 4
          *   128h+96+l : high nibble of ql[l+32]| bits 6..7 of qh[l] << 4
          * Element e is scaled by the signed sub-scale scales[e/16]
-         * ("SIGNED per-16 sub-scales", k5/k6 commit); its weight is q-32. */
+         * (k5/k6 commit: one signed sub-scale per 16 weights); its weight
+         * is q-32. */
         const uint8_t *ql = b;
         const uint8_t *qh = b + 128;
         const int8_t *s = (const int8_t *)(b + 192);
@@ -146,8 +148,9 @@ int ko_dequant(int fmt, const uint8_t *blk, double *w) {
     return 0;
 }
 
-/* Q8_K quantization (kq-arc, k4 kq-v2 commit: "ONE fp32 scale per
- * 256-superblock + per-16 bsums").  The page gives no formula; the reading:
+/* Q8_K quantization ([kq-arc], k4 kq-v2 commit: a single fp32 scale for each
+ * 256-value block plus the sum of every 16 quants).  The page gives no
+ * formula; the reading:
  *   amax = max |x| over the block
  *   amax == 0  ->  d8 = 0, every q = 0
  *   otherwise  ->  iscale = 127/amax (fp32 division),
@@ -195,11 +198,14 @@ void ko_quantize_q8k(const float *x, int64_t M, int64_t K,
     fesetround(saved_round);
 }
 
-/* The integer fold of one superblock (kq-arc, k4 kq-v2 commit:
- * "integer sub-scale x int32-dot and bsums x mins accumulation per
- * superblock"; k5/k6 commit for Q6_K: "iacc += sc0*lo + sc1*hi;
- * bacc += sc0*Sa16lo + sc1*Sa16hi, closed as float(iacc - 32*bacc)*(d*d8)").
- * All sums are int32; the page bounds |iacc|, |32*bacc| below 2^28. */
+/* The integer fold of one superblock ([kq-arc], k4 kq-v2 commit: per
+ * superblock, the integer sub-scales multiply int32 dot products and the
+ * sub-mins multiply the activation bsums, both accumulated in int32;
+ * k5/k6 commit for Q6_K: each signed sub-scale multiplies both the int32
+ * dot of its 16 stored quants and the bsum of the same 16 activations,
+ * giving iacc and bacc, and the superblock closes as float(iacc - 32*bacc)
+ * times d*d8).  All sums are int32; the page bounds |iacc| and |32*bacc|
+ * below 2^28. */
 void ko_partials_block(int fmt, const uint8_t *blk, const int8_t *a8,
                        const int16_t *bs, int32_t *isum, int32_t *msum) {
     double d, dmin;
@@ -247,8 +253,9 @@ int ko_partials(int fmt, const uint8_t *disk, int64_t N, int64_t K,
     return 0;
 }
 
-/* One output: the fold closed once per superblock (kq-arc, "The pieces":
- * "one float fold per superblock"), d*d8*isum - dmin*d8*msum, summed over
+/* One output: the fold closed once per superblock ([kq-arc], "The pieces",
+ * kq v2 bullet: a single float fold per superblock), d*d8*isum -
+ * dmin*d8*msum, summed over
  * the superblocks of the row.  Evaluated in double: d (fp16) times d8 (fp32)
  * is exact in double, so this is the quantized product to ~1e-16. */
 double ko_dot(int fmt, const uint8_t *row, int64_t nsb, const float *d8,

@@ -6,19 +6,19 @@
  * the test suite, the smoke check and the benchmark's CPU-baseline leg may
  * load it.  The product path never calls it and has no CPU fallback.
  *
- * Source of the method ("kq-arc" below) is the page
- *   "dasLLAMA: K-quant kernel arc - kq v2 integer folds, kq v3 panel-scratch
- *    tiles, chain regrain, parity gates" (daScript pull request #3450).
- * Sections cited: "The pieces" (kq v2 bullet), the k4 kq-v2 commit message
- * ("Adopts llama.cpp's proven K-quant kernel design for the k4 family") and
- * the k5/k6 kq-v2 commit message ("Finishes what the k4 rework proved").
+ * Source of the method, cited as [kq-arc]: the page "dasLLAMA: K-quant
+ * kernel arc - kq v2 integer folds, kq v3 panel-scratch tiles, chain
+ * regrain, parity gates" (daScript pull request #3450): its section
+ * "The pieces" (kq v2 bullet) and its k4 and k5/k6 kq-v2 commit messages.
  *
- * Formats.  The page names the blocks (Q4_K, Q5_K, Q6_K, Q8_K), their
- * 256-weight superblocks, the "f16 d/dmin + 12B 6-bit packing" scale block
- * of Q4_K/Q5_K, the "SIGNED per-16 sub-scales" and fp16 d of Q6_K, and the
- * Q8_K activation form "ONE fp32 scale per 256-superblock + per-16 bsums".
- * It prints no bit layout; this oracle reads the layouts as the public GGUF
- * block formats (byte order given in kq_oracle.c beside each decoder).
+ * Formats.  The page names the blocks (Q4_K, Q5_K, Q6_K, Q8_K) and their
+ * 256-weight superblocks; it says the Q4_K/Q5_K scale block is an fp16 d
+ * and dmin followed by 12 bytes of packed 6-bit sub-scales and sub-mins,
+ * that Q6_K carries signed 8-bit sub-scales (one per 16 weights) and an
+ * fp16 d, and that a Q8_K activation block has one fp32 scale per 256
+ * values plus a sum per 16.  It prints no bit layout; this oracle reads
+ * the layouts as the public GGUF block formats (byte order given in
+ * kq_oracle.c beside each decoder).
  *
  * All pointers are host pointers.  Sizes are 64-bit.
  */

@@ -2,7 +2,7 @@
 // the packed-image layout, streaming loads, and the per-lane unpack + integer
 // fold of one 256-weight superblock for each K-quant format.
 //
-// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// [kq-arc] = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
 // kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
 //
 // Lane geometry (GEMV, small-M and partials kernels).  Four consecutive lanes
@@ -108,9 +108,9 @@ __device__ __forceinline__ float half_hi(uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
-// The 12-byte six-bit scale/min block of Q4_K and Q5_K (kq-arc, k4 kq-v2
-// commit: "f16 d/dmin + 12B 6-bit packing"; k5/k6 commit: the Q5_K scale
-// block is the Q4_K one).  With y, z, w = scale bytes 0..3, 4..7, 8..11
+// The 12-byte six-bit scale/min block of Q4_K and Q5_K ([kq-arc], k4 kq-v2
+// commit: fp16 d and dmin, then 12 bytes of packed 6-bit fields; k5/k6
+// commit: the Q5_K scale block is the Q4_K one).  With y, z, w = scale bytes 0..3, 4..7, 8..11
 // (little-endian words), byte j of the results is:
 //   sc_lo: sub-scale j   (j < 4) = low 6 bits of scale byte j
 //   m_lo : sub-min j     (j < 4) = low 6 bits of scale byte 4+j
@@ -252,8 +252,8 @@ __device__ __forceinline__ void decode_lane(const WQ4 &w, int c, LaneQ &L) {
     L.dmin = half_hi(w.hdr.x);
 }
 
-// Q5_K: the Q4_K walk plus the fifth bit (kq-arc, k5/k6 commit: "only the
-// high-bit OR in the quant walk differs").  Element 64k+l takes bit 2k of
+// Q5_K: the Q4_K walk plus the fifth bit ([kq-arc], k5/k6 commit: Q5_K
+// differs from Q4_K only by OR-ing that high bit into each quant).  Element 64k+l takes bit 2k of
 // qh[l], element 64k+32+l bit 2k+1; this lane's qh bytes are l in [o, o+16).
 __device__ __forceinline__ uint4 q5_bit(uint4 qh, int bit) {
     // move bit `bit` of every byte to bit 4
@@ -281,7 +281,7 @@ __device__ __forceinline__ void decode_lane(const WQ5 &w, int c, LaneQ &L) {
     L.g[3] = or4(L.g[3], q5_bit(w.qh, 2 * k + 5));
 }
 
-// Q6_K (kq-arc, k5/k6 commit: "SIGNED per-16 sub-scales"): group t of lane
+// Q6_K ([kq-arc], k5/k6 commit: signed sub-scales, one per 16 weights): group t of lane
 // (h, p) holds elements 128h + 32t + 16p .. +15 of sub-block 8h + 2t + p.
 __device__ __forceinline__ void decode_lane(const WQ6 &w, int c, LaneQ &L) {
     const int h = c >> 1, p = c & 1;
@@ -308,9 +308,9 @@ __device__ __forceinline__ void decode_lane(const WQ6 &w, int c, LaneQ &L) {
 // The lane's integer partials against one token's Q8_K superblock.
 //   a8: the token's 256 quants of this superblock, bs: its 16 bsums.
 // Q4_K/Q5_K: isum_lane = sum_g sc_g * dot16_g, msum_lane = m0*(bs_4c+bs_4c+1)
-//            + m1*(bs_4c+2 + bs_4c+3)   (kq-arc, k4 kq-v2 commit)
+//            + m1*(bs_4c+2 + bs_4c+3)   ([kq-arc], k4 kq-v2 commit)
 // Q6_K     : isum_lane = sum_t sc_t * dot16_t - 32 * sum_t sc_t * bs_(8h+2t+p),
-//            msum_lane = 0                (kq-arc, k5/k6 commit)
+//            msum_lane = 0                ([kq-arc], k5/k6 commit)
 template <int F, bool SMEM = false>
 __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, const int16_t *bs, int c,
                                               int &isum, int &msum) {
@@ -346,8 +346,8 @@ __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, 
     }
 }
 
-// Q8_K quantization of one 256-block by one warp (kq-arc, k4 kq-v2 commit:
-// quantize_q8_k_into, "ONE fp32 scale per 256-superblock + per-16 bsums").
+// Q8_K quantization of one 256-block by one warp ([kq-arc], k4 kq-v2 commit,
+// quantize_q8_k_into: one fp32 scale per 256 values and a sum per 16).
 // Lane l owns elements 8l .. 8l+7.  amax = max|x| (a max over the bit
 // patterns of |x|, which order like the values for finite floats);
 // iscale = 127/amax and q = round_half_even(x*iscale), clamped to +-127,

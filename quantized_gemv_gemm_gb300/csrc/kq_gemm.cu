@@ -1,6 +1,6 @@
 // kq_gemm.cu - tensor-core prefill GEMM (tcgen05) and its MoE grouped form.
 //
-// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// [kq-arc] = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
 // kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
 //
 // The contraction the page folds in int32 runs on the fp16 tensor pipe with
@@ -11,7 +11,7 @@
 //   - each block owns 128 weight rows x up to 128 tokens; per superblock its
 //     unpack warps expand the packed weights once into shared memory as fp16
 //     w' = sc*q with the sub-scale folded in (Q4_K <= 945, Q5_K <= 1953:
-//     exact), the kq v3 "panel scratch" unpacked once per token block;
+//     exact): the kq v3 panel scratch, unpacked once per token block;
 //     Q6_K's w' = sc*(q-32) is exact for |sc| <= 64, and when a tile holds a
 //     larger sub-scale the weight is split into two exact planes,
 //     sc*(v - (v&1)) (even, |.| <= 4096) and sc*(v&1), both multiplied into
@@ -20,7 +20,7 @@
 //     iacc - 32*bacc for Q6_K) in fp32 TMEM; for Q4_K/Q5_K a second K=16 MMA
 //     of the sub-mins (duplicated per 16) against the bsums gives msum;
 //   - the epilogue folds once per superblock, y += d8*(d*I - dmin*msum), in
-//     fp32 registers (kq-arc, "The pieces": one float fold per superblock).
+//     fp32 registers ([kq-arc], "The pieces": one float fold per superblock).
 // The fp32 accumulator is exact while every partial sum stays below 2^24 in
 // magnitude (true for realistic activations; at adversarial extremes the
 // sum is rounded like the fold's own float(isum)).

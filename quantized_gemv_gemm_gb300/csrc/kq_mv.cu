@@ -2,19 +2,19 @@
 // small-token-count product (a group of up to 8 tokens per pass) and its MoE
 // grouped form, plus the two test hooks (int32 partials, packed decode).
 //
-// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// [kq-arc] = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
 // kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
 //
-// The GEMV streams the packed planes once from HBM (kq-arc, kq v3 commit:
-// "decode is model-level DRAM-bound, so plane bytes are decode time"; no
-// byte-expanded planes in DRAM).  Work split: a 256-thread block = 8 warps =
+// The GEMV streams the packed planes once from HBM ([kq-arc], kq v3 commit:
+// decode time is set by DRAM traffic, so the planes stay bit-packed and no
+// byte-expanded copy of them exists in DRAM).  Work split: a 256-thread block = 8 warps =
 // WR row groups x WK superblock slices (WR * WK = 8).  A warp owns 8 rows
 // (one per quad, see kq_device.cuh) and walks its slice of superblocks,
 // loading the next superblock's weights before folding the current one.
 // Per superblock the quad's lanes add their int32 partials with two xor
 // shuffles and fold once in fp32: acc += d*d8*isum - dmin*d8*msum (Q6_K:
-// acc += d*d8*(iacc - 32*bacc)) (kq-arc, "The pieces": "one float fold per
-// superblock").  Slices of one row are summed through shared memory.
+// acc += d*d8*(iacc - 32*bacc)) ([kq-arc], "The pieces": a single float fold
+// per superblock).  Slices of one row are summed through shared memory.
 #include "kq_internal.h"
 
 #include <algorithm>

@@ -1,6 +1,6 @@
 // kq_quant.cu - Q8_K activation quantization and the one-time weight repack.
 //
-// "kq-arc" = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
+// [kq-arc] = the page "dasLLAMA: K-quant kernel arc - kq v2 integer folds,
 // kq v3 panel-scratch tiles, chain regrain, parity gates" (daScript #3450).
 #include "kq_internal.h"
 
@@ -43,7 +43,7 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8
 }
 
 // ---------------------------------------------------------------------------
-// Repack (kq-arc, k4 kq-v2 commit: the transcode keeps the disk scale block
+// Repack ([kq-arc], k4 kq-v2 commit: the transcode keeps the disk scale block
 // verbatim and the plane dequant is bit-identical to the disk dequant).
 // One thread per superblock moves each field of the GGUF-order block into
 // its plane; no value is changed.  The disk block is read as 16-bit words
