@@ -100,15 +100,21 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
  * Returns 0 for an unknown format, N < 0 or K not a positive multiple of 256.
  *
  * Packed image ([kq-arc], k4 kq-v2 commit: the scale block is stored as it
- * is on disk; kq v3 commit: the planes in DRAM stay bit-packed, never byte-
- * expanded), planes back to back,
- * each starting on a 256-byte boundary, every plane row-major over
- * (row n, superblock sb):
- *   Q4_K: qs  [N][K/256][128] | hdr [N][K/256][16] (d, dmin, scales[12] verbatim)
- *   Q5_K: qs  [N][K/256][128] | qh [N][K/256][32] | hdr [N][K/256][16]
- *   Q6_K: ql  [N][K/256][128] | qh [N][K/256][64] | sc [N][K/256][16] | d [N][K/256] f16
+ * is on disk and the rows are repacked into interleaved groups; kq v3
+ * commit: the planes in DRAM stay bit-packed, never byte-expanded).  Rows
+ * are taken in groups of 16 (the last group padded with zero rows).  Each
+ * plane holds, for every (row group g, superblock sb) in the order
+ * g * K/256 + sb, one contiguous chunk with that plane's bytes of the 16
+ * rows' superblock sb; planes start on 256-byte boundaries:
+ *   Q4_K: qs  (2048 B chunks) | hdr (256 B: d, dmin, scales[12] per row)
+ *   Q5_K: qs  (2048) | qh (512) | hdr (256)
+ *   Q6_K: ql  (2048) | qh (1024) | sc (256) | d (32, fp16 per row)
+ * Inside a chunk, row r's 16-byte piece i (disk bytes 16i .. 16i+15 of that
+ * field) sits at: qs/ql 512*(i%4) + 16*(r + 16*(i/4)); Q6_K qh
+ * 512*(i%2) + 16*(r + 16*(i/2)); Q5_K qh 256*i + 16*r; hdr/sc 16*r; d 2*r.
  * Every byte of the disk superblock is kept once, so the image is the disk
- * size plus at most 3 x 255 bytes of plane padding.
+ * size of the rows padded to a multiple of 16, plus at most 3 x 255 bytes
+ * of plane padding.
  */
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
 

@@ -188,9 +188,9 @@ unsigned kq_set_launch_flags(unsigned flags) {
 unsigned kq_get_launch_flags(void) { return launch_flags(); }
 
 int kq_device_status(cudaStream_t s) {
-    int st = 0;
-    if (read_and_clear_status(s, &st)) return KQ_ERR_LAUNCH;
-    return st ? KQ_ERR_TIMEOUT : KQ_OK;
+    int st = 0, sg = 0;
+    if (read_and_clear_status(s, &st) || read_and_clear_gemv_status(s, &sg)) return KQ_ERR_LAUNCH;
+    return (st || sg) ? KQ_ERR_TIMEOUT : KQ_OK;
 }
 
 }  // extern "C"

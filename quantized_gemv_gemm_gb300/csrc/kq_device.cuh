@@ -33,7 +33,30 @@ __host__ __device__ inline int block_bytes(int f) {
 
 __host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
 
-// Bytes per superblock of each plane of the packed image.
+// ---------------------------------------------------------------------------
+// The packed image ("grp16"; the row interleave of [kq-arc]'s grp<mr>
+// repack, with mr = 16 rows).  Rows are taken in groups of 16 (the last one
+// padded with zero rows); each plane holds, for every (row group g,
+// superblock sb) in the order g * nsb + sb, one chunk with that plane's
+// bytes of the 16 rows' superblock sb.  Inside a chunk (r = row in the
+// group, h = half of the superblock, lane = r + 16h):
+//   qs / ql  128 B per row:  piece k (bytes 64h+16k .. +15) of row r at
+//                            512k + 16*lane                  chunk 2048 B
+//   hdr      Q4_K/Q5_K d, dmin, scales[12] of row r at 16r     256 B
+//   qh (Q5)  32 B per row:   piece j (bytes 16j .. +15) at 256j + 16r      512 B
+//   qh (Q6)  64 B per row:   piece j of half h (bytes 32h+16j ..) at
+//                            512j + 16*lane                 1024 B
+//   sc (Q6)  16 signed scales of row r at 16r                 256 B
+//   d  (Q6)  fp16 d of row r at 2r                              32 B
+// So every chunk is contiguous and 16-byte aligned (one bulk copy), a warp
+// serving 16 rows x one superblock reads consecutive 16-byte pieces, and a
+// row's next superblock is one chunk further on in every plane.  Every disk
+// byte is kept as it is; only its place changes.
+constexpr int GROUP_ROWS = 16;
+
+__host__ __device__ inline int64_t row_groups(int64_t N) { return (N + GROUP_ROWS - 1) / GROUP_ROWS; }
+
+// Bytes per row and superblock of each plane (chunk = 16 x this).
 __host__ __device__ inline void plane_unit_bytes(int f, int u[4]) {
     u[0] = 128; u[1] = 0; u[2] = 0; u[3] = 0;
     if (f == FMT_Q4_K) { u[1] = 16; }
@@ -45,7 +68,7 @@ __host__ __device__ inline void plane_unit_bytes(int f, int u[4]) {
 __host__ __device__ inline void plane_offsets(int f, int64_t N, int64_t nsb, uint64_t off[5]) {
     int u[4];
     plane_unit_bytes(f, u);
-    const uint64_t units = (uint64_t)N * (uint64_t)nsb;
+    const uint64_t units = (uint64_t)row_groups(N) * GROUP_ROWS * (uint64_t)nsb;
     off[0] = 0;
     for (int i = 0; i < 4; ++i) off[i + 1] = off[i] + align256(units * (uint64_t)u[i]);
 }
@@ -60,6 +83,21 @@ __host__ __device__ inline Planes make_planes(int f, const void *base, int64_t N
     plane_offsets(f, N, nsb, off);
     const uint8_t *b = static_cast<const uint8_t *>(base);
     return Planes{b + off[0], b + off[1], b + off[2], b + off[3]};
+}
+
+// Chunk index of (row n, superblock sb): the chunk of n's row group at sb.
+__host__ __device__ inline uint64_t chunk_of(int64_t n, int64_t sb, int64_t nsb) {
+    return (uint64_t)(n / GROUP_ROWS) * (uint64_t)nsb + (uint64_t)sb;
+}
+
+// Byte offset, inside a chunk, of the 16-byte piece holding row r's bytes
+// [16i, 16i+16) of a plane with `ub` bytes per row (ub = 128, 64, 32, 16);
+// the d plane (ub = 2) is at 2r.
+__host__ __device__ inline uint32_t piece_offset(int ub, int r, int i) {
+    if (ub == 128) return 512u * (i & 3) + 16u * (r + 16 * (i >> 2));
+    if (ub == 64) return 512u * (i & 1) + 16u * (r + 16 * (i >> 1));
+    if (ub == 32) return 256u * i + 16u * r;
+    return 16u * r;  // ub == 16
 }
 
 // ---------------------------------------------------------------------------
@@ -143,76 +181,75 @@ template <> struct WRegs<FMT_Q4_K> { using T = WQ4; };
 template <> struct WRegs<FMT_Q5_K> { using T = WQ5; };
 template <> struct WRegs<FMT_Q6_K> { using T = WQ6; };
 
-// u = n * nsb + sb, the superblock's index in the row-major planes.
-__device__ __forceinline__ void load_w(WQ4 &w, const Planes &P, uint64_t u, int c) {
-    const uint8_t *qs = P.p0 + u * 128;
-    w.qa = ld_stream(qs + 16 * c);
-    w.qb = ld_stream(qs + 64 + 16 * c);
-    w.hdr = ld_keep(P.p1 + u * 16);
-}
-__device__ __forceinline__ void load_w(WQ5 &w, const Planes &P, uint64_t u, int c) {
-    const uint8_t *qs = P.p0 + u * 128;
-    w.qa = ld_stream(qs + 16 * c);
-    w.qb = ld_stream(qs + 64 + 16 * c);
-    w.qh = ld_stream(P.p1 + u * 32 + 16 * (c & 1));
-    w.hdr = ld_keep(P.p2 + u * 16);
-}
-__device__ __forceinline__ void load_w(WQ6 &w, const Planes &P, uint64_t u, int c) {
-    const int h = c >> 1, p = c & 1;
-    const uint8_t *ql = P.p0 + u * 128 + 64 * h + 16 * p;
-    w.la = ld_stream(ql);
-    w.lb = ld_stream(ql + 32);
-    w.qh = ld_stream(P.p1 + u * 64 + 32 * h + 16 * p);
-    w.sc = ld_keep(P.p2 + u * 16);
-    w.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3) + u);
-}
-
-// Per-lane plane pointers at one superblock of a row; the row's next
-// superblocks follow at fixed strides (128 / 16 / 32 / 64 / 2 bytes), so a
-// lane walks a row by adding i * stride (load_at).
+// Per-lane plane pointers at (row n, superblock sb) for the quad geometry
+// above; the row's next superblock is one chunk further on in every plane
+// (chunk bytes 2048 / 256 / 512 / 1024 / 32), so a lane walks a row by
+// adding i chunks (load_at).
 struct LanePtr {
     const uint8_t *p0, *p1, *p2, *p3;
 };
 
 template <int F>
-__device__ __forceinline__ LanePtr lane_ptr(const Planes &P, uint64_t u, int c) {
-    LanePtr r;
-    if constexpr (F == FMT_Q4_K) {
-        r.p0 = P.p0 + u * 128 + 16 * c;
-        r.p1 = P.p1 + u * 16;
-        r.p2 = r.p3 = nullptr;
-    } else if constexpr (F == FMT_Q5_K) {
-        r.p0 = P.p0 + u * 128 + 16 * c;
-        r.p1 = P.p1 + u * 32 + 16 * (c & 1);
-        r.p2 = P.p2 + u * 16;
-        r.p3 = nullptr;
+__device__ __forceinline__ LanePtr lane_ptr(const Planes &P, int64_t n, int64_t sb, int64_t nsb, int c) {
+    const uint64_t ch = chunk_of(n, sb, nsb);
+    const int r = (int)(n % GROUP_ROWS);
+    LanePtr q;
+    if constexpr (F == FMT_Q4_K || F == FMT_Q5_K) {
+        // qs bytes [16c, 16c+16) = piece c; [64+16c, ..) = piece 4 + c
+        q.p0 = P.p0 + ch * 2048 + piece_offset(128, r, c);
+        if constexpr (F == FMT_Q4_K) {
+            q.p1 = P.p1 + ch * 256 + 16 * r;
+            q.p2 = q.p3 = nullptr;
+        } else {
+            q.p1 = P.p1 + ch * 512 + piece_offset(32, r, c & 1);
+            q.p2 = P.p2 + ch * 256 + 16 * r;
+            q.p3 = nullptr;
+        }
     } else {
-        const int h = c >> 1, q = c & 1;
-        r.p0 = P.p0 + u * 128 + 64 * h + 16 * q;
-        r.p1 = P.p1 + u * 64 + 32 * h + 16 * q;
-        r.p2 = P.p2 + u * 16;
-        r.p3 = P.p3 + u * 2;
+        const int h = c >> 1, p = c & 1;
+        // ql bytes [64h+16p, ..) = piece 4h + p; [64h+32+16p, ..) = piece 4h + 2 + p
+        q.p0 = P.p0 + ch * 2048 + piece_offset(128, r, 4 * h + p);
+        q.p1 = P.p1 + ch * 1024 + piece_offset(64, r, 2 * h + p);
+        q.p2 = P.p2 + ch * 256 + 16 * r;
+        q.p3 = P.p3 + ch * 32 + 2 * r;
     }
-    return r;
+    return q;
 }
 
+// piece 4 + c of qs sits 16 rows further on: +256 bytes; piece 2 + p of ql: +1024
 __device__ __forceinline__ void load_at(WQ4 &w, const LanePtr &lp, int64_t i) {
-    w.qa = ld_stream(lp.p0 + i * 128);
-    w.qb = ld_stream(lp.p0 + i * 128 + 64);
-    w.hdr = ld_keep(lp.p1 + i * 16);
+    w.qa = ld_stream(lp.p0 + i * 2048);
+    w.qb = ld_stream(lp.p0 + i * 2048 + 256);
+    w.hdr = ld_keep(lp.p1 + i * 256);
 }
 __device__ __forceinline__ void load_at(WQ5 &w, const LanePtr &lp, int64_t i) {
-    w.qa = ld_stream(lp.p0 + i * 128);
-    w.qb = ld_stream(lp.p0 + i * 128 + 64);
-    w.qh = ld_stream(lp.p1 + i * 32);
-    w.hdr = ld_keep(lp.p2 + i * 16);
+    w.qa = ld_stream(lp.p0 + i * 2048);
+    w.qb = ld_stream(lp.p0 + i * 2048 + 256);
+    w.qh = ld_stream(lp.p1 + i * 512);
+    w.hdr = ld_keep(lp.p2 + i * 256);
 }
 __device__ __forceinline__ void load_at(WQ6 &w, const LanePtr &lp, int64_t i) {
-    w.la = ld_stream(lp.p0 + i * 128);
-    w.lb = ld_stream(lp.p0 + i * 128 + 32);
-    w.qh = ld_stream(lp.p1 + i * 64);
-    w.sc = ld_keep(lp.p2 + i * 16);
-    w.d = __ldg(reinterpret_cast<const unsigned short *>(lp.p3) + i);
+    w.la = ld_stream(lp.p0 + i * 2048);
+    w.lb = ld_stream(lp.p0 + i * 2048 + 1024);
+    w.qh = ld_stream(lp.p1 + i * 1024);
+    w.sc = ld_keep(lp.p2 + i * 256);
+    w.d = __ldg(reinterpret_cast<const unsigned short *>(lp.p3 + i * 32));
+}
+
+// one superblock of row n
+template <typename W>
+__device__ __forceinline__ void load_w(W &w, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int c);
+template <>
+__device__ __forceinline__ void load_w(WQ4 &w, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int c) {
+    load_at(w, lane_ptr<FMT_Q4_K>(P, n, sb, nsb, c), 0);
+}
+template <>
+__device__ __forceinline__ void load_w(WQ5 &w, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int c) {
+    load_at(w, lane_ptr<FMT_Q5_K>(P, n, sb, nsb, c), 0);
+}
+template <>
+__device__ __forceinline__ void load_w(WQ6 &w, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int c) {
+    load_at(w, lane_ptr<FMT_Q6_K>(P, n, sb, nsb, c), 0);
 }
 
 // ---------------------------------------------------------------------------
@@ -348,16 +385,14 @@ __device__ __forceinline__ void lane_partials(const LaneQ &L, const int8_t *a8, 
 
 // Q8_K quantization of one 256-block by one warp ([kq-arc], k4 kq-v2 commit,
 // quantize_q8_k_into: one fp32 scale per 256 values and a sum per 16).
-// Lane l owns elements 8l .. 8l+7.  amax = max|x| (a max over the bit
-// patterns of |x|, which order like the values for finite floats);
-// iscale = 127/amax and q = round_half_even(x*iscale), clamped to +-127,
-// both single IEEE fp32 operations; d8 = amax/127 (0 when amax = 0, with
-// every q = 0); bsum i = sum of q over 16i .. 16i+15 (lanes 2i and 2i+1).
-// xb: the block's 256 floats (16-byte aligned); qb / bb / db: its 256
-// quants, 16 bsums and scale, in global or shared memory.
-__device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, int8_t *qb, int16_t *bb, float *db) {
-    const float4 v0 = *reinterpret_cast<const float4 *>(xb + 8 * lane);
-    const float4 v1 = *reinterpret_cast<const float4 *>(xb + 8 * lane + 4);
+// Lane l owns elements 8l .. 8l+7, given in v0 (8l .. 8l+3) and v1.
+// amax = max|x| (a max over the bit patterns of |x|, which order like the
+// values for finite floats); iscale = 127/amax and q = round_half_even(
+// x*iscale), clamped to +-127, both single IEEE fp32 operations; d8 =
+// amax/127 (0 when amax = 0, with every q = 0).  Returns the lane's eight
+// quants packed in two words (element 8l in the low byte of .x) and sets
+// part = the sum of the lane's eight quants, d8 = the block scale.
+__device__ __forceinline__ uint2 q8k_lane(float4 v0, float4 v1, int &part, float &d8) {
     const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     float ax = 0.0f;
 #pragma unroll
@@ -381,11 +416,48 @@ __device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, i
         lo |= (static_cast<uint32_t>(q[i]) & 0xFFu) << (8 * i);
         hi |= (static_cast<uint32_t>(q[i + 4]) & 0xFFu) << (8 * i);
     }
-    *reinterpret_cast<uint2 *>(qb + 8 * lane) = make_uint2(lo, hi);
-    int part = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    part = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    d8 = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+    return make_uint2(lo, hi);
+}
+
+// The Q8_K planes of one block: xb its 256 floats (16-byte aligned); qb /
+// bb / db its 256 quants, 16 bsums (bsum i = sum of q over 16i .. 16i+15,
+// lanes 2i and 2i+1) and scale, in global or shared memory.
+__device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, int8_t *qb, int16_t *bb, float *db) {
+    const float4 v0 = *reinterpret_cast<const float4 *>(xb + 8 * lane);
+    const float4 v1 = *reinterpret_cast<const float4 *>(xb + 8 * lane + 4);
+    int part;
+    float d8;
+    const uint2 w = q8k_lane(v0, v1, part, d8);
+    *reinterpret_cast<uint2 *>(qb + 8 * lane) = w;
     part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
     if ((lane & 1) == 0) bb[lane >> 1] = static_cast<int16_t>(part);
-    if (lane == 0) *db = (amax == 0.0f) ? 0.0f : __fdiv_rn(amax, 127.0f);
+    if (lane == 0) *db = d8;
+}
+
+// ---------------------------------------------------------------------------
+// Decode-GEMV staging of one activation superblock in shared memory: the
+// 256 quants, the block scale, and the sums the fold needs -- for Q4_K and
+// Q5_K the int32 sum of each 32-element sub-block (bs_2j + bs_2j+1, the
+// factor of sub-min j), for Q6_K the 16 int16 bsums.  Both forms take 32
+// bytes per superblock.
+
+// From fp32 values (the fused quantize): v0 / v1 as for q8k_lane.
+template <bool PAIRS>
+__device__ __forceinline__ void stage_block_from_x(float4 v0, float4 v1, int lane, int8_t *qb, void *sb, float *db) {
+    int part;
+    float d8;
+    const uint2 w = q8k_lane(v0, v1, part, d8);
+    *reinterpret_cast<uint2 *>(qb + 8 * lane) = w;
+    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);        // 16-element sums
+    if constexpr (PAIRS) {
+        part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);    // 32-element sums
+        if ((lane & 3) == 0) static_cast<int *>(sb)[lane >> 2] = part;
+    } else {
+        if ((lane & 1) == 0) static_cast<int16_t *>(sb)[lane >> 1] = static_cast<int16_t>(part);
+    }
+    if (lane == 0) *db = d8;
 }
 
 // Bulk prefetch of [p, p + bytes) from HBM into L2 by the TMA engine
@@ -402,6 +474,64 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint64_t bytes) 
         bytes -= n;
     }
 }
+
+// Asynchronous 16-byte copies global -> shared (cp.async, L2 only), in
+// commit groups; cp_async_wait<N>() returns once at most N of this thread's
+// groups are still in flight.  Both addresses must be 16-byte aligned.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// the same copy, issued only where pred != 0 (predicated, no branch)
+__device__ __forceinline__ void cp_async16_if(uint32_t dst_smem, const void *src, uint32_t pred) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(dst_smem),
+        "l"(src), "r"(pred)
+        : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// The same with immediate byte offsets added to both addresses in the
+// instruction itself (no address arithmetic in the caller).
+template <int DST_OFF, int SRC_OFF>
+__device__ __forceinline__ void cp_async16_if_off(uint32_t dst_smem, const void *src, uint32_t pred) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0+%3], [%1+%4], 16;\n}\n" ::"r"(
+            dst_smem),
+        "l"(src), "r"(pred), "n"(DST_OFF), "n"(SRC_OFF)
+        : "memory");
+}
+
+// Shared-memory loads at 32-bit shared-window addresses (OFF: an immediate
+// byte offset folded into the instruction).
+template <int OFF>
+__device__ __forceinline__ uint4 lds128o(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4+%5];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a), "n"(OFF));
+    return v;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
 
 // Programmatic dependent launch.  griddep_wait() blocks until the grids this
 // one depends on have completed and their memory is visible (a no-op when

@@ -218,31 +218,37 @@ __device__ __forceinline__ void ld16w(uint32_t *dst, const uint8_t *src) {
     const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src));
     dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
 }
-// u = packed superblock index, h = half
-__device__ __forceinline__ void load_raw(RawQ4 &r, const Planes &P, uint64_t u, int h) {
-    const uint8_t *q = P.p0 + u * 128 + 64 * h;
+// half h of row n's superblock sb, from the grp16 image (kq_device.cuh)
+__device__ __forceinline__ void load_raw(RawQ4 &r, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int h) {
+    const uint64_t ch = chunk_of(n, sb, nsb);
+    const int rr = (int)(n % GROUP_ROWS);
+    const uint8_t *q = P.p0 + ch * 2048 + 16 * (rr + 16 * h);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 16 * i);
-    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p1 + u * 16));
+    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 512 * i);
+    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p1 + ch * 256 + 16 * rr));
 }
-__device__ __forceinline__ void load_raw(RawQ5 &r, const Planes &P, uint64_t u, int h) {
-    const uint8_t *q = P.p0 + u * 128 + 64 * h;
+__device__ __forceinline__ void load_raw(RawQ5 &r, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int h) {
+    const uint64_t ch = chunk_of(n, sb, nsb);
+    const int rr = (int)(n % GROUP_ROWS);
+    const uint8_t *q = P.p0 + ch * 2048 + 16 * (rr + 16 * h);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 16 * i);
-    ld16w(r.qh, P.p1 + u * 32);
-    ld16w(r.qh + 4, P.p1 + u * 32 + 16);
-    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p2 + u * 16));
+    for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 512 * i);
+    ld16w(r.qh, P.p1 + ch * 512 + 16 * rr);
+    ld16w(r.qh + 4, P.p1 + ch * 512 + 256 + 16 * rr);
+    r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p2 + ch * 256 + 16 * rr));
 }
-__device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, uint64_t u, int h) {
-    const uint8_t *l = P.p0 + u * 128 + 64 * h;
+__device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int h) {
+    const uint64_t ch = chunk_of(n, sb, nsb);
+    const int rr = (int)(n % GROUP_ROWS);
+    const uint8_t *l = P.p0 + ch * 2048 + 16 * (rr + 16 * h);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ld16w(r.ql + 4 * i, l + 16 * i);
-    ld16w(r.qh, P.p1 + u * 64 + 32 * h);
-    ld16w(r.qh + 4, P.p1 + u * 64 + 32 * h + 16);
-    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(P.p2 + u * 16 + 8 * h));
+    for (int i = 0; i < 4; ++i) ld16w(r.ql + 4 * i, l + 512 * i);
+    ld16w(r.qh, P.p1 + ch * 1024 + 16 * (rr + 16 * h));
+    ld16w(r.qh + 4, P.p1 + ch * 1024 + 512 + 16 * (rr + 16 * h));
+    const uint2 sc = __ldg(reinterpret_cast<const uint2 *>(P.p2 + ch * 256 + 16 * rr + 8 * h));
     r.sc[0] = sc.x;
     r.sc[1] = sc.y;
-    r.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3) + u);
+    r.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3 + ch * 32) + rr);
 }
 
 // ---------------------------------------------------------------------------
@@ -357,7 +363,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // streaming them into L2 for the unpack warps
             int u[4];
             plane_unit_bytes(F, u);
-            const int64_t r1 = (n0 + BM < p.N ? n0 + BM : p.N);
+            const int64_t rows = row_groups(p.N) * GROUP_ROWS;
+            const int64_t r1 = (n0 + BM < rows ? n0 + BM : rows);
             const uint8_t *base[4] = {P.p0, P.p1, P.p2, P.p3};
             for (int q = 0; q < 4; ++q)
                 if (u[q] && r1 > n0)
@@ -450,12 +457,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         Raw cur, nxt;
         bool p2_dirty[2][2] = {{true, true}, {true, true}};  // Q6_K: this row's P2 may be non-zero
         const int64_t nstage = 2 * nsb;
-        if (nstage > 0) load_raw(cur, P, (uint64_t)nc * nsb, 0);
+        if (nstage > 0) load_raw(cur, P, nc, 0, nsb, 0);
         for (int64_t hs = 0; hs < nstage && ok; ++hs) {
             const int64_t sb = hs >> 1;
             const int h = (int)(hs & 1);
             // the next half's bytes are in flight while this one is converted
-            if (hs + 1 < nstage) load_raw(nxt, P, (uint64_t)nc * nsb + ((hs + 1) >> 1), (int)((hs + 1) & 1));
+            if (hs + 1 < nstage) load_raw(nxt, P, nc, (hs + 1) >> 1, nsb, (int)((hs + 1) & 1));
             if (!mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((sb & 1) ^ 1))) { ok = false; break; }
             if (h == 0 && !mbar_wait(&bar[BAR_ACC_EMPTY + (sb & 1)], (uint32_t)(((sb >> 1) & 1) ^ 1))) {
                 ok = false;

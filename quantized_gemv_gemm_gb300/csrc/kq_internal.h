@@ -55,7 +55,8 @@ cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K 
                            const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
                            void *workspace, size_t workspace_bytes, cudaStream_t s);
 
-// Device status word of the bounded waits.
+// Device status words of the bounded waits (tensor-core GEMM; decode GEMV).
 int read_and_clear_status(cudaStream_t s, int *status);
+int read_and_clear_gemv_status(cudaStream_t s, int *status);
 
 }  // namespace kq

@@ -44,55 +44,60 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8
 
 // ---------------------------------------------------------------------------
 // Repack ([kq-arc], k4 kq-v2 commit: the transcode keeps the disk scale block
-// verbatim and the plane dequant is bit-identical to the disk dequant).
-// One thread per superblock moves each field of the GGUF-order block into
-// its plane; no value is changed.  The disk block is read as 16-bit words
-// (210-byte Q6_K blocks are only 2-byte aligned).
+// as it is, and the planes dequantize bit-identically to the disk blocks).
+// One thread per (row n, superblock sb) of the rows padded to whole groups
+// of 16 moves each 16-byte piece of the GGUF-order block to its place in the
+// grp16 image (kq_device.cuh); no value is changed, and the padding rows are
+// zero.  The disk block is read as 16-bit words (210-byte Q6_K blocks are
+// only 2-byte aligned).
 
-__device__ __forceinline__ void copy16s(uint8_t *dst, const uint16_t *src, int n16) {
-    // dst 16-byte aligned, n16 = bytes / 16
-    for (int i = 0; i < n16; ++i) {
-        uint32_t w[4];
+__device__ __forceinline__ uint4 piece16(const uint16_t *src) {
+    uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j] = static_cast<uint32_t>(src[8 * i + 2 * j]) | (static_cast<uint32_t>(src[8 * i + 2 * j + 1]) << 16);
-        *reinterpret_cast<uint4 *>(dst + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    for (int j = 0; j < 4; ++j) w[j] = static_cast<uint32_t>(src[2 * j]) | (static_cast<uint32_t>(src[2 * j + 1]) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 template <int F>
-__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ disk, int64_t units,
-                                                     Planes P) {
+__global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ disk, int64_t N, int64_t nsb,
+                                                     int64_t units, Planes P) {
     const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (u >= units) return;
-    const uint16_t *b = reinterpret_cast<const uint16_t *>(disk + u * (int64_t)block_bytes(F));
+    const int64_t n = u / nsb, sb = u % nsb;
+    const uint64_t ch = chunk_of(n, sb, nsb);
+    const int r = (int)(n % GROUP_ROWS);
     uint8_t *p0 = const_cast<uint8_t *>(P.p0), *p1 = const_cast<uint8_t *>(P.p1);
     uint8_t *p2 = const_cast<uint8_t *>(P.p2), *p3 = const_cast<uint8_t *>(P.p3);
+    const bool real = n < N;
+    const uint16_t *b = reinterpret_cast<const uint16_t *>(disk + (real ? u : 0) * (int64_t)block_bytes(F));
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    auto piece = [&](int off16) { return real ? piece16(b + off16) : zero; };  // off16 in 16-bit words
+    auto put = [&](uint8_t *dst, uint4 v) { *reinterpret_cast<uint4 *>(dst) = v; };
     if constexpr (F == FMT_Q4_K) {
-        copy16s(p1 + u * 16, b, 1);            // d, dmin, scales[12]
-        copy16s(p0 + u * 128, b + 8, 8);       // qs
+        put(p1 + ch * 256 + 16 * r, piece(0));                                     // d, dmin, scales[12]
+        for (int i = 0; i < 8; ++i) put(p0 + ch * 2048 + piece_offset(128, r, i), piece(8 + 8 * i));   // qs
     } else if constexpr (F == FMT_Q5_K) {
-        copy16s(p2 + u * 16, b, 1);            // d, dmin, scales[12]
-        copy16s(p1 + u * 32, b + 8, 2);        // qh
-        copy16s(p0 + u * 128, b + 24, 8);      // qs
+        put(p2 + ch * 256 + 16 * r, piece(0));                                     // d, dmin, scales[12]
+        for (int i = 0; i < 2; ++i) put(p1 + ch * 512 + piece_offset(32, r, i), piece(8 + 8 * i));     // qh
+        for (int i = 0; i < 8; ++i) put(p0 + ch * 2048 + piece_offset(128, r, i), piece(24 + 8 * i));  // qs
     } else {
-        copy16s(p0 + u * 128, b, 8);           // ql
-        copy16s(p1 + u * 64, b + 64, 4);       // qh
-        copy16s(p2 + u * 16, b + 96, 1);       // scales (int8)
-        reinterpret_cast<uint16_t *>(p3)[u] = b[104];  // d
+        for (int i = 0; i < 8; ++i) put(p0 + ch * 2048 + piece_offset(128, r, i), piece(8 * i));       // ql
+        for (int i = 0; i < 4; ++i) put(p1 + ch * 1024 + piece_offset(64, r, i), piece(64 + 8 * i));   // qh
+        put(p2 + ch * 256 + 16 * r, piece(96));                                    // scales (int8)
+        reinterpret_cast<uint16_t *>(p3 + ch * 32)[r] = real ? b[104] : uint16_t(0);  // d
     }
 }
 
 cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,
                           cudaStream_t s) {
     const int64_t nsb = K / QK;
-    const int64_t units = N * nsb;
+    const int64_t units = row_groups(N) * GROUP_ROWS * nsb;
     if (units == 0) return cudaSuccess;
     const Planes P = make_planes(f, packed, N, nsb);
     const unsigned grid = (unsigned)((units + 255) / 256);
-    if (f == FMT_Q4_K) repack_kernel<FMT_Q4_K><<<grid, 256, 0, s>>>(disk, units, P);
-    else if (f == FMT_Q5_K) repack_kernel<FMT_Q5_K><<<grid, 256, 0, s>>>(disk, units, P);
-    else repack_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(disk, units, P);
+    if (f == FMT_Q4_K) repack_kernel<FMT_Q4_K><<<grid, 256, 0, s>>>(disk, N, nsb, units, P);
+    else if (f == FMT_Q5_K) repack_kernel<FMT_Q5_K><<<grid, 256, 0, s>>>(disk, N, nsb, units, P);
+    else repack_kernel<FMT_Q6_K><<<grid, 256, 0, s>>>(disk, N, nsb, units, P);
     return cudaGetLastError();
 }
 
