@@ -67,7 +67,8 @@ typedef enum {
     KQ_ERR_LAUNCH = -4,    /* CUDA reported an error at launch */
     KQ_ERR_TIMEOUT = -5,   /* a device-side bounded wait gave up (see kq_device_status) */
     KQ_ERR_WORKSPACE = -6, /* workspace missing or smaller than required */
-    KQ_ERR_DEVICE = -7     /* the current device is not sm_103 / cannot run the kernel */
+    KQ_ERR_DEVICE = -7,    /* the current device is not sm_103 / cannot run the kernel */
+    KQ_ERR_TOO_LARGE = -8  /* the problem needs more scratch than kq_gemm_noalloc's fixed array */
 } kq_status;
 
 /* Q8_K planes (device pointers), see the format note above. */
@@ -244,6 +245,42 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
 #define KQ_LAUNCH_PDL 1u
 unsigned kq_set_launch_flags(unsigned flags);
 unsigned kq_get_launch_flags(void);
+
+/*
+ * Prefill GEMM without any allocation by anyone: kq_gemm with its scratch
+ * (the fp16 activation image and the transposed scales) held in a fixed
+ * array that the library reserves in device memory on every GPU that loads
+ * it, KQ_NOALLOC_SCRATCH_BYTES (32 MiB), kept until the process exits.  The
+ * source pages have no counterpart of this entry point.
+ *
+ * It is for callers that cannot call cudaMalloc or hand the library a
+ * workspace: for example a serving runtime that plans its whole device
+ * memory budget at start-up and forbids allocation on the request path, a
+ * latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation, or plain C host code that only receives device pointers
+ * for its inputs and outputs and has no allocator of its own.  The caller
+ * still passes the inputs and the output, as for kq_gemm.
+ *
+ *   arguments  as kq_gemm, without workspace / workspace_bytes
+ * Limits and behaviour:
+ *   - The scratch needed, kq_gemm_workspace_bytes(f, M, N, K), must not
+ *     exceed KQ_NOALLOC_SCRATCH_BYTES; larger problems return
+ *     KQ_ERR_TOO_LARGE before anything is enqueued (M*K up to about 15.9
+ *     million activations, e.g. 512 tokens x K = 31744).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, and the array keeps what
+ *     the last call wrote; each call rewrites every scratch byte it reads,
+ *     so nothing needs clearing.  Calls whose work may overlap on the GPU
+ *     (different streams, no ordering between them) race on the array and
+ *     must not be issued; calls on one stream are ordered and safe.
+ *   - Errors as kq_gemm, plus KQ_ERR_TOO_LARGE; KQ_ERR_LAUNCH if the address
+ *     lookup fails.
+ */
+#define KQ_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+int kq_gemm_noalloc(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M,
+                    float *y, cudaStream_t s);
 
 /*
  * Synchronise stream s and return the device status word of the library's

@@ -38,6 +38,33 @@ int launch_status(cudaError_t e) {
 
 }  // namespace
 
+namespace kq {
+// Shared body of kq_gemm, kq_gemm_grouped and kq_gemm_noalloc: argument
+// checks, then the tensor-core GEMM (or the small-M kernel below its token
+// threshold).
+int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offsets, int64_t N, int64_t K,
+                kq_q8k_const a, int64_t M, float *y, void *ws, size_t ws_bytes, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (M < 0 || E < 1) return KQ_ERR_ARG;
+    if (M == 0 || N == 0) return KQ_OK;
+    if (!packed || !y) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    const size_t need = gemm_workspace_bytes(f, M, N, K);
+    if (need && (!ws || ws_bytes < need)) return KQ_ERR_WORKSPACE;
+    if (ws && !aligned(ws, 256)) return KQ_ERR_ALIGN;
+    const Q8K q{a.d, a.qs, a.bsums};
+    const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
+    cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        e = launch_mv(f, packed, N, K, q, M, offsets, E, expert_bytes, y, s);
+    }
+    return launch_status(e);
+}
+}  // namespace kq
+
 extern "C" {
 
 const char *kq_strerror(int code) {
@@ -50,6 +77,7 @@ const char *kq_strerror(int code) {
     case KQ_ERR_TIMEOUT: return "a device-side bounded wait timed out";
     case KQ_ERR_WORKSPACE: return "workspace missing or too small";
     case KQ_ERR_DEVICE: return "unsupported device";
+    case KQ_ERR_TOO_LARGE: return "problem needs more scratch than the fixed array of kq_gemm_noalloc";
     default: return "unknown kq status";
     }
 }
@@ -122,28 +150,6 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
     if (!fmt_ok(f) || M < 0 || check_shape(N, K)) return 0;
     return gemm_workspace_bytes(f, M, N, K);
-}
-
-static int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offsets, int64_t N, int64_t K,
-                       kq_q8k_const a, int64_t M, float *y, void *ws, size_t ws_bytes, cudaStream_t s) {
-    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
-    if (int r = check_shape(N, K)) return r;
-    if (M < 0 || E < 1) return KQ_ERR_ARG;
-    if (M == 0 || N == 0) return KQ_OK;
-    if (!packed || !y) return KQ_ERR_ARG;
-    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
-    if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
-    const size_t need = gemm_workspace_bytes(f, M, N, K);
-    if (need && (!ws || ws_bytes < need)) return KQ_ERR_WORKSPACE;
-    if (ws && !aligned(ws, 256)) return KQ_ERR_ALIGN;
-    const Q8K q{a.d, a.qs, a.bsums};
-    const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
-    cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
-    if (e == cudaErrorNotSupported) {
-        cudaGetLastError();
-        e = launch_mv(f, packed, N, K, q, M, offsets, E, expert_bytes, y, s);
-    }
-    return launch_status(e);
 }
 
 int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M, float *y,

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "kq_device.cuh"
+#include "../../include/kq.h"
 
 namespace kq {
 
@@ -54,6 +55,10 @@ size_t gemm_workspace_bytes(int f, int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                            const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
                            void *workspace, size_t workspace_bytes, cudaStream_t s);
+
+// The C-ABI body of the three GEMM entry points (kq_api.cu).
+int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offsets, int64_t N, int64_t K,
+                kq_q8k_const a, int64_t M, float *y, void *ws, size_t ws_bytes, cudaStream_t s);
 
 // Device status words of the bounded waits (tensor-core GEMM; decode GEMV).
 int read_and_clear_status(cudaStream_t s, int *status);

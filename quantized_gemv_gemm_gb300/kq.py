@@ -46,6 +46,7 @@ _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_grouped.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
+_lib.kq_gemm_noalloc.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P]
 _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
@@ -53,7 +54,7 @@ _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
-for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemm", "kq_gemm_grouped",
+for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
     getattr(_lib, _f).restype = _INT
 
@@ -207,6 +208,24 @@ def kq_gemm_grouped(fmt: int, packed: torch.Tensor, E: int, row_offsets: torch.T
     workspace, ws_bytes = _workspace(fmt, M, N, K, workspace, packed.device)
     _check(_lib.kq_gemm_grouped(int(fmt), _ptr(packed), E, _ptr(row_offsets), N, K, _q8k_struct(a), M, _ptr(y),
                                 _ptr(workspace), ws_bytes, _stream(stream)), "kq_gemm_grouped")
+    return y
+
+
+KQ_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def kq_gemm_noalloc(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, y: Optional[torch.Tensor] = None,
+                    stream=None) -> torch.Tensor:
+    """kq_gemm with the library's fixed scratch array instead of a workspace
+    (for callers that cannot allocate device memory); y must be given by
+    such callers, it is only allocated here when omitted."""
+    _need_cuda(packed, *a)
+    M = a.qs.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=packed.device)
+    _need_cuda(y)
+    _check(_lib.kq_gemm_noalloc(int(fmt), _ptr(packed), N, K, _q8k_struct(a), M, _ptr(y), _stream(stream)),
+           "kq_gemm_noalloc")
     return y
 
 
