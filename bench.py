@@ -404,6 +404,7 @@ def run_ours(args, world, rank, local):
                          "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)",
                          "alg_bytes_per_step": sum(alg),
                          "traffic": traffic,
+                         "traffic_unit": "DRAM bytes per step (4 launches), ncu, profiles/gemv_decode_layer.traffic.txt",
                          "per_launch_diag": {"how": "event nodes between launches in a graph replay (they break "
                                                     "the launch overlap, so these durations read long)",
                                              "launches": per_launch}},
