@@ -425,9 +425,41 @@ def run_ours(args, world, rank, local):
 # --------------------------------------------------------------------------
 # M = 512 GEMMs (secondary metric)
 
+def int8_tensor_peak(torch):
+    """Dense int8 tensor-core throughput of this GPU, measured with the
+    library GEMM (torch._int_mm -> cuBLASLt IMMA), best of 10 on 8192^3.
+    sm_103a has no integer tcgen05 MMA, so this is the int8 rate there is."""
+    try:
+        n = 8192
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device="cuda")
+        for _ in range(3):
+            torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception as ex:  # no int8 GEMM on this torch / device
+        print(f"int8 peak unavailable: {ex}", file=sys.stderr)
+        return None
+
+
 def bench_gemm(kq, torch, peaks, args):
     out = []
     tc_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    i8_peak = int8_tensor_peak(torch)
+    out.append({"int8_tensor_peak_tops": None if i8_peak is None else round(i8_peak, 1),
+                "how": "measured: torch._int_mm (cuBLASLt int8 GEMM) 8192^3, best of 10",
+                "fp16_tensor_peak_tflops": tc_peak, "fp16_how": "MEASURED_PEAKS.json bf16_tflops (cuBLAS, burst)"})
 
     def time_it(fn, reps):
         fn()
@@ -464,6 +496,7 @@ def bench_gemm(kq, torch, peaks, args):
         tops = ops / (ms * 1e-3) / 1e12
         out.append({"workload": name, "M": M, "ms": round(ms, 4), "tops": round(tops, 2),
                     "frac_of_fp16_tensor_peak": round(tops / tc_peak, 4),
+                    "frac_of_int8_tensor_peak": None if i8_peak is None else round(tops / i8_peak, 4),
                     "weight_gbs": round(sum(m.weight_bytes for m in mats) / (ms * 1e-3) / 1e9, 1)})
         del items
         torch.cuda.empty_cache()
