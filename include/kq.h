@@ -130,17 +130,38 @@ size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
 int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s);
 
 /*
+ * Workspace of the decode GEMV (kq_gemv, kq_gemv_fused): KQ_GEMV_WORKSPACE_BYTES
+ * (64 KiB) of device memory, 16-byte aligned, zero-filled once before its
+ * first use; every call leaves it zero-filled again.  With it the GEMV gives
+ * every SM an even share of the superblocks, cutting a row group between two
+ * blocks where needed and finishing that row group through the workspace;
+ * without it (NULL) each block takes whole row groups, which leaves SMs idle
+ * when the row groups do not divide evenly among them.  Either way the
+ * result does not depend on timing (every sum has a fixed order; the two
+ * ways differ only in float rounding).  Calls on one stream may share a workspace (each reads it only
+ * after the previous kernels in the stream have completed); calls that may
+ * run at the same time on different streams need one each.  The source
+ * pages have no counterpart of this buffer (their decode kernels run one
+ * row per work-group, on hardware where that fills the device).
+ * kq_gemv_workspace_bytes() returns the same number, for bindings.
+ */
+#define KQ_GEMV_WORKSPACE_BYTES ((size_t)64 << 10)
+size_t kq_gemv_workspace_bytes(void);
+
+/*
  * Decode GEMV, M = 1 ([kq-arc], "The pieces", kq v2: the GEMV unpacks the
  * packed planes in the kernel; kq v3 bullet: decode is bound by DRAM
  * traffic, so every byte of the weight planes costs decode time).  y[n]
  * for n < N, as in the header note.
- *   packed device image from kq_repack (256-byte aligned)
- *   a      device Q8_K planes of one row of K
- *   y      device float32 [N]
- * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ *   packed     device image from kq_repack (256-byte aligned)
+ *   a          device Q8_K planes of one row of K
+ *   y          device float32 [N]
+ *   workspace  NULL, or KQ_GEMV_WORKSPACE_BYTES as described above
+ * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_WORKSPACE
+ * (workspace_bytes too small), KQ_ERR_LAUNCH.
  */
 int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
-            float *y, cudaStream_t s);
+            float *y, void *workspace, size_t workspace_bytes, cudaStream_t s);
 
 /*
  * Fused decode GEMV: quantize + GEMV in one launch, over up to four matrices
@@ -157,12 +178,14 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
  *   K       shared inner dimension: a multiple of 256, at most 40960
  *   x       device float32 [K], 16-byte aligned, finite values
  *   y       host array of n_mats device pointers, y[m] float32 [N[m]]
+ *   workspace  NULL, or KQ_GEMV_WORKSPACE_BYTES as for kq_gemv
  * The host arrays are read during the call only.
  * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (n_mats out of range, null, K), KQ_ERR_ALIGN,
- * KQ_ERR_LAUNCH.
+ * KQ_ERR_WORKSPACE, KQ_ERR_LAUNCH.
  */
 int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K,
-                  const float *x, float *const *y, cudaStream_t s);
+                  const float *x, float *const *y, void *workspace, size_t workspace_bytes,
+                  cudaStream_t s);
 
 /*
  * Size of the device workspace kq_gemm / kq_gemm_grouped need for M token
@@ -243,6 +266,16 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
  *   Default: off.
  */
 #define KQ_LAUNCH_PDL 1u
+/*
+ * KQ_LAUNCH_GEMV_SPLIT: a decode GEMV given a workspace always gives every SM
+ * an even share of the superblocks, cutting row groups between blocks
+ * wherever the shares fall.  Default (off): it cuts only where taking whole
+ * row groups would leave the busiest warp three or more superblocks above an
+ * even share, since the exchange at a cut costs about as much as folding a
+ * few superblocks.  The results differ between the two only in float
+ * rounding.
+ */
+#define KQ_LAUNCH_GEMV_SPLIT 2u
 unsigned kq_set_launch_flags(unsigned flags);
 unsigned kq_get_launch_flags(void);
 

@@ -109,23 +109,36 @@ int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed,
     return launch_status(launch_repack(f, static_cast<const uint8_t *>(disk), N, K, static_cast<uint8_t *>(packed), s));
 }
 
-int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, float *y, cudaStream_t s) {
+size_t kq_gemv_workspace_bytes(void) { return GEMV_WORKSPACE_BYTES; }
+
+// a GEMV workspace: none, or at least GEMV_WORKSPACE_BYTES, 16-byte aligned
+static int check_gemv_ws(const void *ws, size_t bytes) {
+    if (!ws) return KQ_OK;
+    if (bytes < GEMV_WORKSPACE_BYTES) return KQ_ERR_WORKSPACE;
+    return aligned(ws, 16) ? KQ_OK : KQ_ERR_ALIGN;
+}
+
+int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, float *y, void *workspace,
+            size_t workspace_bytes, cudaStream_t s) {
     if (!fmt_ok(f)) return KQ_ERR_FORMAT;
     if (int r = check_shape(N, K)) return r;
     if (N == 0) return KQ_OK;
     if (!packed || !y) return KQ_ERR_ARG;
     if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
     if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    if (int r = check_gemv_ws(workspace, workspace_bytes)) return r;
     const Q8K q{a.d, a.qs, a.bsums};
-    if (K <= GEMV_MAX_K) return launch_status(launch_gemv(f, 1, &packed, &N, K, nullptr, q, &y, s));
+    if (K <= GEMV_MAX_K)
+        return launch_status(launch_gemv(f, 1, &packed, &N, K, nullptr, q, &y, workspace, workspace_bytes, s));
     return launch_status(launch_mv(f, packed, N, K, q, 1, nullptr, 1, 0, y, s));
 }
 
 int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K, const float *x,
-                  float *const *y, cudaStream_t s) {
+                  float *const *y, void *workspace, size_t workspace_bytes, cudaStream_t s) {
     if (!fmt_ok(f)) return KQ_ERR_FORMAT;
     if (n_mats < 1 || n_mats > GEMV_MAX_MATRICES || !packed || !N || !y) return KQ_ERR_ARG;
     if (K <= 0 || K % QK != 0 || K > GEMV_MAX_K) return KQ_ERR_ARG;
+    if (int r = check_gemv_ws(workspace, workspace_bytes)) return r;
     int64_t total = 0;
     for (int m = 0; m < n_mats; ++m) {
         if (N[m] < 0) return KQ_ERR_ARG;
@@ -144,7 +157,8 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
     int k = 0;
     for (int m = 0; m < n_mats; ++m)
         if (N[m] > 0) { pk[k] = packed[m]; nn[k] = N[m]; yy[k] = y[m]; ++k; }
-    return launch_status(launch_gemv(f, k, pk, nn, K, x, Q8K{nullptr, nullptr, nullptr}, yy, s));
+    return launch_status(
+        launch_gemv(f, k, pk, nn, K, x, Q8K{nullptr, nullptr, nullptr}, yy, workspace, workspace_bytes, s));
 }
 
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
@@ -188,7 +202,7 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
 }
 
 unsigned kq_set_launch_flags(unsigned flags) {
-    return g_launch_flags.exchange(flags & KQ_LAUNCH_PDL, std::memory_order_relaxed);
+    return g_launch_flags.exchange(flags & (KQ_LAUNCH_PDL | KQ_LAUNCH_GEMV_SPLIT), std::memory_order_relaxed);
 }
 
 unsigned kq_get_launch_flags(void) { return launch_flags(); }

@@ -22,20 +22,27 @@
 // superblock, so the activation reads are broadcasts and the weight reads
 // are consecutive 16-byte pieces: no bank conflicts.
 //
-// Work split.  Rows are taken in groups of 16 (one per warp) across all the
-// matrices; G groups.  A task is R = 8/S row groups x S superblock slices,
-// one (group, slice) per warp of a 256-thread block; the S partial sums of
-// a row are added in shared memory in a fixed order, so the result does not
-// depend on timing.  The grid is persistent: every block takes the same
-// number of consecutive tasks; S is the smallest of 1, 2, 4, 8 that gives
-// every block slot at least one task.
+// Work split.  Rows are taken in groups of 16 across all the matrices (G
+// groups); an item is one row group x one superblock, items ordered
+// g * K/256 + sb.  The grid has one block per SM, and block b takes the
+// items [b*I/B, (b+1)*I/B) of the I = G*K/256, its eight warps an even
+// eighth of those each, so every warp folds the same number of items (to
+// one) whatever the matrix shapes.  A block is given at most half an SM
+// (110 KB of shared memory, 128 registers a thread), so the next GEMV's
+// block fits beside it.  A warp stores the rows of a row group it folds
+// whole; a row group split between warps is added in shared memory in warp
+// order; one split between two blocks (at most two, as every block holds at
+// least K/256 items) is finished by the block that arrives second, which
+// adds the two partial sums kept in the caller's workspace.  Every sum has
+// a fixed order (two terms commute exactly), so the result does not depend
+// on timing.  Without a workspace the blocks take whole row groups instead.
 //
 // Memory pipeline.  Each warp has a ring of D superblock stages in shared
 // memory.  An item (16 rows x one superblock) is one contiguous chunk of
 // each plane of the grp16 image, already in the stage's order, so lane 0
 // fetches it with one TMA bulk copy (cp.async.bulk) per plane, completing
 // on the stage's mbarrier; the copies run D items ahead of the fold along
-// the block's tasks, and the bytes in flight cost neither registers nor
+// the warp's range, and the bytes in flight cost neither registers nor
 // per-lane instructions.  Before griddepcontrol.wait a block touches only the packed
 // weights (read-only on this path), so under programmatic dependent launch
 // its first stages stream while the previous kernel finishes; every block
@@ -49,21 +56,6 @@
 
 namespace kq {
 
-// Tuning constants (compile time; the defaults are the measured choice):
-// resident blocks per SM, whether a block lets the next kernel launch on
-// entry (1) or once its activation row is staged (0), and the bytes of
-// weights each block keeps streaming into L2 ahead of the task it folds
-// (0: no bulk prefetch).
-#ifndef KQ_GEMV_BLOCKS_PER_SM
-#define KQ_GEMV_BLOCKS_PER_SM 2
-#endif
-#ifndef KQ_GEMV_EARLY_TRIGGER
-#define KQ_GEMV_EARLY_TRIGGER 1
-#endif
-#ifndef KQ_GEMV_L2_WINDOW_KB
-#define KQ_GEMV_L2_WINDOW_KB 0
-#endif
-
 // ---------------------------------------------------------------------------
 // One superblock item of a warp = 16 rows x one superblock = the item's
 // chunk of every plane, back to back (kq_device.cuh gives each chunk's
@@ -72,19 +64,13 @@ namespace kq {
 //   Q5_K: qs 2048 | qh 512 | hdr 256            = 2816 B
 //   Q6_K: ql 2048 | qh 1024 | sc 256 | d 32     = 3360 B
 template <int F> struct GemvFmt;
-template <> struct GemvFmt<FMT_Q4_K> { static constexpr int SLOT = 2304, D = 4; };
-template <> struct GemvFmt<FMT_Q5_K> { static constexpr int SLOT = 2816, D = 4; };
-template <> struct GemvFmt<FMT_Q6_K> { static constexpr int SLOT = 3360, D = 3; };
-constexpr int GEMV_MAX_D = 4;
+template <> struct GemvFmt<FMT_Q4_K> { static constexpr int SLOT = 2304; };
+template <> struct GemvFmt<FMT_Q5_K> { static constexpr int SLOT = 2816; };
+template <> struct GemvFmt<FMT_Q6_K> { static constexpr int SLOT = 3360; };
+constexpr int GEMV_MAX_D = 6;
 
-template <int F> constexpr int gemv_ring_bytes() { return 8 * GemvFmt<F>::D * GemvFmt<F>::SLOT; }
-
-// staged row after the rings: quants [K] | sums [K/256][32 B] | d8 [K/256]
-template <int F>
-inline size_t gemv_smem_bytes(int64_t K) {
-    return (size_t)gemv_ring_bytes<F>() + (size_t)(K + K / 8 + K / 64);
-}
-
+// Shared memory of one block: the warps' rings (8 x D x SLOT), then the
+// staged row: quants [K] | sums [K/256][32 B] | d8 [K/256].
 struct ItemQ4 { uint4 q[4]; uint4 hdr; };
 struct ItemQ5 { uint4 q[4]; uint4 qh[2]; uint4 hdr; };
 struct ItemQ6 { uint4 ql[4]; uint4 qh[2]; uint2 sc; uint32_t d; };
@@ -119,33 +105,45 @@ __device__ __forceinline__ ChunkPtr chunk_ptr(const Planes &P, uint64_t ch) {
 }
 
 // TMA bulk copy global -> shared of `bytes` (16-byte aligned, a multiple of
-// 16), completing as transaction bytes on the mbarrier at shared address bar
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(src), "r"(bytes), "r"(bar)
-                 : "memory");
+// 16), completing as transaction bytes on the mbarrier at shared address
+// bar, with the L2 cache policy pol
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+// L2 policy of the weight stream: every packed byte is read once per call,
+// so its lines go first when L2 needs room, and the activations and other
+// data the surrounding kernels reuse stay in L2
+__device__ __forceinline__ uint64_t weight_stream_policy() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
 }
 
 // Lane 0: fetch one item into the stage at st (its mbarrier at bar) and step
 // the chunk pointers; with on = 0 only arrive, so the stage's phase still
 // completes for an item of a row group past the end.
 template <int F>
-__device__ __forceinline__ void item_issue(ChunkPtr &cp, uint32_t st, uint32_t bar, bool on) {
+__device__ __forceinline__ void item_issue(ChunkPtr &cp, uint32_t st, uint32_t bar, bool on, uint64_t pol) {
     constexpr int SLOT = GemvFmt<F>::SLOT;
     if (!on) {
         asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
     } else {
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(SLOT) : "memory");
-        bulk_g2s(st, cp.a, 2048, bar);
+        bulk_g2s(st, cp.a, 2048, bar, pol);
         if constexpr (F == FMT_Q4_K) {
-            bulk_g2s(st + 2048, cp.b, 256, bar);
+            bulk_g2s(st + 2048, cp.b, 256, bar, pol);
         } else if constexpr (F == FMT_Q5_K) {
-            bulk_g2s(st + 2048, cp.b, 512, bar);
-            bulk_g2s(st + 2560, cp.c, 256, bar);
+            bulk_g2s(st + 2048, cp.b, 512, bar, pol);
+            bulk_g2s(st + 2560, cp.c, 256, bar, pol);
         } else {
-            bulk_g2s(st + 2048, cp.b, 1024, bar);
-            bulk_g2s(st + 3072, cp.c, 256, bar);
-            bulk_g2s(st + 3328, cp.d, 32, bar);
+            bulk_g2s(st + 2048, cp.b, 1024, bar, pol);
+            bulk_g2s(st + 3072, cp.c, 256, bar, pol);
+            bulk_g2s(st + 3328, cp.d, 32, bar, pol);
         }
     }
     cp.a += 2048;
@@ -329,9 +327,10 @@ struct GemvParams {
     float *y[GEMV_MAX_MATRICES];
     int64_t gpre[GEMV_MAX_MATRICES + 1];  // prefix sums of 16-row groups
     int64_t K, nsb;
-    int S;                                 // slices per row group (1, 2, 4, 8)
-    int64_t tasks, tpc;                    // task count, tasks per block
-    int64_t pf;                            // tasks kept streaming into L2 ahead (0: none)
+    int64_t items;                         // G * nsb (row group x superblock items)
+    int split;                             // block ranges may cut a row group in two
+    int D;                                 // ring stages per warp
+    unsigned long long *ws;                // [grid][16] words of the row groups cut between blocks
     const float *x;                        // fp32 row (fused quantize), or nullptr
     const float *d8;                       // else: the Q8_K planes of the row
     const int8_t *qs;
@@ -347,95 +346,97 @@ __device__ __forceinline__ void stage_wait(uint64_t *bar, uint32_t parity) {
     if (!sm100::mbar_wait(bar, parity)) atomicExch(&g_gemv_status, 1);
 }
 
+// a workspace word holding a partial sum (low 32 bits) carries this tag
+constexpr unsigned long long GEMV_TAG = 1ull << 32;
+
+// first item of block b's range: whole row groups when split == 0
+__device__ __forceinline__ int64_t block_item(const GemvParams &p, int64_t b, int64_t B, int64_t G) {
+    return p.split ? b * p.items / B : (b * G / B) * p.nsb;
+}
+
 template <int F>
-__global__ void __launch_bounds__(256, KQ_GEMV_BLOCKS_PER_SM) gemv_kernel(const GemvParams p) {
-    constexpr int D = GemvFmt<F>::D, SLOT = GemvFmt<F>::SLOT;
+__global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
+    constexpr int SLOT = GemvFmt<F>::SLOT;
     using Item = typename ItemOf<F>::T;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ Planes s_planes[GEMV_MAX_MATRICES];
-    __shared__ float red[2][8][16];
+    // the matrices' row-group prefix sums, row counts and outputs
+    __shared__ int64_t s_gpre[GEMV_MAX_MATRICES + 1], s_n[GEMV_MAX_MATRICES];
+    __shared__ float *s_y[GEMV_MAX_MATRICES];
     __shared__ uint64_t s_bar[8][GEMV_MAX_D];
+    // a warp's partial sums of the row groups it shares with other warps:
+    // slot 0 = the group its range starts inside, slot 1 = the group it ends inside
+    __shared__ float s_rec[8][2][16];
+    __shared__ int64_t s_rec_g[8][2];
     // the next kernel may be scheduled now: it waits for this grid to
     // complete before it reads anything this grid writes
-    if (KQ_GEMV_EARLY_TRIGGER) griddep_launch_dependents();
+    griddep_launch_dependents();
     const int64_t K = p.K, nsb = p.nsb;
+    const int D = p.D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r16 = lane & 15, h = lane >> 4;
     const uint32_t ring_s = smem_addr(smem + (size_t)warp * D * SLOT);
     uint64_t *bars = s_bar[warp];
-    int8_t *s_qs = reinterpret_cast<int8_t *>(smem + gemv_ring_bytes<F>());
-    uint8_t *s_sum = smem + gemv_ring_bytes<F>() + K;
-    float *s_d8 = reinterpret_cast<float *>(smem + gemv_ring_bytes<F>() + K + K / 8);
+    const size_t ring_bytes = (size_t)8 * D * SLOT;
+    int8_t *s_qs = reinterpret_cast<int8_t *>(smem + ring_bytes);
+    uint8_t *s_sum = smem + ring_bytes + K;
+    float *s_d8 = reinterpret_cast<float *>(smem + ring_bytes + K + K / 8);
     const uint32_t qs_s = smem_addr(s_qs), sum_s = smem_addr(s_sum), d8_s = smem_addr(s_d8);
 
-    const int S = p.S, R = 8 / S;
-    const int rg = warp / S, slice = warp % S;
-    const int s0 = (int)(slice * nsb / S), len = (int)((slice + 1) * nsb / S) - s0;
-    const int64_t t_begin = (int64_t)blockIdx.x * p.tpc;
-    const int64_t left = p.tasks - t_begin;
-    const int ntask = (int)(left <= 0 ? 0 : (left < p.tpc ? left : p.tpc));
-    const int64_t G = p.gpre[p.nmat];
-    if (threadIdx.x < p.nmat) s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
+    // this block's items [I0, I1) and this warp's [w0, w1), in the order
+    // item = g * nsb + sb over the row groups of all the matrices
+    const int64_t G = p.gpre[p.nmat], B = gridDim.x;
+    const int64_t I0 = block_item(p, blockIdx.x, B, G), I1 = block_item(p, blockIdx.x + 1, B, G);
+    const int64_t w0 = I0 + warp * (I1 - I0) / 8, w1 = I0 + (warp + 1) * (I1 - I0) / 8;
+    if (threadIdx.x < p.nmat) {
+        s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
+        s_n[threadIdx.x] = p.N[threadIdx.x];
+        s_y[threadIdx.x] = p.y[threadIdx.x];
+    }
+    if (threadIdx.x <= p.nmat) s_gpre[threadIdx.x] = p.gpre[threadIdx.x];
     if (lane == 0) {
         for (int i = 0; i < D; ++i) sm100::mbar_init(&bars[i], 1);
         sm100::mbar_fence_init();
+        s_rec_g[warp][0] = s_rec_g[warp][1] = -1;
     }
     __syncthreads();
 
-    // task tl of this block -> this warp's matrix, row group (and this lane's
-    // row) and the chunk pointers of its slice's first superblock
-    auto task_ptr = [&](int tl, int &m, int64_t &n, bool &valid) {
-        const int64_t g = (t_begin + tl) * R + rg;
-        valid = g < G;
-        m = 0;
-        while (m + 1 < p.nmat && g >= p.gpre[m + 1]) ++m;
-        const int64_t gl = valid ? g - p.gpre[m] : 0;
-        n = gl * GROUP_ROWS + r16;
-        return chunk_ptr<F>(s_planes[m], (uint64_t)gl * nsb + s0);
+    // matrix holding row group g
+    const int nmat = p.nmat;
+    auto matrix_of_group = [&](int64_t g) {
+        int m = 0;
+        while (m + 1 < nmat && g >= s_gpre[m + 1]) ++m;
+        return m;
     };
-    // L2 prefetch of a whole task (its row groups are contiguous in every plane)
-    auto prefetch_task = [&](int64_t tl) {
-        if (tl >= ntask) return;
-        const int64_t g0 = (t_begin + tl) * R, g1 = g0 + R < G ? g0 + R : G;
-        int u[4];
-        plane_unit_bytes(F, u);
-        for (int m = 0; m < p.nmat; ++m) {
-            const int64_t a = g0 > p.gpre[m] ? g0 : p.gpre[m], b = g1 < p.gpre[m + 1] ? g1 : p.gpre[m + 1];
-            if (a >= b) continue;
-            const uint64_t c0 = (uint64_t)(a - p.gpre[m]) * nsb, c1 = (uint64_t)(b - p.gpre[m]) * nsb;
-            const uint8_t *base[4] = {s_planes[m].p0, s_planes[m].p1, s_planes[m].p2, s_planes[m].p3};
-            for (int q = 0; q < 4; ++q)
-                if (u[q]) prefetch_l2_bulk(base[q] + c0 * GROUP_ROWS * u[q], (c1 - c0) * GROUP_ROWS * u[q]);
-        }
-    };
-    if (threadIdx.x == 0 && p.pf > 0)
-        for (int64_t tl = 0; tl < p.pf; ++tl) prefetch_task(tl);
 
-    // issue side (lane 0): runs D items ahead of the fold along the block's
-    // tasks; one mbarrier phase per item and stage
+    // issue side (lane 0): runs D items ahead of the fold along the warp's
+    // range; one mbarrier phase per item and stage.  Within a matrix the
+    // items are consecutive chunks of every plane.
     const LaneOff lo = lane_off(lane);
-    const int total = ntask * len;
+    const uint64_t pol = weight_stream_policy();
+    int64_t iit = w0, inext = 0;
+    int im = 0, iss = 0;
     ChunkPtr icp{};
-    int irem = 0, itl = 0, iss = 0, it = 0;
-    bool ion = false;
-    if (ntask > 0) {
-        int mm;
-        int64_t nn;
-        icp = task_ptr(0, mm, nn, ion);
-        irem = len;
+    // fold side: row group g (of matrix m), superblock sb of the current item
+    const int64_t g0 = w0 / nsb;
+    const int sb0 = (int)(w0 - g0 * nsb);
+    const int m0 = matrix_of_group(g0);
+    if (w0 < w1) {
+        im = m0;
+        icp = chunk_ptr<F>(s_planes[im], (uint64_t)(w0 - s_gpre[im] * nsb));
+        inext = s_gpre[im + 1] * nsb;
     }
     auto issue = [&]() {
-        if (it < total) {
-            if (lane == 0) item_issue<F>(icp, ring_s + iss * SLOT, smem_addr(&bars[iss]), ion);
-            iss = iss + 1 == D ? 0 : iss + 1;
-            if (--irem == 0 && ++itl < ntask) {
-                int mm;
-                int64_t nn;
-                icp = task_ptr(itl, mm, nn, ion);
-                irem = len;
+        if (iit < w1) {
+            if (iit == inext) {
+                im = matrix_of_group(s_gpre[im + 1]);
+                icp = chunk_ptr<F>(s_planes[im], 0);
+                inext = s_gpre[im + 1] * nsb;
             }
+            if (lane == 0) item_issue<F>(icp, ring_s + iss * SLOT, smem_addr(&bars[iss]), true, pol);
+            iss = iss + 1 == D ? 0 : iss + 1;
+            ++iit;
         }
-        ++it;
     };
     for (int i = 0; i < D; ++i) issue();
 
@@ -443,11 +444,11 @@ __global__ void __launch_bounds__(256, KQ_GEMV_BLOCKS_PER_SM) gemv_kernel(const 
     griddep_wait();
     constexpr bool PAIRS = F != FMT_Q6_K;
     if (p.x) {
-        // up to four blocks per warp per round, all loads issued first
-        for (int64_t b0 = warp; b0 < nsb; b0 += 32) {
-            float4 v[4][2];
+        // up to eight blocks per warp per round, all loads issued first
+        for (int64_t b0 = warp; b0 < nsb; b0 += 64) {
+            float4 v[8][2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 const int64_t b = b0 + 8 * j;
                 if (b < nsb) {
                     const float4 *xp = reinterpret_cast<const float4 *>(p.x + b * QK + 8 * lane);
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(256, KQ_GEMV_BLOCKS_PER_SM) gemv_kernel(const 
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
                 const int64_t b = b0 + 8 * j;
                 if (b < nsb) stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, s_qs + b * QK, s_sum + b * 32, s_d8 + b);
             }
@@ -478,35 +479,31 @@ __global__ void __launch_bounds__(256, KQ_GEMV_BLOCKS_PER_SM) gemv_kernel(const 
         for (int64_t i = threadIdx.x; i < nsb; i += 256) s_d8[i] = p.d8[i];
     }
     __syncthreads();
-    if (!KQ_GEMV_EARLY_TRIGGER) griddep_launch_dependents();
 
-    int tl = 0, j = 0, rs = 0;
+    int rs = 0;
     uint32_t rph = 0;  // parity of the current use of stage rs
-    int m = 0;
-    int64_t n = 0;
-    bool valid = false;
-    if (ntask > 0) task_ptr(0, m, n, valid);
+    int64_t g = g0;
+    int sb = sb0;
+    int m = m0;
     // running shared addresses of the current item's activation superblock
     // (the lane's half), sums and scale
-    uint32_t a_cur = qs_s + (uint32_t)s0 * QK + 128 * h, s_cur = sum_s + (uint32_t)s0 * 32 + 16 * h;
-    uint32_t d_cur = d8_s + 4 * (uint32_t)s0;
+    uint32_t a_cur = qs_s + (uint32_t)sb * QK + 128 * h, s_cur = sum_s + (uint32_t)sb * 32 + 16 * h;
+    uint32_t d_cur = d8_s + 4 * (uint32_t)sb;
     float acc = 0.0f;
 #pragma unroll 1
-    for (int i = 0; i < total; ++i) {
+    for (int64_t it = w0; it < w1; ++it) {
         stage_wait(&bars[rs], rph);
         const uint32_t st = ring_s + rs * SLOT;
         Item cur;
         item_read(cur, st, lo, h);
         // every lane's reads of the stage are done before it is refilled
         __syncwarp();
-        if (lane == 0) sm100::fence_proxy_async_smem();
-        issue();  // item i + D into the stage just read
+        if (lane == 0 && iit < w1) sm100::fence_proxy_async_smem();
+        issue();  // item it + D into the stage just read
         if (++rs == D) {
             rs = 0;
             rph ^= 1u;
         }
-        // rows past the last row group fold whatever the stage holds; their
-        // sums are never written
         int isum, msum;
         item_fold(cur, h, a_cur, s_cur, isum, msum);
         const float d8 = __uint_as_float(lds32(d_cur));
@@ -515,23 +512,69 @@ __global__ void __launch_bounds__(256, KQ_GEMV_BLOCKS_PER_SM) gemv_kernel(const 
         a_cur += QK;
         s_cur += 32;
         d_cur += 4;
-        if (++j == len) {
-            // end of a task: add the row's two halves, then its slices
-            if (threadIdx.x == 0 && p.pf > 0) prefetch_task(tl + p.pf);
-            acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
-            if (h == 0) red[tl & 1][warp][r16] = acc;
-            __syncthreads();
-            if (slice == 0 && h == 0 && valid && n < p.N[m]) {
-                float v = 0.0f;
-                for (int q = 0; q < S; ++q) v += red[tl & 1][rg * S + q][r16];
-                p.y[m][n] = v;
-            }
+        if (++sb == nsb || it + 1 == w1) {
+            // the warp is done with row group g: add the row's two halves
+            const float v = acc + __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
             acc = 0.0f;
-            j = 0;
-            a_cur -= (uint32_t)len * QK;
-            s_cur -= (uint32_t)len * 32;
-            d_cur -= (uint32_t)len * 4;
-            if (++tl < ntask) task_ptr(tl, m, n, valid);
+            if (g * nsb >= w0 && (g + 1) * nsb <= w1) {
+                // the whole row group is this warp's
+                const int64_t n = (g - s_gpre[m]) * GROUP_ROWS + r16;
+                if (h == 0 && n < s_n[m]) s_y[m][n] = v;
+            } else {
+                const int slot = g * nsb < w0 ? 0 : 1;
+                if (h == 0) s_rec[warp][slot][r16] = v;
+                if (lane == 0) s_rec_g[warp][slot] = g;
+            }
+            if (sb == nsb) {
+                sb = 0;
+                ++g;
+                a_cur = qs_s + 128 * h;
+                s_cur = sum_s + 16 * h;
+                d_cur = d8_s;
+                while (m + 1 < nmat && g >= s_gpre[m + 1]) ++m;
+            }
+        }
+    }
+    __syncthreads();
+
+    // Row groups shared by several warps: the lowest of them adds all the
+    // warps' partial sums in warp order.  A row group this block holds only
+    // part of is finished by whichever of its two blocks arrives second,
+    // which adds the two blocks' partial sums: a sum of two terms, so the
+    // result does not depend on which block that is.  No wait and no fence:
+    // the exchanged word carries the value itself.
+#pragma unroll 1
+    for (int slot = 0; slot < 2; ++slot) {
+        const int64_t gg = s_rec_g[warp][slot];
+        if (gg < 0) continue;
+        bool owner = true;
+        for (int w = 0; w < warp; ++w)
+            if (s_rec_g[w][0] == gg || s_rec_g[w][1] == gg) owner = false;
+        if (!owner) continue;
+        float v = 0.0f;
+        for (int w = warp; w < 8; ++w) {
+            if (s_rec_g[w][0] == gg) v += s_rec[w][0][r16];
+            else if (s_rec_g[w][1] == gg) v += s_rec[w][1][r16];
+        }
+        const int mm = matrix_of_group(gg);
+        const int64_t n = (gg - s_gpre[mm]) * GROUP_ROWS + r16;
+        const bool left_cut = gg * nsb < I0, right_cut = (gg + 1) * nsb > I1;
+        if (!left_cut && !right_cut) {
+            if (h == 0 && n < s_n[mm]) s_y[mm][n] = v;
+            continue;
+        }
+        // The row group is cut between blocks cut and cut + 1.  Each of the
+        // two swaps its partial sum, tagged, into the row's workspace word;
+        // the one that gets the other's tagged value back arrives second,
+        // adds the two and empties the word for the next call.
+        const int64_t cut = left_cut ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
+        unsigned long long *word = p.ws + cut * 16 + r16;
+        if (h == 0) {
+            const unsigned long long old = atomicExch(word, GEMV_TAG | __float_as_uint(v));
+            if (old & GEMV_TAG) {
+                if (n < s_n[mm]) s_y[mm][n] = v + __uint_as_float((uint32_t)old);
+                *word = 0ull;
+            }
         }
     }
 }
@@ -548,38 +591,65 @@ static int sm_count() {
     return cached[dev];
 }
 
-constexpr int64_t GEMV_L2_WINDOW = int64_t(KQ_GEMV_L2_WINDOW_KB) * 1024;
+// Above this many items per SM a launch takes two blocks per SM (more warps
+// folding), giving up the room for the next kernel's block.
+#ifndef KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM
+#define KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM 1000000000
+#endif
+
+#ifndef KQ_GEMV_CUT_ITEMS
+#define KQ_GEMV_CUT_ITEMS 3
+#endif
+
+// Shared memory of one block (dynamic part), at most half an SM's so that
+// a block of the next GEMV in the stream fits beside it and starts its
+// weight stream while this one finishes.
+constexpr int64_t GEMV_SMEM_BUDGET = 110 * 1024;
+
+template <int F> constexpr int gemv_max_d() { return F == FMT_Q6_K ? 4 : (F == FMT_Q5_K ? 5 : 6); }
 
 template <int F>
-static cudaError_t launch_gemv_t(GemvParams p, cudaStream_t s) {
+static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaStream_t s) {
     p.gpre[0] = 0;
     for (int m = 0; m < p.nmat; ++m) p.gpre[m + 1] = p.gpre[m] + (p.N[m] + 15) / 16;
     const int64_t G = p.gpre[p.nmat];
     if (G == 0) return cudaSuccess;
-    const int64_t slots = (int64_t)KQ_GEMV_BLOCKS_PER_SM * sm_count();
-    int S = 1;
-    while (S < 8 && 2 * S <= p.nsb && (G * S + 7) / 8 < slots) S *= 2;
-    p.S = S;
-    const int64_t R = 8 / S;
-    p.tasks = (G + R - 1) / R;
-    p.tpc = (p.tasks + slots - 1) / slots;
-    const int64_t blocks = (p.tasks + p.tpc - 1) / p.tpc;
-    const int64_t task_bytes = (R * 16) * p.nsb * block_bytes(F) / S;
-    const int64_t pf = (GEMV_L2_WINDOW + task_bytes - 1) / task_bytes;
-    p.pf = GEMV_L2_WINDOW == 0 ? 0 : (pf < 1 ? 1 : (pf > p.tpc ? p.tpc : pf));
+    p.items = G * p.nsb;
+    // one block per SM, each with an even share of the items; a row group
+    // may then be cut between two blocks, which needs the workspace
+    int64_t blocks = sm_count();
+    if (p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks) blocks *= 2;
+    if (blocks > GEMV_MAX_BLOCKS) blocks = GEMV_MAX_BLOCKS;
+    if (blocks > G) blocks = G;  // every row group spans at most two blocks
+    // cut row groups between blocks only where whole row groups would leave
+    // the busiest warp KQ_GEMV_CUT_ITEMS or more items above an even share:
+    // the exchange at a cut costs about as much as folding a few items
+    const int64_t whole = (G + blocks - 1) / blocks * p.nsb, even = (p.items + blocks - 1) / blocks;
+    p.split = ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
+              ((launch_flags() & LAUNCH_GEMV_SPLIT) || (whole + 7) / 8 - (even + 7) / 8 >= KQ_GEMV_CUT_ITEMS);
+    p.ws = static_cast<unsigned long long *>(ws);
+    const int64_t stage_bytes = p.K + p.K / 8 + p.K / 64;
+    int64_t D = (GEMV_SMEM_BUDGET - stage_bytes) / (8 * GemvFmt<F>::SLOT);
+    if (D > gemv_max_d<F>()) D = gemv_max_d<F>();
+    if (D < 2) D = 2;
+    p.D = (int)D;
+    const size_t smem = (size_t)(8 * D * GemvFmt<F>::SLOT + stage_bytes);
     static bool attr_set[64][4] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     if (!attr_set[dev][F]) {
-        const cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)gemv_smem_bytes<F>(GEMV_MAX_K));
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)GEMV_SMEM_BUDGET);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(gemv_kernel<F>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         attr_set[dev][F] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = gemv_smem_bytes<F>(p.K);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -590,7 +660,7 @@ static cudaError_t launch_gemv_t(GemvParams p, cudaStream_t s) {
 }
 
 cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
-                        Q8K a, float *const *y, cudaStream_t s) {
+                        Q8K a, float *const *y, void *ws, size_t ws_bytes, cudaStream_t s) {
     GemvParams p{};
     p.nmat = nmat;
     for (int m = 0; m < nmat; ++m) {
@@ -604,9 +674,9 @@ cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_
     p.d8 = a.d;
     p.qs = a.qs;
     p.bs = a.bsums;
-    if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K>(p, s);
-    if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K>(p, s);
-    return launch_gemv_t<FMT_Q6_K>(p, s);
+    if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K>(p, ws, ws_bytes, s);
+    if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K>(p, ws, ws_bytes, s);
+    return launch_gemv_t<FMT_Q6_K>(p, ws, ws_bytes, s);
 }
 
 // ---------------------------------------------------------------------------
@@ -643,7 +713,7 @@ __global__ void __launch_bounds__(256) partials_kernel(const uint8_t *packed, in
     __syncwarp();
     const Planes P = make_planes(F, packed, N, nsb);
     ChunkPtr cp = chunk_ptr<F>(P, (uint64_t)(on ? g : 0) * nsb + sb);
-    if (lane == 0) item_issue<F>(cp, smem_addr(s_item[warp]), smem_addr(&s_bar[warp]), on);
+    if (lane == 0) item_issue<F>(cp, smem_addr(s_item[warp]), smem_addr(&s_bar[warp]), on, weight_stream_policy());
     stage_wait(&s_bar[warp], 0);
     typename ItemOf<F>::T w;
     item_read(w, smem_addr(s_item[warp]), lane_off(lane), h);

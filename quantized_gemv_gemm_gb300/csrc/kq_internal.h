@@ -13,6 +13,7 @@ namespace kq {
 
 // Library-wide launch options (kq_set_launch_flags).
 constexpr unsigned LAUNCH_PDL = 1u;
+constexpr unsigned LAUNCH_GEMV_SPLIT = 2u;
 unsigned launch_flags();
 
 struct Q8K {
@@ -38,10 +39,15 @@ cudaError_t launch_mv(int f, const void *packed, int64_t N, int64_t K, Q8K a, in
 
 // Decode GEMV over nmat (<= 4) matrices sharing one input row: either the
 // fp32 row x (quantized inside the kernel) or, when x is null, Q8_K planes a.
+// ws: null, or a zero-filled workspace of GEMV_WORKSPACE_BYTES: one 64-bit
+// word per row of a row group cut between two blocks, [GEMV_MAX_BLOCKS][16].
 constexpr int GEMV_MAX_MATRICES = 4;
 constexpr int64_t GEMV_MAX_K = 40960;
+constexpr int64_t GEMV_MAX_BLOCKS = 512;
+constexpr size_t GEMV_WORKSPACE_BYTES = KQ_GEMV_WORKSPACE_BYTES;
+static_assert(GEMV_MAX_BLOCKS * 16 * 8 <= (int64_t)KQ_GEMV_WORKSPACE_BYTES, "GEMV workspace layout");
 cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
-                        Q8K a, float *const *y, cudaStream_t s);
+                        Q8K a, float *const *y, void *ws, size_t ws_bytes, cudaStream_t s);
 
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);

@@ -40,8 +40,10 @@ _lib.kq_quantize_q8k.argtypes = [_P, _I64, _I64, _Q8KConst, _P]
 _lib.kq_repack_bytes.argtypes = [_INT, _I64, _I64]
 _lib.kq_repack_bytes.restype = _SZ
 _lib.kq_repack.argtypes = [_INT, _P, _I64, _I64, _P, _P]
-_lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P]
-_lib.kq_gemv_fused.argtypes = [_INT, _INT, _P, _P, _I64, _P, _P, _P]
+_lib.kq_gemv_workspace_bytes.argtypes = []
+_lib.kq_gemv_workspace_bytes.restype = _SZ
+_lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P, _SZ, _P]
+_lib.kq_gemv_fused.argtypes = [_INT, _INT, _P, _P, _I64, _P, _P, _P, _SZ, _P]
 _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
@@ -145,17 +147,46 @@ def kq_repack(fmt: int, disk: torch.Tensor, N: int, K: int, packed: Optional[tor
     return packed
 
 
+KQ_GEMV_WORKSPACE_BYTES = int(_lib.kq_gemv_workspace_bytes())
+_gemv_ws: dict = {}
+
+
+def gemv_workspace(device=None) -> torch.Tensor:
+    """A zero-filled decode-GEMV workspace (KQ_GEMV_WORKSPACE_BYTES) for the
+    device, allocated on first use and then shared by every kq_gemv /
+    kq_gemv_fused call that passes none.  Calls that may run at the same time
+    on different streams must each pass a workspace of their own."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _gemv_ws.get(key)
+    if ws is None:
+        ws = torch.zeros(KQ_GEMV_WORKSPACE_BYTES, dtype=torch.uint8, device=torch.device("cuda", key))
+        _gemv_ws[key] = ws
+    return ws
+
+
+def _gemv_ws_args(workspace, device):
+    """workspace=None: the device's shared one; False: none (whole row groups per block)."""
+    if workspace is False:
+        return None, 0
+    if workspace is None:
+        workspace = gemv_workspace(device)
+    _need_cuda(workspace)
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
 def kq_gemv(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, y: Optional[torch.Tensor] = None,
-            stream=None) -> torch.Tensor:
+            workspace=None, stream=None) -> torch.Tensor:
     _need_cuda(packed, *a)
     if y is None:
         y = torch.empty(N, dtype=torch.float32, device=packed.device)
     _need_cuda(y)
-    _check(_lib.kq_gemv(int(fmt), _ptr(packed), N, K, _q8k_struct(a), _ptr(y), _stream(stream)), "kq_gemv")
+    wp, wn = _gemv_ws_args(workspace, packed.device)
+    _check(_lib.kq_gemv(int(fmt), _ptr(packed), N, K, _q8k_struct(a), _ptr(y), wp, wn, _stream(stream)), "kq_gemv")
     return y
 
 
-def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list=None, stream=None):
+def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list=None, workspace=None, stream=None):
     """Quantize the fp32 row x and multiply it by up to 4 matrices in one launch."""
     n = len(packed_list)
     _need_cuda(x, *packed_list)
@@ -167,7 +198,8 @@ def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list
     pk = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in packed_list])
     nn = (ctypes.c_int64 * max(n, 1))(*[int(v) for v in N_list])
     yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
-    _check(_lib.kq_gemv_fused(int(fmt), n, pk, nn, int(K), _ptr(x), yy, _stream(stream)), "kq_gemv_fused")
+    wp, wn = _gemv_ws_args(workspace, x.device)
+    _check(_lib.kq_gemv_fused(int(fmt), n, pk, nn, int(K), _ptr(x), yy, wp, wn, _stream(stream)), "kq_gemv_fused")
     return y_list
 
 
@@ -258,10 +290,11 @@ def kq_device_status(stream=None) -> int:
 
 
 KQ_LAUNCH_PDL = 1
+KQ_LAUNCH_GEMV_SPLIT = 2
 
 
 def kq_set_launch_flags(flags: int) -> int:
-    """Set the process-wide launch flags (KQ_LAUNCH_PDL); returns the old ones."""
+    """Set the process-wide launch flags (KQ_LAUNCH_PDL, KQ_LAUNCH_GEMV_SPLIT); returns the old ones."""
     return int(_lib.kq_set_launch_flags(int(flags)))
 
 

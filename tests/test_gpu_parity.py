@@ -148,6 +148,43 @@ def test_gemv_full_size_layers(K, cfg_index):
         assert_row_tol(y, oracle.gemm(m.fmt, disk, *planes)[0])
 
 
+@pytest.mark.parametrize("fmt,N,Kdim", [(synth.Q6_K, 2560, 9728), (synth.Q4_K, 2563, 4096),
+                                        (synth.Q5_K, 3000, 768), (synth.Q4_K, 4096 + 16 * 3, 256),
+                                        (synth.Q6_K, 17, 1024)])
+@pytest.mark.parametrize("always_cut", [False, True])
+def test_gemv_workspace_modes(K, fmt, N, Kdim, always_cut):
+    """With a workspace an SM gets an even share of the superblocks (always,
+    under KQ_LAUNCH_GEMV_SPLIT; else where whole row groups leave a warp well
+    above it) and the row groups cut between two blocks are finished through
+    it; without one the blocks take whole row groups.  All agree with the
+    oracle, each gives the same bits on every call, and the workspace is left
+    zero-filled."""
+    rng = synth.rng_for(112, fmt * 100000 + N + Kdim)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    x = synth.activations(1, Kdim, rng, outliers=True)
+    planes = oracle_q8k(x)
+    ref = oracle.gemm(fmt, disk, *planes)[0]
+    packed = pack(K, fmt, disk)
+    a = q8k_to_dev(K, planes)
+    ws = torch.zeros(K.KQ_GEMV_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    old = K.kq_set_launch_flags(K.KQ_LAUNCH_GEMV_SPLIT if always_cut else 0)
+    try:
+        for mode in (ws, False):
+            outs = []
+            for _ in range(3):
+                full, y = poisoned((N,))
+                K.kq_gemv(fmt, packed, N, Kdim, a, y=y, workspace=mode)
+                torch.cuda.synchronize()
+                check_guard(full, N)
+                outs.append(y.cpu().numpy())
+            assert_row_tol(outs[0], ref)
+            np.testing.assert_array_equal(outs[1], outs[0])
+            np.testing.assert_array_equal(outs[2], outs[0])
+    finally:
+        K.kq_set_launch_flags(old)
+    assert int(torch.count_nonzero(ws)) == 0   # every exchange word emptied again
+
+
 def test_gemv_row_stride(K):
     """8 rows, each perturbed differently: each output equals its own row's
     dot (the page's multi-row stride gate)."""
@@ -354,6 +391,29 @@ def test_gemv_fused_multi_matrix_bit_identical(K, fmt):
         y_sep = K.kq_gemv(fmt, pk, N, Kdim, a)
         torch.cuda.synchronize()
         assert_row_tol(y.cpu().numpy(), y_sep.cpu().numpy().astype(np.float64), rel=1e-5)
+        assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes)[0])
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_gemv_fused_cuts_across_matrices(K, fmt):
+    """Ragged matrices and few superblocks per row group: the blocks' item
+    ranges cut row groups at matrix edges and inside them."""
+    rng = synth.rng_for(113, fmt)
+    Kdim = 768
+    Ns = [1000, 8, 333, 4100]
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for N in Ns]
+    packs = [pack(K, fmt, d) for d in disks]
+    x = synth.activations(1, Kdim, rng)
+    planes = oracle_q8k(x)
+    old = K.kq_set_launch_flags(K.KQ_LAUNCH_GEMV_SPLIT)
+    try:
+        fulls = [poisoned((N,)) for N in Ns]
+        K.kq_gemv_fused(fmt, packs, Ns, Kdim, to_dev(x[0]), [f[1] for f in fulls])
+        torch.cuda.synchronize()
+    finally:
+        K.kq_set_launch_flags(old)
+    for N, disk, (full, y) in zip(Ns, disks, fulls):
+        check_guard(full, N)
         assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes)[0])
 
 

@@ -59,29 +59,49 @@ def test_host_argument_checks(kq):
     goodq = Q(0x10000, 0x10000, 0x10000)
     ARG, ALIGN, FMT, WS = -1, -2, -3, -6
     # format
-    assert lib.kq_gemv(9, fake, 8, 256, goodq, fake, None) == FMT
+    assert lib.kq_gemv(9, fake, 8, 256, goodq, fake, None, 0, None) == FMT
     assert lib.kq_repack(0, fake, 8, 256, fake, None) == FMT
     # shapes
-    assert lib.kq_gemv(1, fake, 8, 100, goodq, fake, None) == ARG
-    assert lib.kq_gemv(1, fake, -1, 256, goodq, fake, None) == ARG
+    assert lib.kq_gemv(1, fake, 8, 100, goodq, fake, None, 0, None) == ARG
+    assert lib.kq_gemv(1, fake, -1, 256, goodq, fake, None, 0, None) == ARG
     assert lib.kq_quantize_q8k(fake, -1, 256, goodq, None) == ARG
     assert lib.kq_quantize_q8k(fake, 2, 300, goodq, None) == ARG
     # null pointers
-    assert lib.kq_gemv(1, None, 8, 256, goodq, fake, None) == ARG
-    assert lib.kq_gemv(1, fake, 8, 256, nullq, fake, None) == ARG
+    assert lib.kq_gemv(1, None, 8, 256, goodq, fake, None, 0, None) == ARG
+    assert lib.kq_gemv(1, fake, 8, 256, nullq, fake, None, 0, None) == ARG
     assert lib.kq_gemm(1, fake, 8, 256, goodq, 4, None, None, 0, None) == ARG
     assert lib.kq_gemm_grouped(1, fake, 4, None, 8, 256, goodq, 4, fake, None, 0, None) == ARG
     assert lib.kq_quantize_q8k(None, 2, 256, goodq, None) == ARG
     # alignment
-    assert lib.kq_gemv(1, odd, 8, 256, goodq, fake, None) == ALIGN
-    assert lib.kq_gemv(1, fake, 8, 256, Q(0x10000, 0x10004, 0x10000), fake, None) == ALIGN
+    assert lib.kq_gemv(1, odd, 8, 256, goodq, fake, None, 0, None) == ALIGN
+    assert lib.kq_gemv(1, fake, 8, 256, Q(0x10000, 0x10004, 0x10000), fake, None, 0, None) == ALIGN
     assert lib.kq_quantize_q8k(odd, 2, 256, goodq, None) == ALIGN
     assert lib.kq_repack(1, odd, 8, 256, fake, None) == ALIGN
+    # GEMV workspace: too small / misaligned
+    wsn = kq.KQ_GEMV_WORKSPACE_BYTES
+    assert wsn == lib.kq_gemv_workspace_bytes() == 64 * 1024
+    assert lib.kq_gemv(1, fake, 8, 256, goodq, fake, fake, wsn - 1, None) == WS
+    assert lib.kq_gemv(1, fake, 8, 256, goodq, fake, odd, wsn, None) == ALIGN
+    pk1 = (ctypes.c_void_p * 1)(0x10000)
+    n1 = (ctypes.c_int64 * 1)(8)
+    y1 = (ctypes.c_void_p * 1)(0x10000)
+    assert lib.kq_gemv_fused(1, 1, pk1, n1, 256, fake, y1, fake, 16, None) == WS
     # empty problems are no-ops that touch nothing
-    assert lib.kq_gemv(1, None, 0, 256, nullq, None, None) == 0
+    assert lib.kq_gemv(1, None, 0, 256, nullq, None, None, 0, None) == 0
     assert lib.kq_gemm(2, None, 16, 512, nullq, 0, None, None, 0, None) == 0
     assert lib.kq_quantize_q8k(None, 0, 256, nullq, None) == 0
     # workspace: required size must be provided when non-zero
     need = kq.kq_gemm_workspace_bytes(1, 512, 4096, 2560)
     if need:
         assert lib.kq_gemm(1, fake, 4096, 2560, goodq, 512, fake, None, 0, None) == WS
+
+
+def test_launch_flags_mask(kq):
+    """Unknown flag bits are dropped; the two defined ones are kept."""
+    old = kq.kq_set_launch_flags(0xFFFF)
+    try:
+        assert kq.kq_get_launch_flags() == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT
+        assert kq.kq_set_launch_flags(0) == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT
+        assert kq.kq_get_launch_flags() == 0
+    finally:
+        kq.kq_set_launch_flags(old)
