@@ -364,10 +364,15 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     __shared__ int64_t s_gpre[GEMV_MAX_MATRICES + 1], s_n[GEMV_MAX_MATRICES];
     __shared__ float *s_y[GEMV_MAX_MATRICES];
     __shared__ uint64_t s_bar[8][GEMV_MAX_D];
-    // a warp's partial sums of the row groups it shares with other warps:
-    // slot 0 = the group its range starts inside, slot 1 = the group it ends inside
+    // a warp's partial sums of the row groups it shares with other warps or
+    // blocks: slot 0 = the group its range starts inside, slot 1 = the group
+    // it ends inside; and, where the warp finishes such a group, how: the
+    // mask of the warps that hold a part (0: another warp finishes it), the
+    // matrix, the group's first output row in it, and the cut between blocks
+    // (-1: none)
     __shared__ float s_rec[8][2][16];
-    __shared__ int64_t s_rec_g[8][2];
+    __shared__ int s_fin_mask[8][2], s_fin_m[8][2];
+    __shared__ int64_t s_fin_row[8][2], s_fin_cut[8][2];
     // the next kernel may be scheduled now: it waits for this grid to
     // complete before it reads anything this grid writes
     griddep_launch_dependents();
@@ -397,7 +402,6 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     if (lane == 0) {
         for (int i = 0; i < D; ++i) sm100::mbar_init(&bars[i], 1);
         sm100::mbar_fence_init();
-        s_rec_g[warp][0] = s_rec_g[warp][1] = -1;
     }
     __syncthreads();
 
@@ -421,6 +425,27 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     const int64_t g0 = w0 / nsb;
     const int sb0 = (int)(w0 - g0 * nsb);
     const int m0 = matrix_of_group(g0);
+    // Plan of the shared row groups, made before the wait so that none of
+    // it is on the path after the previous kernel completes.
+    if (lane < 2) {
+        const int slot = lane;
+        const int64_t g = slot == 0 ? g0 : (w1 - 1) / nsb;
+        const bool rec = w0 < w1 && (slot == 0 ? g * nsb < w0 : (g * nsb >= w0 && (g + 1) * nsb > w1));
+        int mask = 0;
+        if (rec) {
+            const int64_t lo = g * nsb, hi = lo + nsb;
+            for (int w = 0; w < 8; ++w) {
+                const int64_t a = I0 + w * (I1 - I0) / 8, b = I0 + (w + 1) * (I1 - I0) / 8;
+                if (a < b && a < hi && b > lo) mask |= 1 << w;
+            }
+            if ((mask & ((1 << warp) - 1)) != 0) mask = 0;  // a lower warp finishes it
+            const int mm = matrix_of_group(g);
+            s_fin_m[warp][slot] = mm;
+            s_fin_row[warp][slot] = (g - s_gpre[mm]) * GROUP_ROWS;
+            s_fin_cut[warp][slot] = lo < I0 ? (int64_t)blockIdx.x - 1 : (hi > I1 ? (int64_t)blockIdx.x : -1);
+        }
+        s_fin_mask[warp][slot] = rec ? mask : -1;
+    }
     if (w0 < w1) {
         im = m0;
         icp = chunk_ptr<F>(s_planes[im], (uint64_t)(w0 - s_gpre[im] * nsb));
@@ -520,10 +545,8 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                 // the whole row group is this warp's
                 const int64_t n = (g - s_gpre[m]) * GROUP_ROWS + r16;
                 if (h == 0 && n < s_n[m]) s_y[m][n] = v;
-            } else {
-                const int slot = g * nsb < w0 ? 0 : 1;
-                if (h == 0) s_rec[warp][slot][r16] = v;
-                if (lane == 0) s_rec_g[warp][slot] = g;
+            } else if (h == 0) {
+                s_rec[warp][g * nsb < w0 ? 0 : 1][r16] = v;
             }
             if (sb == nsb) {
                 sb = 0;
@@ -545,21 +568,17 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // the exchanged word carries the value itself.
 #pragma unroll 1
     for (int slot = 0; slot < 2; ++slot) {
-        const int64_t gg = s_rec_g[warp][slot];
-        if (gg < 0) continue;
-        bool owner = true;
-        for (int w = 0; w < warp; ++w)
-            if (s_rec_g[w][0] == gg || s_rec_g[w][1] == gg) owner = false;
-        if (!owner) continue;
-        float v = 0.0f;
-        for (int w = warp; w < 8; ++w) {
-            if (s_rec_g[w][0] == gg) v += s_rec[w][0][r16];
-            else if (s_rec_g[w][1] == gg) v += s_rec[w][1][r16];
-        }
-        const int mm = matrix_of_group(gg);
-        const int64_t n = (gg - s_gpre[mm]) * GROUP_ROWS + r16;
-        const bool left_cut = gg * nsb < I0, right_cut = (gg + 1) * nsb > I1;
-        if (!left_cut && !right_cut) {
+        const int mask = s_fin_mask[warp][slot];
+        if (mask <= 0) continue;
+        // every warp after the first that holds part of the group holds it
+        // in its slot 0
+        float v = s_rec[warp][slot][r16];
+#pragma unroll
+        for (int w = 1; w < 8; ++w)
+            if (w > warp && ((mask >> w) & 1)) v += s_rec[w][0][r16];
+        const int mm = s_fin_m[warp][slot];
+        const int64_t n = s_fin_row[warp][slot] + r16, cut = s_fin_cut[warp][slot];
+        if (cut < 0) {
             if (h == 0 && n < s_n[mm]) s_y[mm][n] = v;
             continue;
         }
@@ -567,7 +586,6 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
         // two swaps its partial sum, tagged, into the row's workspace word;
         // the one that gets the other's tagged value back arrives second,
         // adds the two and empties the word for the next call.
-        const int64_t cut = left_cut ? (int64_t)blockIdx.x - 1 : (int64_t)blockIdx.x;
         unsigned long long *word = p.ws + cut * 16 + r16;
         if (h == 0) {
             const unsigned long long old = atomicExch(word, GEMV_TAG | __float_as_uint(v));
