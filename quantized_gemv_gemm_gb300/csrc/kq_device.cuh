@@ -436,30 +436,6 @@ __device__ __forceinline__ void quantize_block_warp(const float *xb, int lane, i
     if (lane == 0) *db = d8;
 }
 
-// ---------------------------------------------------------------------------
-// Decode-GEMV staging of one activation superblock in shared memory: the
-// 256 quants, the block scale, and the sums the fold needs -- for Q4_K and
-// Q5_K the int32 sum of each 32-element sub-block (bs_2j + bs_2j+1, the
-// factor of sub-min j), for Q6_K the 16 int16 bsums.  Both forms take 32
-// bytes per superblock.
-
-// From fp32 values (the fused quantize): v0 / v1 as for q8k_lane.
-template <bool PAIRS>
-__device__ __forceinline__ void stage_block_from_x(float4 v0, float4 v1, int lane, int8_t *qb, void *sb, float *db) {
-    int part;
-    float d8;
-    const uint2 w = q8k_lane(v0, v1, part, d8);
-    *reinterpret_cast<uint2 *>(qb + 8 * lane) = w;
-    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);        // 16-element sums
-    if constexpr (PAIRS) {
-        part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);    // 32-element sums
-        if ((lane & 3) == 0) static_cast<int *>(sb)[lane >> 2] = part;
-    } else {
-        if ((lane & 1) == 0) static_cast<int16_t *>(sb)[lane >> 1] = static_cast<int16_t>(part);
-    }
-    if (lane == 0) *db = d8;
-}
-
 // Bulk prefetch of [p, p + bytes) from HBM into L2 by the TMA engine
 // (cp.async.bulk.prefetch.L2, a hint: nothing is written, nothing waits).
 // p must be 16-byte aligned; the size is rounded down to 16 bytes and split

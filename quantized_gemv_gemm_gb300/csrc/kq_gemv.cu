@@ -320,6 +320,29 @@ __device__ __forceinline__ float item_dmin(const ItemQ5 &w) { return half_hi(w.h
 __device__ __forceinline__ float item_dmin(const ItemQ6 &) { return 0.0f; }
 
 // ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// Staging of one activation superblock from the fp32 row (the fused
+// quantize, bit-identical to kq_quantize_q8k through q8k_lane): the 256
+// quants, the block scale, and the sums the fold needs -- for Q4_K and Q5_K
+// the int32 sum of each 32-element sub-block (bs_2j + bs_2j+1, the factor of
+// sub-min j), for Q6_K the 16 int16 bsums; both forms take 32 bytes.  The
+// lane holds elements 8*lane .. 8*lane+7 in v0, v1.
+template <bool PAIRS>
+__device__ __forceinline__ void stage_block_from_x(float4 v0, float4 v1, int lane, int8_t *qb, void *sb, float *db) {
+    int part;
+    float d8;
+    const uint2 w = q8k_lane(v0, v1, part, d8);
+    *reinterpret_cast<uint2 *>(qb + 8 * lane) = w;
+    part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);        // 16-element sums
+    if constexpr (PAIRS) {
+        part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);    // 32-element sums
+        if ((lane & 3) == 0) static_cast<int *>(sb)[lane >> 2] = part;
+    } else {
+        if ((lane & 1) == 0) static_cast<int16_t *>(sb)[lane >> 1] = static_cast<int16_t>(part);
+    }
+    if (lane == 0) *db = d8;
+}
+
 struct GemvParams {
     int nmat;
     const uint8_t *packed[GEMV_MAX_MATRICES];
@@ -610,9 +633,13 @@ static int sm_count() {
 }
 
 // Above this many items per SM a launch takes two blocks per SM (more warps
-// folding), giving up the room for the next kernel's block.
+// folding), giving up the room for the next kernel's block -- unless K is
+// long, since every block quantizes the whole row.
 #ifndef KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM
-#define KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM 1000000000
+#define KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM 100
+#endif
+#ifndef KQ_GEMV_TWO_BLOCKS_MAX_NSB
+#define KQ_GEMV_TWO_BLOCKS_MAX_NSB 32
 #endif
 
 #ifndef KQ_GEMV_CUT_ITEMS
@@ -636,7 +663,8 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     // one block per SM, each with an even share of the items; a row group
     // may then be cut between two blocks, which needs the workspace
     int64_t blocks = sm_count();
-    if (p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks) blocks *= 2;
+    if (p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
+        blocks *= 2;
     if (blocks > GEMV_MAX_BLOCKS) blocks = GEMV_MAX_BLOCKS;
     if (blocks > G) blocks = G;  // every row group spans at most two blocks
     // cut row groups between blocks only where whole row groups would leave
