@@ -12,7 +12,7 @@
 //     unpack warps expand the packed weights once into shared memory as fp16
 //     w' = sc*q with the sub-scale folded in (Q4_K <= 945, Q5_K <= 1953:
 //     exact): the kq v3 panel scratch, unpacked once per token block;
-//     Q6_K's w' = sc*(q-32) is exact for |sc| <= 64, and when a tile holds a
+//     Q6_K's w' = sc*(q-32) is one exact fp16 FMA for |sc| <= 62, and when a tile holds a
 //     larger sub-scale the weight is split into two exact planes,
 //     sc*(v - (v&1)) (even, |.| <= 4096) and sc*(v&1), both multiplied into
 //     the same accumulator;
@@ -164,36 +164,44 @@ __device__ __forceinline__ void unpack_q45(uint32_t a_tile, int r, const uint32_
 // Q6_K: sub-tile j of half h holds groups t = 2j (K 0..31) and 2j+1 (K 32..63)
 // of the half: element 128h + 32t + l is the low (t < 2) or high (t >= 2)
 // nibble of ql[64h + 32(t&1) + l] with bits 2t..2t+1 of qh[32h + l] on top,
-// sub-scale sc[8h + 2t + l/16] (byte 2(t - 2j) + l/16 of `scw`).  v = q - 32:
-// P1 = v*sc is exact for |sc| <= 64; with `split`, P1 = (v - (v&1))*sc and
-// P2 = (v&1)*sc.  `zero2` writes zeros to this thread's P2 rows instead.
+// sub-scale sc[8h + 2t + l/16] (byte 2(t - 2j) + l/16 of `scw`).  The 6-bit
+// q of four elements is assembled in one word, then spread into fp16 lanes
+// 1024 + q.  v = q - 32: P1 = v*sc = (1024 + q)*sc - 1056*sc in one fp16 FMA,
+// exact for |sc| <= 62 (1056*sc and the result are exact fp16 integers); with
+// `split` (some |sc| > 62), P1 = (v - (v&1))*sc and P2 = (v&1)*sc, each exact.
+// `zero2` writes zeros to this thread's P2 rows instead.
 __device__ __forceinline__ void unpack_q6(uint32_t a_tile, uint32_t a2_tile, int r, const uint32_t (&ql)[16],
                                           const uint32_t (&qh)[8], uint32_t scw, int j, bool split, bool zero2) {
     const uint32_t off1056 = h2_splat(1056.0f);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
         const int t = 2 * j + tt;
+        // the group's two sub-scales (l < 16, l >= 16) and -1056 * each
+        uint32_t s2v[2], c2v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int scv = (int)(int8_t)((scw >> (8 * (2 * tt + u))) & 0xFF);
+            s2v[u] = h2_splat((float)scv);
+            c2v[u] = h2_splat(-1056.0f * (float)scv);
+        }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // K 32tt + 8q .. +7: l = 8q .. 8q+7
-            const int scv = (int)(int8_t)((scw >> (8 * (2 * tt + (q >> 1)))) & 0xFF);
-            const uint32_t s2 = h2_splat((float)scv);
+            const uint32_t s2 = s2v[q >> 1], c2 = c2v[q >> 1];
             uint32_t p1[4], p2[4];
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 const uint32_t lword = ql[8 * (t & 1) + 2 * q + w];
-                const uint32_t nib = (t >= 2) ? (lword >> 4) : lword;
-                const uint32_t hword = qh[2 * q + w] >> (2 * t);
+                const uint32_t nib = ((t >= 2) ? (lword >> 4) : lword) & 0x0F0F0F0Fu;
+                const uint32_t q6 = nib | (((qh[2 * q + w] >> (2 * t)) & 0x03030303u) << 4);  // four q, 0..63
 #pragma unroll
                 for (int pr = 0; pr < 2; ++pr) {
-                    const uint32_t sel = pr ? SEL_23 : SEL_01;
-                    uint32_t x = prmt(nib, MAGIC, sel) & 0xFF0FFF0Fu;
-                    x |= (prmt(hword, 0u, sel) << 4) & 0x00300030u;   // fp16 1024 + q, q = 0..63
+                    const uint32_t x = prmt(q6, MAGIC, pr ? SEL_23 : SEL_01);  // fp16 1024 + q
                     if (split) {
                         const uint32_t odd = x & 0x00010001u;
                         p1[2 * w + pr] = h2_mul(h2_sub(x ^ odd, off1056), s2);
                         p2[2 * w + pr] = h2_mul(odd * 0x3C00u, s2);     // fp16 1.0 in each odd lane
                     } else {
-                        p1[2 * w + pr] = h2_mul(h2_sub(x, off1056), s2);
+                        p1[2 * w + pr] = h2_fma(x, s2, c2);
                         p2[2 * w + pr] = 0u;
                     }
                 }
@@ -477,7 +485,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int v = (int)(int8_t)((cur.sc[jj] >> (8 * i)) & 0xFF);
-                        big[jj] |= (v > 64 || v < -64);
+                        big[jj] |= (v > 62 || v < -62);
                     }
                 const unsigned any = __ballot_sync(0xFFFFFFFFu, big[0] || big[1]);
                 if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;

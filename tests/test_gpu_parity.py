@@ -443,10 +443,10 @@ def test_gemv_fused_layer_groups_and_edges(K):
 
 
 # ---------------------------------------------------------------- Q6_K sub-scale range
-@pytest.mark.parametrize("sc_range", [(-128, 128), (-64, 65), (60, 70)])
+@pytest.mark.parametrize("sc_range", [(-128, 128), (-64, 65), (60, 70), (-62, 63)])
 def test_gemm_q6k_full_subscale_range(K, sc_range):
     """Real Q6_K files use signed sub-scales over the whole int8 range, beyond
-    what one exact fp16 plane holds (|sc| <= 64); the tensor-core path splits
+    what one exact fp16 plane holds (|sc| <= 62); the tensor-core path splits
     those superblocks into two exact planes.  Checked against the oracle."""
     fmt, M, N, Kdim = synth.Q6_K, 64, 256, 1024
     rng = synth.rng_for(111, sc_range[0] + 1000)
