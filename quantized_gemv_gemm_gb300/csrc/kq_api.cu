@@ -56,6 +56,9 @@ int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offse
     if (ws && !aligned(ws, 256)) return KQ_ERR_ALIGN;
     const Q8K q{a.d, a.qs, a.bsums};
     const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
+    // a few token rows: the decode GEMV's weight stream, each item read once
+    // for up to 8 tokens
+    if (!offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K) return launch_status(launch_gemv_batch(f, packed, N, K, q, M, y, s));
     cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();

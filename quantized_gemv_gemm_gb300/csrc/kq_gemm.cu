@@ -688,7 +688,6 @@ static WsLayout ws_layout(int64_t M, int64_t K) {
 }
 
 // M below which the CUDA-core token-group kernel is used instead
-constexpr int64_t GEMM_TC_MIN_M = 16;
 
 size_t gemm_workspace_bytes(int, int64_t M, int64_t, int64_t K) {
     if (M < GEMM_TC_MIN_M) return 0;

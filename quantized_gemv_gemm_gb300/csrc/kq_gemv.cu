@@ -355,9 +355,11 @@ struct GemvParams {
     int D;                                 // ring stages per warp
     unsigned long long *ws;                // [grid][16] words of the row groups cut between blocks
     const float *x;                        // fp32 row (fused quantize), or nullptr
-    const float *d8;                       // else: the Q8_K planes of the row
+    const float *d8;                       // else: the Q8_K planes of the rows
     const int8_t *qs;
     const int16_t *bs;
+    int ntok;                              // token rows folded per pass (1..T of the kernel)
+    int64_t stage_stride;                  // bytes between the staged rows of two tokens
 };
 
 // Bounded wait on a stage's mbarrier (about one second): on expiry the
@@ -377,7 +379,11 @@ __device__ __forceinline__ int64_t block_item(const GemvParams &p, int64_t b, in
     return p.split ? b * p.items / B : (b * G / B) * p.nsb;
 }
 
-template <int F>
+// T: the most token rows one pass folds (1 for decode; 2, 4, 8 for small
+// batches, which read each weight item once for all their tokens).  Token t's
+// activation row is staged at stage_stride * t, and its output row is
+// y[m] + t * N[m].
+template <int F, int T>
 __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     constexpr int SLOT = GemvFmt<F>::SLOT;
     using Item = typename ItemOf<F>::T;
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // mask of the warps that hold a part (0: another warp finishes it), the
     // matrix, the group's first output row in it, and the cut between blocks
     // (-1: none)
-    __shared__ float s_rec[8][2][16];
+    __shared__ float s_rec[8][2][T][16];
     __shared__ int s_fin_mask[8][2], s_fin_m[8][2];
     __shared__ int64_t s_fin_row[8][2], s_fin_cut[8][2];
     // the next kernel may be scheduled now: it waits for this grid to
@@ -401,6 +407,8 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     griddep_launch_dependents();
     const int64_t K = p.K, nsb = p.nsb;
     const int D = p.D;
+    const int ntok = T == 1 ? 1 : p.ntok;
+    const uint32_t tstride = T == 1 ? 0u : (uint32_t)p.stage_stride;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r16 = lane & 15, h = lane >> 4;
     const uint32_t ring_s = smem_addr(smem + (size_t)warp * D * SLOT);
@@ -511,20 +519,25 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
             }
         }
     } else {
-        const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs);
-        for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(s_qs)[i] = gq[i];
-        if constexpr (PAIRS) {
-            // sum of each 32-element sub-block = two consecutive bsums
-            const int *gb = reinterpret_cast<const int *>(p.bs);
-            for (int64_t i = threadIdx.x; i < K / 32; i += 256) {
-                const int v = gb[i];
-                reinterpret_cast<int *>(s_sum)[i] = (int)(int16_t)(v & 0xFFFF) + (v >> 16);
+        for (int t = 0; t < ntok; ++t) {
+            uint8_t *tq = reinterpret_cast<uint8_t *>(s_qs) + (size_t)t * tstride;
+            uint8_t *ts = s_sum + (size_t)t * tstride;
+            float *td = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + (size_t)t * tstride);
+            const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs + t * K);
+            for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(tq)[i] = gq[i];
+            if constexpr (PAIRS) {
+                // sum of each 32-element sub-block = two consecutive bsums
+                const int *gb = reinterpret_cast<const int *>(p.bs + t * (K / 16));
+                for (int64_t i = threadIdx.x; i < K / 32; i += 256) {
+                    const int v = gb[i];
+                    reinterpret_cast<int *>(ts)[i] = (int)(int16_t)(v & 0xFFFF) + (v >> 16);
+                }
+            } else {
+                const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs + t * (K / 16));
+                for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(ts)[i] = gb[i];
             }
-        } else {
-            const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs);
-            for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(s_sum)[i] = gb[i];
+            for (int64_t i = threadIdx.x; i < nsb; i += 256) td[i] = p.d8[t * nsb + i];
         }
-        for (int64_t i = threadIdx.x; i < nsb; i += 256) s_d8[i] = p.d8[i];
     }
     __syncthreads();
 
@@ -537,7 +550,9 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // (the lane's half), sums and scale
     uint32_t a_cur = qs_s + (uint32_t)sb * QK + 128 * h, s_cur = sum_s + (uint32_t)sb * 32 + 16 * h;
     uint32_t d_cur = d8_s + 4 * (uint32_t)sb;
-    float acc = 0.0f;
+    float acc[T];
+#pragma unroll
+    for (int t = 0; t < T; ++t) acc[t] = 0.0f;
 #pragma unroll 1
     for (int64_t it = w0; it < w1; ++it) {
         stage_wait(&bars[rs], rph);
@@ -552,24 +567,55 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
             rs = 0;
             rph ^= 1u;
         }
-        int isum, msum;
-        item_fold(cur, h, a_cur, s_cur, isum, msum);
-        const float d8 = __uint_as_float(lds32(d_cur));
-        acc = fmaf(item_d(cur) * d8, static_cast<float>(isum), acc);
-        if constexpr (F != FMT_Q6_K) acc = fmaf(-(item_dmin(cur) * d8), static_cast<float>(msum), acc);
+        if constexpr (T == 1) {
+            int isum, msum;
+            item_fold(cur, h, a_cur, s_cur, isum, msum);
+            const float d8 = __uint_as_float(lds32(d_cur));
+            acc[0] = fmaf(item_d(cur) * d8, static_cast<float>(isum), acc[0]);
+            if constexpr (F != FMT_Q6_K) acc[0] = fmaf(-(item_dmin(cur) * d8), static_cast<float>(msum), acc[0]);
+        } else {
+            const float dw = item_d(cur), dmw = item_dmin(cur);
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                if (t < ntok) {
+                    int isum, msum;
+                    item_fold(cur, h, a_cur + t * tstride, s_cur + t * tstride, isum, msum);
+                    const float d8 = __uint_as_float(lds32(d_cur + t * tstride));
+                    acc[t] = fmaf(dw * d8, static_cast<float>(isum), acc[t]);
+                    if constexpr (F != FMT_Q6_K) acc[t] = fmaf(-(dmw * d8), static_cast<float>(msum), acc[t]);
+                }
+            }
+        }
         a_cur += QK;
         s_cur += 32;
         d_cur += 4;
         if (++sb == nsb || it + 1 == w1) {
             // the warp is done with row group g: add the row's two halves
-            const float v = acc + __shfl_xor_sync(0xFFFFFFFFu, acc, 16);
-            acc = 0.0f;
-            if (g * nsb >= w0 && (g + 1) * nsb <= w1) {
-                // the whole row group is this warp's
+            if constexpr (T == 1) {
+                const float v = acc[0] + __shfl_xor_sync(0xFFFFFFFFu, acc[0], 16);
+                acc[0] = 0.0f;
+                if (g * nsb >= w0 && (g + 1) * nsb <= w1) {
+                    // the whole row group is this warp's
+                    const int64_t n = (g - s_gpre[m]) * GROUP_ROWS + r16;
+                    if (h == 0 && n < s_n[m]) s_y[m][n] = v;
+                } else if (h == 0) {
+                    s_rec[warp][g * nsb < w0 ? 0 : 1][0][r16] = v;
+                }
+            } else {
+                const bool whole = g * nsb >= w0 && (g + 1) * nsb <= w1;
                 const int64_t n = (g - s_gpre[m]) * GROUP_ROWS + r16;
-                if (h == 0 && n < s_n[m]) s_y[m][n] = v;
-            } else if (h == 0) {
-                s_rec[warp][g * nsb < w0 ? 0 : 1][r16] = v;
+#pragma unroll
+                for (int t = 0; t < T; ++t) {
+                    const float v = acc[t] + __shfl_xor_sync(0xFFFFFFFFu, acc[t], 16);
+                    acc[t] = 0.0f;
+                    if (t < ntok && h == 0) {
+                        if (whole) {
+                            if (n < s_n[m]) s_y[m][t * s_n[m] + n] = v;
+                        } else {
+                            s_rec[warp][g * nsb < w0 ? 0 : 1][t][r16] = v;
+                        }
+                    }
+                }
             }
             if (sb == nsb) {
                 sb = 0;
@@ -595,12 +641,23 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
         if (mask <= 0) continue;
         // every warp after the first that holds part of the group holds it
         // in its slot 0
-        float v = s_rec[warp][slot][r16];
-#pragma unroll
-        for (int w = 1; w < 8; ++w)
-            if (w > warp && ((mask >> w) & 1)) v += s_rec[w][0][r16];
         const int mm = s_fin_m[warp][slot];
         const int64_t n = s_fin_row[warp][slot] + r16, cut = s_fin_cut[warp][slot];
+        if constexpr (T > 1) {
+            // (a launch folding several tokens never cuts row groups)
+            for (int t = 0; t < ntok; ++t) {
+                float v = s_rec[warp][slot][t][r16];
+#pragma unroll
+                for (int w = 1; w < 8; ++w)
+                    if (w > warp && ((mask >> w) & 1)) v += s_rec[w][0][t][r16];
+                if (h == 0 && n < s_n[mm]) s_y[mm][t * s_n[mm] + n] = v;
+            }
+            continue;
+        }
+        float v = s_rec[warp][slot][0][r16];
+#pragma unroll
+        for (int w = 1; w < 8; ++w)
+            if (w > warp && ((mask >> w) & 1)) v += s_rec[w][0][0][r16];
         if (cut < 0) {
             if (h == 0 && n < s_n[mm]) s_y[mm][n] = v;
             continue;
@@ -653,7 +710,17 @@ constexpr int64_t GEMV_SMEM_BUDGET = 110 * 1024;
 
 template <int F> constexpr int gemv_max_d() { return F == FMT_Q6_K ? 4 : (F == FMT_Q5_K ? 5 : 6); }
 
-template <int F>
+// Shared memory of a block folding several tokens per pass: it holds their
+// staged rows, so it takes up to 200 KB for the ring and rows (212 KB when a
+// long row leaves only the minimum ring): one block per SM, no room for the
+// next kernel's block.
+constexpr int64_t GEMV_BATCH_SMEM_BUDGET = 200 * 1024;
+constexpr int64_t GEMV_BATCH_MAX_SMEM = 212 * 1024;  // + the static ~9 KB stays within 227 KB
+
+// bytes of one token's staged row (quants, sums, scales), 16-byte aligned
+inline int64_t gemv_stage_stride(int64_t K) { return (K + K / 8 + K / 64 + 15) & ~int64_t(15); }
+
+template <int F, int T>
 static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaStream_t s) {
     p.gpre[0] = 0;
     for (int m = 0; m < p.nmat; ++m) p.gpre[m + 1] = p.gpre[m] + (p.N[m] + 15) / 16;
@@ -663,7 +730,7 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     // one block per SM, each with an even share of the items; a row group
     // may then be cut between two blocks, which needs the workspace
     int64_t blocks = sm_count();
-    if (p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
+    if (T == 1 && p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
         blocks *= 2;
     if (blocks > GEMV_MAX_BLOCKS) blocks = GEMV_MAX_BLOCKS;
     if (blocks > G) blocks = G;  // every row group spans at most two blocks
@@ -671,26 +738,29 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     // the busiest warp KQ_GEMV_CUT_ITEMS or more items above an even share:
     // the exchange at a cut costs about as much as folding a few items
     const int64_t whole = (G + blocks - 1) / blocks * p.nsb, even = (p.items + blocks - 1) / blocks;
-    p.split = ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
+    p.split = T == 1 && ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
               ((launch_flags() & LAUNCH_GEMV_SPLIT) || (whole + 7) / 8 - (even + 7) / 8 >= KQ_GEMV_CUT_ITEMS);
     p.ws = static_cast<unsigned long long *>(ws);
-    const int64_t stage_bytes = p.K + p.K / 8 + p.K / 64;
-    int64_t D = (GEMV_SMEM_BUDGET - stage_bytes) / (8 * GemvFmt<F>::SLOT);
+    p.stage_stride = gemv_stage_stride(p.K);
+    if (T == 1) p.ntok = 1;
+    const int64_t budget = T == 1 ? GEMV_SMEM_BUDGET : GEMV_BATCH_SMEM_BUDGET;
+    const int64_t stage_bytes = T * p.stage_stride;
+    int64_t D = (budget - stage_bytes) / (8 * GemvFmt<F>::SLOT);
     if (D > gemv_max_d<F>()) D = gemv_max_d<F>();
     if (D < 2) D = 2;
     p.D = (int)D;
     const size_t smem = (size_t)(8 * D * GemvFmt<F>::SLOT + stage_bytes);
-    static bool attr_set[64][4] = {};
+    static bool attr_set[64][4][9] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!attr_set[dev][F]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)GEMV_SMEM_BUDGET);
+    if (!attr_set[dev][F][T]) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(T == 1 ? GEMV_SMEM_BUDGET : GEMV_BATCH_MAX_SMEM));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gemv_kernel<F>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(gemv_kernel<F, T>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        attr_set[dev][F] = true;
+        attr_set[dev][F][T] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
@@ -702,7 +772,12 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<F>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, T>, p);
+}
+
+template <int F>
+static cudaError_t launch_gemv_f(GemvParams p, void *ws, size_t ws_bytes, cudaStream_t s) {
+    return launch_gemv_t<F, 1>(p, ws, ws_bytes, s);
 }
 
 cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
@@ -720,9 +795,60 @@ cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_
     p.d8 = a.d;
     p.qs = a.qs;
     p.bs = a.bsums;
-    if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K>(p, ws, ws_bytes, s);
-    if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K>(p, ws, ws_bytes, s);
-    return launch_gemv_t<FMT_Q6_K>(p, ws, ws_bytes, s);
+    if (f == FMT_Q4_K) return launch_gemv_f<FMT_Q4_K>(p, ws, ws_bytes, s);
+    if (f == FMT_Q5_K) return launch_gemv_f<FMT_Q5_K>(p, ws, ws_bytes, s);
+    return launch_gemv_f<FMT_Q6_K>(p, ws, ws_bytes, s);
+}
+
+// Small batches (M token rows, M < the tensor-core GEMM's minimum): passes of
+// up to 8 tokens, each reading every weight item once for all its tokens.
+int64_t gemv_batch_max_tokens(int64_t K) {
+    int64_t t = 8;
+    while (t > 1 && t * gemv_stage_stride(K) + 2 * 8 * 3360 > GEMV_BATCH_MAX_SMEM) t >>= 1;
+    return t;
+}
+
+template <int F>
+static cudaError_t launch_gemv_batch_f(GemvParams p, int64_t M, int64_t tmax, cudaStream_t s) {
+    const float *y0 = p.y[0];
+    const int8_t *q0 = p.qs;
+    const int16_t *b0 = p.bs;
+    const float *d0 = p.d8;
+    for (int64_t t0 = 0; t0 < M; t0 += tmax) {
+        const int64_t n = M - t0 < tmax ? M - t0 : tmax;
+        p.ntok = (int)n;
+        p.y[0] = const_cast<float *>(y0) + t0 * p.N[0];
+        p.qs = q0 + t0 * p.K;
+        p.bs = b0 + t0 * (p.K / 16);
+        p.d8 = d0 + t0 * p.nsb;
+        cudaError_t e;
+        if (n > 4) e = launch_gemv_t<F, 8>(p, nullptr, 0, s);
+        else if (n > 2) e = launch_gemv_t<F, 4>(p, nullptr, 0, s);
+        else if (n > 1) e = launch_gemv_t<F, 2>(p, nullptr, 0, s);
+        else e = launch_gemv_t<F, 1>(p, nullptr, 0, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
+                              cudaStream_t s) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    GemvParams p{};
+    p.nmat = 1;
+    p.packed[0] = static_cast<const uint8_t *>(packed);
+    p.N[0] = N;
+    p.y[0] = y;
+    p.K = K;
+    p.nsb = K / QK;
+    p.x = nullptr;
+    p.d8 = a.d;
+    p.qs = a.qs;
+    p.bs = a.bsums;
+    const int64_t tmax = gemv_batch_max_tokens(K);
+    if (f == FMT_Q4_K) return launch_gemv_batch_f<FMT_Q4_K>(p, M, tmax, s);
+    if (f == FMT_Q5_K) return launch_gemv_batch_f<FMT_Q5_K>(p, M, tmax, s);
+    return launch_gemv_batch_f<FMT_Q6_K>(p, M, tmax, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -49,6 +49,12 @@ static_assert(GEMV_MAX_BLOCKS * 16 * 8 <= (int64_t)KQ_GEMV_WORKSPACE_BYTES, "GEM
 cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K, const float *x,
                         Q8K a, float *const *y, void *ws, size_t ws_bytes, cudaStream_t s);
 
+// Small batches (M < GEMM_TC_MIN_M token rows) on the decode GEMV's stream:
+// passes of up to 8 tokens that read each weight item once.
+constexpr int64_t GEMM_TC_MIN_M = 16;
+cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
+                              cudaStream_t s);
+
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);
 

@@ -221,6 +221,25 @@ def test_gemm_small_shapes(K, fmt, M, N, Kdim):
     assert_row_tol(y, oracle.gemm(fmt, disk, *planes))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,N,Kdim", [(5, 333, 2560), (8, 2560, 9728), (9, 1000, 768), (15, 77, 1024),
+                                      (6, 40, 17408)])
+def test_gemm_small_batch(K, fmt, M, N, Kdim):
+    """Small batches (M < 16) run on the decode GEMV's weight stream in passes
+    of up to 8 tokens (4 when K is long): every output against the oracle, and
+    each token row equal to the GEMV of that token alone."""
+    rng = synth.rng_for(114, fmt * 100000 + M * 1000 + N)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    planes = oracle_q8k(synth.activations(M, Kdim, rng, outliers=True))
+    y = run_gemm(K, fmt, disk, planes, M)
+    assert_row_tol(y, oracle.gemm(fmt, disk, *planes))
+    packed = pack(K, fmt, disk)
+    for m in (0, M - 1):
+        one = tuple(p[m:m + 1] for p in planes)
+        g = K.kq_gemv(fmt, packed, N, Kdim, q8k_to_dev(K, one)).cpu().numpy()
+        assert_row_tol(y[m], g.astype(np.float64), rel=1e-5)
+
+
 def sample_check(y, fmt, disk, planes, rng, n_rows=48, n_toks=6):
     """Oracle on all tokens x sampled rows, and sampled tokens x all rows."""
     M, N = y.shape
