@@ -8,7 +8,8 @@ Steps rotate over L distinct copies of the layer's weights (8 by default,
 505 MB, about 4x the 126 MB L2) so that every step streams its weights from
 HBM, as consecutive layers of a model do.  `value` = weight bytes streamed
 per second (GB/s), timed on the device with CUDA events around K steps
-replayed from CUDA graphs.
+replayed from CUDA graphs of 32 layer steps (about one decode pass of a
+36-layer model).
 
 Also reported: the same metric end to end (activations copied in from pinned
 host memory and outputs copied back every step), the roofline of the GEMV
@@ -154,6 +155,9 @@ class ClockSampler:
 # the decode-layer workload on the GPU
 
 LAYER_INPUTS = [("x_attn", 2560), ("x_o", 4096), ("x_ffn", 2560), ("x_down", 9728)]
+# rotations of the layer copies captured in one CUDA graph (4 x 8 = 32 layer
+# steps, about one decode pass of a 36-layer model)
+GRAPH_ROTATIONS = 4
 # matrix -> index of its input
 LAYER_USES = {"wq": 0, "wk": 0, "wv": 0, "wo": 1, "gate": 2, "up": 2, "down": 3}
 
@@ -256,8 +260,11 @@ def run_ours(args, world, rank, local):
     L = args.layers
     layers = DecodeLayers(kq, torch, L)
     NG = len(layers.GROUPS)
-    g_plain = graph_of(torch, lambda: [layers.step(l) for l in range(L)])
-    g_sep = graph_of(torch, lambda: [layers.step(l, fused=False) for l in range(L)])
+    # one graph holds GRAPH_STEPS layer steps (the layer copies in rotation),
+    # as one decode pass of a 36-layer model is one graph
+    G = GRAPH_ROTATIONS * L
+    g_plain = graph_of(torch, lambda: [layers.step(l % L) for l in range(G)])
+    g_sep = graph_of(torch, lambda: [layers.step(l % L, fused=False) for l in range(G)])
 
     # events around every launch of every step of one rotation
     def timing_event():
@@ -274,9 +281,9 @@ def run_ours(args, world, rank, local):
         ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(NG)] for _ in range(L)]
 
-    reps = max(1, args.steps // L)
-    steps = reps * L
-    warm_reps = max(1, -(-args.warmup // L))
+    reps = max(1, args.steps // G)
+    steps = reps * G
+    warm_reps = max(1, -(-args.warmup // G))
     for _ in range(warm_reps):
         g_plain.replay()
         g_sep.replay()
@@ -327,7 +334,7 @@ def run_ours(args, world, rank, local):
     ms_sep = max_over_ranks(ms_sep)
     bytes_per_step = layers.weight_bytes
     value = bytes_per_step * steps * world / (ms_max * 1e-3) / 1e9
-    value_sep = bytes_per_step * max(1, reps // 2) * L * world / (ms_sep * 1e-3) / 1e9
+    value_sep = bytes_per_step * max(1, reps // 2) * G * world / (ms_sep * 1e-3) / 1e9
 
     # roofline of the GEMV kernel: the timed region holds nothing but its
     # launches (4 per step), so its average launch duration is the region's
@@ -350,9 +357,9 @@ def run_ours(args, world, rank, local):
     x_views = [x_dev[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))]
 
     def e2e_rot():
-        for l in range(L):
+        for l in range(G):
             x_dev.copy_(x_host, non_blocking=True)
-            layers.step(l, x_override=x_views)
+            layers.step(l % L, x_override=x_views)
             y_host.copy_(layers.y, non_blocking=True)
 
     g_e2e = graph_of(torch, e2e_rot)
@@ -372,10 +379,11 @@ def run_ours(args, world, rank, local):
         tt = torch.tensor([e_ms], device="cuda")
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e_ms = float(tt.item())
-    e2e_value = bytes_per_step * e_reps * L * world / (e_ms * 1e-3) / 1e9
+    e2e_value = bytes_per_step * e_reps * G * world / (e_ms * 1e-3) / 1e9
     y_check = y_host.numpy()
     assert np.isfinite(y_check).all()
 
+    small_batch = bench_small_batch(kq, torch, layers, peaks, args)
     gemv_27b = bench_gemv_27b(kq, torch, peaks, args)
     gemm = None if args.no_gemm else bench_gemm(kq, torch, peaks, args)
 
@@ -386,7 +394,7 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": warm_reps * L, "ms_per_step": round(ms_max / steps, 6),
+            "steps": steps, "warmup": warm_reps * G, "ms_per_step": round(ms_max / steps, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic (seeded random K-quant superblocks and N(0,1) activations)",
             "config": {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
@@ -395,7 +403,7 @@ def run_ours(args, world, rank, local):
                        "weight_bytes_per_step": bytes_per_step, "layer_copies": L,
                        "l2": f"inputs larger than L2: {L} rotating layer copies, "
                              f"{bytes_per_step * L / 1e6:.1f} MB of weights",
-                       "timing": "CUDA events around graph replays of K steps",
+                       "timing": f"CUDA events around graph replays of {G} layer steps each, K steps in all",
                        "pdl": not args.no_pdl,
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "kernel": "kq gemv_kernel (fused quantize + GEMV, 4 launches per step)",
@@ -418,10 +426,60 @@ def run_ours(args, world, rank, local):
             "gpu_launches": layers.launches_per_step() * steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "small_batch": small_batch,
             "gemv_27b": gemv_27b,
             "gemm": gemm,
         }
         print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# small batches on the decode layer (secondary line)
+
+def bench_small_batch(kq, torch, layers, peaks, args):
+    """The Qwen3-4B-shaped decode layer for a batch of M = 2, 4, 8 tokens:
+    per step, kq_quantize_q8k of the four [M, K] inputs and kq_gemm of the
+    seven matrices (small M runs on the GEMV's weight stream, each weight
+    item read once for all M tokens), over the same rotating layer copies,
+    replayed from a CUDA graph."""
+    out = []
+    idx = {m.name: i for i, m in enumerate(layers.mats)}
+    hbm = float(peaks["hbm_gbs"])
+    for M in (2, 4, 8):
+        xs = [torch.from_numpy(synth.activations(M, k, synth.rng_for(1, 9000 + 10 * M + j))).cuda()
+              for j, (_, k) in enumerate(LAYER_INPUTS)]
+        q8 = [kq.q8k_empty(M, k) for _, k in LAYER_INPUTS]
+        ys = [torch.empty((M, m.N), dtype=torch.float32, device="cuda") for m in layers.mats]
+
+        def step(l):
+            c = layers.copies[l]
+            for j, names in enumerate(layers.GROUPS):
+                kq.kq_quantize_q8k(xs[j], out=q8[j])
+                for nm in names:
+                    i = idx[nm]
+                    mt = layers.mats[i]
+                    kq.kq_gemm(mt.fmt, c["packed"][i], mt.N, mt.K, q8[j], y=ys[i])
+
+        L = len(layers.copies)
+        g = graph_of(torch, lambda: [step(l) for l in range(L)])
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        reps = max(3, min(200, args.steps // (8 * L)))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) * 1e3 / (reps * L)
+        gbs = layers.weight_bytes / (us * 1e-6) / 1e9
+        out.append({"M": M, "us_per_step": round(us, 3), "weight_gbs": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / hbm, 4), "tokens_per_s": round(M / (us * 1e-6), 1),
+                    "launches_per_step": 11})
+        del g
+    return {"workload": "Qwen3-4B-shaped decode layer, batch of M tokens (4 quantize + 7 kq_gemm launches per step)",
+            "lines": out}
 
 
 # --------------------------------------------------------------------------
