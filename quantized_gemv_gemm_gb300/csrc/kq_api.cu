@@ -59,6 +59,9 @@ int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offse
     // a few token rows: the decode GEMV's weight stream, each item read once
     // for up to 8 tokens
     if (!offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K) return launch_status(launch_gemv_batch(f, packed, N, K, q, M, y, s));
+    // a few grouped rows (MoE decode): one GEMV over every row's expert
+    if (offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K && gemv_grouped_fits(M, K))
+        return launch_status(launch_gemv_grouped(f, packed, E, offsets, expert_bytes, N, K, q, M, y, s));
     cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();
@@ -139,7 +142,7 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
 int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K, const float *x,
                   float *const *y, void *workspace, size_t workspace_bytes, cudaStream_t s) {
     if (!fmt_ok(f)) return KQ_ERR_FORMAT;
-    if (n_mats < 1 || n_mats > GEMV_MAX_MATRICES || !packed || !N || !y) return KQ_ERR_ARG;
+    if (n_mats < 1 || n_mats > GEMV_FUSED_MAX || !packed || !N || !y) return KQ_ERR_ARG;
     if (K <= 0 || K % QK != 0 || K > GEMV_MAX_K) return KQ_ERR_ARG;
     if (int r = check_gemv_ws(workspace, workspace_bytes)) return r;
     int64_t total = 0;

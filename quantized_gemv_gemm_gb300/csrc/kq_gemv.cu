@@ -360,6 +360,12 @@ struct GemvParams {
     const int16_t *bs;
     int ntok;                              // token rows folded per pass (1..T of the kernel)
     int64_t stage_stride;                  // bytes between the staged rows of two tokens
+    // grouped (MoE) rows: matrix m is row m of the activations times the
+    // weights of the expert whose row range [offsets[e], offsets[e+1])
+    // holds m; experts of expert_bytes each from packed[0]
+    const int32_t *offsets;
+    int64_t E;
+    uint64_t expert_bytes;
 };
 
 // Bounded wait on a stage's mbarrier (about one second): on expiry the
@@ -383,7 +389,9 @@ __device__ __forceinline__ int64_t block_item(const GemvParams &p, int64_t b, in
 // batches, which read each weight item once for all their tokens).  Token t's
 // activation row is staged at stage_stride * t, and its output row is
 // y[m] + t * N[m].
-template <int F, int T>
+// GR: grouped rows (MoE decode) -- the matrices are found on the device from
+// the expert offsets, after the wait, and matrix m folds activation row m.
+template <int F, int T, bool GR>
 __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     constexpr int SLOT = GemvFmt<F>::SLOT;
     using Item = typename ItemOf<F>::T;
@@ -407,8 +415,10 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     griddep_launch_dependents();
     const int64_t K = p.K, nsb = p.nsb;
     const int D = p.D;
-    const int ntok = T == 1 ? 1 : p.ntok;
-    const uint32_t tstride = T == 1 ? 0u : (uint32_t)p.stage_stride;
+    const int ntok = (T == 1 && !GR) ? 1 : p.ntok;
+    const uint32_t tstride = (T == 1 && !GR) ? 0u : (uint32_t)p.stage_stride;
+    // grouped: matrix m's staged row is at m * mstride
+    const uint32_t mstride = GR ? tstride : 0u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r16 = lane & 15, h = lane >> 4;
     const uint32_t ring_s = smem_addr(smem + (size_t)warp * D * SLOT);
@@ -424,7 +434,23 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     const int64_t G = p.gpre[p.nmat], B = gridDim.x;
     const int64_t I0 = block_item(p, blockIdx.x, B, G), I1 = block_item(p, blockIdx.x + 1, B, G);
     const int64_t w0 = I0 + warp * (I1 - I0) / 8, w1 = I0 + (warp + 1) * (I1 - I0) / 8;
-    if (threadIdx.x < p.nmat) {
+    if constexpr (GR) {
+        // the expert offsets are written by the kernels before this one
+        griddep_wait();
+        if (threadIdx.x < p.nmat) {
+            const int m = threadIdx.x;
+            int64_t lo = 0, hi = p.E;  // last e with offsets[e] <= m, among [0, E)
+            while (hi - lo > 1) {
+                const int64_t mid = (lo + hi) >> 1;
+                if (p.offsets[mid] <= m) lo = mid;
+                else hi = mid;
+            }
+            const bool in = p.offsets[lo] <= m && m < p.offsets[lo + 1];
+            s_planes[m] = make_planes(F, p.packed[0] + (in ? (uint64_t)lo * p.expert_bytes : 0), p.N[0], nsb);
+            s_n[m] = in ? p.N[0] : 0;  // a row of no expert is not written
+            s_y[m] = p.y[0] + (int64_t)m * p.N[0];
+        }
+    } else if (threadIdx.x < p.nmat) {
         s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
         s_n[threadIdx.x] = p.N[threadIdx.x];
         s_y[threadIdx.x] = p.y[threadIdx.x];
@@ -497,7 +523,7 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     for (int i = 0; i < D; ++i) issue();
 
     // activations: written by the kernels before this one
-    griddep_wait();
+    if constexpr (!GR) griddep_wait();
     constexpr bool PAIRS = F != FMT_Q6_K;
     if (p.x) {
         // up to eight blocks per warp per round, all loads issued first
@@ -548,8 +574,9 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     int m = m0;
     // running shared addresses of the current item's activation superblock
     // (the lane's half), sums and scale
-    uint32_t a_cur = qs_s + (uint32_t)sb * QK + 128 * h, s_cur = sum_s + (uint32_t)sb * 32 + 16 * h;
-    uint32_t d_cur = d8_s + 4 * (uint32_t)sb;
+    uint32_t a_cur = qs_s + m * mstride + (uint32_t)sb * QK + 128 * h;
+    uint32_t s_cur = sum_s + m * mstride + (uint32_t)sb * 32 + 16 * h;
+    uint32_t d_cur = d8_s + m * mstride + 4 * (uint32_t)sb;
     float acc[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[t] = 0.0f;
@@ -620,10 +647,10 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
             if (sb == nsb) {
                 sb = 0;
                 ++g;
-                a_cur = qs_s + 128 * h;
-                s_cur = sum_s + 16 * h;
-                d_cur = d8_s;
                 while (m + 1 < nmat && g >= s_gpre[m + 1]) ++m;
+                a_cur = qs_s + m * mstride + 128 * h;
+                s_cur = sum_s + m * mstride + 16 * h;
+                d_cur = d8_s + m * mstride;
             }
         }
     }
@@ -720,7 +747,7 @@ constexpr int64_t GEMV_BATCH_MAX_SMEM = 212 * 1024;  // + the static ~9 KB stays
 // bytes of one token's staged row (quants, sums, scales), 16-byte aligned
 inline int64_t gemv_stage_stride(int64_t K) { return (K + K / 8 + K / 64 + 15) & ~int64_t(15); }
 
-template <int F, int T>
+template <int F, int T, bool GR = false>
 static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaStream_t s) {
     p.gpre[0] = 0;
     for (int m = 0; m < p.nmat; ++m) p.gpre[m + 1] = p.gpre[m] + (p.N[m] + 15) / 16;
@@ -730,7 +757,7 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     // one block per SM, each with an even share of the items; a row group
     // may then be cut between two blocks, which needs the workspace
     int64_t blocks = sm_count();
-    if (T == 1 && p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
+    if (T == 1 && !GR && p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
         blocks *= 2;
     if (blocks > GEMV_MAX_BLOCKS) blocks = GEMV_MAX_BLOCKS;
     if (blocks > G) blocks = G;  // every row group spans at most two blocks
@@ -738,29 +765,31 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     // the busiest warp KQ_GEMV_CUT_ITEMS or more items above an even share:
     // the exchange at a cut costs about as much as folding a few items
     const int64_t whole = (G + blocks - 1) / blocks * p.nsb, even = (p.items + blocks - 1) / blocks;
-    p.split = T == 1 && ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
+    p.split = T == 1 && !GR && ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
               ((launch_flags() & LAUNCH_GEMV_SPLIT) || (whole + 7) / 8 - (even + 7) / 8 >= KQ_GEMV_CUT_ITEMS);
     p.ws = static_cast<unsigned long long *>(ws);
     p.stage_stride = gemv_stage_stride(p.K);
-    if (T == 1) p.ntok = 1;
-    const int64_t budget = T == 1 ? GEMV_SMEM_BUDGET : GEMV_BATCH_SMEM_BUDGET;
-    const int64_t stage_bytes = T * p.stage_stride;
+    if (T == 1 && !GR) p.ntok = 1;
+    // (a grouped launch stages one row per matrix)
+    const bool wide = T > 1 || GR;
+    const int64_t budget = wide ? GEMV_BATCH_SMEM_BUDGET : GEMV_SMEM_BUDGET;
+    const int64_t stage_bytes = (GR ? p.nmat : T) * p.stage_stride;
     int64_t D = (budget - stage_bytes) / (8 * GemvFmt<F>::SLOT);
     if (D > gemv_max_d<F>()) D = gemv_max_d<F>();
     if (D < 2) D = 2;
     p.D = (int)D;
     const size_t smem = (size_t)(8 * D * GemvFmt<F>::SLOT + stage_bytes);
-    static bool attr_set[64][4][9] = {};
+    static bool attr_set[64][4][9][2] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!attr_set[dev][F][T]) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(T == 1 ? GEMV_SMEM_BUDGET : GEMV_BATCH_MAX_SMEM));
+    if (!attr_set[dev][F][T][GR]) {
+        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)(wide ? GEMV_BATCH_MAX_SMEM : GEMV_SMEM_BUDGET));
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(gemv_kernel<F, T>, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        attr_set[dev][F][T] = true;
+        attr_set[dev][F][T][GR] = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
@@ -772,7 +801,7 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, T>, p);
+    return cudaLaunchKernelEx(&cfg, gemv_kernel<F, T, GR>, p);
 }
 
 template <int F>
@@ -829,6 +858,39 @@ static cudaError_t launch_gemv_batch_f(GemvParams p, int64_t M, int64_t tmax, cu
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
+}
+
+// Grouped rows (MoE decode: a few token rows, each routed to an expert):
+// one launch over every row's expert matrix, from one read of each weight
+// item per row.  False when the rows' staged activations do not fit.
+bool gemv_grouped_fits(int64_t M, int64_t K) {
+    return M >= 1 && M <= GEMV_MAX_MATRICES && M * gemv_stage_stride(K) + 2 * 8 * 3360 <= GEMV_BATCH_MAX_SMEM;
+}
+
+cudaError_t launch_gemv_grouped(int f, const void *packed, int64_t E, const int32_t *offsets,
+                                uint64_t expert_bytes, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
+                                cudaStream_t s) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    GemvParams p{};
+    p.nmat = (int)M;
+    p.packed[0] = static_cast<const uint8_t *>(packed);
+    for (int m = 0; m < p.nmat; ++m) {
+        p.N[m] = N;     // every matrix has the experts' shape; launch_gemv_t
+        p.y[m] = y;     // takes the row-group prefix sums from N
+    }
+    p.K = K;
+    p.nsb = K / QK;
+    p.x = nullptr;
+    p.d8 = a.d;
+    p.qs = a.qs;
+    p.bs = a.bsums;
+    p.ntok = (int)M;
+    p.offsets = offsets;
+    p.E = E;
+    p.expert_bytes = expert_bytes;
+    if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K, 1, true>(p, nullptr, 0, s);
+    if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K, 1, true>(p, nullptr, 0, s);
+    return launch_gemv_t<FMT_Q6_K, 1, true>(p, nullptr, 0, s);
 }
 
 cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, float *y,

@@ -41,7 +41,8 @@ cudaError_t launch_mv(int f, const void *packed, int64_t N, int64_t K, Q8K a, in
 // fp32 row x (quantized inside the kernel) or, when x is null, Q8_K planes a.
 // ws: null, or a zero-filled workspace of GEMV_WORKSPACE_BYTES: one 64-bit
 // word per row of a row group cut between two blocks, [GEMV_MAX_BLOCKS][16].
-constexpr int GEMV_MAX_MATRICES = 4;
+constexpr int GEMV_MAX_MATRICES = 16;  // kernel tables (kq_gemv_fused takes at most GEMV_FUSED_MAX)
+constexpr int GEMV_FUSED_MAX = 4;
 constexpr int64_t GEMV_MAX_K = 40960;
 constexpr int64_t GEMV_MAX_BLOCKS = 512;
 constexpr size_t GEMV_WORKSPACE_BYTES = KQ_GEMV_WORKSPACE_BYTES;
@@ -54,6 +55,13 @@ cudaError_t launch_gemv(int f, int nmat, const void *const *packed, const int64_
 constexpr int64_t GEMM_TC_MIN_M = 16;
 cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
                               cudaStream_t s);
+
+// Grouped rows (MoE decode): M < GEMM_TC_MIN_M token rows grouped by expert
+// (device offsets [E+1]), one GEMV launch over every row's expert.
+bool gemv_grouped_fits(int64_t M, int64_t K);
+cudaError_t launch_gemv_grouped(int f, const void *packed, int64_t E, const int32_t *offsets,
+                                uint64_t expert_bytes, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
+                                cudaStream_t s);
 
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);

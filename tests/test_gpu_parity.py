@@ -326,6 +326,27 @@ def test_grouped_uneven_and_empty_experts(K, fmt):
         assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts", [[0, 1, 0, 0, 1, 1, 0, 1, 0, 1, 1, 0, 0, 1, 0, 1],
+                                    [0, 3, 0, 1, 2, 0, 0, 5, 0, 0, 1, 0, 0, 0, 1, 0]])
+def test_grouped_decode_rows(K, fmt, counts):
+    """A few rows grouped by expert (MoE decode: one token routed to 8 of 16
+    experts; and 13 rows with several on one expert) run as one GEMV over
+    every row's expert: each row against the oracle with its own expert."""
+    rng = synth.rng_for(115, fmt * 10 + sum(counts))
+    E, N, Kdim = len(counts), 200, 1024
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    planes = oracle_q8k(synth.activations(int(offsets[-1]), Kdim, rng))
+    y = run_grouped(K, fmt, disks, planes, offsets)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        sl = tuple(p[a:b] for p in planes)
+        assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
+
+
 def test_grouped_moe_30b_a3b(K):
     """The MoE workload: 128 experts, top-8 of 512 tokens (4096 rows grouped by
     expert); gate/up Q4_K [768 x 2048], down Q6_K [2048 x 768]."""
