@@ -26,8 +26,12 @@
 // sum is rounded like the fold's own float(isum)).
 //
 // Warp roles (14 warps): 0 TMA producer of the activation tiles, 1 MMA issuer
-// (and TMEM owner), 2..5 weight unpack (thread = weight row), 6..13 epilogue
-// (thread = row x 64 token columns; TMEM lane quadrant = warp % 4).  Stages are half superblocks (K = 128): an A ring of 2 slots,
+// (and TMEM owner); Q4_K/Q5_K: 2..5 weight unpack (thread = weight row),
+// 6..13 epilogue (thread = row x 64 token columns, y in registers); Q6_K,
+// whose unpack is the longer chain: 2..9 weight unpack (two threads per row,
+// one 64-wide K sub-tile each), 10..13 epilogue (thread = row x every token
+// column, y accumulated in TMEM columns 128..255, which Q6_K's missing mins
+// leave free).  TMEM lane quadrant = warp % 4.  Stages are half superblocks (K = 128): an A ring of 2 slots,
 // a B ring of 3 (Q6_K: 2); accumulators I and msum double-buffered by
 // superblock parity.  Every mbarrier wait is bounded; on timeout the block
 // records KQ_ERR_TIMEOUT in the device status word and winds down.
@@ -47,7 +51,12 @@ using namespace sm100;
 constexpr int BM = 128;      // weight rows per tile (MMA M)
 constexpr int BT = 128;      // tokens per tile (MMA N, at most)
 constexpr int NTHREADS = 448;
-constexpr int W_TMA = 0, W_MMA = 1, W_UNPACK = 2, W_EPI = 6;
+constexpr int W_TMA = 0, W_MMA = 1, W_UNPACK = 2;
+// first epilogue warp: Q4_K/Q5_K 4 unpack + 8 epilogue warps; Q6_K 8 unpack
+// (two threads per weight row) + 4 epilogue warps that keep y in TMEM
+template <int F> constexpr int w_epi() { return F == FMT_Q6_K ? 10 : 6; }
+template <int F> constexpr int n_unpack() { return w_epi<F>() - W_UNPACK; }
+template <int F> constexpr int n_epi() { return NTHREADS / 32 - w_epi<F>(); }
 
 template <int F>
 struct Cfg {
@@ -334,8 +343,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- setup
     if (threadIdx.x == 0) {
-        mbar_init(&bar[BAR_FULL_A + 0], 4);
-        mbar_init(&bar[BAR_FULL_A + 1], 4);
+        mbar_init(&bar[BAR_FULL_A + 0], n_unpack<F>());
+        mbar_init(&bar[BAR_FULL_A + 1], n_unpack<F>());
         mbar_init(&bar[BAR_EMPTY_A + 0], 1);
         mbar_init(&bar[BAR_EMPTY_A + 1], 1);
         for (int i = 0; i < C::NB; ++i) {
@@ -344,8 +353,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         mbar_init(&bar[BAR_ACC_FULL + 0], 1);
         mbar_init(&bar[BAR_ACC_FULL + 1], 1);
-        mbar_init(&bar[BAR_ACC_EMPTY + 0], 8);
-        mbar_init(&bar[BAR_ACC_EMPTY + 1], 8);
+        mbar_init(&bar[BAR_ACC_EMPTY + 0], n_epi<F>());
+        mbar_init(&bar[BAR_ACC_EMPTY + 1], n_epi<F>());
         mbar_init(&bar[BAR_SD_FULL + 0], 4);
         mbar_init(&bar[BAR_SD_FULL + 1], 4);
         mbar_init(&bar[BAR_MMA_DONE], 1);
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     int planes = 1;
                     if constexpr (F == FMT_Q6_K) {
                         int any = 0;
-                        for (int w = 0; w < 4; ++w) any |= s_flag[8 * h + w];
+                        for (int w = 0; w < n_unpack<F>(); ++w) any |= s_flag[8 * h + w];
                         planes = any ? 2 : 1;
                     }
                     for (int pl = 0; pl < planes; ++pl) {
@@ -454,16 +463,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!mbar_wait(&bar[BAR_MMA_DONE], 0)) ok = false;
             if (!ok) set_timeout();
         }
-    } else if (warp < W_EPI) {
+    } else if (warp < w_epi<F>()) {
         // ------------------------------------------------ weight unpack
-        const int uw = warp - W_UNPACK;          // 0..3
-        const int r = 32 * uw + lane;            // tile row
+        const int uw = warp - W_UNPACK;          // 0..3 (Q6_K 0..7)
+        const int r = 32 * (uw & 3) + lane;      // tile row
+        const int my_jj = uw >> 2;               // Q6_K: this thread's K sub-tile of each half
         const int64_t n = n0 + r;
         const int64_t nc = n < p.N ? n : p.N - 1;
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         using Raw = typename RawOf<F>::T;
         Raw cur, nxt;
-        bool p2_dirty[2][2] = {{true, true}, {true, true}};  // Q6_K: this row's P2 may be non-zero
+        // Q6_K: this thread's P2 rows of the half-0 / half-1 slot may be non-zero
+        bool p2_dirty0 = true, p2_dirty1 = true;
         const int64_t nstage = 2 * nsb;
         if (nstage > 0) load_raw(cur, P, nc, 0, nsb, 0);
         for (int64_t hs = 0; hs < nstage && ok; ++hs) {
@@ -479,23 +490,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const uint32_t a_slot = a_base + h * C::A_SLOT;
             float d = 0.0f, dmin = 0.0f;
             if constexpr (F == FMT_Q6_K) {
-                bool big[2] = {false, false};
+                const uint32_t scj = my_jj ? cur.sc[1] : cur.sc[0];
+                bool big = false;
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int v = (int)(int8_t)((cur.sc[jj] >> (8 * i)) & 0xFF);
-                        big[jj] |= (v > 62 || v < -62);
-                    }
-                const unsigned any = __ballot_sync(0xFFFFFFFFu, big[0] || big[1]);
-                if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
-#pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const uint32_t a_tile = a_slot + jj * 16384;
-                    unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, cur.sc[jj], jj, big[jj],
-                              !big[jj] && p2_dirty[h][jj]);
-                    p2_dirty[h][jj] = big[jj];
+                for (int i = 0; i < 4; ++i) {
+                    const int v = (int)(int8_t)((scj >> (8 * i)) & 0xFF);
+                    big |= (v > 62 || v < -62);
                 }
+                const unsigned any = __ballot_sync(0xFFFFFFFFu, big);
+                if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
+                const uint32_t a_tile = a_slot + my_jj * 16384;
+                const bool dirty = h ? p2_dirty1 : p2_dirty0;
+                unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, scj, my_jj, big, !big && dirty);
+                if (h) p2_dirty1 = big;
+                else p2_dirty0 = big;
                 d = __half2float(__ushort_as_half((unsigned short)cur.d));
             } else {
                 const ScaleMin sm = unpack_scale_min(cur.hdr);
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 d = half_lo(cur.hdr.x);
                 dmin = half_hi(cur.hdr.x);
             }
-            if (h == 0) {
+            if (h == 0 && my_jj == 0) {
                 s_d[(sb & 1) * BM + r] = d;
                 s_dmin[(sb & 1) * BM + r] = dmin;
             }
@@ -535,14 +543,76 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&bar[BAR_FULL_A + h]);
-                if (h == 0) mbar_arrive(&bar[BAR_SD_FULL + (sb & 1)]);
+                if (h == 0 && my_jj == 0) mbar_arrive(&bar[BAR_SD_FULL + (sb & 1)]);
             }
             cur = nxt;
         }
         if (!ok && lane == 0) set_timeout();
+    } else if constexpr (F == FMT_Q6_K) {
+        // ------------------------------------------------ epilogue, Q6_K
+        // 4 warps, thread = weight row x every token column; y accumulates
+        // in TMEM columns 128..255 (the mins slot of buffer 0, which Q6_K
+        // does not use), read back once at the end
+        const int ew = warp - w_epi<F>();    // 0..3
+        const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
+        const int r = 32 * quad + lane;
+        const int64_t n = n0 + r;
+        float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 128 * ew;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
+        const uint32_t y_tm = lane_addr + 128;
+        const int nchunk = n_mma / 8;
+        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
+            const int b = (int)(sb & 1);
+            // the 128 token scales d8 of the superblock
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t tc = t0 + 32 * q + lane;
+                s_d8[32 * q + lane] = tc < t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
+            }
+            __syncwarp();
+            if (!mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((sb >> 1) & 1)) ||
+                !mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((sb >> 1) & 1))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float dd = s_d[b * BM + r];
+            for (int c = 0; c < nchunk; ++c) {
+                uint32_t vi[8], vy[8];
+                tmem_ld8(lane_addr + 256 * b + 8 * c, vi);
+                if (sb > 0) tmem_ld8(y_tm + 8 * c, vy);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float yo = sb > 0 ? __uint_as_float(vy[i]) : 0.0f;
+                    vy[i] = __float_as_uint(fmaf(s_d8[8 * c + i], dd * __uint_as_float(vi[i]), yo));
+                }
+                tmem_st8(y_tm + 8 * c, vy);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+        }
+        if (ok) {
+            tc_fence_after();
+            for (int c = 0; c < nchunk; ++c) {
+                uint32_t vy[8];
+                tmem_ld8(y_tm + 8 * c, vy);
+                tmem_wait_ld();
+                if (n < p.N) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int64_t t = t0 + 8 * c + i;
+                        if (t < t_end) p.y[t * p.N + n] = __uint_as_float(vy[i]);
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) set_timeout();
     } else {
         // ------------------------------------------------ epilogue
-        const int ew = warp - W_EPI;         // 0..7
+        const int ew = warp - w_epi<F>();    // 0..7
         const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
         const int ch = ew >> 2;              // token columns 64*ch .. +63
         const int r = 32 * quad + lane;
