@@ -254,16 +254,18 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
  * Launch options, process-wide (a plain atomic word; the new value applies
  * to launches enqueued after the call).  Returns the previous flags.
  *
- * KQ_LAUNCH_PDL: launch kq_quantize_q8k and kq_gemv with programmatic
- *   dependent launch, so that each may start while the previous kernel in
- *   the stream is still running.  Both wait (griddepcontrol.wait) for the
- *   previous kernels to complete before reading activations or writing any
- *   output, except that kq_gemv reads the packed weight image BEFORE that
- *   wait, to overlap its weight stream with the previous kernel.  With the
- *   flag set, a packed image must not be written by work that may still be
- *   running on the stream when kq_gemv is enqueued (synchronise, or wait on
- *   an event recorded after kq_repack, before the first kq_gemv).
- *   Default: off.
+ * KQ_LAUNCH_PDL: launch the kernels of kq_quantize_q8k, kq_gemv,
+ *   kq_gemv_fused, kq_gemm, kq_gemm_grouped and kq_gemm_noalloc with
+ *   programmatic dependent launch, so that each may start while the previous
+ *   kernel in the stream is still running.  They wait (griddepcontrol.wait)
+ *   for the previous kernels to complete before reading activations, scales
+ *   or expert offsets and before writing any output, except that the GEMV
+ *   and GEMM kernels read the packed weight image BEFORE that wait, to
+ *   overlap their weight stream (GEMM: the first weight unpack) with the
+ *   previous kernel.  With the flag set, a packed image must not be written
+ *   by work that may still be running on the stream when one of them is
+ *   enqueued (synchronise, or wait on an event recorded after kq_repack,
+ *   before the first use).  Default: off.
  */
 #define KQ_LAUNCH_PDL 1u
 /*

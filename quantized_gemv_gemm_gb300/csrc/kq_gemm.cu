@@ -284,6 +284,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = p.nsb;
+    // Programmatic dependent launch: the next kernel may be scheduled now.
+    // This grid reads what earlier kernels wrote (the activation image, the
+    // scales, the expert offsets) only after griddepcontrol.wait; the unpack
+    // warps, which read only the packed weights, start before it.
+    griddep_launch_dependents();
 
     // ---- tile of this block
     int64_t t0 = 0, t_end = p.M, w_tile = blockIdx.y;
@@ -291,6 +296,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (p.offsets) {
         // grouped: blockIdx.x enumerates the experts' token tiles in order
         if (warp == 0) {
+            griddep_wait();
             int64_t base = 0;
             int found = -1;
             int64_t tb = 0, te = 0;
@@ -373,6 +379,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == W_TMA) {
         // ------------------------------------------------ activation tiles
+        griddep_wait();
         if (lane == 0) {
             tma_prefetch_desc(&map_a16);
             if (C::kMins) tma_prefetch_desc(&map_b16);
@@ -561,6 +568,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
         const uint32_t y_tm = lane_addr + 128;
         const int nchunk = n_mma / 8;
+        griddep_wait();  // the scales are written by the kernels before this one
         for (int64_t sb = 0; sb < nsb && ok; ++sb) {
             const int b = (int)(sb & 1);
             // the 128 token scales d8 of the superblock
@@ -621,6 +629,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float y[64];
 #pragma unroll
         for (int i = 0; i < 64; ++i) y[i] = 0.0f;
+        griddep_wait();  // the scales are written by the kernels before this one
         for (int64_t sb = 0; sb < nsb && ok; ++sb) {
             const int b = (int)(sb & 1);
             // this warp's 64 token scales d8 for the superblock
@@ -683,6 +692,7 @@ __global__ void __launch_bounds__(256) act_image_kernel(const int8_t *__restrict
                                                         const float *__restrict__ d8, int64_t M, int64_t K,
                                                         int64_t Mp, __half *__restrict__ a16,
                                                         __half *__restrict__ b16, float *__restrict__ d8t) {
+    griddep_launch_dependents();
     griddep_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 quants
     const int64_t groups = M * K / 8;
@@ -709,7 +719,6 @@ __global__ void __launch_bounds__(256) act_image_kernel(const int8_t *__restrict
             d8t[s * Mp + m] = d8[blk];
         }
     }
-    griddep_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -774,8 +783,16 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     float *d8t = reinterpret_cast<float *>(ws + L.d8t);
     {
         const int64_t groups = M * K / 8;
-        act_image_kernel<<<(unsigned)((groups + 255) / 256), 256, 0, s>>>(a.qs, a.bsums, a.d, M, K, L.Mp, a16, b16, d8t);
-        cudaError_t e = cudaGetLastError();
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)((groups + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, act_image_kernel, a.qs, a.bsums, a.d, M, K, L.Mp, a16, b16, d8t);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap ma, mb;
@@ -805,8 +822,17 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     const int64_t w_tiles = (N + BM - 1) / BM;
     const int64_t t_tiles = offsets ? (M + BT - 1) / BT + E : (M + BT - 1) / BT;
     dim3 grid((unsigned)t_tiles, (unsigned)w_tiles);
-    gemm_kernel<F><<<grid, NTHREADS, Cf::SMEM, s>>>(ma, mb, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = Cf::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<F>, ma, mb, p);
 }
 
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,

@@ -411,6 +411,48 @@ def test_pdl_chain_matches_plain_launches(K):
     assert_row_tol(pdl[5] / 2.0, oracle.gemm(fmt, disk, *planes)[0])
 
 
+def test_pdl_gemm_chain_matches_plain_launches(K):
+    """The same for the tensor-core GEMM (dense and grouped): with programmatic
+    dependent launch the GEMM's unpack starts before the activation image is
+    written, and every output still equals the plain launches' bits."""
+    fmt, N, Kdim, M = synth.Q5_K, 384, 1024, 96
+    rng = synth.rng_for(116, 0)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    packed = pack(K, fmt, disk)
+    E = 3
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    per = K.kq_repack_bytes(fmt, N, Kdim)
+    packed_e = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        K.kq_repack(fmt, to_dev(disks[e].reshape(-1)), N, Kdim, packed=packed_e[e * per:(e + 1) * per])
+    offsets = to_dev(np.array([0, 40, 40, M], np.int32))
+    x0 = to_dev(synth.activations(M, Kdim, rng))
+    torch.cuda.synchronize()
+
+    def chain():
+        outs = []
+        a = K.q8k_empty(M, Kdim)
+        for i in range(4):
+            x = x0 * (1.0 + 0.25 * i)          # produced by the kernel right before
+            K.kq_quantize_q8k(x, out=a)
+            y = K.kq_gemm(fmt, packed, N, Kdim, a)
+            yg = K.kq_gemm_grouped(fmt, packed_e, E, offsets, N, Kdim, a)
+            outs.append(torch.cat([y * 2.0, yg * 2.0]))   # consumed right after
+        torch.cuda.synchronize()
+        return torch.stack(outs).cpu().numpy()
+
+    old = K.kq_set_launch_flags(0)
+    try:
+        plain = chain()
+        K.kq_set_launch_flags(K.KQ_LAUNCH_PDL)
+        pdl = chain()
+    finally:
+        K.kq_set_launch_flags(old)
+    np.testing.assert_array_equal(pdl, plain)
+    planes = oracle_q8k((x0 * 1.75).cpu().numpy())
+    assert_row_tol(pdl[3][:M] / 2.0, oracle.gemm(fmt, disk, *planes))
+
+
 # ---------------------------------------------------------------- fused GEMV
 @pytest.mark.parametrize("fmt", FMTS)
 def test_gemv_fused_multi_matrix_bit_identical(K, fmt):
