@@ -438,47 +438,46 @@ def run_ours(args, world, rank, local):
 
 def bench_small_batch(kq, torch, layers, peaks, args):
     """The Qwen3-4B-shaped decode layer for a batch of M = 2, 4, 8 tokens:
-    per step, kq_quantize_q8k of the four [M, K] inputs and kq_gemm of the
-    seven matrices (small M runs on the GEMV's weight stream, each weight
-    item read once for all M tokens), over the same rotating layer copies,
-    replayed from a CUDA graph."""
+    per step, four kq_gemv_fused_batch launches (q/k/v, o, gate/up, down),
+    each quantizing its [M, K] input inside the kernel and reading every
+    weight item once for all M tokens, over the same rotating layer copies,
+    replayed from CUDA graphs of 32 steps."""
     out = []
     idx = {m.name: i for i, m in enumerate(layers.mats)}
     hbm = float(peaks["hbm_gbs"])
     for M in (2, 4, 8):
         xs = [torch.from_numpy(synth.activations(M, k, synth.rng_for(1, 9000 + 10 * M + j))).cuda()
               for j, (_, k) in enumerate(LAYER_INPUTS)]
-        q8 = [kq.q8k_empty(M, k) for _, k in LAYER_INPUTS]
         ys = [torch.empty((M, m.N), dtype=torch.float32, device="cuda") for m in layers.mats]
 
         def step(l):
             c = layers.copies[l]
             for j, names in enumerate(layers.GROUPS):
-                kq.kq_quantize_q8k(xs[j], out=q8[j])
-                for nm in names:
-                    i = idx[nm]
-                    mt = layers.mats[i]
-                    kq.kq_gemm(mt.fmt, c["packed"][i], mt.N, mt.K, q8[j], y=ys[i])
+                ii = [idx[nm] for nm in names]
+                m0 = layers.mats[ii[0]]
+                kq.kq_gemv_fused_batch(m0.fmt, [c["packed"][i] for i in ii], [layers.mats[i].N for i in ii],
+                                       m0.K, xs[j], [ys[i] for i in ii])
 
         L = len(layers.copies)
-        g = graph_of(torch, lambda: [step(l) for l in range(L)])
+        G = GRAPH_ROTATIONS * L
+        g = graph_of(torch, lambda: [step(l % L) for l in range(G)])
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        reps = max(3, min(200, args.steps // (8 * L)))
+        reps = max(3, min(100, args.steps // (8 * G)))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(reps):
             g.replay()
         b.record()
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * L)
+        us = a.elapsed_time(b) * 1e3 / (reps * G)
         gbs = layers.weight_bytes / (us * 1e-6) / 1e9
         out.append({"M": M, "us_per_step": round(us, 3), "weight_gbs": round(gbs, 1),
                     "frac_of_hbm": round(gbs / hbm, 4), "tokens_per_s": round(M / (us * 1e-6), 1),
-                    "launches_per_step": 11})
+                    "launches_per_step": 4})
         del g
-    return {"workload": "Qwen3-4B-shaped decode layer, batch of M tokens (4 quantize + 7 kq_gemm launches per step)",
+    return {"workload": "Qwen3-4B-shaped decode layer, batch of M tokens (4 kq_gemv_fused_batch launches per step)",
             "lines": out}
 
 

@@ -188,6 +188,23 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
                   cudaStream_t s);
 
 /*
+ * Fused quantize + GEMV of a small batch: as kq_gemv_fused for M token rows
+ * at once (batched decode).  Each weight item is read once per pass of up to
+ * 8 rows (4 when K > 8192, fewer for longer K), and every row is quantized
+ * inside the kernel bit-identically to kq_quantize_q8k.  M = 1 is
+ * kq_gemv_fused.  There is no counterpart of a batched entry point in the
+ * source pages; it is the decode chain's fused quantize ([kq-arc], "The
+ * pieces") for several sequences decoding together.
+ *   x          device float32 [M][K] (row-major, 16-byte aligned), finite
+ *   y          host array of n_mats device pointers, y[m] float32 [M][N[m]]
+ *   workspace  as for kq_gemv (used by the single-row passes)
+ * Errors: as kq_gemv_fused; KQ_ERR_ARG also for M < 0.  M == 0 is a no-op.
+ */
+int kq_gemv_fused_batch(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K,
+                        const float *x, int64_t M, float *const *y, void *workspace,
+                        size_t workspace_bytes, cudaStream_t s);
+
+/*
  * Size of the device workspace kq_gemm / kq_gemm_grouped need for M token
  * rows of K (an fp16 image of the activation quants and bsums, plus tile
  * bookkeeping).  0 means no workspace is needed for this shape.

@@ -139,9 +139,12 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
     return launch_status(launch_mv(f, packed, N, K, q, 1, nullptr, 1, 0, y, s));
 }
 
-int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K, const float *x,
-                  float *const *y, void *workspace, size_t workspace_bytes, cudaStream_t s) {
+// The body of kq_gemv_fused (M = 1) and kq_gemv_fused_batch.
+static int gemv_fused_common(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K,
+                             const float *x, int64_t M, float *const *y, void *workspace, size_t workspace_bytes,
+                             cudaStream_t s) {
     if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (M < 0) return KQ_ERR_ARG;
     if (n_mats < 1 || n_mats > GEMV_FUSED_MAX || !packed || !N || !y) return KQ_ERR_ARG;
     if (K <= 0 || K % QK != 0 || K > GEMV_MAX_K) return KQ_ERR_ARG;
     if (int r = check_gemv_ws(workspace, workspace_bytes)) return r;
@@ -153,7 +156,7 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
         if (!packed[m] || !y[m]) return KQ_ERR_ARG;
         if (!aligned(packed[m], 256) || !aligned(y[m], 4)) return KQ_ERR_ALIGN;
     }
-    if (total == 0) return KQ_OK;
+    if (total == 0 || M == 0) return KQ_OK;
     if (!x) return KQ_ERR_ARG;
     if (!aligned(x, 16)) return KQ_ERR_ALIGN;
     // matrices with N = 0 are dropped
@@ -163,8 +166,21 @@ int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int6
     int k = 0;
     for (int m = 0; m < n_mats; ++m)
         if (N[m] > 0) { pk[k] = packed[m]; nn[k] = N[m]; yy[k] = y[m]; ++k; }
-    return launch_status(
-        launch_gemv(f, k, pk, nn, K, x, Q8K{nullptr, nullptr, nullptr}, yy, workspace, workspace_bytes, s));
+    if (M == 1)
+        return launch_status(
+            launch_gemv(f, k, pk, nn, K, x, Q8K{nullptr, nullptr, nullptr}, yy, workspace, workspace_bytes, s));
+    return launch_status(launch_gemv_fused_batch(f, k, pk, nn, K, x, M, yy, workspace, workspace_bytes, s));
+}
+
+int kq_gemv_fused(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K, const float *x,
+                  float *const *y, void *workspace, size_t workspace_bytes, cudaStream_t s) {
+    return gemv_fused_common(f, n_mats, packed, N, K, x, 1, y, workspace, workspace_bytes, s);
+}
+
+int kq_gemv_fused_batch(kq_format f, int n_mats, const void *const *packed, const int64_t *N, int64_t K,
+                        const float *x, int64_t M, float *const *y, void *workspace, size_t workspace_bytes,
+                        cudaStream_t s) {
+    return gemv_fused_common(f, n_mats, packed, N, K, x, M, y, workspace, workspace_bytes, s);
 }
 
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {

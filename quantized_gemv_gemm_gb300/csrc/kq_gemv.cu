@@ -525,7 +525,34 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // activations: written by the kernels before this one
     if constexpr (!GR) griddep_wait();
     constexpr bool PAIRS = F != FMT_Q6_K;
-    if (p.x) {
+    if (T > 1 && p.x) {
+        // several fp32 rows: block vb of the rows laid end to end is block
+        // vb % nsb of token row vb / nsb, staged in that token's row
+        const int64_t nvb = (int64_t)ntok * nsb;
+        for (int64_t vb0 = warp; vb0 < nvb; vb0 += 64) {
+            float4 v[8][2];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int64_t vb = vb0 + 8 * j;
+                if (vb < nvb) {
+                    const float4 *xp = reinterpret_cast<const float4 *>(p.x + vb * QK + 8 * lane);
+                    v[j][0] = xp[0];
+                    v[j][1] = xp[1];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int64_t vb = vb0 + 8 * j;
+                if (vb < nvb) {
+                    const int64_t t = vb / nsb, b = vb - t * nsb;
+                    const size_t o = (size_t)t * tstride;
+                    stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, reinterpret_cast<int8_t *>(
+                                              reinterpret_cast<uint8_t *>(s_qs) + o) + b * QK, s_sum + o + b * 32,
+                                              reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + o) + b);
+                }
+            }
+        }
+    } else if (p.x) {
         // up to eight blocks per warp per round, all loads issued first
         for (int64_t b0 = warp; b0 < nsb; b0 += 64) {
             float4 v[8][2];
@@ -770,8 +797,10 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     p.ws = static_cast<unsigned long long *>(ws);
     p.stage_stride = gemv_stage_stride(p.K);
     if (T == 1 && !GR) p.ntok = 1;
-    // (a grouped launch stages one row per matrix)
-    const bool wide = T > 1 || GR;
+    // (a grouped launch stages one row per matrix; a pass of a few tokens
+    // keeps to half an SM while its rows leave room for a 3-stage ring)
+    const int64_t rows_bytes = (GR ? p.nmat : T) * gemv_stage_stride(p.K);
+    const bool wide = GR || (T > 1 && (GEMV_SMEM_BUDGET - rows_bytes) / (8 * GemvFmt<F>::SLOT) < 3);
     const int64_t budget = wide ? GEMV_BATCH_SMEM_BUDGET : GEMV_SMEM_BUDGET;
     const int64_t stage_bytes = (GR ? p.nmat : T) * p.stage_stride;
     int64_t D = (budget - stage_bytes) / (8 * GemvFmt<F>::SLOT);
@@ -783,8 +812,9 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
     if (!attr_set[dev][F][T][GR]) {
+        // the largest this instantiation may ask for (a launch asks for what it uses)
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(wide ? GEMV_BATCH_MAX_SMEM : GEMV_SMEM_BUDGET));
+                                             (int)((T > 1 || GR) ? GEMV_BATCH_MAX_SMEM : GEMV_SMEM_BUDGET));
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
@@ -838,23 +868,30 @@ int64_t gemv_batch_max_tokens(int64_t K) {
 }
 
 template <int F>
-static cudaError_t launch_gemv_batch_f(GemvParams p, int64_t M, int64_t tmax, cudaStream_t s) {
-    const float *y0 = p.y[0];
+static cudaError_t launch_gemv_batch_f(GemvParams p, int64_t M, int64_t tmax, void *ws, size_t ws_bytes,
+                                       cudaStream_t s) {
+    float *y0[GEMV_MAX_MATRICES];
+    for (int m = 0; m < p.nmat; ++m) y0[m] = p.y[m];
+    const float *x0 = p.x;
     const int8_t *q0 = p.qs;
     const int16_t *b0 = p.bs;
     const float *d0 = p.d8;
     for (int64_t t0 = 0; t0 < M; t0 += tmax) {
         const int64_t n = M - t0 < tmax ? M - t0 : tmax;
         p.ntok = (int)n;
-        p.y[0] = const_cast<float *>(y0) + t0 * p.N[0];
-        p.qs = q0 + t0 * p.K;
-        p.bs = b0 + t0 * (p.K / 16);
-        p.d8 = d0 + t0 * p.nsb;
+        for (int m = 0; m < p.nmat; ++m) p.y[m] = y0[m] + t0 * p.N[m];
+        if (x0) {
+            p.x = x0 + t0 * p.K;
+        } else {
+            p.qs = q0 + t0 * p.K;
+            p.bs = b0 + t0 * (p.K / 16);
+            p.d8 = d0 + t0 * p.nsb;
+        }
         cudaError_t e;
         if (n > 4) e = launch_gemv_t<F, 8>(p, nullptr, 0, s);
         else if (n > 2) e = launch_gemv_t<F, 4>(p, nullptr, 0, s);
         else if (n > 1) e = launch_gemv_t<F, 2>(p, nullptr, 0, s);
-        else e = launch_gemv_t<F, 1>(p, nullptr, 0, s);
+        else e = launch_gemv_t<F, 1>(p, ws, ws_bytes, s);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -908,9 +945,31 @@ cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q
     p.qs = a.qs;
     p.bs = a.bsums;
     const int64_t tmax = gemv_batch_max_tokens(K);
-    if (f == FMT_Q4_K) return launch_gemv_batch_f<FMT_Q4_K>(p, M, tmax, s);
-    if (f == FMT_Q5_K) return launch_gemv_batch_f<FMT_Q5_K>(p, M, tmax, s);
-    return launch_gemv_batch_f<FMT_Q6_K>(p, M, tmax, s);
+    if (f == FMT_Q4_K) return launch_gemv_batch_f<FMT_Q4_K>(p, M, tmax, nullptr, 0, s);
+    if (f == FMT_Q5_K) return launch_gemv_batch_f<FMT_Q5_K>(p, M, tmax, nullptr, 0, s);
+    return launch_gemv_batch_f<FMT_Q6_K>(p, M, tmax, nullptr, 0, s);
+}
+
+// The fused quantize + GEMV for a small batch: M fp32 rows x, up to four
+// matrices sharing them, y[m] [M][N[m]].
+cudaError_t launch_gemv_fused_batch(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K,
+                                    const float *x, int64_t M, float *const *y, void *ws, size_t ws_bytes,
+                                    cudaStream_t s) {
+    if (M == 0) return cudaSuccess;
+    GemvParams p{};
+    p.nmat = nmat;
+    for (int m = 0; m < nmat; ++m) {
+        p.packed[m] = static_cast<const uint8_t *>(packed[m]);
+        p.N[m] = N[m];
+        p.y[m] = y[m];
+    }
+    p.K = K;
+    p.nsb = K / QK;
+    p.x = x;
+    const int64_t tmax = gemv_batch_max_tokens(K);
+    if (f == FMT_Q4_K) return launch_gemv_batch_f<FMT_Q4_K>(p, M, tmax, ws, ws_bytes, s);
+    if (f == FMT_Q5_K) return launch_gemv_batch_f<FMT_Q5_K>(p, M, tmax, ws, ws_bytes, s);
+    return launch_gemv_batch_f<FMT_Q6_K>(p, M, tmax, ws, ws_bytes, s);
 }
 
 // ---------------------------------------------------------------------------

@@ -56,6 +56,12 @@ constexpr int64_t GEMM_TC_MIN_M = 16;
 cudaError_t launch_gemv_batch(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
                               cudaStream_t s);
 
+// Fused quantize + GEMV of a small batch: M fp32 rows, up to GEMV_FUSED_MAX
+// matrices sharing them, y[m] [M][N[m]].
+cudaError_t launch_gemv_fused_batch(int f, int nmat, const void *const *packed, const int64_t *N, int64_t K,
+                                    const float *x, int64_t M, float *const *y, void *ws, size_t ws_bytes,
+                                    cudaStream_t s);
+
 // Grouped rows (MoE decode): M < GEMM_TC_MIN_M token rows grouped by expert
 // (device offsets [E+1]), one GEMV launch over every row's expert.
 bool gemv_grouped_fits(int64_t M, int64_t K);

@@ -44,6 +44,7 @@ _lib.kq_gemv_workspace_bytes.argtypes = []
 _lib.kq_gemv_workspace_bytes.restype = _SZ
 _lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P, _SZ, _P]
 _lib.kq_gemv_fused.argtypes = [_INT, _INT, _P, _P, _I64, _P, _P, _P, _SZ, _P]
+_lib.kq_gemv_fused_batch.argtypes = [_INT, _INT, _P, _P, _I64, _P, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
@@ -56,7 +57,7 @@ _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
-for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
+for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
     getattr(_lib, _f).restype = _INT
 
@@ -200,6 +201,27 @@ def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list
     yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
     wp, wn = _gemv_ws_args(workspace, x.device)
     _check(_lib.kq_gemv_fused(int(fmt), n, pk, nn, int(K), _ptr(x), yy, wp, wn, _stream(stream)), "kq_gemv_fused")
+    return y_list
+
+
+def kq_gemv_fused_batch(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list=None, workspace=None,
+                        stream=None):
+    """Quantize the M fp32 rows of x [M, K] and multiply them by up to 4 matrices
+    in one launch per pass of up to 8 rows; y_list[m] is [M, N_list[m]]."""
+    n = len(packed_list)
+    _need_cuda(x, *packed_list)
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 [M, K] tensor")
+    M = x.shape[0]
+    if y_list is None:
+        y_list = [torch.empty((M, int(N)), dtype=torch.float32, device=x.device) for N in N_list]
+    _need_cuda(*y_list)
+    pk = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in packed_list])
+    nn = (ctypes.c_int64 * max(n, 1))(*[int(v) for v in N_list])
+    yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
+    wp, wn = _gemv_ws_args(workspace, x.device)
+    _check(_lib.kq_gemv_fused_batch(int(fmt), n, pk, nn, int(K), _ptr(x), int(M), yy, wp, wn, _stream(stream)),
+           "kq_gemv_fused_batch")
     return y_list
 
 

@@ -499,6 +499,30 @@ def test_gemv_fused_cuts_across_matrices(K, fmt):
         assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes)[0])
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("M,Kdim", [(2, 2560), (3, 1024), (5, 4096), (8, 768), (11, 256), (6, 9728)])
+def test_gemv_fused_batch(K, fmt, M, Kdim):
+    """Fused quantize + GEMV of a small batch over several matrices sharing the
+    rows: every output of every row against the oracle on that row's Q8_K
+    planes (the in-kernel quantization is bit-identical to kq_quantize_q8k),
+    and row 0 equal to kq_gemv_fused of that row alone."""
+    rng = synth.rng_for(117, fmt * 1000 + M * 10 + Kdim // 256)
+    Ns = [300, 16, 77]
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for N in Ns]
+    packs = [pack(K, fmt, d) for d in disks]
+    x = synth.activations(M, Kdim, rng, outliers=True)
+    fulls = [poisoned((M, N)) for N in Ns]
+    K.kq_gemv_fused_batch(fmt, packs, Ns, Kdim, to_dev(x), [f[1] for f in fulls])
+    torch.cuda.synchronize()
+    planes = oracle_q8k(x)
+    for N, disk, (full, y) in zip(Ns, disks, fulls):
+        check_guard(full, M * N)
+        assert_row_tol(y.cpu().numpy(), oracle.gemm(fmt, disk, *planes))
+    one = K.kq_gemv_fused(fmt, packs, Ns, Kdim, to_dev(x[0]))
+    for (full, y), y1 in zip(fulls, one):
+        assert_row_tol(y[0].cpu().numpy(), y1.cpu().numpy().astype(np.float64), rel=1e-5)
+
+
 def test_gemv_fused_layer_groups_and_edges(K):
     """The decode layer's launch groups (q/k/v; gate/up), a single-superblock
     K, N = 1, a skipped empty matrix, and the host-side argument checks."""
