@@ -268,6 +268,19 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
                     int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
 
 /*
+ * Measurement hook: the int8 rate of the warp-level integer MMA
+ * (mma.sync m16n8k32, s8 x s8 -> s32), the only integer tensor-core MMA on
+ * sm_103a.  Launches `blocks` blocks of 8 warps; every warp issues iters x 8
+ * independent MMAs of 16 x 8 x 32, i.e. blocks * 8 * iters * 8 * 8192 int8
+ * operations (multiply and add counted separately).  Time it with events on
+ * `s`.  All operands are ones, so every thread writes the checksum
+ * 1024 * iters to out[block * 256 + thread].
+ *   out   device int32 [blocks * 256]
+ * Errors: KQ_ERR_ARG for blocks < 0, iters < 0 or a null out; KQ_ERR_LAUNCH.
+ */
+int kq_measure_mma_s8(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s);
+
+/*
  * Launch options, process-wide (a plain atomic word; the new value applies
  * to launches enqueued after the call).  Returns the previous flags.
  *

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkq.so")
-SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_gemv.cu", "kq_mv.cu", "kq_gemm.cu", "kq_noalloc.cu"]
+SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_gemv.cu", "kq_mv.cu", "kq_gemm.cu", "kq_noalloc.cu", "kq_peak.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

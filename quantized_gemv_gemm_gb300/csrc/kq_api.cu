@@ -223,6 +223,13 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
     return launch_status(launch_debug_decode(f, packed, N, K, q, sc, mn, d, dmin, s));
 }
 
+int kq_measure_mma_s8(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s) {
+    if (blocks < 0 || iters < 0 || blocks > (int64_t)INT32_MAX) return KQ_ERR_ARG;
+    if (blocks == 0) return KQ_OK;
+    if (!out) return KQ_ERR_ARG;
+    return launch_status(launch_mma_s8_rate(blocks, iters, out, s));
+}
+
 unsigned kq_set_launch_flags(unsigned flags) {
     return g_launch_flags.exchange(flags & (KQ_LAUNCH_PDL | KQ_LAUNCH_GEMV_SPLIT), std::memory_order_relaxed);
 }

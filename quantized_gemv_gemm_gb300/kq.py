@@ -53,12 +53,13 @@ _lib.kq_gemm_noalloc.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P]
 _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
+_lib.kq_measure_mma_s8.argtypes = [_I64, _I64, _P, _P]
 _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
-           "kq_debug_partials", "kq_debug_decode", "kq_device_status"):
+           "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -305,6 +306,17 @@ def kq_debug_decode(fmt: int, packed: torch.Tensor, N: int, K: int, stream=None)
     _check(_lib.kq_debug_decode(int(fmt), _ptr(packed), N, K, _ptr(q), _ptr(sc), _ptr(mn), _ptr(d), _ptr(dmin),
                                 _stream(stream)), "kq_debug_decode")
     return {"q": q, "sc": sc, "m": mn, "d": d, "dmin": dmin}
+
+
+def kq_measure_mma_s8(blocks: int, iters: int, out: torch.Tensor = None, device=None, stream=None) -> torch.Tensor:
+    """Launch the int8 mma.sync rate kernel (blocks x 8 warps, iters x 8 MMAs
+    of 16x8x32 per warp); returns the per-thread checksums (1024 * iters)."""
+    if out is None:
+        out = torch.empty(max(int(blocks), 1) * 256, dtype=torch.int32,
+                          device=device if device is not None else "cuda")
+    _need_cuda(out)
+    _check(_lib.kq_measure_mma_s8(int(blocks), int(iters), _ptr(out), _stream(stream)), "kq_measure_mma_s8")
+    return out
 
 
 def kq_device_status(stream=None) -> int:

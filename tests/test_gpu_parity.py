@@ -571,3 +571,12 @@ def test_gemm_q6k_full_subscale_range(K, sc_range):
 def test_gemm_device_status_clean(K):
     """After the tensor-core launches above, no bounded wait has timed out."""
     assert K.kq_device_status() == 0
+
+
+def test_measure_mma_s8_checksum(K):
+    """The int8 mma.sync rate kernel does the MMAs it claims: all-ones
+    operands give 32 per MMA per accumulator, 1024 * iters per thread."""
+    out = K.kq_measure_mma_s8(3, 7)
+    torch.cuda.synchronize()
+    assert out.shape == (3 * 256,)
+    assert bool((out == 1024 * 7).all())

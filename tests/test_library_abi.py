@@ -86,6 +86,16 @@ def test_host_argument_checks(kq):
     n1 = (ctypes.c_int64 * 1)(8)
     y1 = (ctypes.c_void_p * 1)(0x10000)
     assert lib.kq_gemv_fused(1, 1, pk1, n1, 256, fake, y1, fake, 16, None) == WS
+    # fused batch: negative M, and M = 0 is a no-op that needs no x
+    assert lib.kq_gemv_fused_batch(1, 1, pk1, n1, 256, fake, -1, y1, None, 0, None) == ARG
+    assert lib.kq_gemv_fused_batch(1, 1, pk1, n1, 256, None, 0, y1, None, 0, None) == 0
+    assert lib.kq_gemv_fused_batch(1, 1, pk1, n1, 256, odd, 2, y1, None, 0, None) == ALIGN
+    assert lib.kq_gemv_fused_batch(1, 5, pk1, n1, 256, fake, 2, y1, None, 0, None) == ARG
+    # int8 MMA rate hook: argument checks only (no launch)
+    assert lib.kq_measure_mma_s8(-1, 10, fake, None) == ARG
+    assert lib.kq_measure_mma_s8(4, -1, fake, None) == ARG
+    assert lib.kq_measure_mma_s8(4, 10, None, None) == ARG
+    assert lib.kq_measure_mma_s8(0, 10, None, None) == 0
     # empty problems are no-ops that touch nothing
     assert lib.kq_gemv(1, None, 0, 256, nullq, None, None, 0, None) == 0
     assert lib.kq_gemm(2, None, 16, 512, nullq, 0, None, None, 0, None) == 0
