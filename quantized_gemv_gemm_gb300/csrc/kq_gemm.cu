@@ -21,6 +21,9 @@
 //     of the sub-mins (duplicated per 16) against the bsums gives msum;
 //   - the epilogue folds once per superblock, y += d8*(d*I - dmin*msum), in
 //     fp32 registers ([kq-arc], "The pieces": one float fold per superblock).
+// The grouped (MoE) form runs one block per SM over a list of tiles (see the
+// tile comment below), so short expert tiles do not pay a block's start-up
+// and drain each.
 // The fp32 accumulator is exact while every partial sum stays below 2^24 in
 // magnitude (true for realistic activations; at adversarial extremes the
 // sum is rounded like the fold's own float(isum)).
@@ -52,6 +55,8 @@ constexpr int BM = 128;      // weight rows per tile (MMA M)
 constexpr int BT = 128;      // tokens per tile (MMA N, at most)
 constexpr int NTHREADS = 448;
 constexpr int W_TMA = 0, W_MMA = 1, W_UNPACK = 2;
+constexpr int TILE_CAP = 128;          // grouped: most tiles one block runs
+constexpr int MAX_GROUPED_E = 1024;    // grouped: most experts (more take the CUDA-core kernel)
 // first epilogue warp: Q4_K/Q5_K 4 unpack + 8 epilogue warps; Q6_K 8 unpack
 // (two threads per weight row) + 4 epilogue warps that keep y in TMEM
 template <int F> constexpr int w_epi() { return F == FMT_Q6_K ? 10 : 6; }
@@ -72,14 +77,16 @@ struct Cfg {
     static constexpr int OFF_D8 = OFF_SD + 2 * 2 * BM * 4;        // per epilogue warp [64] floats
     static constexpr int OFF_BAR = OFF_D8 + 8 * 64 * 4;
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
-    static constexpr int SMEM = OFF_MISC + 128 + 1024;            // + alignment slack
+    static constexpr int OFF_TILES = OFF_MISC + 128;              // grouped: the block's tile list
+    static constexpr int OFF_OFFS = OFF_TILES + TILE_CAP * 16;    // grouped: the row offsets [E + 1]
+    static constexpr int SMEM = OFF_OFFS + (MAX_GROUPED_E + 4) * 4 + 1024;  // + alignment slack
     static_assert(OFF_B % 1024 == 0, "B tiles need 1024-byte alignment");
     static_assert(B_SLOT % 1024 == 0, "B slots need 1024-byte alignment");
 };
 
 // barrier indices
 enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_ACC_FULL = 10, BAR_ACC_EMPTY = 12,
-       BAR_SD_FULL = 14, BAR_MMA_DONE = 16 };
+       BAR_SD_FULL = 14, BAR_MMA_DONE = 16, BAR_TILES = 17 };
 
 struct GemmParams {
     const uint8_t *packed;
@@ -269,7 +276,157 @@ __device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, int64_t n, i
 }
 
 // ---------------------------------------------------------------------------
+// Output tiles: 128 weight rows x up to 128 tokens of one expert.
+//
+// Dense: one block per tile, tile i = blockIdx.x of t_tiles x w_tiles (token
+// tile fastest, so neighbouring blocks share a weight panel).
+//
+// Grouped: a block per SM (at most), each running a list of tiles, and every
+// role walks the same list, so the rings, the TMEM buffers and their phases
+// run on across tiles (the unpack of a tile's first superblock overlaps the
+// epilogue of the previous tile).  Tile indices: i < E * w_tiles is the first
+// token tile of expert i / w_tiles, rows [o_e, min(o_e+1, o_e + 128)); the
+// experts' later token tiles (past their first 128 rows) follow, in expert
+// order.  Block b takes i = b, b + grid, ...: its first tile is known
+// without the offsets, so its unpack starts before the dependency wait and
+// the tile runs even when the expert has no rows (no MMA, no activation
+// copy, no stores); its later tiles without rows are left out of the list.
+// The TMA warp builds the list in shared memory once (the offsets staged
+// there first), and the other roles read it from there.
+struct Tile {
+    int n0, t0, t_end;
+    int e, ntok, n_mma;
+};
+
+__device__ __forceinline__ int w_tiles_of(const GemmParams &p) { return (int)((p.N + BM - 1) / BM); }
+
+__device__ __forceinline__ void finish_tile(Tile &t) {
+    const int nt = t.t_end - t.t0;
+    t.ntok = nt < 0 ? 0 : nt;
+    t.n_mma = (t.ntok + 15) & ~15;
+}
+
+// Dense tile of this block.
+__device__ __forceinline__ Tile dense_tile(const GemmParams &p) {
+    const int t_tiles = (int)((p.M + BT - 1) / BT);
+    const int i = (int)blockIdx.x;
+    Tile t;
+    t.e = 0;
+    t.n0 = (i / t_tiles) * BM;
+    t.t0 = (i % t_tiles) * BT;
+    t.t_end = (t.t0 + BT < p.M) ? t.t0 + BT : (int)p.M;
+    finish_tile(t);
+    return t;
+}
+
+// Grouped list entry k (written by build_tile_list).
+__device__ __forceinline__ Tile list_tile(const int4 *list, int k) {
+    const int4 v = list[k];
+    Tile t;
+    t.e = v.x;
+    t.n0 = v.y;
+    t.t0 = v.z;
+    t.t_end = v.w;
+    finish_tile(t);
+    return t;
+}
+
+// Rows [a, b) of expert e from the staged offsets, clamped to [0, M].
+__device__ __forceinline__ void expert_rows(const int *offs, int M, int e, int &a, int &b) {
+    a = offs[e];
+    b = offs[e + 1];
+    a = a < 0 ? 0 : (a > M ? M : a);
+    b = b < a ? a : (b > M ? M : b);
+}
+
+// Exclusive warp prefix sum of v; *total gets the warp's sum.
+__device__ __forceinline__ int warp_excl_sum(int v, int lane, int *total) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    *total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    return incl - v;
+}
+
+// Grouped: the block's tile list (warp-collective, after the dependency
+// wait); returns the number of tiles.  list entries: {e, n0, t0, t_end}.
+__device__ int build_tile_list(const GemmParams &p, int *offs, int4 *list, int lane) {
+    const int E = (int)p.E, M = (int)p.M, w_tiles = w_tiles_of(p);
+    for (int i = lane; i <= E; i += 32) offs[i] = p.offsets[i];
+    __syncwarp();
+    const int64_t S = (int64_t)E * w_tiles;
+    const int64_t bid = blockIdx.x, grid = gridDim.x;
+    int count = 0;
+    // first token tiles: i = bid + k * grid < S
+    const int n_first = bid < S ? (int)((S - 1 - bid) / grid + 1) : 0;
+    for (int k0 = 0; k0 < n_first; k0 += 32) {
+        const int k = k0 + lane;
+        int4 v = make_int4(0, 0, 0, 0);
+        bool run = false;
+        if (k < n_first) {
+            const int64_t i = bid + (int64_t)k * grid;
+            int a, b;
+            v.x = (int)(i / w_tiles);
+            v.y = (int)(i % w_tiles) * BM;
+            expert_rows(offs, M, v.x, a, b);
+            v.z = a;
+            v.w = (a + BT < b) ? a + BT : b;
+            run = k == 0 || v.w > v.z;
+        }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, run);
+        const int pos = count + __popc(m & ((1u << lane) - 1));
+        if (run && pos < TILE_CAP) list[pos] = v;
+        count += __popc(m);
+    }
+    // later token tiles: index S + j * w_tiles + wt for the j-th later token
+    // tile in expert order; this block takes those congruent to bid
+    int base = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        int a = 0, b = 0, later = 0;
+        if (e < E) {
+            expert_rows(offs, M, e, a, b);
+            const int tiles = (b - a + BT - 1) / BT;
+            later = tiles > 1 ? tiles - 1 : 0;
+        }
+        int sum;
+        const int j0 = base + warp_excl_sum(later, lane, &sum);
+        // this lane's index range [lo, hi) and the first index congruent to bid
+        const int64_t lo = S + (int64_t)j0 * w_tiles, hi = lo + (int64_t)later * w_tiles;
+        const int64_t first = lo + ((bid - lo) % grid + grid) % grid;
+        const int n = first < hi ? (int)((hi - 1 - first) / grid + 1) : 0;
+        int n_all;
+        const int pos0 = count + warp_excl_sum(n, lane, &n_all);
+        for (int q = 0; q < n; ++q) {
+            const int64_t o = first + (int64_t)q * grid - S;
+            const int j = (int)(o / w_tiles);
+            const int t0 = a + (1 + j - j0) * BT;
+            if (pos0 + q < TILE_CAP)
+                list[pos0 + q] = make_int4(e, (int)(o % w_tiles) * BM, t0, (t0 + BT < b) ? t0 + BT : b);
+        }
+        count += n_all;
+        base += sum;
+    }
+    return count < TILE_CAP ? count : TILE_CAP;
+}
+
+// Start streaming a tile's weight rows (contiguous in every plane) into L2.
 template <int F>
+__device__ __forceinline__ void prefetch_tile(const GemmParams &p, const Tile &t) {
+    const Planes P = make_planes(F, p.packed + (uint64_t)t.e * p.expert_bytes, p.N, p.nsb);
+    int u[4];
+    plane_unit_bytes(F, u);
+    const int64_t rows = row_groups(p.N) * GROUP_ROWS;
+    const int64_t n0 = t.n0, r1 = (n0 + BM < rows ? n0 + BM : rows);
+    const uint8_t *base[4] = {P.p0, P.p1, P.p2, P.p3};
+    for (int q = 0; q < 4; ++q)
+        if (u[q] && r1 > n0) prefetch_l2_bulk(base[q] + (uint64_t)n0 * p.nsb * u[q], (uint64_t)(r1 - n0) * p.nsb * u[q]);
+}
+
+template <int F, bool G>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a16, const __grid_constant__ CUtensorMap map_b16,
                 const GemmParams p) {
@@ -279,8 +436,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     float *s_d = reinterpret_cast<float *>(smem + C::OFF_SD);
     float *s_dmin = s_d + 2 * BM;
-    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);  // [0] tmem base, [1..] tile info
+    uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);  // [0] tmem base, [1] tile count
     int *s_flag = reinterpret_cast<int *>(misc + 8);                     // Q6_K split flags [2 halves][8 warps]
+    int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_TILES);        // grouped tile list
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nsb = p.nsb;
@@ -290,62 +448,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // warps, which read only the packed weights, start before it.
     griddep_launch_dependents();
 
-    // ---- tile of this block
-    int64_t t0 = 0, t_end = p.M, w_tile = blockIdx.y;
-    int e = 0;
-    if (p.offsets) {
-        // grouped: blockIdx.x enumerates the experts' token tiles in order
-        if (warp == 0) {
-            griddep_wait();
-            int64_t base = 0;
-            int found = -1;
-            int64_t tb = 0, te = 0;
-            for (int64_t e0 = 0; e0 < p.E && found < 0; e0 += 32) {
-                const int64_t ee = e0 + lane;
-                int64_t a = 0, b = 0, tiles = 0;
-                if (ee < p.E) {
-                    a = p.offsets[ee];
-                    b = p.offsets[ee + 1];
-                    a = a < 0 ? 0 : (a > p.M ? p.M : a);
-                    b = b < a ? a : (b > p.M ? p.M : b);
-                    tiles = (b - a + BT - 1) / BT;
-                }
-                int64_t incl = tiles;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += v;
-                }
-                const int64_t excl = base + incl - tiles;
-                const bool mine = tiles > 0 && (int64_t)blockIdx.x >= excl && (int64_t)blockIdx.x < excl + tiles;
-                const unsigned mask = __ballot_sync(0xFFFFFFFFu, mine);
-                if (mask) {
-                    const int src = __ffs(mask) - 1;
-                    found = (int)(e0 + src);
-                    const int64_t jt = (int64_t)blockIdx.x - __shfl_sync(0xFFFFFFFFu, excl, src);
-                    tb = __shfl_sync(0xFFFFFFFFu, a, src) + jt * BT;
-                    te = __shfl_sync(0xFFFFFFFFu, b, src);
-                }
-                base += __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            if (lane == 0) {
-                misc[1] = (uint32_t)found;
-                misc[2] = (uint32_t)tb;
-                misc[3] = (uint32_t)te;
-            }
-        }
-        __syncthreads();
-        if ((int)misc[1] < 0) return;  // no token tile for this block
-        e = (int)misc[1];
-        t0 = misc[2];
-        t_end = misc[3];
-    } else {
-        t0 = (int64_t)blockIdx.x * BT;
-    }
-    const int ntok = (int)((t_end - t0) < BT ? (t_end - t0) : BT);
-    const int n_mma = (ntok + 15) & ~15;
-    const int64_t n0 = w_tile * BM;
-    const Planes P = make_planes(F, p.packed + (uint64_t)e * p.expert_bytes, p.N, nsb);
+    // grouped: blocks below E * w_tiles start on the first token tile of an
+    // expert, known without the offsets
+    const bool static_first = !G || (int64_t)blockIdx.x < p.E * w_tiles_of(p);
 
     // ---- setup
     if (threadIdx.x == 0) {
@@ -364,6 +469,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(&bar[BAR_SD_FULL + 0], 4);
         mbar_init(&bar[BAR_SD_FULL + 1], 4);
         mbar_init(&bar[BAR_MMA_DONE], 1);
+        mbar_init(&bar[BAR_TILES], 1);
         mbar_fence_init();
     }
     if (warp == W_MMA) {
@@ -374,38 +480,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns: I[b] at 256b, msum[b] at 256b + 128
+    // TMEM columns: I[b] at 256b, msum[b] at 256b + 128.  Buffer b and the
+    // phases follow g, the block's count of superblock steps over all tiles.
     bool ok = true;
 
     if (warp == W_TMA) {
         // ------------------------------------------------ activation tiles
         griddep_wait();
+        int ntiles = 1;
+        if constexpr (G) {
+            ntiles = build_tile_list(p, reinterpret_cast<int *>(smem + C::OFF_OFFS), s_list, lane);
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) {
+                misc[1] = (uint32_t)ntiles;
+                mbar_arrive(&bar[BAR_TILES]);
+            }
+        }
+        int64_t use = 0;
         if (lane == 0) {
             tma_prefetch_desc(&map_a16);
             if (C::kMins) tma_prefetch_desc(&map_b16);
-            // the block's weight rows are contiguous in every plane: start
-            // streaming them into L2 for the unpack warps
-            int u[4];
-            plane_unit_bytes(F, u);
-            const int64_t rows = row_groups(p.N) * GROUP_ROWS;
-            const int64_t r1 = (n0 + BM < rows ? n0 + BM : rows);
-            const uint8_t *base[4] = {P.p0, P.p1, P.p2, P.p3};
-            for (int q = 0; q < 4; ++q)
-                if (u[q] && r1 > n0)
-                    prefetch_l2_bulk(base[q] + (uint64_t)n0 * nsb * u[q], (uint64_t)(r1 - n0) * nsb * u[q]);
-            int64_t use = 0;
-            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-                for (int h = 0; h < 2 && ok; ++h, ++use) {
-                    const int slot = (int)(use % C::NB);
-                    const uint32_t par = (uint32_t)((use / C::NB) & 1);
-                    if (!mbar_wait(&bar[BAR_EMPTY_B + slot], par ^ 1)) { ok = false; break; }
-                    uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
-                    const bool mins = C::kMins && h == 0;
-                    mbar_arrive_expect_tx(&bar[BAR_FULL_B + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
-                    const int k0 = (int)(sb * QK + 128 * h);
-                    tma_load_2d(bs, &map_a16, k0, (int)t0, &bar[BAR_FULL_B + slot]);
-                    tma_load_2d(bs + C::B_SUB, &map_a16, k0 + 64, (int)t0, &bar[BAR_FULL_B + slot]);
-                    if (mins) tma_load_2d(bs + 2 * C::B_SUB, &map_b16, (int)(sb * 16), (int)t0, &bar[BAR_FULL_B + slot]);
+            if (ntiles > 0) prefetch_tile<F>(p, G ? list_tile(s_list, 0) : dense_tile(p));
+            for (int k = 0; k < ntiles && ok; ++k) {
+                const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+                // the next tile's weights stream into L2 while this one runs
+                if (k + 1 < ntiles) prefetch_tile<F>(p, list_tile(s_list, k + 1));
+                for (int64_t sb = 0; sb < nsb && ok && t.ntok > 0; ++sb) {
+                    for (int h = 0; h < 2 && ok; ++h, ++use) {
+                        const int slot = (int)(use % C::NB);
+                        const uint32_t par = (uint32_t)((use / C::NB) & 1);
+                        if (!mbar_wait(&bar[BAR_EMPTY_B + slot], par ^ 1)) { ok = false; break; }
+                        uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
+                        const bool mins = C::kMins && h == 0;
+                        mbar_arrive_expect_tx(&bar[BAR_FULL_B + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
+                        const int k0 = (int)(sb * QK + 128 * h);
+                        tma_load_2d(bs, &map_a16, k0, t.t0, &bar[BAR_FULL_B + slot]);
+                        tma_load_2d(bs + C::B_SUB, &map_a16, k0 + 64, t.t0, &bar[BAR_FULL_B + slot]);
+                        if (mins) tma_load_2d(bs + 2 * C::B_SUB, &map_b16, (int)(sb * 16), t.t0, &bar[BAR_FULL_B + slot]);
+                    }
                 }
             }
             if (!ok) {
@@ -417,53 +530,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     } else if (warp == W_MMA) {
         // ------------------------------------------------ MMA issue
+        const uint32_t a_base = smem_u32(smem + C::OFF_A);
+        const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+        const uint32_t b_base = smem_u32(smem + C::OFF_B);
+        int64_t g = 0, use = 0;
         if (lane == 0) {
-            const uint32_t idesc = idesc_f16_f32(BM, n_mma);
-            const uint32_t a_base = smem_u32(smem + C::OFF_A);
-            const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
-            const uint32_t b_base = smem_u32(smem + C::OFF_B);
-            int64_t use = 0;
-            for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-                const int b = (int)(sb & 1);
-                const uint32_t acc_i = tmem + 256 * b, acc_m = tmem + 256 * b + 128;
-                if (!mbar_wait(&bar[BAR_ACC_EMPTY + b], (uint32_t)(((sb >> 1) & 1) ^ 1))) { ok = false; break; }
-                tc_fence_after();
-                for (int h = 0; h < 2; ++h, ++use) {
-                    const int slot = (int)(use % C::NB);
-                    if (!mbar_wait(&bar[BAR_FULL_A + h], (uint32_t)(sb & 1)) ||
-                        !mbar_wait(&bar[BAR_FULL_B + slot], (uint32_t)((use / C::NB) & 1))) {
-                        ok = false;
-                        break;
-                    }
+            int ntiles = 1;
+            if constexpr (G) {
+                ok = mbar_wait(&bar[BAR_TILES], 0);
+                ntiles = ok ? (int)misc[1] : 0;
+            }
+            for (int k = 0; k < ntiles && ok; ++k) {
+                const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+                const uint32_t idesc = idesc_f16_f32(BM, t.n_mma > 0 ? t.n_mma : 16);
+                for (int64_t sb = 0; sb < nsb && ok; ++sb, ++g) {
+                    const int b = (int)(g & 1);
+                    const uint32_t acc_i = tmem + 256 * b, acc_m = tmem + 256 * b + 128;
+                    if (!mbar_wait(&bar[BAR_ACC_EMPTY + b], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t a_slot = a_base + h * C::A_SLOT;
-                    const uint32_t b_slot = b_base + slot * C::B_SLOT;
-                    int planes = 1;
-                    if constexpr (F == FMT_Q6_K) {
-                        int any = 0;
-                        for (int w = 0; w < n_unpack<F>(); ++w) any |= s_flag[8 * h + w];
-                        planes = any ? 2 : 1;
-                    }
-                    for (int pl = 0; pl < planes; ++pl) {
-                        for (int j = 0; j < 2; ++j) {
-                            for (int k = 0; k < 4; ++k) {
-                                const uint64_t ad =
-                                    smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * k, 16, 1024, SWZ_128B);
-                                const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * k, 16, 1024, SWZ_128B);
-                                umma_f16(acc_i, ad, bd, idesc, (h | j | k | pl) != 0);
+                    for (int h = 0; h < 2; ++h) {
+                        const int slot = (int)(use % C::NB);
+                        if (!mbar_wait(&bar[BAR_FULL_A + h], (uint32_t)(g & 1)) ||
+                            (t.ntok > 0 && !mbar_wait(&bar[BAR_FULL_B + slot], (uint32_t)((use / C::NB) & 1)))) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (t.ntok == 0) {  // a first tile without rows: release the A slot unread
+                            mbar_arrive(&bar[BAR_EMPTY_A + h]);
+                            continue;
+                        }
+                        const uint32_t a_slot = a_base + h * C::A_SLOT;
+                        const uint32_t b_slot = b_base + slot * C::B_SLOT;
+                        int planes = 1;
+                        if constexpr (F == FMT_Q6_K) {
+                            int any = 0;
+                            for (int w = 0; w < n_unpack<F>(); ++w) any |= s_flag[8 * h + w];
+                            planes = any ? 2 : 1;
+                        }
+                        for (int pl = 0; pl < planes; ++pl) {
+                            for (int j = 0; j < 2; ++j) {
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t ad =
+                                        smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * kk, 16, 1024, SWZ_128B);
+                                    const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * kk, 16, 1024, SWZ_128B);
+                                    umma_f16(acc_i, ad, bd, idesc, (h | j | kk | pl) != 0);
+                                }
                             }
                         }
+                        if (C::kMins && h == 0) {
+                            const uint64_t ad = smem_desc(amin, 16, 256, SWZ_32B);
+                            const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
+                            umma_f16(acc_m, ad, bd, idesc, 0);
+                        }
+                        umma_commit(&bar[BAR_EMPTY_A + h]);
+                        umma_commit(&bar[BAR_EMPTY_B + slot]);
+                        ++use;
                     }
-                    if (C::kMins && h == 0) {
-                        const uint64_t ad = smem_desc(amin, 16, 256, SWZ_32B);
-                        const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
-                        umma_f16(acc_m, ad, bd, idesc, 0);
-                    }
-                    umma_commit(&bar[BAR_EMPTY_A + h]);
-                    umma_commit(&bar[BAR_EMPTY_B + slot]);
+                    if (!ok) break;
+                    if (t.ntok > 0) umma_commit(&bar[BAR_ACC_FULL + b]);
+                    else mbar_arrive(&bar[BAR_ACC_FULL + b]);
                 }
-                if (!ok) break;
-                umma_commit(&bar[BAR_ACC_FULL + b]);
             }
             // all MMAs issued by this thread complete before TMEM is released
             umma_commit(&bar[BAR_MMA_DONE]);
@@ -475,134 +602,192 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int uw = warp - W_UNPACK;          // 0..3 (Q6_K 0..7)
         const int r = 32 * (uw & 3) + lane;      // tile row
         const int my_jj = uw >> 2;               // Q6_K: this thread's K sub-tile of each half
-        const int64_t n = n0 + r;
-        const int64_t nc = n < p.N ? n : p.N - 1;
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         using Raw = typename RawOf<F>::T;
         Raw cur, nxt;
         // Q6_K: this thread's P2 rows of the half-0 / half-1 slot may be non-zero
         bool p2_dirty0 = true, p2_dirty1 = true;
-        const int64_t nstage = 2 * nsb;
-        if (nstage > 0) load_raw(cur, P, nc, 0, nsb, 0);
-        for (int64_t hs = 0; hs < nstage && ok; ++hs) {
-            const int64_t sb = hs >> 1;
-            const int h = (int)(hs & 1);
-            // the next half's bytes are in flight while this one is converted
-            if (hs + 1 < nstage) load_raw(nxt, P, nc, (hs + 1) >> 1, nsb, (int)((hs + 1) & 1));
-            if (!mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((sb & 1) ^ 1))) { ok = false; break; }
-            if (h == 0 && !mbar_wait(&bar[BAR_ACC_EMPTY + (sb & 1)], (uint32_t)(((sb >> 1) & 1) ^ 1))) {
-                ok = false;
-                break;
-            }
-            const uint32_t a_slot = a_base + h * C::A_SLOT;
-            float d = 0.0f, dmin = 0.0f;
-            if constexpr (F == FMT_Q6_K) {
-                const uint32_t scj = my_jj ? cur.sc[1] : cur.sc[0];
-                bool big = false;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int v = (int)(int8_t)((scj >> (8 * i)) & 0xFF);
-                    big |= (v > 62 || v < -62);
+        const int nstage = 2 * (int)nsb;
+        int k = 0, g = 0, ntiles = -1;  // ntiles: grouped list length, read once it is needed
+        Tile t;
+        bool have = true;
+        if constexpr (!G) {
+            t = dense_tile(p);
+        } else if (static_first) {
+            const int w_tiles = w_tiles_of(p);
+            t.e = (int)(blockIdx.x / w_tiles);
+            t.n0 = (int)(blockIdx.x % w_tiles) * BM;
+        } else {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
+            ntiles = ok ? (int)misc[1] : 0;
+            have = ntiles > 0;
+            if (have) t = list_tile(s_list, 0);
+        }
+        // this thread's weight row of the tile
+        int e_cur = t.e, row = t.n0 + r < p.N ? t.n0 + r : (int)p.N - 1;
+        if (have) load_raw(cur, make_planes(F, p.packed + (uint64_t)e_cur * p.expert_bytes, p.N, nsb), row, 0, nsb, 0);
+        while (have && ok) {
+            bool have_n = false;
+            int e_nxt = e_cur, n0_nxt = 0;
+            const Planes P = make_planes(F, p.packed + (uint64_t)e_cur * p.expert_bytes, p.N, nsb);
+            for (int hs = 0; hs < nstage; ++hs) {
+                const int sb = hs >> 1, gg = g + sb;
+                const int h = hs & 1;
+                // the next half's bytes (the next tile's first half at the
+                // end of a tile) are in flight while this one is converted
+                if (hs + 1 < nstage) {
+                    load_raw(nxt, P, row, (hs + 1) >> 1, nsb, (hs + 1) & 1);
+                } else if constexpr (G) {
+                    if (ntiles < 0) {
+                        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0))) {
+                            ok = false;
+                            break;
+                        }
+                        ntiles = (int)misc[1];
+                    }
+                    have_n = k + 1 < ntiles;
+                    if (have_n) {
+                        const int4 v = s_list[k + 1];
+                        e_nxt = v.x;
+                        n0_nxt = v.y;
+                        // the next tile's planes: this expert's, shifted by whole expert images
+                        const int64_t delta = (int64_t)(e_nxt - e_cur) * (int64_t)p.expert_bytes;
+                        const Planes Q{P.p0 + delta, P.p1 + delta, P.p2 + delta, P.p3 + delta};
+                        const int rn = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
+                        load_raw(nxt, Q, rn, 0, nsb, 0);
+                    }
                 }
-                const unsigned any = __ballot_sync(0xFFFFFFFFu, big);
-                if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
-                const uint32_t a_tile = a_slot + my_jj * 16384;
-                const bool dirty = h ? p2_dirty1 : p2_dirty0;
-                unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, scj, my_jj, big, !big && dirty);
-                if (h) p2_dirty1 = big;
-                else p2_dirty0 = big;
-                d = __half2float(__ushort_as_half((unsigned short)cur.d));
-            } else {
-                const ScaleMin sm = unpack_scale_min(cur.hdr);
-                uint32_t qh0[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if constexpr (F == FMT_Q5_K) qh0[i] = cur.qh[i];
-                    else qh0[i] = 0u;
+                bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
+                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_ACC_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
+                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t a_slot = a_base + h * C::A_SLOT;
+                float d = 0.0f, dmin = 0.0f;
+                if constexpr (F == FMT_Q6_K) {
+                    const uint32_t scj = my_jj ? cur.sc[1] : cur.sc[0];
+                    bool big = false;
 #pragma unroll
-                for (int jj = 0; jj < 2; ++jj) {
-                    const int cch = 2 * h + jj;  // chunk of the superblock; sub-blocks 2c, 2c+1
-                    const uint32_t scw = cch < 2 ? sm.sc_lo : sm.sc_hi;
-                    const int sc_lo = byte_of(scw, 2 * (cch & 1)), sc_hi = byte_of(scw, 2 * (cch & 1) + 1);
-                    uint32_t qsc[8];
+                    for (int i = 0; i < 4; ++i) {
+                        const int v = (int)(int8_t)((scj >> (8 * i)) & 0xFF);
+                        big |= (v > 62 || v < -62);
+                    }
+                    const unsigned any = __ballot_sync(0xFFFFFFFFu, big);
+                    if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
+                    const uint32_t a_tile = a_slot + my_jj * 16384;
+                    const bool dirty = h ? p2_dirty1 : p2_dirty0;
+                    unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, scj, my_jj, big, !big && dirty);
+                    if (h) p2_dirty1 = big;
+                    else p2_dirty0 = big;
+                    d = __half2float(__ushort_as_half((unsigned short)cur.d));
+                } else {
+                    const ScaleMin sm = unpack_scale_min(cur.hdr);
+                    uint32_t qh0[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) qsc[i] = cur.qs[8 * jj + i];
-                    unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                    for (int i = 0; i < 8; ++i) {
+                        if constexpr (F == FMT_Q5_K) qh0[i] = cur.qh[i];
+                        else qh0[i] = 0u;
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int cch = 2 * h + jj;  // chunk of the superblock; sub-blocks 2c, 2c+1
+                        const uint32_t scw = cch < 2 ? sm.sc_lo : sm.sc_hi;
+                        const int sc_lo = byte_of(scw, 2 * (cch & 1)), sc_hi = byte_of(scw, 2 * (cch & 1) + 1);
+                        uint32_t qsc[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) qsc[i] = cur.qs[8 * jj + i];
+                        unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                    }
+                    if (h == 0) {
+                        // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
+                        const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+                        uint32_t mw[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
+                        sts128(amin + sw32_offset(r, 0), mw[0], mw[1], mw[2], mw[3]);
+                        sts128(amin + sw32_offset(r, 8), mw[4], mw[5], mw[6], mw[7]);
+                    }
+                    d = half_lo(cur.hdr.x);
+                    dmin = half_hi(cur.hdr.x);
                 }
-                if (h == 0) {
-                    // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
-                    const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
-                    uint32_t mw[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
-                    sts128(amin + sw32_offset(r, 0), mw[0], mw[1], mw[2], mw[3]);
-                    sts128(amin + sw32_offset(r, 8), mw[4], mw[5], mw[6], mw[7]);
+                if (h == 0 && my_jj == 0) {
+                    s_d[(gg & 1) * BM + r] = d;
+                    s_dmin[(gg & 1) * BM + r] = dmin;
                 }
-                d = half_lo(cur.hdr.x);
-                dmin = half_hi(cur.hdr.x);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar[BAR_FULL_A + h]);
+                    if (h == 0 && my_jj == 0) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
+                }
+                cur = nxt;
             }
-            if (h == 0 && my_jj == 0) {
-                s_d[(sb & 1) * BM + r] = d;
-                s_dmin[(sb & 1) * BM + r] = dmin;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&bar[BAR_FULL_A + h]);
-                if (h == 0 && my_jj == 0) mbar_arrive(&bar[BAR_SD_FULL + (sb & 1)]);
-            }
-            cur = nxt;
+            g += (int)nsb;
+            ++k;
+            have = have_n;
+            e_cur = e_nxt;
+            row = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
         }
         if (!ok && lane == 0) set_timeout();
     } else if constexpr (F == FMT_Q6_K) {
         // ------------------------------------------------ epilogue, Q6_K
         // 4 warps, thread = weight row x every token column; y accumulates
         // in TMEM columns 128..255 (the mins slot of buffer 0, which Q6_K
-        // does not use), read back once at the end
+        // does not use), read back once at the end of each tile
         const int ew = warp - w_epi<F>();    // 0..3
         const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
         const int r = 32 * quad + lane;
-        const int64_t n = n0 + r;
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 128 * ew;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
         const uint32_t y_tm = lane_addr + 128;
-        const int nchunk = n_mma / 8;
         griddep_wait();  // the scales are written by the kernels before this one
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-            const int b = (int)(sb & 1);
-            // the 128 token scales d8 of the superblock
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int64_t tc = t0 + 32 * q + lane;
-                s_d8[32 * q + lane] = tc < t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
-            }
-            __syncwarp();
-            if (!mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((sb >> 1) & 1)) ||
-                !mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((sb >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float dd = s_d[b * BM + r];
-            for (int c = 0; c < nchunk; ++c) {
-                uint32_t vi[8], vy[8];
-                tmem_ld8(lane_addr + 256 * b + 8 * c, vi);
-                if (sb > 0) tmem_ld8(y_tm + 8 * c, vy);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float yo = sb > 0 ? __uint_as_float(vy[i]) : 0.0f;
-                    vy[i] = __float_as_uint(fmaf(s_d8[8 * c + i], dd * __uint_as_float(vi[i]), yo));
-                }
-                tmem_st8(y_tm + 8 * c, vy);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+        int ntiles = 1;
+        if constexpr (G) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
+            ntiles = ok ? (int)misc[1] : 0;
         }
-        if (ok) {
+        int64_t g = 0;
+        for (int k = 0; k < ntiles && ok; ++k) {
+            const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+            const int64_t n = t.n0 + r;
+            const int nchunk = t.n_mma / 8;
+            for (int64_t sb = 0; sb < nsb; ++sb) {
+                const int64_t gg = g + sb;
+                const int b = (int)(gg & 1);
+                // the 128 token scales d8 of the superblock
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int64_t tc = t.t0 + 32 * q + lane;
+                    s_d8[32 * q + lane] = tc < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
+                }
+                __syncwarp();
+                bool w_ok = mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1));
+                if (w_ok) w_ok = mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((gg >> 1) & 1));
+                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float dd = s_d[b * BM + r];
+                for (int c = 0; c < nchunk; ++c) {
+                    uint32_t vi[8], vy[8];
+                    tmem_ld8(lane_addr + 256 * b + 8 * c, vi);
+                    if (sb > 0) tmem_ld8(y_tm + 8 * c, vy);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float yo = sb > 0 ? __uint_as_float(vy[i]) : 0.0f;
+                        vy[i] = __float_as_uint(fmaf(s_d8[8 * c + i], dd * __uint_as_float(vi[i]), yo));
+                    }
+                    tmem_st8(y_tm + 8 * c, vy);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+            }
+            if (!ok) break;
             tc_fence_after();
             for (int c = 0; c < nchunk; ++c) {
                 uint32_t vy[8];
@@ -611,11 +796,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (n < p.N) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const int64_t t = t0 + 8 * c + i;
-                        if (t < t_end) p.y[t * p.N + n] = __uint_as_float(vy[i]);
+                        const int64_t tt = t.t0 + 8 * c + i;
+                        if (tt < t.t_end) p.y[tt * p.N + n] = __uint_as_float(vy[i]);
                     }
                 }
             }
+            g += nsb;
         }
         if (!ok && lane == 0) set_timeout();
     } else {
@@ -624,55 +810,69 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
         const int ch = ew >> 2;              // token columns 64*ch .. +63
         const int r = 32 * quad + lane;
-        const int64_t n = n0 + r;
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 64 * ew;
-        float y[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) y[i] = 0.0f;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
         griddep_wait();  // the scales are written by the kernels before this one
-        for (int64_t sb = 0; sb < nsb && ok; ++sb) {
-            const int b = (int)(sb & 1);
-            // this warp's 64 token scales d8 for the superblock
-            {
-                const int64_t tc = t0 + 64 * ch + lane;
-                s_d8[lane] = tc < t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
-                s_d8[lane + 32] = (tc + 32) < t_end ? __ldg(p.d8t + sb * p.Mp + tc + 32) : 0.0f;
-                __syncwarp();
-            }
-            if (!mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((sb >> 1) & 1)) ||
-                !mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((sb >> 1) & 1))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const float dd = s_d[b * BM + r], dm = s_dmin[b * BM + r];
-            const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
-            if (64 * ch < n_mma) {
+        int ntiles = 1;
+        if constexpr (G) {
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
+            ntiles = ok ? (int)misc[1] : 0;
+        }
+        int64_t g = 0;
+        for (int k = 0; k < ntiles && ok; ++k) {
+            const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+            float y[64];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t vi[16], vm[16];
-                    tmem_ld16(lane_addr + 256 * b + 64 * ch + 16 * cc, vi);
-                    if (C::kMins) tmem_ld16(lane_addr + 256 * b + 128 + 64 * ch + 16 * cc, vm);
-                    tmem_wait_ld();
+            for (int i = 0; i < 64; ++i) y[i] = 0.0f;
+            const bool cols = 64 * ch < t.n_mma;
+            for (int64_t sb = 0; sb < nsb; ++sb) {
+                const int64_t gg = g + sb;
+                const int b = (int)(gg & 1);
+                // this warp's 64 token scales d8 for the superblock
+                {
+                    const int64_t tc = t.t0 + 64 * ch + lane;
+                    s_d8[lane] = tc < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
+                    s_d8[lane + 32] = (tc + 32) < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc + 32) : 0.0f;
+                    __syncwarp();
+                }
+                bool w_ok = mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1));
+                if (w_ok) w_ok = mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((gg >> 1) & 1));
+                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const float dd = s_d[b * BM + r], dm = s_dmin[b * BM + r];
+                if (cols) {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float iv = __uint_as_float(vi[i]);
-                        float t = dd * iv;
-                        if (C::kMins) t = fmaf(-dm, __uint_as_float(vm[i]), t);
-                        y[16 * cc + i] = fmaf(s_d8[16 * cc + i], t, y[16 * cc + i]);
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t vi[16], vm[16];
+                        tmem_ld16(lane_addr + 256 * b + 64 * ch + 16 * cc, vi);
+                        if (C::kMins) tmem_ld16(lane_addr + 256 * b + 128 + 64 * ch + 16 * cc, vm);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float iv = __uint_as_float(vi[i]);
+                            float tv = dd * iv;
+                            if (C::kMins) tv = fmaf(-dm, __uint_as_float(vm[i]), tv);
+                            y[16 * cc + i] = fmaf(s_d8[16 * cc + i], tv, y[16 * cc + i]);
+                        }
                     }
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
-        }
-        if (ok && n < p.N) {
+            if (!ok) break;
+            const int n = t.n0 + r;
+            if (n < p.N && cols) {
+                const int c0 = t.t0 + 64 * ch, lim = t.t_end - c0;
+                float *yp = p.y + (int64_t)c0 * p.N + n;
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const int64_t t = t0 + 64 * ch + i;
-                if (t < t_end) p.y[t * p.N + n] = y[i];
+                for (int i = 0; i < 64; ++i)
+                    if (i < lim) yp[(int64_t)i * p.N] = y[i];
             }
+            g += nsb;
         }
         if (!ok && lane == 0) set_timeout();
     }
@@ -803,7 +1003,9 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
         return cudaErrorInvalidValue;
     static bool attr_set[4] = {false, false, false, false};
     if (!attr_set[F]) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
         if (e != cudaSuccess) return e;
         attr_set[F] = true;
     }
@@ -819,11 +1021,29 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     p.d8t = d8t;
     p.Mp = L.Mp;
     p.y = y;
+    // dense: one block per tile; grouped: a block per SM walking a list of
+    // tiles (the experts' first token tiles, plus at most M / BT later ones),
+    // with enough blocks that no list exceeds TILE_CAP
     const int64_t w_tiles = (N + BM - 1) / BM;
-    const int64_t t_tiles = offsets ? (M + BT - 1) / BT + E : (M + BT - 1) / BT;
-    dim3 grid((unsigned)t_tiles, (unsigned)w_tiles);
+    const int64_t t_tiles = (M + BT - 1) / BT;
+    const int64_t tiles = offsets ? (E + M / BT) * w_tiles : t_tiles * w_tiles;
+    if (tiles <= 0) return cudaSuccess;
+    if (tiles > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX - BM) return cudaErrorNotSupported;
+    if (offsets && E > MAX_GROUPED_E) return cudaErrorNotSupported;
+    int64_t blocks = tiles;
+    if (offsets) {
+        static int sms[64] = {0};
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+        int &n_sm = sms[dev & 63];
+        if (!n_sm && cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidDevice;
+        const int64_t need = (tiles + TILE_CAP - 3) / (TILE_CAP - 2);
+        blocks = tiles < n_sm ? tiles : n_sm;
+        if (blocks < need) blocks = need;
+    }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = Cf::SMEM;
     cfg.stream = s;
@@ -832,7 +1052,8 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<F>, ma, mb, p);
+    if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true>, ma, mb, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false>, ma, mb, p);
 }
 
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,

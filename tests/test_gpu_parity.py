@@ -327,6 +327,28 @@ def test_grouped_uneven_and_empty_experts(K, fmt):
 
 
 @pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts", [[0, 300, 0, 129, 1, 0, 270], [0, 0, 600], [128, 0, 256, 17]])
+def test_grouped_later_token_tiles(K, fmt, counts):
+    """Experts with more rows than one 128-token tile (the later tiles are
+    found from the offsets), empty experts among them (also first, whose
+    weights the kernel unpacks before it knows the expert is empty), a weight
+    tile count with a ragged tail (N = 300), and all rows on one expert:
+    every output against the oracle with its expert."""
+    rng = synth.rng_for(118, fmt * 100 + len(counts))
+    E, N, Kdim = len(counts), 300, 512
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    planes = oracle_q8k(synth.activations(int(offsets[-1]), Kdim, rng))
+    y = run_grouped(K, fmt, disks, planes, offsets)
+    for e in range(E):
+        a, b = offsets[e], offsets[e + 1]
+        if a == b:
+            continue
+        sl = tuple(p[a:b] for p in planes)
+        assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
 @pytest.mark.parametrize("counts", [[0, 1, 0, 0, 1, 1, 0, 1, 0, 1, 1, 0, 0, 1, 0, 1],
                                     [0, 3, 0, 1, 2, 0, 0, 5, 0, 0, 1, 0, 0, 0, 1, 0]])
 def test_grouped_decode_rows(K, fmt, counts):
