@@ -75,6 +75,11 @@ def lib():
             L.ko_gemm.argtypes = [i32, P, i64, i64, P, P, P, i64, P, i64, P, i64, P]
             L.ko_bruteforce_dot.argtypes = [i32, P, i64, P, P]
             L.ko_bruteforce_dot.restype = ctypes.c_double
+            L.ko_quantize_q8_0.argtypes = [P, i64, i64, P, P]
+            L.ko_quantize_q8_0.restype = None
+            L.ko_gemv_q8_0.argtypes = [P, i64, i64, P, P, i64, P]
+            L.ko_bruteforce_q8_0.argtypes = [P, i64, P, P]
+            L.ko_bruteforce_q8_0.restype = ctypes.c_double
             L.ko_num_threads.argtypes = []
             L.ko_set_num_threads.argtypes = [i32]
             L.ko_set_num_threads.restype = None
@@ -185,3 +190,47 @@ def bruteforce_dot(fmt: int, row: np.ndarray, d8: np.ndarray, q8: np.ndarray) ->
     d8 = np.ascontiguousarray(d8, dtype=np.float32)
     q8 = np.ascontiguousarray(q8, dtype=np.int8)
     return lib().ko_bruteforce_dot(fmt, _p(row), row.shape[0], _p(d8), _p(q8))
+
+
+# ---- Q8_0 (the q8 rail: Q8_0 weights x Q8_0-form activations, blocks of 32)
+Q8_0 = 4
+Q8_0_BLOCK = 34
+QK8_0 = 32
+
+
+def quantize_q8_0(x: np.ndarray):
+    """Q8_0 activations of float32 [M, K] -> (d f32 [M, K/32], q i8 [M, K])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        x = x[None, :]
+    M, K = x.shape
+    assert K % QK8_0 == 0
+    d = np.zeros((M, K // QK8_0), np.float32)
+    q = np.zeros((M, K), np.int8)
+    lib().ko_quantize_q8_0(_p(x), M, K, _p(d), _p(q))
+    return d, q
+
+
+def gemv_q8_0(disk: np.ndarray, d_a: np.ndarray, q_a: np.ndarray) -> np.ndarray:
+    """Y[M, N] in float64 for disk Q8_0 weights [N, K/32, 34] and M activation rows."""
+    disk = np.ascontiguousarray(disk, dtype=np.uint8)
+    d_a = np.ascontiguousarray(d_a, dtype=np.float32)
+    q_a = np.ascontiguousarray(q_a, dtype=np.int8)
+    N, nb, bb = disk.shape
+    assert bb == Q8_0_BLOCK
+    if q_a.ndim == 1:
+        q_a, d_a = q_a[None, :], d_a[None, :]
+    M, K = q_a.shape
+    assert K == nb * QK8_0
+    Y = np.zeros((M, N), np.float64)
+    if lib().ko_gemv_q8_0(_p(disk), N, K, _p(d_a), _p(q_a), M, _p(Y)):
+        raise ValueError("ko_gemv_q8_0 rejected its arguments")
+    return Y
+
+
+def bruteforce_q8_0(row: np.ndarray, d_a: np.ndarray, q_a: np.ndarray) -> float:
+    """Dequantize-then-dot in double for one Q8_0 row [K/32, 34] and one activation row."""
+    row = np.ascontiguousarray(row, dtype=np.uint8)
+    d_a = np.ascontiguousarray(d_a, dtype=np.float32)
+    q_a = np.ascontiguousarray(q_a, dtype=np.int8)
+    return lib().ko_bruteforce_q8_0(_p(row), row.shape[0], _p(d_a), _p(q_a))

@@ -316,6 +316,80 @@ double ko_bruteforce_dot(int fmt, const uint8_t *row, int64_t nsb,
     return acc;
 }
 
+/* ---- Q8_0 ---------------------------------------------------------------- */
+
+void ko_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *q) {
+    const int64_t nb = K / KO_QK8_0;
+    const int saved_round = fegetround();
+    fesetround(FE_TONEAREST);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *xb = x + m * K + b * KO_QK8_0;
+            int8_t *qb = q + m * K + b * KO_QK8_0;
+            float amax = 0.0f;
+            for (int j = 0; j < KO_QK8_0; ++j) {
+                float ax = fabsf(xb[j]);
+                if (ax > amax) amax = ax;
+            }
+            if (amax == 0.0f) {
+                d[m * nb + b] = 0.0f;
+                memset(qb, 0, KO_QK8_0);
+                continue;
+            }
+            volatile float iscale = 127.0f / amax;
+            for (int j = 0; j < KO_QK8_0; ++j) {
+                volatile float t = xb[j] * iscale;
+                long v = lrintf(t);
+                if (v > 127) v = 127;
+                if (v < -127) v = -127;
+                qb[j] = (int8_t)v;
+            }
+            d[m * nb + b] = amax / 127.0f;
+        }
+    }
+    fesetround(saved_round);
+}
+
+/* One output: the integer dot of each 32-block, closed by one float fold
+ * per block (d_w * d_a * isum), summed over the row in double.  d_w (fp16)
+ * times d_a (fp32) is exact in double. */
+static double q8_0_dot(const uint8_t *row, int64_t nb, const float *d_a, const int8_t *q_a) {
+    double acc = 0.0;
+    for (int64_t b = 0; b < nb; ++b) {
+        const uint8_t *blk = row + b * KO_Q8_0_BLOCK;
+        const double dw = half_bits_to_double(le16(blk));
+        int32_t isum = 0;
+        for (int k = 0; k < KO_QK8_0; ++k) isum += (int32_t)(int8_t)blk[2 + k] * (int32_t)q_a[b * KO_QK8_0 + k];
+        acc += dw * (double)d_a[b] * (double)isum;
+    }
+    return acc;
+}
+
+int ko_gemv_q8_0(const uint8_t *disk, int64_t N, int64_t K, const float *d_a,
+                 const int8_t *q_a, int64_t M, double *Y) {
+    if (K % KO_QK8_0 || N < 0 || M < 0) return -1;
+    const int64_t nb = K / KO_QK8_0;
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t m = 0; m < M; ++m)
+            Y[m * N + n] = q8_0_dot(disk + n * nb * KO_Q8_0_BLOCK, nb, d_a + m * nb, q_a + m * K);
+    return 0;
+}
+
+double ko_bruteforce_q8_0(const uint8_t *row, int64_t nblk, const float *d_a, const int8_t *q_a) {
+    double acc = 0.0;
+    for (int64_t b = 0; b < nblk; ++b) {
+        const uint8_t *blk = row + b * KO_Q8_0_BLOCK;
+        const double dw = half_bits_to_double(le16(blk));
+        for (int k = 0; k < KO_QK8_0; ++k) {
+            const double w = dw * (double)(int8_t)blk[2 + k];
+            const double a = (double)d_a[b] * (double)q_a[b * KO_QK8_0 + k];
+            acc += w * a;
+        }
+    }
+    return acc;
+}
+
 int ko_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

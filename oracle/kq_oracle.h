@@ -88,6 +88,32 @@ int ko_gemm(int fmt, const uint8_t *disk, int64_t N, int64_t K,
 double ko_bruteforce_dot(int fmt, const uint8_t *row, int64_t nsb,
                          const float *d8, const int8_t *a8);
 
+/* ---- Q8_0 (the pages' "q8 rail": Q8_0 weights read with Q8_0-form
+ * activations, one activation image per consumed form; [kq-arc], the
+ * chain-regrain commit and the grouped-prefill fix of the MoE page).
+ * A block holds 32 values: on disk an fp16 d then 32 int8 q (34 bytes,
+ * the public GGUF block), weight = d * q.  The activation form has one
+ * fp32 scale per 32 values, quantized like Q8_K but per 32:
+ * d = amax / 127, q = clamp(round_half_even(x * (127 / amax)), -127, 127),
+ * amax == 0 giving d = 0 and q = 0. */
+enum { KO_Q8_0_BLOCK = 34, KO_QK8_0 = 32 };
+
+/* Q8_0 activations of M rows of K floats (K % 32 == 0): d [M][K/32],
+ * q [M][K], row-major. */
+void ko_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *q);
+
+/* Y[m][n] = sum over the K/32 blocks b of d_w(n,b) * d_a(m,b) * isum, with
+ * isum = sum_k q_w * q_a in int32 and the sum over blocks in double.
+ * disk is [N][K/32][34]; d_a / q_a are the activation planes of M rows.
+ * Returns 0, or -1 on a bad argument. */
+int ko_gemv_q8_0(const uint8_t *disk, int64_t N, int64_t K, const float *d_a,
+                 const int8_t *q_a, int64_t M, double *Y);
+
+/* Brute force for one row and one activation row: both dequantized to
+ * double (d * q), plain dot product.  Independent of the fold. */
+double ko_bruteforce_q8_0(const uint8_t *row, int64_t nblk, const float *d_a,
+                          const int8_t *q_a);
+
 /* Threads the OpenMP loops use (1 without OpenMP). */
 int ko_num_threads(void);
 void ko_set_num_threads(int n);

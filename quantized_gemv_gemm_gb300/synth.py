@@ -55,6 +55,22 @@ def disk_weights(fmt: int, N: int, K: int, rng: np.random.Generator) -> np.ndarr
     return raw
 
 
+Q8_0 = 4
+Q8_0_BLOCK = 34   # fp16 d + 32 int8 quants (GGUF order)
+QK8_0 = 32
+
+
+def disk_weights_q8_0(N: int, K: int, rng: np.random.Generator) -> np.ndarray:
+    """Random GGUF-order Q8_0 blocks, uint8 [N, K/32, 34]: fp16 d ~ U(1e-3, 1e-2),
+    quants ~ U{-127..127}."""
+    assert K % QK8_0 == 0
+    nb = K // QK8_0
+    raw = np.empty((N, nb, Q8_0_BLOCK), np.uint8)
+    raw[..., 2:] = rng.integers(-127, 128, size=(N, nb, QK8_0)).astype(np.int8).view(np.uint8)
+    _put_f16(raw, 0, rng.uniform(1e-3, 1e-2, size=(N, nb)))
+    return raw
+
+
 def activations(M: int, K: int, rng: np.random.Generator, outliers: bool = False) -> np.ndarray:
     x = rng.standard_normal((M, K), dtype=np.float32)
     if outliers:

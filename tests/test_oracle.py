@@ -174,3 +174,73 @@ def test_oracle_rejects_bad_arguments():
                     np.zeros((1, 16), np.int16), tok_idx=np.array([2]))
     assert oracle.lib().ko_block_bytes(9) == 0
     assert oracle.lib().ko_decode(9, None, None, None, None, None, None) == -1
+
+
+# ---------------------------------------------------------------- Q8_0 rail
+def _q8_0_row(d_bits, quants):
+    """One Q8_0 row [nb, 34] from fp16 bit patterns [nb] and int quants [nb, 32]."""
+    quants = np.asarray(quants, np.int64).reshape(len(d_bits), 32)
+    row = np.zeros((len(d_bits), 34), np.uint8)
+    for b, h in enumerate(d_bits):
+        row[b, 0], row[b, 1] = h & 0xFF, h >> 8
+        row[b, 2:] = quants[b].astype(np.int8).view(np.uint8)
+    return row
+
+
+def test_q8_0_quantize_closed_forms():
+    """Q8_0 activations: zero block, ties to even at iscale = 1 (amax 127),
+    the extreme value mapped to +-127, one scale per 32 values."""
+    x = np.zeros((1, 64), np.float32)
+    x[0, 32:36] = [127.0, 2.5, 3.5, -2.5]
+    x[0, 36] = -0.5
+    d, q = oracle.quantize_q8_0(x)
+    assert d[0, 0] == 0.0 and not q[0, :32].any()
+    assert d[0, 1] == np.float32(1.0)
+    assert q[0, 32:37].tolist() == [127, 2, 4, -2, 0]
+    x2 = np.full((1, 32), -3.0, np.float32)
+    d2, q2 = oracle.quantize_q8_0(x2)
+    assert q2[0].tolist() == [-127] * 32 and d2[0, 0] == np.float32(3.0) / np.float32(127.0)
+
+
+def test_q8_0_quantize_invariants_random():
+    rng = synth.rng_for(900, 1)
+    x = synth.activations(3, 512, rng, outliers=True)
+    d, q = oracle.quantize_q8_0(x)
+    xb = x.reshape(3, -1, 32).astype(np.float64)
+    db = d.astype(np.float64)[..., None]
+    assert np.all(np.abs(q.reshape(3, -1, 32)).max(axis=2) == 127)
+    assert np.all(np.abs(xb - db * q.reshape(3, -1, 32)) <= db / 2 * (1 + 1e-6))
+
+
+def test_q8_0_gemv_closed_forms():
+    K = 256
+    x = np.ones((1, K), np.float32)
+    d_a, q_a = oracle.quantize_q8_0(x)               # q = 127, d = fl32(1/127)
+    one = 0x3C00                                      # fp16 1.0
+    rows = np.stack([
+        _q8_0_row([one] * 8, np.ones(K)),                              # all ones
+        _q8_0_row([one] * 8, np.tile([1, -1], K // 2)),                # cancels exactly
+        _q8_0_row([0] * 3 + [0x4000] + [0] * 4, np.arange(K) % 7 - 3),  # only block 3, d = 2
+    ])
+    y = oracle.gemv_q8_0(rows, d_a, q_a)[0]
+    inv = float(np.float32(1.0) / np.float32(127.0))
+    assert y[0] == pytest.approx(K * 127 * inv, rel=1e-15)
+    assert y[1] == 0.0
+    blk3 = (np.arange(K) % 7 - 3)[96:128]
+    assert y[2] == pytest.approx(2.0 * inv * 127 * blk3.sum(), rel=1e-15)
+
+
+@pytest.mark.parametrize("K", [32, 256, 1024])
+def test_q8_0_fold_matches_fp64_bruteforce(K):
+    rng = synth.rng_for(900, K)
+    disk = synth.disk_weights_q8_0(5, K, rng)
+    d_a, q_a = oracle.quantize_q8_0(synth.activations(2, K, rng, outliers=True))
+    Y = oracle.gemv_q8_0(disk, d_a, q_a)
+    for m in range(2):
+        for n in range(5):
+            bf = oracle.bruteforce_q8_0(disk[n], d_a[m], q_a[m])
+            assert Y[m, n] == pytest.approx(bf, rel=1e-12, abs=1e-12)
+    # a permuted weight block must change the result (pins the element order)
+    d2 = disk.copy()
+    d2[0, 0, 2:] = disk[0, 0, 2:][::-1]
+    assert oracle.gemv_q8_0(d2, d_a, q_a)[0, 0] != Y[0, 0]
