@@ -57,7 +57,10 @@
 extern "C" {
 #endif
 
-typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3 } kq_format;
+/* KQ_Q8_0: Q8_0 weights (blocks of 32 values: fp16 d, 32 int8 q), accepted
+ * only by kq_block_bytes, kq_repack_bytes, kq_repack and kq_gemv_q8_0; every
+ * K-quant entry point returns KQ_ERR_FORMAT for it. */
+typedef enum { KQ_Q4_K = 1, KQ_Q5_K = 2, KQ_Q6_K = 3, KQ_Q8_0 = 4 } kq_format;
 
 typedef enum {
     KQ_OK = 0,
@@ -78,7 +81,9 @@ typedef struct { float *d; int8_t *qs; int16_t *bsums; } kq_q8k;
 /* Human-readable name of a kq_status. */
 const char *kq_strerror(int code);
 
-/* Bytes of one disk superblock of format f (144 / 176 / 210), 0 if unknown. */
+/* Bytes of one disk block of format f: a 256-weight superblock for the
+ * K-quants (144 / 176 / 210), a 32-weight block for KQ_Q8_0 (34); 0 if
+ * unknown. */
 size_t kq_block_bytes(kq_format f);
 
 /*
@@ -118,12 +123,19 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
  * of plane padding.
  */
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
+/*
+ * KQ_Q8_0 images (K a positive multiple of 256): rows in groups of 16 as
+ * above, two planes: qs (4096-byte chunks; row r's 16 quants of columns
+ * 16k..16k+15 of the superblock at 256*k + 16*r) | d (256-byte chunks; row
+ * r's 8 fp16 block scales at 16*r).  1.0625 bytes per weight, as on disk.
+ */
 
 /*
  * One-time repack of disk superblocks into the packed image ([kq-arc], k4
  * kq-v2 commit: the weights are transcoded and repacked once at load, and
  * the repacked planes dequantize bit-identically to the file).
- *   disk   device uint8 [N][K/256][block_bytes] (GGUF order), 16-byte aligned
+ *   disk   device uint8 [N][K/256][block_bytes] (GGUF order; KQ_Q8_0:
+ *          [N][K/32][34]), 16-byte aligned
  *   packed device, kq_repack_bytes(f, N, K) bytes, 256-byte aligned
  * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
  */
@@ -266,6 +278,36 @@ int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_
  */
 int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32_t *q,
                     int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
+
+/*
+ * The Q8_0 rail ([kq-arc], chain-regrain commit: one activation image per
+ * consumed form, the Q8_0 projections reading a Q8_0-form image; grouped-
+ * prefill fix: the Q8_0 weights' fp16 scale plane).  Q8_0-form activations:
+ * per 32 values of each row of x, amax = max|x|; amax == 0 gives d = 0 and
+ * q = 0, else q = clamp(round_half_even(x * (127/amax)), -127, 127) in IEEE
+ * fp32 and d = amax/127 (the Q8_K arithmetic, per 32).
+ *   x   device float32 [M][K] row-major (K % 32 == 0), 16-byte aligned, finite
+ *   d   device float32 [M][K/32], 4-byte aligned
+ *   qs  device int8 [M][K], 16-byte aligned
+ * Errors: KQ_ERR_ARG (null, M < 0, K % 32), KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ * M == 0 is a no-op.
+ */
+int kq_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *qs, cudaStream_t s);
+
+/*
+ * Q8_0 GEMV (M = 1): y[n] = sum over the 32-blocks b of row n of
+ * d_w(n, b) * d(b) * isum_b, isum_b the int32 dot of the block's weight and
+ * activation quants (one float fold per block).  Reads every packed byte once.
+ *   packed  device KQ_Q8_0 image from kq_repack (256-byte aligned)
+ *   d, qs   one activation row from kq_quantize_q8_0 (K/32 floats, K int8;
+ *           qs 16-byte aligned)
+ *   y       device float32 [N]
+ *   K       a positive multiple of 256, at most 40960
+ * The result is independent of scheduling (fixed summation order).
+ * Errors: KQ_ERR_ARG, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.  N == 0 is a no-op.
+ */
+int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, float *y,
+                 cudaStream_t s);
 
 /*
  * Measurement hook: the int8 rate of the warp-level integer MMA

@@ -88,7 +88,10 @@ const char *kq_strerror(int code) {
     }
 }
 
-size_t kq_block_bytes(kq_format f) { return fmt_ok(f) ? (size_t)block_bytes(f) : 0; }
+size_t kq_block_bytes(kq_format f) {
+    if (f == KQ_Q8_0) return 34;
+    return fmt_ok(f) ? (size_t)block_bytes(f) : 0;
+}
 
 int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream_t s) {
     if (M < 0 || K <= 0 || K % QK != 0) return KQ_ERR_ARG;
@@ -100,6 +103,7 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
 }
 
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K) {
+    if (f == KQ_Q8_0) return check_shape(N, K) ? 0 : (size_t)q8_0_image_bytes(N, K);
     if (!fmt_ok(f) || check_shape(N, K)) return 0;
     uint64_t off[5];
     plane_offsets(f, N, K / QK, off);
@@ -107,12 +111,32 @@ size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K) {
 }
 
 int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s) {
-    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (!fmt_ok(f) && f != KQ_Q8_0) return KQ_ERR_FORMAT;
     if (int r = check_shape(N, K)) return r;
     if (N == 0) return KQ_OK;
     if (!disk || !packed) return KQ_ERR_ARG;
     if (!aligned(disk, 16) || !aligned(packed, 256)) return KQ_ERR_ALIGN;
+    if (f == KQ_Q8_0)
+        return launch_status(launch_repack_q8_0(static_cast<const uint8_t *>(disk), N, K, static_cast<uint8_t *>(packed), s));
     return launch_status(launch_repack(f, static_cast<const uint8_t *>(disk), N, K, static_cast<uint8_t *>(packed), s));
+}
+
+int kq_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *qs, cudaStream_t s) {
+    if (M < 0 || K <= 0 || K % 32 != 0) return KQ_ERR_ARG;
+    if (M == 0) return KQ_OK;
+    if (!x || !d || !qs) return KQ_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(qs, 16) || !aligned(d, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_quantize_q8_0(x, M, K, d, qs, s));
+}
+
+int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, float *y,
+                 cudaStream_t s) {
+    if (int r = check_shape(N, K)) return r;
+    if (K > GEMV_MAX_K) return KQ_ERR_ARG;
+    if (N == 0) return KQ_OK;
+    if (!packed || !d || !qs || !y) return KQ_ERR_ARG;
+    if (!aligned(packed, 256) || !aligned(qs, 16) || !aligned(d, 4) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_gemv_q8_0(packed, N, K, d, qs, y, s));
 }
 
 size_t kq_gemv_workspace_bytes(void) { return GEMV_WORKSPACE_BYTES; }

@@ -13,7 +13,7 @@ from typing import NamedTuple, Optional
 
 import torch
 
-Q4_K, Q5_K, Q6_K = 1, 2, 3
+Q4_K, Q5_K, Q6_K, Q8_0 = 1, 2, 3, 4
 QK = 256
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkq.so")
@@ -54,12 +54,15 @@ _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
 _lib.kq_measure_mma_s8.argtypes = [_I64, _I64, _P, _P]
+_lib.kq_quantize_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P]
+_lib.kq_gemv_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
 _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
-           "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8"):
+           "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
+           "kq_quantize_q8_0", "kq_gemv_q8_0"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -306,6 +309,34 @@ def kq_debug_decode(fmt: int, packed: torch.Tensor, N: int, K: int, stream=None)
     _check(_lib.kq_debug_decode(int(fmt), _ptr(packed), N, K, _ptr(q), _ptr(sc), _ptr(mn), _ptr(d), _ptr(dmin),
                                 _stream(stream)), "kq_debug_decode")
     return {"q": q, "sc": sc, "m": mn, "d": d, "dmin": dmin}
+
+
+def kq_quantize_q8_0(x: torch.Tensor, d: Optional[torch.Tensor] = None, qs: Optional[torch.Tensor] = None,
+                     stream=None):
+    """Q8_0-form activations of float32 x [M, K] (or [K]): (d f32 [M, K/32], qs i8 [M, K])."""
+    if x.dim() == 1:
+        x = x.view(1, -1)
+    _need_cuda(x)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    M, K = x.shape
+    if d is None:
+        d = torch.empty((M, K // 32), dtype=torch.float32, device=x.device)
+    if qs is None:
+        qs = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    _check(_lib.kq_quantize_q8_0(_ptr(x), M, K, _ptr(d), _ptr(qs), _stream(stream)), "kq_quantize_q8_0")
+    return d, qs
+
+
+def kq_gemv_q8_0(packed: torch.Tensor, N: int, K: int, d: torch.Tensor, qs: torch.Tensor,
+                 y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y [N] = Q8_0 weights (packed image) x one Q8_0-form activation row (d, qs)."""
+    _need_cuda(packed, d, qs)
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=packed.device)
+    _check(_lib.kq_gemv_q8_0(_ptr(packed), int(N), int(K), _ptr(d), _ptr(qs), _ptr(y), _stream(stream)),
+           "kq_gemv_q8_0")
+    return y
 
 
 def kq_measure_mma_s8(blocks: int, iters: int, out: torch.Tensor = None, device=None, stream=None) -> torch.Tensor:

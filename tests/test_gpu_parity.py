@@ -602,3 +602,71 @@ def test_measure_mma_s8_checksum(K):
     torch.cuda.synchronize()
     assert out.shape == (3 * 256,)
     assert bool((out == 1024 * 7).all())
+
+
+# ---------------------------------------------------------------- Q8_0 rail
+@pytest.mark.parametrize("M,Kdim,outliers", [(1, 256, False), (3, 5120, True), (2, 96, False), (5, 17408, False)])
+def test_q8_0_quantize_bit_exact(K, M, Kdim, outliers):
+    """Q8_0-form activations: scales and quants bit-identical to the oracle,
+    including a zero block, 1e-30 values, exact ties and a large outlier."""
+    rng = synth.rng_for(120, M * 7 + Kdim)
+    x = synth.activations(M, Kdim, rng, outliers=outliers)
+    if M >= 3:
+        x[0, :32] = 0.0
+        x[1, 32:64] *= np.float32(1e-30)
+        x[2, :32] = np.float32(2.5)
+        x[2, 0] = np.float32(127.0)
+        x[2, 40] = np.float32(3e4)
+    ref_d, ref_q = oracle.quantize_q8_0(x)
+    d, q = K.kq_quantize_q8_0(to_dev(x))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(d.cpu().numpy(), ref_d)
+    np.testing.assert_array_equal(q.cpu().numpy(), ref_q)
+
+
+def _q8_0_image(disk: np.ndarray) -> np.ndarray:
+    """The Q8_0 image layout written out independently (test side): qs plane of
+    4096-byte chunks (row r's 16 quants of columns 16k.. at 256k + 16r), then
+    the fp16 scale plane of 256-byte chunks (row r's 8 scales at 16r)."""
+    N, nb, _ = disk.shape
+    nsb, groups = nb // 8, -(-N // 16)
+    rows = np.zeros((groups * 16, nb, 34), np.uint8)
+    rows[:N] = disk
+    q = rows[:, :, 2:].reshape(groups, 16, nsb, 16, 16)          # g, r, sb, piece k, byte
+    qs = q.transpose(0, 2, 3, 1, 4).reshape(-1)                    # chunk (g, sb), 256k + 16r + byte
+    d = rows[:, :, :2].reshape(groups, 16, nsb, 16).transpose(0, 2, 1, 3).reshape(-1)
+    pad = lambda a: np.concatenate([a, np.zeros(-len(a) % 256, np.uint8)])
+    return np.concatenate([pad(qs), pad(d)])
+
+
+@pytest.mark.parametrize("N,Kdim", [(1, 256), (37, 512), (200, 2560)])
+def test_q8_0_repack_layout(K, N, Kdim):
+    """The repacked Q8_0 image equals the documented layout byte for byte
+    (every disk byte kept once, padding rows zero)."""
+    disk = synth.disk_weights_q8_0(N, Kdim, synth.rng_for(121, N))
+    packed = K.kq_repack(synth.Q8_0, to_dev(disk.reshape(-1)), N, Kdim)
+    torch.cuda.synchronize()
+    want = _q8_0_image(disk)
+    got = packed.cpu().numpy()
+    assert got.size == K.kq_repack_bytes(synth.Q8_0, N, Kdim) == want.size
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("N,Kdim", [(256, 1024), (300, 2560), (17, 256), (1, 5120), (4096, 2560),
+                                    (5120, 17408), (40, 40960)])
+def test_q8_0_gemv(K, N, Kdim):
+    """Q8_0 GEMV against the oracle on every output (ragged row groups, one
+    superblock, the longest K), and bit-identical on a second run."""
+    rng = synth.rng_for(122, N + Kdim)
+    disk = synth.disk_weights_q8_0(N, Kdim, rng)
+    x = synth.activations(1, Kdim, rng, outliers=True)
+    d_a, q_a = oracle.quantize_q8_0(x)
+    packed = K.kq_repack(synth.Q8_0, to_dev(disk.reshape(-1)), N, Kdim)
+    full, y = poisoned((N,))
+    dd, qd = to_dev(d_a[0]), to_dev(q_a[0])
+    K.kq_gemv_q8_0(packed, N, Kdim, dd, qd, y=y)
+    y2 = K.kq_gemv_q8_0(packed, N, Kdim, dd, qd)
+    torch.cuda.synchronize()
+    check_guard(full, N)
+    assert_row_tol(y.cpu().numpy()[None, :], oracle.gemv_q8_0(disk, d_a, q_a))
+    assert torch.equal(y, y2)

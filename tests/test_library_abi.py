@@ -45,7 +45,14 @@ def test_sizes_and_names(kq):
             assert disk <= nb <= padded + 4 * 255
     assert kq.kq_repack_bytes(1, 10, 100) == 0
     assert kq.kq_repack_bytes(1, -1, 256) == 0
-    assert kq.kq_repack_bytes(4, 10, 256) == 0
+    assert kq.kq_repack_bytes(5, 10, 256) == 0
+    # Q8_0 images: qs plane (4096 B per 16 rows x 256 columns) + fp16 scale plane (256 B)
+    assert kq.kq_block_bytes(4) == 34
+    assert kq.kq_repack_bytes(4, 10, 256) == 4096 + 256
+    for N, K in ((17408, 5120), (1, 256), (33, 768)):
+        ch = -(-N // 16) * (K // 256)
+        assert kq.kq_repack_bytes(4, N, K) == -(-ch * 4096 // 256) * 256 + -(-ch * 256 // 256) * 256
+    assert kq.kq_repack_bytes(4, 10, 32) == 0
     assert "invalid" in kq.kq_strerror(-1)
     assert kq.kq_strerror(12345) == "unknown kq status"
 
@@ -58,8 +65,21 @@ def test_host_argument_checks(kq):
     odd = ctypes.c_void_p(0x10004)
     goodq = Q(0x10000, 0x10000, 0x10000)
     ARG, ALIGN, FMT, WS = -1, -2, -3, -6
-    # format
+    # format (Q8_0 is not a K-quant: the K-quant entry points reject it)
     assert lib.kq_gemv(9, fake, 8, 256, goodq, fake, None, 0, None) == FMT
+    assert lib.kq_gemv(4, fake, 8, 256, goodq, fake, None, 0, None) == FMT
+    assert lib.kq_gemm(4, fake, 8, 256, goodq, 32, fake, None, 0, None) == FMT
+    # Q8_0 rail
+    assert lib.kq_quantize_q8_0(fake, 2, 48, fake, fake, None) == ARG
+    assert lib.kq_quantize_q8_0(fake, -1, 64, fake, fake, None) == ARG
+    assert lib.kq_quantize_q8_0(None, 0, 64, None, None, None) == 0
+    assert lib.kq_quantize_q8_0(odd, 2, 64, fake, fake, None) == ALIGN
+    assert lib.kq_gemv_q8_0(fake, 8, 200, fake, fake, fake, None) == ARG
+    assert lib.kq_gemv_q8_0(fake, 8, 256 * 161, fake, fake, fake, None) == ARG
+    assert lib.kq_gemv_q8_0(None, 0, 256, None, None, None, None) == 0
+    assert lib.kq_gemv_q8_0(None, 8, 256, fake, fake, fake, None) == ARG
+    assert lib.kq_gemv_q8_0(odd, 8, 256, fake, fake, fake, None) == ALIGN
+    assert lib.kq_gemv_q8_0(fake, 8, 256, fake, odd, fake, None) == ALIGN
     assert lib.kq_repack(0, fake, 8, 256, fake, None) == FMT
     # shapes
     assert lib.kq_gemv(1, fake, 8, 100, goodq, fake, None, 0, None) == ARG
