@@ -385,6 +385,7 @@ def run_ours(args, world, rank, local):
 
     small_batch = bench_small_batch(kq, torch, layers, peaks, args)
     gemv_27b = bench_gemv_27b(kq, torch, peaks, args)
+    q8_0_line = bench_q8_0(kq, torch, peaks, args)
     gemm = None if args.no_gemm else bench_gemm(kq, torch, peaks, args)
 
     cpu = None
@@ -428,6 +429,7 @@ def run_ours(args, world, rank, local):
             "cpu_baseline": cpu,
             "small_batch": small_batch,
             "gemv_27b": gemv_27b,
+            "q8_0_gemv": q8_0_line,
             "gemm": gemm,
         }
         print(json.dumps(line), flush=True)
@@ -483,6 +485,57 @@ def bench_small_batch(kq, torch, layers, peaks, args):
 
 # --------------------------------------------------------------------------
 # 27B-shaped FFN at M = 1 (secondary GEMV line)
+
+def bench_q8_0(kq, torch, peaks, args):
+    """The Q8_0 rail on the 27B-shaped FFN at M = 1: per step kq_quantize_q8_0
+    of x (5120) and of the down input (17408), and kq_gemv_q8_0 of gate, up
+    (17408x5120) and down (5120x17408), over rotating copies of the 284 MB of
+    Q8_0 weights, replayed from a CUDA graph with programmatic dependent launch."""
+    shapes = [(17408, 5120), (17408, 5120), (5120, 17408)]
+    step_bytes = sum(N * K * 34 // 32 for N, K in shapes)
+    C = max(2, -(-600_000_000 // step_bytes))
+    base = []
+    for i, (N, K) in enumerate(shapes):
+        disk = torch.from_numpy(synth.disk_weights_q8_0(N, K, synth.rng_for(3, 50 + i)).reshape(-1)).cuda()
+        base.append(kq.kq_repack(synth.Q8_0, disk, N, K))
+        del disk
+    copies = [base] + [[b.clone() for b in base] for _ in range(C - 1)]
+    x = torch.from_numpy(synth.activations(1, 5120, synth.rng_for(3, 150), outliers=True)[0]).cuda()
+    h = torch.from_numpy(synth.activations(1, 17408, synth.rng_for(3, 151))[0]).cuda()
+    dx, qx = kq.kq_quantize_q8_0(x)
+    dh, qh = kq.kq_quantize_q8_0(h)
+    ys = [torch.empty(N, dtype=torch.float32, device="cuda") for N, _ in shapes]
+
+    def rot():
+        for c in copies:
+            kq.kq_quantize_q8_0(x, d=dx, qs=qx)
+            kq.kq_gemv_q8_0(c[0], 17408, 5120, dx, qx, y=ys[0])
+            kq.kq_gemv_q8_0(c[1], 17408, 5120, dx, qx, y=ys[1])
+            kq.kq_quantize_q8_0(h, d=dh, qs=qh)
+            kq.kq_gemv_q8_0(c[2], 5120, 17408, dh, qh, y=ys[2])
+
+    g = graph_of(torch, rot)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(200, args.steps // (4 * C)))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (reps * C)
+    gbs = step_bytes / (us * 1e-6) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    del copies, base, g
+    torch.cuda.empty_cache()
+    return {"workload": "27B-shaped dense FFN in Q8_0 at M=1 (gate/up 17408x5120, down 5120x17408), "
+                        "2 kq_quantize_q8_0 + 3 kq_gemv_q8_0 launches",
+            "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
+            "weight_bytes_per_step": step_bytes, "copies": C,
+            "timing": f"CUDA events around {reps} graph replays of {C} steps (weights {C * step_bytes / 1e6:.0f} MB)"}
+
 
 def bench_gemv_27b(kq, torch, peaks, args):
     """The 27B-shaped dense FFN decoded at M = 1: gate+up in one fused launch
