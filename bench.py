@@ -386,6 +386,7 @@ def run_ours(args, world, rank, local):
     small_batch = bench_small_batch(kq, torch, layers, peaks, args)
     gemv_27b = bench_gemv_27b(kq, torch, peaks, args)
     q8_0_line = bench_q8_0(kq, torch, peaks, args)
+    moe_decode = bench_moe_decode(kq, torch, peaks, args)
     gemm = None if args.no_gemm else bench_gemm(kq, torch, peaks, args)
 
     cpu = None
@@ -430,6 +431,7 @@ def run_ours(args, world, rank, local):
             "small_batch": small_batch,
             "gemv_27b": gemv_27b,
             "q8_0_gemv": q8_0_line,
+            "moe_decode": moe_decode,
             "gemm": gemm,
         }
         print(json.dumps(line), flush=True)
@@ -485,6 +487,73 @@ def bench_small_batch(kq, torch, layers, peaks, args):
 
 # --------------------------------------------------------------------------
 # 27B-shaped FFN at M = 1 (secondary GEMV line)
+
+def bench_moe_decode(kq, torch, peaks, args):
+    """MoE decode on the 30B-A3B shapes: one token routed to 8 of 128 experts.
+    Per step: kq_quantize_q8k of the token's 8 routed rows, kq_gemm_grouped of
+    gate and up (Q4_K 768x2048 per expert), kq_quantize_q8k of the 8 down
+    inputs and kq_gemm_grouped of down (Q6_K 2048x768): with 8 rows the grouped
+    call runs the decode GEMV over every row's expert.  Each of the 32 steps of
+    a graph routes to 8 fresh experts (uniform, distinct), so the 392 MB of
+    experts stream from HBM; value = expert bytes read per second."""
+    cfg = synth.configs()[4]
+    E, topk = cfg.experts, cfg.topk
+    mats = cfg.matrices
+    packed, per = [], []
+    for i, m in enumerate(mats):
+        b = kq.kq_repack_bytes(m.fmt, m.N, m.K)
+        buf = torch.empty(b * E, dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(4, 10 + 1000 * i + e))
+            kq.kq_repack(m.fmt, torch.from_numpy(disk.reshape(-1)).cuda(), m.N, m.K, packed=buf[e * b:(e + 1) * b])
+        packed.append(buf)
+        per.append(b)
+    S = 32
+    rng = synth.rng_for(4, 7000)
+    offs = []
+    for _ in range(S):
+        chosen = np.sort(rng.choice(E, topk, replace=False))
+        cnt = np.zeros(E, np.int64)
+        cnt[chosen] = 1
+        offs.append(torch.from_numpy(np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)).cuda())
+    x = torch.from_numpy(np.repeat(synth.activations(1, mats[0].K, synth.rng_for(4, 7001)), topk, axis=0)).cuda()
+    h = torch.from_numpy(synth.activations(topk, mats[2].K, synth.rng_for(4, 7002))).cuda()
+    ax = kq.q8k_empty(topk, mats[0].K)
+    ah = kq.q8k_empty(topk, mats[2].K)
+    ys = [torch.empty((topk, m.N), dtype=torch.float32, device="cuda") for m in mats]
+
+    def steps():
+        for r in range(S):
+            kq.kq_quantize_q8k(x, out=ax)
+            kq.kq_gemm_grouped(mats[0].fmt, packed[0], E, offs[r], mats[0].N, mats[0].K, ax, y=ys[0])
+            kq.kq_gemm_grouped(mats[1].fmt, packed[1], E, offs[r], mats[1].N, mats[1].K, ax, y=ys[1])
+            kq.kq_quantize_q8k(h, out=ah)
+            kq.kq_gemm_grouped(mats[2].fmt, packed[2], E, offs[r], mats[2].N, mats[2].K, ah, y=ys[2])
+
+    g = graph_of(torch, steps)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    reps = max(3, min(100, args.steps // (4 * S)))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) * 1e3 / (reps * S)
+    step_bytes = topk * sum(per)
+    gbs = step_bytes / (us * 1e-6) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    del packed, g
+    torch.cuda.empty_cache()
+    return {"workload": "30B-A3B-shaped MoE decode: 1 token, top-8 of 128 experts, gate/up Q4_K 768x2048 + "
+                        "down Q6_K 2048x768 (2 kq_quantize_q8k + 3 kq_gemm_grouped launches per step)",
+            "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
+            "expert_bytes_per_step": step_bytes,
+            "timing": f"CUDA events around {reps} graph replays of {S} steps, each step routed to 8 fresh experts "
+                      f"(experts {E * sum(per) / 1e6:.0f} MB)"}
+
 
 def bench_q8_0(kq, torch, peaks, args):
     """The Q8_0 rail on the 27B-shaped FFN at M = 1: per step kq_quantize_q8_0

@@ -670,3 +670,60 @@ def test_q8_0_gemv(K, N, Kdim):
     check_guard(full, N)
     assert_row_tol(y.cpu().numpy()[None, :], oracle.gemv_q8_0(disk, d_a, q_a))
     assert torch.equal(y, y2)
+
+
+def test_q8_0_pdl_chain_matches_plain_launches(K):
+    """The Q8_0 rail under programmatic dependent launch: the GEMV loads its
+    first weights before the dependency wait, while the activations are still
+    being written by the quantize launched just before it; every output equals
+    the plain launches' bits, and the last against the oracle."""
+    N, Kdim = 300, 2560
+    rng = synth.rng_for(123, 0)
+    disk = synth.disk_weights_q8_0(N, Kdim, rng)
+    disk2 = synth.disk_weights_q8_0(N, 5120, rng)
+    packed = K.kq_repack(synth.Q8_0, to_dev(disk.reshape(-1)), N, Kdim)
+    packed2 = K.kq_repack(synth.Q8_0, to_dev(disk2.reshape(-1)), N, 5120)
+    x0 = to_dev(synth.activations(1, Kdim, rng)[0])
+    h0 = to_dev(synth.activations(1, 5120, rng)[0])
+    torch.cuda.synchronize()
+
+    def chain():
+        outs = []
+        for i in range(4):
+            x = x0 * (1.0 + 0.25 * i)            # produced by the kernel right before
+            d, q = K.kq_quantize_q8_0(x)
+            y = K.kq_gemv_q8_0(packed, N, Kdim, d, q)
+            d2, q2 = K.kq_quantize_q8_0(h0 + y.sum() * 0.0 + 0.1 * i)
+            y2 = K.kq_gemv_q8_0(packed2, N, 5120, d2, q2)
+            outs.append(torch.cat([y * 2.0, y2 * 2.0]))   # consumed right after
+        torch.cuda.synchronize()
+        return torch.stack(outs).cpu().numpy()
+
+    old = K.kq_set_launch_flags(0)
+    try:
+        plain = chain()
+        K.kq_set_launch_flags(K.KQ_LAUNCH_PDL)
+        pdl = chain()
+    finally:
+        K.kq_set_launch_flags(old)
+    np.testing.assert_array_equal(pdl, plain)
+    d_a, q_a = oracle.quantize_q8_0((x0 * 1.75).cpu().numpy())
+    assert_row_tol(pdl[3][None, :N] / 2.0, oracle.gemv_q8_0(disk, d_a, q_a))
+
+
+def test_grouped_more_experts_than_the_tensor_core_path(K):
+    """E above the grouped tensor-core kernel's expert limit: the call runs
+    on the CUDA-core token-group kernel; every row against the oracle with its
+    own expert (empty experts among them)."""
+    fmt, E, N, Kdim = synth.Q4_K, 1100, 64, 256
+    rng = synth.rng_for(124, 0)
+    counts = np.zeros(E, np.int64)
+    counts[rng.choice(E, 30, replace=False)] = rng.integers(1, 4, size=30)
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    disks = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    planes = oracle_q8k(synth.activations(int(offsets[-1]), Kdim, rng))
+    y = run_grouped(K, fmt, disks, planes, offsets)
+    for e in np.nonzero(counts)[0]:
+        a, b = offsets[e], offsets[e + 1]
+        sl = tuple(p[a:b] for p in planes)
+        assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
