@@ -490,11 +490,10 @@ def bench_small_batch(kq, torch, layers, peaks, args):
 
 def bench_moe_decode(kq, torch, peaks, args):
     """MoE decode on the 30B-A3B shapes: one token routed to 8 of 128 experts.
-    Per step: kq_quantize_q8k of the token's 8 routed rows, kq_gemm_grouped of
-    gate and up (Q4_K 768x2048 per expert), kq_quantize_q8k of the 8 down
-    inputs and kq_gemm_grouped of down (Q6_K 2048x768): with 8 rows the grouped
-    call runs the decode GEMV over every row's expert.  Each of the 32 steps of
-    a graph routes to 8 fresh experts (uniform, distinct), so the 392 MB of
+    Per step two kq_gemv_grouped_fused launches: gate and up (Q4_K 768x2048 per
+    expert) over the token's 8 routed fp32 rows, quantized in the kernel, then
+    down (Q6_K 2048x768) over the 8 down inputs.  Each of the 32 steps of a
+    graph routes to 8 fresh experts (uniform, distinct), so the 392 MB of
     experts stream from HBM; value = expert bytes read per second."""
     cfg = synth.configs()[4]
     E, topk = cfg.experts, cfg.topk
@@ -518,17 +517,13 @@ def bench_moe_decode(kq, torch, peaks, args):
         offs.append(torch.from_numpy(np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32)).cuda())
     x = torch.from_numpy(np.repeat(synth.activations(1, mats[0].K, synth.rng_for(4, 7001)), topk, axis=0)).cuda()
     h = torch.from_numpy(synth.activations(topk, mats[2].K, synth.rng_for(4, 7002))).cuda()
-    ax = kq.q8k_empty(topk, mats[0].K)
-    ah = kq.q8k_empty(topk, mats[2].K)
     ys = [torch.empty((topk, m.N), dtype=torch.float32, device="cuda") for m in mats]
 
     def steps():
         for r in range(S):
-            kq.kq_quantize_q8k(x, out=ax)
-            kq.kq_gemm_grouped(mats[0].fmt, packed[0], E, offs[r], mats[0].N, mats[0].K, ax, y=ys[0])
-            kq.kq_gemm_grouped(mats[1].fmt, packed[1], E, offs[r], mats[1].N, mats[1].K, ax, y=ys[1])
-            kq.kq_quantize_q8k(h, out=ah)
-            kq.kq_gemm_grouped(mats[2].fmt, packed[2], E, offs[r], mats[2].N, mats[2].K, ah, y=ys[2])
+            kq.kq_gemv_grouped_fused(mats[0].fmt, packed[:2], [mats[0].N, mats[1].N], mats[0].K, E, offs[r], x,
+                                     ys[:2])
+            kq.kq_gemv_grouped_fused(mats[2].fmt, packed[2:], [mats[2].N], mats[2].K, E, offs[r], h, ys[2:])
 
     g = graph_of(torch, steps)
     for _ in range(3):
@@ -548,7 +543,7 @@ def bench_moe_decode(kq, torch, peaks, args):
     del packed, g
     torch.cuda.empty_cache()
     return {"workload": "30B-A3B-shaped MoE decode: 1 token, top-8 of 128 experts, gate/up Q4_K 768x2048 + "
-                        "down Q6_K 2048x768 (2 kq_quantize_q8k + 3 kq_gemm_grouped launches per step)",
+                        "down Q6_K 2048x768 (2 kq_gemv_grouped_fused launches per step)",
             "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
             "expert_bytes_per_step": step_bytes,
             "timing": f"CUDA events around {reps} graph replays of {S} steps, each step routed to 8 fresh experts "

@@ -260,6 +260,30 @@ int kq_gemm_grouped(kq_format f, const void *packed, int64_t E, const int32_t *r
                     void *workspace, size_t workspace_bytes, cudaStream_t s);
 
 /*
+ * MoE decode, fused: M token rows routed to experts (rows grouped by expert),
+ * quantized to Q8_K inside the kernel (bit-identical to kq_quantize_q8k) and
+ * multiplied by their experts' matrices of n_sets weight sets that share the
+ * rows (gate and up, say) in one launch: the decode GEMV over every row's
+ * expert, its weights streamed once.  It is the page's fused decode chain
+ * ([kq-arc], "The pieces": chain regrain) for the grouped MoE form; there is
+ * no counterpart of the multi-set call in the pages.
+ *   packed[s]    device: the E expert images of set s back to back, expert e
+ *                at packed[s] + e * kq_repack_bytes(f, N[s], K), 256-byte aligned
+ *   N[s]         rows of set s's expert matrices (>= 1)
+ *   row_offsets  device int32 [E+1], as for kq_gemm_grouped (clamped to [0, M])
+ *   x            device float32 [M][K] row-major, 16-byte aligned, finite
+ *   y[s]         device float32 [M][N[s]]; a row that no expert range holds is
+ *                left as it was
+ * Limits: 1 <= n_sets <= 4, 1 <= n_sets * M <= 16, K % 256 == 0, K <= 40960
+ * and the M staged rows within the kernel's shared memory (M * (K + K/8 +
+ * K/64) plus two 16-row items per warp at most 212 KB).
+ * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (outside the limits, null), KQ_ERR_ALIGN,
+ * KQ_ERR_LAUNCH.  M == 0 is a no-op.
+ */
+int kq_gemv_grouped_fused(kq_format f, int n_sets, const void *const *packed, const int64_t *N, int64_t K, int64_t E,
+                          const int32_t *row_offsets, const float *x, int64_t M, float *const *y, cudaStream_t s);
+
+/*
  * Test hook: the int32 partials of the fold, per (token, row, superblock),
  * computed by the same device code the GEMV runs.
  *   isum, msum  device int32 [M][N][K/256]; for Q6_K isum = iacc - 32*bacc

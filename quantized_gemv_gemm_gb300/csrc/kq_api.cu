@@ -60,8 +60,8 @@ int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offse
     // for up to 8 tokens
     if (!offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K) return launch_status(launch_gemv_batch(f, packed, N, K, q, M, y, s));
     // a few grouped rows (MoE decode): one GEMV over every row's expert
-    if (offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K && gemv_grouped_fits(M, K))
-        return launch_status(launch_gemv_grouped(f, packed, E, offsets, expert_bytes, N, K, q, M, y, s));
+    if (offsets && M < GEMM_TC_MIN_M && K <= GEMV_MAX_K && gemv_grouped_fits(M, K, 1))
+        return launch_status(launch_gemv_grouped(f, 1, &packed, &N, E, offsets, &expert_bytes, K, q, nullptr, M, &y, s));
     cudaError_t e = launch_gemm_tc(f, packed, N, K, q, M, offsets, E, expert_bytes, y, ws, ws_bytes, s);
     if (e == cudaErrorNotSupported) {
         cudaGetLastError();
@@ -215,6 +215,25 @@ size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
 int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M, float *y,
             void *workspace, size_t workspace_bytes, cudaStream_t s) {
     return gemm_common(f, packed, 1, nullptr, N, K, a, M, y, workspace, workspace_bytes, s);
+}
+
+int kq_gemv_grouped_fused(kq_format f, int n_sets, const void *const *packed, const int64_t *N, int64_t K, int64_t E,
+                          const int32_t *row_offsets, const float *x, int64_t M, float *const *y, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (M < 0 || E < 1 || n_sets < 1 || n_sets > GEMV_FUSED_MAX || !packed || !N || !y) return KQ_ERR_ARG;
+    if (K <= 0 || K % QK != 0 || K > GEMV_MAX_K) return KQ_ERR_ARG;
+    if (M == 0) return KQ_OK;
+    if (!gemv_grouped_fits(M, K, n_sets)) return KQ_ERR_ARG;
+    if (!x || !row_offsets) return KQ_ERR_ARG;
+    if (!aligned(x, 16) || !aligned(row_offsets, 4)) return KQ_ERR_ALIGN;
+    uint64_t eb[GEMV_FUSED_MAX];
+    for (int st = 0; st < n_sets; ++st) {
+        if (N[st] < 1 || !packed[st] || !y[st]) return KQ_ERR_ARG;
+        if (!aligned(packed[st], 256) || !aligned(y[st], 4)) return KQ_ERR_ALIGN;
+        eb[st] = kq_repack_bytes(f, N[st], K);
+    }
+    return launch_status(launch_gemv_grouped(f, n_sets, packed, N, E, row_offsets, eb, K, Q8K{nullptr, nullptr, nullptr},
+                                             x, M, y, s));
 }
 
 int kq_gemm_grouped(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets, int64_t N, int64_t K,

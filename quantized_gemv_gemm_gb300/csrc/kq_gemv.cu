@@ -360,12 +360,13 @@ struct GemvParams {
     const int16_t *bs;
     int ntok;                              // token rows folded per pass (1..T of the kernel)
     int64_t stage_stride;                  // bytes between the staged rows of two tokens
-    // grouped (MoE) rows: matrix m is row m of the activations times the
-    // weights of the expert whose row range [offsets[e], offsets[e+1])
-    // holds m; experts of expert_bytes each from packed[0]
+    // grouped (MoE) rows: matrix m is row m % ntok of the activations times
+    // the weights, in set m / ntok, of the expert whose row range
+    // [offsets[e], offsets[e+1]) holds that row; packed[m] is the start of
+    // that set's experts (back to back, expert_bytes[set] each)
     const int32_t *offsets;
     int64_t E;
-    uint64_t expert_bytes;
+    uint64_t expert_bytes[GEMV_FUSED_MAX];
 };
 
 // Bounded wait on a stage's mbarrier (about one second): on expiry the
@@ -390,7 +391,9 @@ __device__ __forceinline__ int64_t block_item(const GemvParams &p, int64_t b, in
 // activation row is staged at stage_stride * t, and its output row is
 // y[m] + t * N[m].
 // GR: grouped rows (MoE decode) -- the matrices are found on the device from
-// the expert offsets, after the wait, and matrix m folds activation row m.
+// the expert offsets, after the wait: with ntok activation rows and nmat =
+// sets * ntok matrices, matrix m is activation row m % ntok times that row's
+// expert in weight set m / ntok (e.g. gate and up sharing the rows).
 template <int F, int T, bool GR>
 __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     constexpr int SLOT = GemvFmt<F>::SLOT;
@@ -417,7 +420,7 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     const int D = p.D;
     const int ntok = (T == 1 && !GR) ? 1 : p.ntok;
     const uint32_t tstride = (T == 1 && !GR) ? 0u : (uint32_t)p.stage_stride;
-    // grouped: matrix m's staged row is at m * mstride
+    // grouped: matrix m's staged row (m % ntok) is at (m % ntok) * mstride
     const uint32_t mstride = GR ? tstride : 0u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r16 = lane & 15, h = lane >> 4;
@@ -438,7 +441,8 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
         // the expert offsets are written by the kernels before this one
         griddep_wait();
         if (threadIdx.x < p.nmat) {
-            const int m = threadIdx.x;
+            const int mm = threadIdx.x;
+            const int set = mm / ntok, m = mm - set * ntok;  // weight set, activation row
             int64_t lo = 0, hi = p.E;  // last e with offsets[e] <= m, among [0, E)
             while (hi - lo > 1) {
                 const int64_t mid = (lo + hi) >> 1;
@@ -446,9 +450,10 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                 else hi = mid;
             }
             const bool in = p.offsets[lo] <= m && m < p.offsets[lo + 1];
-            s_planes[m] = make_planes(F, p.packed[0] + (in ? (uint64_t)lo * p.expert_bytes : 0), p.N[0], nsb);
-            s_n[m] = in ? p.N[0] : 0;  // a row of no expert is not written
-            s_y[m] = p.y[0] + (int64_t)m * p.N[0];
+            // (packed, N, y are per matrix: the set's values repeated ntok times)
+            s_planes[mm] = make_planes(F, p.packed[mm] + (in ? (uint64_t)lo * p.expert_bytes[set] : 0), p.N[mm], nsb);
+            s_n[mm] = in ? p.N[mm] : 0;  // a row of no expert is not written
+            s_y[mm] = p.y[mm] + (int64_t)m * p.N[mm];
         }
     } else if (threadIdx.x < p.nmat) {
         s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
@@ -525,7 +530,7 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // activations: written by the kernels before this one
     if constexpr (!GR) griddep_wait();
     constexpr bool PAIRS = F != FMT_Q6_K;
-    if (T > 1 && p.x) {
+    if ((T > 1 || GR) && p.x) {
         // several fp32 rows: block vb of the rows laid end to end is block
         // vb % nsb of token row vb / nsb, staged in that token's row
         const int64_t nvb = (int64_t)ntok * nsb;
@@ -601,9 +606,11 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     int m = m0;
     // running shared addresses of the current item's activation superblock
     // (the lane's half), sums and scale
-    uint32_t a_cur = qs_s + m * mstride + (uint32_t)sb * QK + 128 * h;
-    uint32_t s_cur = sum_s + m * mstride + (uint32_t)sb * 32 + 16 * h;
-    uint32_t d_cur = d8_s + m * mstride + 4 * (uint32_t)sb;
+    // staged activation row of matrix m (grouped: m % ntok; else mstride = 0)
+    auto row_off = [&](int mat) -> uint32_t { return GR ? (uint32_t)(mat % ntok) * mstride : 0u; };
+    uint32_t a_cur = qs_s + row_off(m) + (uint32_t)sb * QK + 128 * h;
+    uint32_t s_cur = sum_s + row_off(m) + (uint32_t)sb * 32 + 16 * h;
+    uint32_t d_cur = d8_s + row_off(m) + 4 * (uint32_t)sb;
     float acc[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[t] = 0.0f;
@@ -675,9 +682,9 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                 sb = 0;
                 ++g;
                 while (m + 1 < nmat && g >= s_gpre[m + 1]) ++m;
-                a_cur = qs_s + m * mstride + 128 * h;
-                s_cur = sum_s + m * mstride + 16 * h;
-                d_cur = d8_s + m * mstride;
+                a_cur = qs_s + row_off(m) + 128 * h;
+                s_cur = sum_s + row_off(m) + 16 * h;
+                d_cur = d8_s + row_off(m);
             }
         }
     }
@@ -797,12 +804,12 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     p.ws = static_cast<unsigned long long *>(ws);
     p.stage_stride = gemv_stage_stride(p.K);
     if (T == 1 && !GR) p.ntok = 1;
-    // (a grouped launch stages one row per matrix; a pass of a few tokens
-    // keeps to half an SM while its rows leave room for a 3-stage ring)
-    const int64_t rows_bytes = (GR ? p.nmat : T) * gemv_stage_stride(p.K);
+    // (a grouped launch stages its ntok activation rows; a pass of a few
+    // tokens keeps to half an SM while its rows leave room for a 3-stage ring)
+    const int64_t rows_bytes = (GR ? p.ntok : T) * gemv_stage_stride(p.K);
     const bool wide = GR || (T > 1 && (GEMV_SMEM_BUDGET - rows_bytes) / (8 * GemvFmt<F>::SLOT) < 3);
     const int64_t budget = wide ? GEMV_BATCH_SMEM_BUDGET : GEMV_SMEM_BUDGET;
-    const int64_t stage_bytes = (GR ? p.nmat : T) * p.stage_stride;
+    const int64_t stage_bytes = (GR ? p.ntok : T) * p.stage_stride;
     int64_t D = (budget - stage_bytes) / (8 * GemvFmt<F>::SLOT);
     if (D > gemv_max_d<F>()) D = gemv_max_d<F>();
     if (D < 2) D = 2;
@@ -900,31 +907,32 @@ static cudaError_t launch_gemv_batch_f(GemvParams p, int64_t M, int64_t tmax, vo
 // Grouped rows (MoE decode: a few token rows, each routed to an expert):
 // one launch over every row's expert matrix, from one read of each weight
 // item per row.  False when the rows' staged activations do not fit.
-bool gemv_grouped_fits(int64_t M, int64_t K) {
-    return M >= 1 && M <= GEMV_MAX_MATRICES && M * gemv_stage_stride(K) + 2 * 8 * 3360 <= GEMV_BATCH_MAX_SMEM;
+bool gemv_grouped_fits(int64_t M, int64_t K, int sets) {
+    return M >= 1 && sets >= 1 && M * sets <= GEMV_MAX_MATRICES &&
+           M * gemv_stage_stride(K) + 2 * 8 * 3360 <= GEMV_BATCH_MAX_SMEM;
 }
 
-cudaError_t launch_gemv_grouped(int f, const void *packed, int64_t E, const int32_t *offsets,
-                                uint64_t expert_bytes, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
-                                cudaStream_t s) {
-    if (M == 0 || N == 0) return cudaSuccess;
+cudaError_t launch_gemv_grouped(int f, int sets, const void *const *packed, const int64_t *N, int64_t E,
+                                const int32_t *offsets, uint64_t const *expert_bytes, int64_t K, Q8K a,
+                                const float *x, int64_t M, float *const *y, cudaStream_t s) {
+    if (M == 0) return cudaSuccess;
     GemvParams p{};
-    p.nmat = (int)M;
-    p.packed[0] = static_cast<const uint8_t *>(packed);
+    p.nmat = (int)(sets * M);
     for (int m = 0; m < p.nmat; ++m) {
-        p.N[m] = N;     // every matrix has the experts' shape; launch_gemv_t
-        p.y[m] = y;     // takes the row-group prefix sums from N
+        p.packed[m] = static_cast<const uint8_t *>(packed[m / M]);  // the matrix's set: its experts,
+        p.N[m] = N[m / M];     // their shape (launch_gemv_t takes the row-group prefix sums from N)
+        p.y[m] = y[m / M];     // and its output
     }
     p.K = K;
     p.nsb = K / QK;
-    p.x = nullptr;
+    p.x = x;
     p.d8 = a.d;
     p.qs = a.qs;
     p.bs = a.bsums;
     p.ntok = (int)M;
     p.offsets = offsets;
     p.E = E;
-    p.expert_bytes = expert_bytes;
+    for (int st = 0; st < sets; ++st) p.expert_bytes[st] = expert_bytes[st];
     if (f == FMT_Q4_K) return launch_gemv_t<FMT_Q4_K, 1, true>(p, nullptr, 0, s);
     if (f == FMT_Q5_K) return launch_gemv_t<FMT_Q5_K, 1, true>(p, nullptr, 0, s);
     return launch_gemv_t<FMT_Q6_K, 1, true>(p, nullptr, 0, s);

@@ -69,12 +69,14 @@ cudaError_t launch_gemv_fused_batch(int f, int nmat, const void *const *packed, 
                                     const float *x, int64_t M, float *const *y, void *ws, size_t ws_bytes,
                                     cudaStream_t s);
 
-// Grouped rows (MoE decode): M < GEMM_TC_MIN_M token rows grouped by expert
-// (device offsets [E+1]), one GEMV launch over every row's expert.
-bool gemv_grouped_fits(int64_t M, int64_t K);
-cudaError_t launch_gemv_grouped(int f, const void *packed, int64_t E, const int32_t *offsets,
-                                uint64_t expert_bytes, int64_t N, int64_t K, Q8K a, int64_t M, float *y,
-                                cudaStream_t s);
+// Grouped rows (MoE decode): M token rows grouped by expert (device offsets
+// [E+1]), one GEMV launch over every row's expert in each of `sets` weight
+// sets sharing the rows (sets * M <= GEMV_MAX_MATRICES); the rows come as
+// Q8_K planes (x == nullptr) or as fp32 x [M][K] quantized in the kernel.
+bool gemv_grouped_fits(int64_t M, int64_t K, int sets);
+cudaError_t launch_gemv_grouped(int f, int sets, const void *const *packed, const int64_t *N, int64_t E,
+                                const int32_t *offsets, uint64_t const *expert_bytes, int64_t K, Q8K a,
+                                const float *x, int64_t M, float *const *y, cudaStream_t s);
 
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);

@@ -45,6 +45,7 @@ _lib.kq_gemv_workspace_bytes.restype = _SZ
 _lib.kq_gemv.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _P, _P, _SZ, _P]
 _lib.kq_gemv_fused.argtypes = [_INT, _INT, _P, _P, _I64, _P, _P, _P, _SZ, _P]
 _lib.kq_gemv_fused_batch.argtypes = [_INT, _INT, _P, _P, _I64, _P, _I64, _P, _P, _SZ, _P]
+_lib.kq_gemv_grouped_fused.argtypes = [_INT, _INT, _P, _P, _I64, _I64, _P, _P, _I64, _P, _P]
 _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
@@ -62,7 +63,7 @@ _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
-           "kq_quantize_q8_0", "kq_gemv_q8_0"):
+           "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -226,6 +227,29 @@ def kq_gemv_fused_batch(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, 
     wp, wn = _gemv_ws_args(workspace, x.device)
     _check(_lib.kq_gemv_fused_batch(int(fmt), n, pk, nn, int(K), _ptr(x), int(M), yy, wp, wn, _stream(stream)),
            "kq_gemv_fused_batch")
+    return y_list
+
+
+def kq_gemv_grouped_fused(fmt: int, packed_list, N_list, K: int, E: int, row_offsets: torch.Tensor,
+                          x: torch.Tensor, y_list=None, stream=None):
+    """MoE decode: the M fp32 rows of x [M, K] (grouped by expert, row_offsets
+    int32 [E+1]) quantized in the kernel and multiplied by their experts of
+    every weight set in packed_list (E images each) in one launch."""
+    n = len(packed_list)
+    _need_cuda(x, row_offsets, *packed_list)
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 [M, K] tensor")
+    if row_offsets.dtype != torch.int32:
+        raise ValueError("row_offsets must be int32")
+    M = x.shape[0]
+    if y_list is None:
+        y_list = [torch.zeros((M, int(N)), dtype=torch.float32, device=x.device) for N in N_list]
+    _need_cuda(*y_list)
+    pk = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in packed_list])
+    nn = (ctypes.c_int64 * max(n, 1))(*[int(v) for v in N_list])
+    yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
+    _check(_lib.kq_gemv_grouped_fused(int(fmt), n, pk, nn, int(K), int(E), _ptr(row_offsets), _ptr(x), int(M), yy,
+                                      _stream(stream)), "kq_gemv_grouped_fused")
     return y_list
 
 

@@ -727,3 +727,68 @@ def test_grouped_more_experts_than_the_tensor_core_path(K):
         a, b = offsets[e], offsets[e + 1]
         sl = tuple(p[a:b] for p in planes)
         assert_row_tol(y[a:b], oracle.gemm(fmt, disks[e], *sl))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("counts,sets", [([0, 1, 0, 0, 1, 1, 0, 1, 0, 1, 1, 0, 0, 1, 0, 1], 2),
+                                         ([0, 3, 0, 1, 2, 0, 0, 5, 0, 0, 1, 0, 0, 0, 1, 0], 1),
+                                         ([2, 0, 1, 0, 0, 1], 4)])
+def test_grouped_decode_fused(K, fmt, counts, sets):
+    """MoE decode with the quantize in the kernel and several weight sets per
+    launch (gate and up): every row of every set against the oracle with its
+    own expert, and bit-identical to quantize + kq_gemm_grouped per set."""
+    rng = synth.rng_for(125, fmt * 100 + sets * 10 + len(counts))
+    E, Kdim = len(counts), 1024
+    Ns = [200, 136, 77, 16][:sets]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    M = int(offsets[-1])
+    disks = [[synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)] for N in Ns]
+    packs = []
+    for st, N in enumerate(Ns):
+        per = K.kq_repack_bytes(fmt, N, Kdim)
+        buf = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+        for e in range(E):
+            K.kq_repack(fmt, to_dev(disks[st][e].reshape(-1)), N, Kdim, packed=buf[e * per:(e + 1) * per])
+        packs.append(buf)
+    x = synth.activations(M, Kdim, rng, outliers=True)
+    off_d = to_dev(offsets.astype(np.int32))
+    fulls = [poisoned((M, N)) for N in Ns]
+    K.kq_gemv_grouped_fused(fmt, packs, Ns, Kdim, E, off_d, to_dev(x), [f[1] for f in fulls])
+    a = K.kq_quantize_q8k(to_dev(x))
+    refs = [K.kq_gemm_grouped(fmt, packs[st], E, off_d, N, Kdim, a) for st, N in enumerate(Ns)]
+    torch.cuda.synchronize()
+    planes = oracle_q8k(x)
+    for st, N in enumerate(Ns):
+        full, y = fulls[st]
+        check_guard(full, M * N)
+        assert torch.equal(y, refs[st])
+        got = y.cpu().numpy()
+        for e in range(E):
+            lo, hi = offsets[e], offsets[e + 1]
+            if lo < hi:
+                sl = tuple(p[lo:hi] for p in planes)
+                assert_row_tol(got[lo:hi], oracle.gemm(fmt, disks[st][e], *sl))
+
+
+def test_grouped_decode_fused_uncovered_row_and_limits(K):
+    """A row that no expert range holds is left untouched; the limits on sets
+    x rows are checked on the host."""
+    fmt, E, N, Kdim = synth.Q4_K, 4, 64, 512
+    rng = synth.rng_for(126, 0)
+    disk = [synth.disk_weights(fmt, N, Kdim, rng) for _ in range(E)]
+    per = K.kq_repack_bytes(fmt, N, Kdim)
+    buf = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+    for e in range(E):
+        K.kq_repack(fmt, to_dev(disk[e].reshape(-1)), N, Kdim, packed=buf[e * per:(e + 1) * per])
+    x = synth.activations(3, Kdim, rng)
+    off_d = to_dev(np.array([0, 1, 1, 2, 2], np.int32))     # row 2 outside every range
+    full, y = poisoned((3, N))
+    K.kq_gemv_grouped_fused(fmt, [buf], [N], Kdim, E, off_d, to_dev(x), [y])
+    torch.cuda.synchronize()
+    got = y.cpu().numpy()
+    assert np.isnan(got[2]).all()
+    planes = oracle_q8k(x)
+    assert_row_tol(got[0:1], oracle.gemm(fmt, disk[0], *(p[0:1] for p in planes)))
+    assert_row_tol(got[1:2], oracle.gemm(fmt, disk[2], *(p[1:2] for p in planes)))
+    with pytest.raises(K.KQError):   # 3 sets x 6 rows > 16 matrices
+        K.kq_gemv_grouped_fused(fmt, [buf] * 3, [N] * 3, Kdim, E, off_d, to_dev(synth.activations(6, Kdim, rng)))

@@ -111,6 +111,17 @@ def test_host_argument_checks(kq):
     assert lib.kq_gemv_fused_batch(1, 1, pk1, n1, 256, None, 0, y1, None, 0, None) == 0
     assert lib.kq_gemv_fused_batch(1, 1, pk1, n1, 256, odd, 2, y1, None, 0, None) == ALIGN
     assert lib.kq_gemv_fused_batch(1, 5, pk1, n1, 256, fake, 2, y1, None, 0, None) == ARG
+    # fused grouped decode: sets x rows over 16, too many sets, K not a multiple of 256, zero rows
+    off = ctypes.c_void_p(0x10000)
+    pk4 = (ctypes.c_void_p * 5)(*([0x10000] * 5))
+    n4 = (ctypes.c_int64 * 5)(*([8] * 5))
+    y4 = (ctypes.c_void_p * 5)(*([0x10000] * 5))
+    assert lib.kq_gemv_grouped_fused(1, 2, pk4, n4, 256, 4, off, fake, 9, y4, None) == ARG
+    assert lib.kq_gemv_grouped_fused(1, 5, pk4, n4, 256, 4, off, fake, 1, y4, None) == ARG
+    assert lib.kq_gemv_grouped_fused(1, 1, pk4, n4, 300, 4, off, fake, 1, y4, None) == ARG
+    assert lib.kq_gemv_grouped_fused(4, 1, pk4, n4, 256, 4, off, fake, 1, y4, None) == FMT
+    assert lib.kq_gemv_grouped_fused(1, 1, pk4, n4, 256, 4, None, None, 0, y4, None) == 0
+    assert lib.kq_gemv_grouped_fused(1, 1, pk4, n4, 256, 4, off, odd, 2, y4, None) == ALIGN
     # int8 MMA rate hook: argument checks only (no launch)
     assert lib.kq_measure_mma_s8(-1, 10, fake, None) == ARG
     assert lib.kq_measure_mma_s8(4, -1, fake, None) == ARG
