@@ -146,3 +146,25 @@ def test_launch_flags_mask(kq):
         assert kq.kq_get_launch_flags() == 0
     finally:
         kq.kq_set_launch_flags(old)
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/kq.h is a C header (the boundary other languages bind to): a C11
+    translation unit that includes it and takes the address of every entry
+    point compiles with gcc -Wall -Werror."""
+    import re
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = "/usr/local/cuda/include"
+    if not gcc or not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("gcc or the CUDA headers not available")
+    hdr = os.path.join(ROOT, "include", "kq.h")
+    names = sorted(set(re.findall(r"^(?:int|size_t|unsigned|const char \*)\s*\**\s*(kq_\w+)\(",
+                                  open(hdr).read(), re.M)))
+    assert len(names) >= 15
+    src = tmp_path / "use_kq.c"
+    src.write_text('#include "kq.h"\n' + "".join(f"void *p_{n} = (void *)&{n};\n" for n in names))
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Werror", "-fsyntax-only", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
