@@ -653,7 +653,7 @@ def test_q8_0_repack_layout(K, N, Kdim):
 
 
 @pytest.mark.parametrize("N,Kdim", [(256, 1024), (300, 2560), (17, 256), (1, 5120), (4096, 2560),
-                                    (5120, 17408), (40, 40960)])
+                                    (5120, 17408), (17408, 5120), (40, 40960)])
 def test_q8_0_gemv(K, N, Kdim):
     """Q8_0 GEMV against the oracle on every output (ragged row groups, one
     superblock, the longest K), and bit-identical on a second run."""
@@ -792,3 +792,42 @@ def test_grouped_decode_fused_uncovered_row_and_limits(K):
     assert_row_tol(got[1:2], oracle.gemm(fmt, disk[2], *(p[1:2] for p in planes)))
     with pytest.raises(K.KQError):   # 3 sets x 6 rows > 16 matrices
         K.kq_gemv_grouped_fused(fmt, [buf] * 3, [N] * 3, Kdim, E, off_d, to_dev(synth.activations(6, Kdim, rng)))
+
+
+def test_moe_decode_bench_shapes(K):
+    """The MoE decode the benchmark times, at its shapes: one token routed to 8
+    of 128 experts, gate and up (Q4_K 768x2048) in one kq_gemv_grouped_fused
+    launch, down (Q6_K 2048x768) in another; every output of every routed
+    row against the oracle with its expert (only the routed experts' images
+    are written: the kernel reads no other)."""
+    cfg = synth.configs()[4]
+    E, topk = cfg.experts, cfg.topk
+    gate, up, down = cfg.matrices
+    rng = synth.rng_for(127, 0)
+    chosen = np.sort(rng.choice(E, topk, replace=False))
+    cnt = np.zeros(E, np.int64)
+    cnt[chosen] = 1
+    off_d = to_dev(np.concatenate([[0], np.cumsum(cnt)]).astype(np.int32))
+
+    def images(m, seed):
+        per = K.kq_repack_bytes(m.fmt, m.N, m.K)
+        buf = torch.empty(per * E, dtype=torch.uint8, device="cuda")
+        disks = {}
+        for e in chosen:
+            disks[e] = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(127, seed + int(e)))
+            K.kq_repack(m.fmt, to_dev(disks[e].reshape(-1)), m.N, m.K, packed=buf[int(e) * per:(int(e) + 1) * per])
+        return buf, disks
+
+    (pg, dg), (pu, du), (pd, dd) = images(gate, 1000), images(up, 2000), images(down, 3000)
+    x = np.repeat(synth.activations(1, gate.K, rng), topk, axis=0)
+    h = synth.activations(topk, down.K, rng)
+    yg, yu = K.kq_gemv_grouped_fused(gate.fmt, [pg, pu], [gate.N, up.N], gate.K, E, off_d, to_dev(x))
+    (yd,) = K.kq_gemv_grouped_fused(down.fmt, [pd], [down.N], down.K, E, off_d, to_dev(h))
+    torch.cuda.synchronize()
+    px, ph = oracle_q8k(x), oracle_q8k(h)
+    for row, e in enumerate(chosen):
+        one = tuple(p[row:row + 1] for p in px)
+        assert_row_tol(yg[row:row + 1].cpu().numpy(), oracle.gemm(gate.fmt, dg[e], *one))
+        assert_row_tol(yu[row:row + 1].cpu().numpy(), oracle.gemm(up.fmt, du[e], *one))
+        oneh = tuple(p[row:row + 1] for p in ph)
+        assert_row_tol(yd[row:row + 1].cpu().numpy(), oracle.gemm(down.fmt, dd[e], *oneh))
