@@ -334,6 +334,16 @@ int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const
                  cudaStream_t s);
 
 /*
+ * Test hook for failure detection: launches one block whose single bounded
+ * mbarrier wait is never satisfied; after limit_ns nanoseconds the wait gives
+ * up and records KQ_ERR_TIMEOUT in the device status word, as a stuck stage
+ * of the GEMM or GEMV would, without any fault or hang.  kq_device_status
+ * then returns KQ_ERR_TIMEOUT once (and clears it).
+ * Errors: KQ_ERR_ARG for limit_ns == 0 or > 1e9 (one second); KQ_ERR_LAUNCH.
+ */
+int kq_debug_wait_timeout(uint64_t limit_ns, cudaStream_t s);
+
+/*
  * Measurement hook: the int8 rate of the warp-level integer MMA
  * (mma.sync m16n8k32, s8 x s8 -> s32), the only integer tensor-core MMA on
  * sm_103a.  Launches `blocks` blocks of 8 warps; every warp issues iters x 8

@@ -266,6 +266,11 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
     return launch_status(launch_debug_decode(f, packed, N, K, q, sc, mn, d, dmin, s));
 }
 
+int kq_debug_wait_timeout(uint64_t limit_ns, cudaStream_t s) {
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return KQ_ERR_ARG;
+    return launch_status(launch_wait_timeout(limit_ns, s));
+}
+
 int kq_measure_mma_s8(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s) {
     if (blocks < 0 || iters < 0 || blocks > (int64_t)INT32_MAX) return KQ_ERR_ARG;
     if (blocks == 0) return KQ_OK;

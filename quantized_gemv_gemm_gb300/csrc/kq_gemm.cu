@@ -1068,6 +1068,24 @@ cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K 
     return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
 }
 
+// Test hook: one block whose single bounded wait is never satisfied, so the
+// wait gives up after limit_ns and records the timeout exactly as a stuck
+// pipeline stage would (no fault, no hang).
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ uint64_t b;
+    if (threadIdx.x == 0) {
+        mbar_init(&b, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !mbar_wait(&b, 0, limit_ns)) set_timeout();
+}
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s) {
+    wait_timeout_kernel<<<1, 32, 0, s>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 int read_and_clear_status(cudaStream_t s, int *status) {
     int v = 0;
     if (cudaMemcpyFromSymbolAsync(&v, g_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s) != cudaSuccess) return -1;

@@ -55,6 +55,7 @@ _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
 _lib.kq_measure_mma_s8.argtypes = [_I64, _I64, _P, _P]
+_lib.kq_debug_wait_timeout.argtypes = [ctypes.c_uint64, _P]
 _lib.kq_quantize_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_gemv_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
 _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
@@ -63,7 +64,7 @@ _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
-           "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused"):
+           "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -372,6 +373,11 @@ def kq_measure_mma_s8(blocks: int, iters: int, out: torch.Tensor = None, device=
     _need_cuda(out)
     _check(_lib.kq_measure_mma_s8(int(blocks), int(iters), _ptr(out), _stream(stream)), "kq_measure_mma_s8")
     return out
+
+
+def kq_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the never-satisfied bounded wait (test hook of the timeout path)."""
+    _check(_lib.kq_debug_wait_timeout(int(limit_ns), _stream(stream)), "kq_debug_wait_timeout")
 
 
 def kq_device_status(stream=None) -> int:

@@ -831,3 +831,21 @@ def test_moe_decode_bench_shapes(K):
         assert_row_tol(yu[row:row + 1].cpu().numpy(), oracle.gemm(up.fmt, du[e], *one))
         oneh = tuple(p[row:row + 1] for p in ph)
         assert_row_tol(yd[row:row + 1].cpu().numpy(), oracle.gemm(down.fmt, dd[e], *oneh))
+
+
+def test_bounded_wait_times_out_and_reports(K):
+    """Failure detection without a GPU fault: a wait that nothing satisfies
+    gives up after its limit (2 ms here), kq_device_status reports
+    KQ_ERR_TIMEOUT once and clears it, and the context stays usable."""
+    assert K.kq_device_status() == 0
+    K.kq_debug_wait_timeout(2_000_000)
+    torch.cuda.synchronize()
+    assert K.kq_device_status() == -5          # KQ_ERR_TIMEOUT
+    assert K.kq_device_status() == 0           # read and cleared
+    fmt, N, Kdim = synth.Q4_K, 64, 512
+    disk = synth.disk_weights(fmt, N, Kdim, synth.rng_for(128, 0))
+    x = synth.activations(1, Kdim, synth.rng_for(128, 1))
+    y = K.kq_gemv(fmt, pack(K, fmt, disk), N, Kdim, q8k_to_dev(K, oracle_q8k(x)))
+    torch.cuda.synchronize()
+    assert_row_tol(y.cpu().numpy()[None, :], oracle.gemm(fmt, disk, *oracle_q8k(x)))
+    assert K.kq_device_status() == 0

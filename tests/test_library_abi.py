@@ -122,6 +122,9 @@ def test_host_argument_checks(kq):
     assert lib.kq_gemv_grouped_fused(4, 1, pk4, n4, 256, 4, off, fake, 1, y4, None) == FMT
     assert lib.kq_gemv_grouped_fused(1, 1, pk4, n4, 256, 4, None, None, 0, y4, None) == 0
     assert lib.kq_gemv_grouped_fused(1, 1, pk4, n4, 256, 4, off, odd, 2, y4, None) == ALIGN
+    # the timeout test hook refuses a zero or over-one-second limit (no launch)
+    assert lib.kq_debug_wait_timeout(0, None) == ARG
+    assert lib.kq_debug_wait_timeout(2_000_000_000, None) == ARG
     # int8 MMA rate hook: argument checks only (no launch)
     assert lib.kq_measure_mma_s8(-1, 10, fake, None) == ARG
     assert lib.kq_measure_mma_s8(4, -1, fake, None) == ARG
