@@ -192,12 +192,13 @@ class DecodeLayers:
     # fused path: one launch per group of matrices sharing an input
     GROUPS = [["wq", "wk", "wv"], ["wo"], ["gate", "up"], ["down"]]
 
-    def step(self, l, events=None, x_override=None, fused=True):
+    def step(self, l, events=None, x_override=None, fused=True, y_override=None):
         """One layer: fused -> 4 launches of kq_gemv_fused (q/k/v, o, gate/up,
         down); separate -> 4 kq_quantize_q8k + 7 kq_gemv launches."""
         kq = self.kq
         c = self.copies[l]
         xs = c["x"] if x_override is None else x_override
+        yv = self.y_views if y_override is None else y_override
         idx = {m.name: i for i, m in enumerate(self.mats)}
         for j, names in enumerate(self.GROUPS):
             ii = [idx[n] for n in names]
@@ -206,14 +207,14 @@ class DecodeLayers:
                 if events is not None:
                     events[j][0].record()
                 kq.kq_gemv_fused(m0.fmt, [c["packed"][i] for i in ii], [self.mats[i].N for i in ii], m0.K,
-                                 xs[j], [self.y_views[i] for i in ii])
+                                 xs[j], [yv[i] for i in ii])
                 if events is not None:
                     events[j][1].record()
             else:
                 kq.kq_quantize_q8k(xs[j], out=self.q8[j])
                 for i in ii:
                     kq.kq_gemv(self.mats[i].fmt, c["packed"][i], self.mats[i].N, self.mats[i].K, self.q8[j],
-                               y=self.y_views[i])
+                               y=yv[i])
 
     def launches_per_step(self, fused=True):
         return len(self.GROUPS) if fused else len(LAYER_INPUTS) + len(self.mats)
@@ -347,20 +348,52 @@ def run_ours(args, world, rank, local):
                   for names, t, b in zip(layers.GROUPS, mean_ms, alg)]
     traffic = recorded_traffic("gemv_decode_layer")
 
-    # end to end through the public API: H2D of the step's activations from
-    # pinned host memory, the step, D2H of all outputs, replayed from a graph
+    # end to end through the public API: every step copies its activations in
+    # from pinned host memory, runs the layer and copies all its outputs back.
+    # The copies run on their own streams into NBUF rotating device rows, so
+    # step l's inputs arrive while earlier steps compute and its outputs leave
+    # while later steps compute (the copy into a buffer waits for the step
+    # that last used it); replayed from a graph
     x_host = torch.from_numpy(np.concatenate(
         [synth.activations(1, k, synth.rng_for(1, 7000 + j))[0] for j, (_, k) in enumerate(LAYER_INPUTS)])).pin_memory()
-    y_host = torch.empty(layers.y_total, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty(layers.x_total, dtype=torch.float32, device="cuda")
+    NBUF = 2    # (3 or 4 measured no faster: the waits on the copies, not their slack, cost the time)
+    y_host = [torch.empty(layers.y_total, dtype=torch.float32).pin_memory() for _ in range(NBUF)]
+    x_dev = [torch.empty(layers.x_total, dtype=torch.float32, device="cuda") for _ in range(NBUF)]
+    y_dev = [torch.empty(layers.y_total, dtype=torch.float32, device="cuda") for _ in range(NBUF)]
     xo = np.cumsum([0] + [k for _, k in LAYER_INPUTS])
-    x_views = [x_dev[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))]
+    yo = np.cumsum([0] + [m.N for m in layers.mats])
+    x_views = [[xd[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))] for xd in x_dev]
+    y_views = [[yd[yo[i]:yo[i + 1]] for i in range(len(layers.mats))] for yd in y_dev]
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_rot():
+        cur = torch.cuda.current_stream()
+        fork = torch.cuda.Event()
+        fork.record(cur)
+        h2d_s.wait_event(fork)
+        d2h_s.wait_event(fork)
+        done_c, done_d = {}, {}
         for l in range(G):
-            x_dev.copy_(x_host, non_blocking=True)
-            layers.step(l % L, x_override=x_views)
-            y_host.copy_(layers.y, non_blocking=True)
+            b = l % NBUF
+            if l >= NBUF:
+                h2d_s.wait_event(done_c[l - NBUF])    # step l-NBUF has read x_dev[b]
+            with torch.cuda.stream(h2d_s):
+                x_dev[b].copy_(x_host, non_blocking=True)
+            arrived = torch.cuda.Event()
+            arrived.record(h2d_s)
+            cur.wait_event(arrived)
+            if l >= NBUF:
+                cur.wait_event(done_d[l - NBUF])      # y_dev[b] of step l-NBUF is back on the host
+            layers.step(l % L, x_override=x_views[b], y_override=y_views[b])
+            done_c[l] = torch.cuda.Event()
+            done_c[l].record(cur)
+            d2h_s.wait_event(done_c[l])
+            with torch.cuda.stream(d2h_s):
+                y_host[b].copy_(y_dev[b], non_blocking=True)
+            done_d[l] = torch.cuda.Event()
+            done_d[l].record(d2h_s)
+        cur.wait_stream(h2d_s)
+        cur.wait_stream(d2h_s)
 
     g_e2e = graph_of(torch, e2e_rot)
     for _ in range(warm_reps):
@@ -380,7 +413,7 @@ def run_ours(args, world, rank, local):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         e_ms = float(tt.item())
     e2e_value = bytes_per_step * e_reps * G * world / (e_ms * 1e-3) / 1e9
-    y_check = y_host.numpy()
+    y_check = np.concatenate([yh.numpy() for yh in y_host])
     assert np.isfinite(y_check).all()
 
     small_batch = bench_small_batch(kq, torch, layers, peaks, args)
@@ -423,8 +456,9 @@ def run_ours(args, world, rank, local):
                               "how": "4 kq_quantize_q8k + 7 kq_gemv launches per step"},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": 4 * layers.x_total, "d2h_bytes_per_step": 4 * layers.y_total,
-                    "how": "graph replay of: H2D of the 4 fp32 inputs from pinned memory, 4 kq_gemv_fused "
-                           "launches, D2H of all 7 outputs"},
+                    "how": "graph replay of, every step: H2D of the 4 fp32 inputs from pinned memory, 4 "
+                           "kq_gemv_fused launches, D2H of all 7 outputs; the copies on their own streams into "
+                           f"{NBUF} rotating device buffers, overlapping the neighbouring steps' compute"},
             "gpu_launches": layers.launches_per_step() * steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
