@@ -849,3 +849,24 @@ def test_bounded_wait_times_out_and_reports(K):
     torch.cuda.synchronize()
     assert_row_tol(y.cpu().numpy()[None, :], oracle.gemm(fmt, disk, *oracle_q8k(x)))
     assert K.kq_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [2, 4, 8])
+def test_gemv_fused_batch_layer_shapes(K, M):
+    """The small-batch line's launches at its shapes: the Qwen3-4B-shaped
+    layer's four groups (q/k/v, o, gate/up, down) through kq_gemv_fused_batch
+    with M rows; every output of every matrix against the oracle."""
+    layer = synth.configs()[1].matrices
+    by = {m.name: m for m in layer}
+    groups = [["wq", "wk", "wv"], ["wo"], ["gate", "up"], ["down"]]
+    rng = synth.rng_for(129, M)
+    for names in groups:
+        ms = [by[n] for n in names]
+        disks = [synth.disk_weights(m.fmt, m.N, m.K, rng) for m in ms]
+        packs = [pack(K, m.fmt, d) for m, d in zip(ms, disks)]
+        x = synth.activations(M, ms[0].K, rng)
+        ys = K.kq_gemv_fused_batch(ms[0].fmt, packs, [m.N for m in ms], ms[0].K, to_dev(x))
+        torch.cuda.synchronize()
+        planes = oracle_q8k(x)
+        for m, d, y in zip(ms, disks, ys):
+            assert_row_tol(y.cpu().numpy(), oracle.gemm(m.fmt, d, *planes))
