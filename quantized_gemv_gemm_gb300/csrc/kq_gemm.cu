@@ -79,7 +79,16 @@ struct Cfg {
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     static constexpr int OFF_TILES = OFF_MISC + 128;              // grouped: the block's tile list
     static constexpr int OFF_OFFS = OFF_TILES + TILE_CAP * 16;    // grouped: the row offsets [E + 1]
-    static constexpr int SMEM = OFF_OFFS + (MAX_GROUPED_E + 4) * 4 + 1024;  // + alignment slack
+    // grouped Q4_K: each unpack thread's row bytes for a half superblock (4
+    // qs pieces + the scale block, 16 B each) staged by cp.async RS - 1 halves
+    // ahead, [RS][RCH chunks][BM rows] x 16 B (rows contiguous per chunk: no
+    // bank conflicts)
+    static constexpr int RS = F == FMT_Q4_K ? 3 : 0, RCH = 5;
+    static constexpr int OFF_RAW = OFF_OFFS + (MAX_GROUPED_E + 4) * 4;
+    static constexpr int SMEM = OFF_RAW + RS * RCH * BM * 16 + 1024;  // + alignment slack
+    static constexpr int SMEM_DENSE = OFF_RAW + 1024;                  // the dense kernel stages no rows
+    static_assert(SMEM <= 232448, "shared memory per block");
+    static_assert(OFF_RAW % 16 == 0, "cp.async needs 16-byte aligned destinations");
     static_assert(OFF_B % 1024 == 0, "B tiles need 1024-byte alignment");
     static_assert(B_SLOT % 1024 == 0, "B slots need 1024-byte alignment");
 };
@@ -603,6 +612,134 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int r = 32 * (uw & 3) + lane;      // tile row
         const int my_jj = uw >> 2;               // Q6_K: this thread's K sub-tile of each half
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
+        if constexpr (F == FMT_Q4_K && G) {
+        // ---- grouped Q4_K: the row's bytes of each half superblock arrive by
+        // cp.async in this thread's shared-memory ring, RS - 1 halves ahead:
+        // the experts' weights stream from HBM, and the register prefetch of
+        // one half left the warp waiting out an HBM latency per half (MoE gate
+        // 116 -> 101 us).  The dense GEMM, whose weight panels are re-read by
+        // its token tiles from L2, keeps the register prefetch (the ring
+        // measured 3 % slower there).
+        const uint32_t raw = smem_u32(smem + C::OFF_RAW);
+        auto slot_addr = [&](int slot, int c) -> uint32_t { return raw + (uint32_t)(((slot * C::RCH + c) * BM + r) * 16); };
+        const int nstage = 2 * (int)nsb;
+        int ntiles = -1;  // the list length, read once it is needed
+        // tile k's expert and first row; false past the last tile
+        auto tile_rows = [&](int k, int &e, int &n0) -> bool {
+            if (k == 0 && static_first) {
+                const int wt = w_tiles_of(p);
+                e = (int)(blockIdx.x / wt);
+                n0 = (int)(blockIdx.x % wt) * BM;
+                return true;
+            }
+            if (ntiles < 0) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0))) {
+                    ok = false;
+                    ntiles = 0;
+                    return false;
+                }
+                ntiles = (int)misc[1];
+            }
+            if (k >= ntiles) return false;
+            const int4 v = s_list[k];
+            e = v.x;
+            n0 = v.y;
+            return true;
+        };
+        // copy cursor: tile kc, half-stage hc of it, this row's plane pointers
+        int kc = 0, hc = 0;
+        bool c_on = false;
+        const uint8_t *cq = nullptr, *chd = nullptr;
+        auto enter_tile = [&](int k) {
+            int e, n0;
+            c_on = tile_rows(k, e, n0);
+            if (!c_on) return;
+            const Planes P = make_planes(F, p.packed + (uint64_t)e * p.expert_bytes, p.N, nsb);
+            const int64_t row = n0 + r < p.N ? n0 + r : p.N - 1;
+            const uint64_t ch0 = chunk_of(row, 0, nsb);
+            const int rr = (int)(row % GROUP_ROWS);
+            cq = P.p0 + ch0 * 2048 + 16 * rr;
+            chd = P.p1 + ch0 * 256 + 16 * rr;
+        };
+        auto issue = [&](int cs) {
+            if (c_on) {
+                const int sb = hc >> 1, h = hc & 1, slot = cs % C::RS;
+                const uint8_t *q = cq + (uint64_t)sb * 2048 + 256 * h;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cp_async16(slot_addr(slot, i), q + 512 * i);
+                cp_async16(slot_addr(slot, 4), chd + (uint64_t)sb * 256);
+                if (++hc == nstage) {
+                    hc = 0;
+                    enter_tile(++kc);
+                }
+            }
+            cp_async_commit();  // one group per half-stage, empty past the end
+        };
+        enter_tile(0);
+        for (int i = 0; i < C::RS - 1; ++i) issue(i);
+        int g = 0, hs_all = 0;
+        for (int k = 0; ok; ++k) {
+            int e_unused, n0_unused;
+            if ((k > 0 || !static_first) && !tile_rows(k, e_unused, n0_unused)) break;
+            for (int hs = 0; hs < nstage; ++hs, ++hs_all) {
+                const int sb = hs >> 1, gg = g + sb, h = hs & 1;
+                issue(hs_all + C::RS - 1);          // into the slot read one half-stage ago
+                cp_async_wait<C::RS - 1>();          // this half-stage's group has landed
+                const int slot = hs_all % C::RS;
+                uint32_t qs[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint4 v = lds128(slot_addr(slot, i));
+                    qs[4 * i] = v.x;
+                    qs[4 * i + 1] = v.y;
+                    qs[4 * i + 2] = v.z;
+                    qs[4 * i + 3] = v.w;
+                }
+                const uint4 hdr = lds128(slot_addr(slot, 4));
+                bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
+                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_ACC_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
+                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t a_slot = a_base + h * C::A_SLOT;
+                const ScaleMin sm = unpack_scale_min(hdr);
+                uint32_t qh0[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) qh0[i] = 0u;
+#pragma unroll
+                for (int jj = 0; jj < 2; ++jj) {
+                    const int cch = 2 * h + jj;  // chunk of the superblock; sub-blocks 2c, 2c+1
+                    const uint32_t scw = cch < 2 ? sm.sc_lo : sm.sc_hi;
+                    const int sc_lo = byte_of(scw, 2 * (cch & 1)), sc_hi = byte_of(scw, 2 * (cch & 1) + 1);
+                    uint32_t qsc[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) qsc[i] = qs[8 * jj + i];
+                    unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                }
+                if (h == 0) {
+                    // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
+                    const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+                    uint32_t mw[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
+                    sts128(amin + sw32_offset(r, 0), mw[0], mw[1], mw[2], mw[3]);
+                    sts128(amin + sw32_offset(r, 8), mw[4], mw[5], mw[6], mw[7]);
+                    s_d[(gg & 1) * BM + r] = half_lo(hdr.x);
+                    s_dmin[(gg & 1) * BM + r] = half_hi(hdr.x);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&bar[BAR_FULL_A + h]);
+                    if (h == 0) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
+                }
+            }
+            g += (int)nsb;
+        }
+        cp_async_wait<0>();  // no copy outlives the block
+        if (!ok && lane == 0) set_timeout();
+        } else {
         using Raw = typename RawOf<F>::T;
         Raw cur, nxt;
         // Q6_K: this thread's P2 rows of the half-0 / half-1 slot may be non-zero
@@ -730,6 +867,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             row = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
         }
         if (!ok && lane == 0) set_timeout();
+        }
     } else if constexpr (F == FMT_Q6_K) {
         // ------------------------------------------------ epilogue, Q6_K
         // 4 warps, thread = weight row x every token column; y accumulates
@@ -1045,7 +1183,7 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = Cf::SMEM;
+    cfg.dynamicSmemBytes = offsets ? Cf::SMEM : Cf::SMEM_DENSE;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
