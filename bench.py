@@ -230,6 +230,22 @@ class DecodeLayers:
         return out
 
 
+def max_over_ranks(torch, v: float, world: int, device="cuda") -> float:
+    """The largest of the ranks' values (a region's time: the whole job ends
+    with its slowest rank); the value itself with one rank."""
+    if world == 1:
+        return v
+    tt = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of N replicas: every rank's units over the
+    slowest rank's time (units per second)."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def graph_of(torch, fn):
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -324,24 +340,17 @@ def run_ours(args, world, rank, local):
                     kt[j].append(ev[l][j][0].elapsed_time(ev[l][j][1]))
     clocks = clk.summary()
 
-    def max_over_ranks(v):
-        if world == 1:
-            return v
-        tt = torch.tensor([v], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        return float(tt.item())
-
-    ms_max = max_over_ranks(ms)
-    ms_sep = max_over_ranks(ms_sep)
+    ms_max = max_over_ranks(torch, ms, world)
+    ms_sep = max_over_ranks(torch, ms_sep, world)
     bytes_per_step = layers.weight_bytes
-    value = bytes_per_step * steps * world / (ms_max * 1e-3) / 1e9
+    value = job_rate(bytes_per_step * steps, world, ms_max) / 1e9
     value_sep = bytes_per_step * max(1, reps // 2) * G * world / (ms_sep * 1e-3) / 1e9
 
     # roofline of the GEMV kernel: the timed region holds nothing but its
     # launches (4 per step), so its average launch duration is the region's
     # time / launches and achieved = algorithmic bytes of a step / step time
     alg = layers.algorithmic_launch_bytes()
-    achieved = sum(alg) * steps * world / (ms_max * 1e-3) / 1e9
+    achieved = job_rate(sum(alg) * steps, world, ms_max) / 1e9
     hbm = float(peaks["hbm_gbs"])
     mean_ms = [float(np.mean(kt[j])) for j in range(NG)]
     per_launch = [{"matrices": "+".join(names), "event_us": round(t * 1e3, 3), "bytes": b}
@@ -407,12 +416,8 @@ def run_ours(args, world, rank, local):
         g_e2e.replay()
     e1.record()
     torch.cuda.synchronize()
-    e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e_ms], device="cuda")
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e_ms = float(tt.item())
-    e2e_value = bytes_per_step * e_reps * G * world / (e_ms * 1e-3) / 1e9
+    e_ms = max_over_ranks(torch, e0.elapsed_time(e1), world)
+    e2e_value = job_rate(bytes_per_step * e_reps * G, world, e_ms) / 1e9
     y_check = np.concatenate([yh.numpy() for yh in y_host])
     assert np.isfinite(y_check).all()
 
