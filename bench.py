@@ -590,10 +590,12 @@ def bench_moe_decode(kq, torch, peaks, args):
 
 
 def bench_q8_0(kq, torch, peaks, args):
-    """The Q8_0 rail on the 27B-shaped FFN at M = 1: per step kq_quantize_q8_0
-    of x (5120) and of the down input (17408), and kq_gemv_q8_0 of gate, up
-    (17408x5120) and down (5120x17408), over rotating copies of the 284 MB of
-    Q8_0 weights, replayed from a CUDA graph with programmatic dependent launch."""
+    """The Q8_0 rail on the 27B-shaped FFN at M = 1: per step gate, up
+    (17408x5120) and down (5120x17408) by kq_gemv_q8_0_fused (the row quantized
+    inside each GEMV), over rotating copies of the 284 MB of Q8_0 weights,
+    replayed from a CUDA graph with programmatic dependent launch.  The same
+    step with the quantize as its own launch (2 kq_quantize_q8_0 + 3
+    kq_gemv_q8_0) is timed beside it."""
     shapes = [(17408, 5120), (17408, 5120), (5120, 17408)]
     step_bytes = sum(N * K * 34 // 32 for N, K in shapes)
     C = max(2, -(-600_000_000 // step_bytes))
@@ -609,7 +611,13 @@ def bench_q8_0(kq, torch, peaks, args):
     dh, qh = kq.kq_quantize_q8_0(h)
     ys = [torch.empty(N, dtype=torch.float32, device="cuda") for N, _ in shapes]
 
-    def rot():
+    def rot_fused():
+        for c in copies:
+            kq.kq_gemv_q8_0_fused(c[0], 17408, 5120, x, y=ys[0])
+            kq.kq_gemv_q8_0_fused(c[1], 17408, 5120, x, y=ys[1])
+            kq.kq_gemv_q8_0_fused(c[2], 5120, 17408, h, y=ys[2])
+
+    def rot_split():
         for c in copies:
             kq.kq_quantize_q8_0(x, d=dx, qs=qx)
             kq.kq_gemv_q8_0(c[0], 17408, 5120, dx, qx, y=ys[0])
@@ -617,25 +625,32 @@ def bench_q8_0(kq, torch, peaks, args):
             kq.kq_quantize_q8_0(h, d=dh, qs=qh)
             kq.kq_gemv_q8_0(c[2], 5120, 17408, dh, qh, y=ys[2])
 
-    g = graph_of(torch, rot)
-    for _ in range(3):
-        g.replay()
-    torch.cuda.synchronize()
     reps = max(3, min(200, args.steps // (4 * C)))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / (reps * C)
+
+    def timed(rot):
+        g = graph_of(torch, rot)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) * 1e3 / (reps * C)
+
+    us = timed(rot_fused)
+    us_split = timed(rot_split)
     gbs = step_bytes / (us * 1e-6) / 1e9
     hbm = float(peaks["hbm_gbs"])
-    del copies, base, g
+    del copies, base
     torch.cuda.empty_cache()
     return {"workload": "27B-shaped dense FFN in Q8_0 at M=1 (gate/up 17408x5120, down 5120x17408), "
-                        "2 kq_quantize_q8_0 + 3 kq_gemv_q8_0 launches",
+                        "3 kq_gemv_q8_0_fused launches",
             "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
+            "split_quantize_us_per_step": round(us_split, 3),
             "weight_bytes_per_step": step_bytes, "copies": C,
             "timing": f"CUDA events around {reps} graph replays of {C} steps (weights {C * step_bytes / 1e6:.0f} MB)"}
 

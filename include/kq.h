@@ -334,6 +334,16 @@ int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const
                  cudaStream_t s);
 
 /*
+ * kq_gemv_q8_0 with the quantize fused in ([kq-arc], "The pieces": the chain
+ * regrain applied to the q8 rail): every block quantizes the fp32 row into its
+ * shared memory bit-identically to kq_quantize_q8_0, so the result equals
+ * kq_quantize_q8_0 + kq_gemv_q8_0 bit for bit, in one launch.
+ *   x   device float32 [K], 16-byte aligned, finite
+ * Other arguments, limits and errors as kq_gemv_q8_0.
+ */
+int kq_gemv_q8_0_fused(const void *packed, int64_t N, int64_t K, const float *x, float *y, cudaStream_t s);
+
+/*
  * Test hook for failure detection: launches one block whose single bounded
  * mbarrier wait is never satisfied; after limit_ns nanoseconds the wait gives
  * up and records KQ_ERR_TIMEOUT in the device status word, as a stuck stage

@@ -136,7 +136,16 @@ int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const
     if (N == 0) return KQ_OK;
     if (!packed || !d || !qs || !y) return KQ_ERR_ARG;
     if (!aligned(packed, 256) || !aligned(qs, 16) || !aligned(d, 4) || !aligned(y, 4)) return KQ_ERR_ALIGN;
-    return launch_status(launch_gemv_q8_0(packed, N, K, d, qs, y, s));
+    return launch_status(launch_gemv_q8_0(packed, N, K, d, qs, nullptr, y, s));
+}
+
+int kq_gemv_q8_0_fused(const void *packed, int64_t N, int64_t K, const float *x, float *y, cudaStream_t s) {
+    if (int r = check_shape(N, K)) return r;
+    if (K > GEMV_MAX_K) return KQ_ERR_ARG;
+    if (N == 0) return KQ_OK;
+    if (!packed || !x || !y) return KQ_ERR_ARG;
+    if (!aligned(packed, 256) || !aligned(x, 16) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_gemv_q8_0(packed, N, K, nullptr, nullptr, x, y, s));
 }
 
 size_t kq_gemv_workspace_bytes(void) { return GEMV_WORKSPACE_BYTES; }

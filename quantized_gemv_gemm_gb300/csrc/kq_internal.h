@@ -30,8 +30,9 @@ cudaError_t launch_quantize(const float *x, int64_t M, int64_t K, float *d, int8
 uint64_t q8_0_image_bytes(int64_t N, int64_t K);
 cudaError_t launch_repack_q8_0(const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed, cudaStream_t s);
 cudaError_t launch_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *qs, cudaStream_t s);
-cudaError_t launch_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, float *y,
-                             cudaStream_t s);
+// (x != nullptr: the fp32 row, quantized in the kernel; d, qs unused)
+cudaError_t launch_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs,
+                             const float *x, float *y, cudaStream_t s);
 
 // Disk superblocks -> packed image.
 cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,

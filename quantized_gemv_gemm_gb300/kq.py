@@ -58,13 +58,15 @@ _lib.kq_measure_mma_s8.argtypes = [_I64, _I64, _P, _P]
 _lib.kq_debug_wait_timeout.argtypes = [ctypes.c_uint64, _P]
 _lib.kq_quantize_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_gemv_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
+_lib.kq_gemv_q8_0_fused.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
-           "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout"):
+           "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout",
+           "kq_gemv_q8_0_fused"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -361,6 +363,19 @@ def kq_gemv_q8_0(packed: torch.Tensor, N: int, K: int, d: torch.Tensor, qs: torc
         y = torch.empty(N, dtype=torch.float32, device=packed.device)
     _check(_lib.kq_gemv_q8_0(_ptr(packed), int(N), int(K), _ptr(d), _ptr(qs), _ptr(y), _stream(stream)),
            "kq_gemv_q8_0")
+    return y
+
+
+def kq_gemv_q8_0_fused(packed: torch.Tensor, N: int, K: int, x: torch.Tensor, y: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """y [N] = Q8_0 weights x the fp32 row x [K], quantized inside the kernel."""
+    _need_cuda(packed, x)
+    if x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 tensor")
+    if y is None:
+        y = torch.empty(N, dtype=torch.float32, device=packed.device)
+    _check(_lib.kq_gemv_q8_0_fused(_ptr(packed), int(N), int(K), _ptr(x), _ptr(y), _stream(stream)),
+           "kq_gemv_q8_0_fused")
     return y
 
 

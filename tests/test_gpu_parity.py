@@ -672,11 +672,35 @@ def test_q8_0_gemv(K, N, Kdim):
     assert torch.equal(y, y2)
 
 
+@pytest.mark.parametrize("N,Kdim", [(300, 2560), (17, 256), (5120, 17408), (17408, 5120), (40, 40960)])
+def test_q8_0_fused_equals_quantize_then_gemv(K, N, Kdim):
+    """The fused Q8_0 GEMV quantizes the row inside every block: its output is
+    bit-identical to kq_quantize_q8_0 followed by kq_gemv_q8_0 (zero block,
+    tiny and outlier values included), and within tolerance of the oracle."""
+    rng = synth.rng_for(124, N + Kdim)
+    disk = synth.disk_weights_q8_0(N, Kdim, rng)
+    x = synth.activations(1, Kdim, rng, outliers=True)
+    x[0, :32] = 0.0
+    x[0, 64:96] *= np.float32(1e-30)
+    packed = K.kq_repack(synth.Q8_0, to_dev(disk.reshape(-1)), N, Kdim)
+    xd = to_dev(x[0])
+    d, q = K.kq_quantize_q8_0(xd)
+    want = K.kq_gemv_q8_0(packed, N, Kdim, d, q)
+    full, y = poisoned((N,))
+    K.kq_gemv_q8_0_fused(packed, N, Kdim, xd, y=y)
+    torch.cuda.synchronize()
+    check_guard(full, N)
+    assert torch.equal(y, want)
+    d_a, q_a = oracle.quantize_q8_0(x)
+    assert_row_tol(y.cpu().numpy()[None, :], oracle.gemv_q8_0(disk, d_a, q_a))
+
+
 def test_q8_0_pdl_chain_matches_plain_launches(K):
     """The Q8_0 rail under programmatic dependent launch: the GEMV loads its
     first weights before the dependency wait, while the activations are still
-    being written by the quantize launched just before it; every output equals
-    the plain launches' bits, and the last against the oracle."""
+    being written by the kernel launched just before it (the quantize, or for
+    the fused form the elementwise op); every output equals the plain
+    launches' bits, and the last against the oracle."""
     N, Kdim = 300, 2560
     rng = synth.rng_for(123, 0)
     disk = synth.disk_weights_q8_0(N, Kdim, rng)
@@ -695,7 +719,8 @@ def test_q8_0_pdl_chain_matches_plain_launches(K):
             y = K.kq_gemv_q8_0(packed, N, Kdim, d, q)
             d2, q2 = K.kq_quantize_q8_0(h0 + y.sum() * 0.0 + 0.1 * i)
             y2 = K.kq_gemv_q8_0(packed2, N, 5120, d2, q2)
-            outs.append(torch.cat([y * 2.0, y2 * 2.0]))   # consumed right after
+            y3 = K.kq_gemv_q8_0_fused(packed2, N, 5120, y2[:1].repeat(5120) * 0.0 + h0 * (0.5 + i))
+            outs.append(torch.cat([y * 2.0, y2 * 2.0, y3]))   # consumed right after
         torch.cuda.synchronize()
         return torch.stack(outs).cpu().numpy()
 
