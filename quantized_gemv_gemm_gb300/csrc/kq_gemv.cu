@@ -752,12 +752,14 @@ static int sm_count() {
 
 // Above this many items per SM a launch takes two blocks per SM (more warps
 // folding), giving up the room for the next kernel's block -- unless K is
-// long, since every block quantizes the whole row.
+// very long, since every block quantizes the whole row.  (Measured on GB300,
+// the 27B-shaped FFN at M = 1 with its down projection of K = 17408 in two
+// blocks per SM: 32.8 vs 34.2 us per gate/up + down step.)
 #ifndef KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM
 #define KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM 100
 #endif
 #ifndef KQ_GEMV_TWO_BLOCKS_MAX_NSB
-#define KQ_GEMV_TWO_BLOCKS_MAX_NSB 32
+#define KQ_GEMV_TWO_BLOCKS_MAX_NSB 80
 #endif
 
 #ifndef KQ_GEMV_CUT_ITEMS
