@@ -411,6 +411,8 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     // matrix, the group's first output row in it, and the cut between blocks
     // (-1: none)
     __shared__ float s_rec[8][2][T][16];
+    // grouped: the expert of each activation row (-1: none)
+    __shared__ int64_t s_row_e[GEMV_MAX_MATRICES];
     __shared__ int s_fin_mask[8][2], s_fin_m[8][2];
     __shared__ int64_t s_fin_row[8][2], s_fin_cut[8][2];
     // the next kernel may be scheduled now: it waits for this grid to
@@ -437,24 +439,103 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     const int64_t G = p.gpre[p.nmat], B = gridDim.x;
     const int64_t I0 = block_item(p, blockIdx.x, B, G), I1 = block_item(p, blockIdx.x + 1, B, G);
     const int64_t w0 = I0 + warp * (I1 - I0) / 8, w1 = I0 + (warp + 1) * (I1 - I0) / 8;
-    if constexpr (GR) {
-        // the expert offsets are written by the kernels before this one
-        griddep_wait();
-        if (threadIdx.x < p.nmat) {
-            const int mm = threadIdx.x;
-            const int set = mm / ntok, m = mm - set * ntok;  // weight set, activation row
-            int64_t lo = 0, hi = p.E;  // last e with offsets[e] <= m, among [0, E)
-            while (hi - lo > 1) {
-                const int64_t mid = (lo + hi) >> 1;
-                if (p.offsets[mid] <= m) lo = mid;
-                else hi = mid;
+    // Stage the activation rows in shared memory (need: bit t set = token
+    // row t is read by this block's matrices).
+    constexpr bool PAIRS = F != FMT_Q6_K;
+    auto stage_rows = [&](uint32_t need) {
+        if ((T > 1 || GR) && p.x) {
+            // several fp32 rows: block vb of the rows laid end to end is block
+            // vb % nsb of token row vb / nsb, staged in that token's row (32-bit
+            // index arithmetic: nvb <= 16 * 160, and a 64-bit division is a
+            // long instruction sequence)
+            const uint32_t nsb32 = (uint32_t)nsb, nvb = (uint32_t)ntok * nsb32;
+            for (uint32_t vb0 = warp; vb0 < nvb; vb0 += 64) {
+                float4 v[8][2];
+                uint32_t tj[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t vb = vb0 + 8 * j;
+                    tj[j] = vb / nsb32;
+                    if (vb < nvb && ((need >> tj[j]) & 1u)) {
+                        const float4 *xp = reinterpret_cast<const float4 *>(p.x + (int64_t)vb * QK + 8 * lane);
+                        v[j][0] = xp[0];
+                        v[j][1] = xp[1];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t vb = vb0 + 8 * j;
+                    if (vb < nvb && ((need >> tj[j]) & 1u)) {
+                        const uint32_t t = tj[j], b = vb - t * nsb32;
+                        const size_t o = (size_t)t * tstride;
+                        stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, reinterpret_cast<int8_t *>(
+                                                  reinterpret_cast<uint8_t *>(s_qs) + o) + b * QK, s_sum + o + b * 32,
+                                                  reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + o) + b);
+                    }
+                }
             }
-            const bool in = p.offsets[lo] <= m && m < p.offsets[lo + 1];
-            // (packed, N, y are per matrix: the set's values repeated ntok times)
-            s_planes[mm] = make_planes(F, p.packed[mm] + (in ? (uint64_t)lo * p.expert_bytes[set] : 0), p.N[mm], nsb);
-            s_n[mm] = in ? p.N[mm] : 0;  // a row of no expert is not written
-            s_y[mm] = p.y[mm] + (int64_t)m * p.N[mm];
+        } else if (p.x) {
+            // up to eight blocks per warp per round, all loads issued first
+            for (int64_t b0 = warp; b0 < nsb; b0 += 64) {
+                float4 v[8][2];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int64_t b = b0 + 8 * j;
+                    if (b < nsb) {
+                        const float4 *xp = reinterpret_cast<const float4 *>(p.x + b * QK + 8 * lane);
+                        v[j][0] = xp[0];
+                        v[j][1] = xp[1];
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int64_t b = b0 + 8 * j;
+                    if (b < nsb) stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, s_qs + b * QK, s_sum + b * 32, s_d8 + b);
+                }
+            }
+        } else {
+            for (int t = 0; t < ntok; ++t) {
+                if (!((need >> t) & 1u)) continue;
+                uint8_t *tq = reinterpret_cast<uint8_t *>(s_qs) + (size_t)t * tstride;
+                uint8_t *ts = s_sum + (size_t)t * tstride;
+                float *td = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + (size_t)t * tstride);
+                const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs + t * K);
+                for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(tq)[i] = gq[i];
+                if constexpr (PAIRS) {
+                    // sum of each 32-element sub-block = two consecutive bsums
+                    const int *gb = reinterpret_cast<const int *>(p.bs + t * (K / 16));
+                    for (int64_t i = threadIdx.x; i < K / 32; i += 256) {
+                        const int v = gb[i];
+                        reinterpret_cast<int *>(ts)[i] = (int)(int16_t)(v & 0xFFFF) + (v >> 16);
+                    }
+                } else {
+                    const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs + t * (K / 16));
+                    for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(ts)[i] = gb[i];
+                }
+                for (int64_t i = threadIdx.x; i < nsb; i += 256) td[i] = p.d8[t * nsb + i];
+            }
         }
+    };
+    // the token rows this block's matrices read (grouped: matrix m reads row
+    // m % ntok, and a block's items span a few consecutive matrices, so it
+    // stages only those rows; otherwise all of them)
+    uint32_t need = 0xFFFFFFFFu;
+    if constexpr (GR) {
+        need = 0u;
+        if (I0 < I1) {
+            auto mat = [&](int64_t g) {
+                int m = 0;
+                while (m + 1 < p.nmat && g >= p.gpre[m + 1]) ++m;
+                return m;
+            };
+            const int mB = mat((I1 - 1) / nsb);
+            for (int mm = mat(I0 / nsb); mm <= mB; ++mm) need |= 1u << (mm % ntok);
+        }
+    }
+    // Set-up that needs nothing written by earlier kernels: the row-group
+    // prefix sums, the mbarriers, the non-grouped matrices' planes.
+    if constexpr (GR) {
+        if (threadIdx.x < GEMV_MAX_MATRICES) s_row_e[threadIdx.x] = -1;
     } else if (threadIdx.x < p.nmat) {
         s_planes[threadIdx.x] = make_planes(F, p.packed[threadIdx.x], p.N[threadIdx.x], nsb);
         s_n[threadIdx.x] = p.N[threadIdx.x];
@@ -508,6 +589,30 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
         }
         s_fin_mask[warp][slot] = rec ? mask : -1;
     }
+    if constexpr (GR) {
+        // the expert offsets are written by the kernels before this one.
+        // Expert e holds rows [offsets[e], offsets[e+1]); the ranges are
+        // disjoint, so each of the first ntok rows is claimed by at most one
+        // expert.  All experts are looked at in parallel: one round trip to
+        // the offsets instead of a binary search's chain of dependent loads.
+        griddep_wait();
+        for (int64_t e = threadIdx.x; e < p.E; e += blockDim.x) {
+            const int64_t lo = p.offsets[e], hi = p.offsets[e + 1];
+            for (int64_t m = lo < 0 ? 0 : lo; m < hi && m < ntok; ++m) s_row_e[m] = e;
+        }
+        __syncthreads();
+        if (threadIdx.x < p.nmat) {
+            const int mm = threadIdx.x;
+            const int set = mm / ntok, m = mm - set * ntok;  // weight set, activation row
+            const int64_t e = s_row_e[m];
+            const bool in = e >= 0;
+            // (packed, N, y are per matrix: the set's values repeated ntok times)
+            s_planes[mm] = make_planes(F, p.packed[mm] + (in ? (uint64_t)e * p.expert_bytes[set] : 0), p.N[mm], nsb);
+            s_n[mm] = in ? p.N[mm] : 0;  // a row of no expert is not written
+            s_y[mm] = p.y[mm] + (int64_t)m * p.N[mm];
+        }
+        __syncthreads();
+    }
     if (w0 < w1) {
         im = m0;
         icp = chunk_ptr<F>(s_planes[im], (uint64_t)(w0 - s_gpre[im] * nsb));
@@ -527,76 +632,10 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     };
     for (int i = 0; i < D; ++i) issue();
 
-    // activations: written by the kernels before this one
+    // activations: written by the kernels before this one (grouped: the
+    // wait is above); staged while the first items stream in
     if constexpr (!GR) griddep_wait();
-    constexpr bool PAIRS = F != FMT_Q6_K;
-    if ((T > 1 || GR) && p.x) {
-        // several fp32 rows: block vb of the rows laid end to end is block
-        // vb % nsb of token row vb / nsb, staged in that token's row
-        const int64_t nvb = (int64_t)ntok * nsb;
-        for (int64_t vb0 = warp; vb0 < nvb; vb0 += 64) {
-            float4 v[8][2];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int64_t vb = vb0 + 8 * j;
-                if (vb < nvb) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(p.x + vb * QK + 8 * lane);
-                    v[j][0] = xp[0];
-                    v[j][1] = xp[1];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int64_t vb = vb0 + 8 * j;
-                if (vb < nvb) {
-                    const int64_t t = vb / nsb, b = vb - t * nsb;
-                    const size_t o = (size_t)t * tstride;
-                    stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, reinterpret_cast<int8_t *>(
-                                              reinterpret_cast<uint8_t *>(s_qs) + o) + b * QK, s_sum + o + b * 32,
-                                              reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + o) + b);
-                }
-            }
-        }
-    } else if (p.x) {
-        // up to eight blocks per warp per round, all loads issued first
-        for (int64_t b0 = warp; b0 < nsb; b0 += 64) {
-            float4 v[8][2];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int64_t b = b0 + 8 * j;
-                if (b < nsb) {
-                    const float4 *xp = reinterpret_cast<const float4 *>(p.x + b * QK + 8 * lane);
-                    v[j][0] = xp[0];
-                    v[j][1] = xp[1];
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int64_t b = b0 + 8 * j;
-                if (b < nsb) stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, s_qs + b * QK, s_sum + b * 32, s_d8 + b);
-            }
-        }
-    } else {
-        for (int t = 0; t < ntok; ++t) {
-            uint8_t *tq = reinterpret_cast<uint8_t *>(s_qs) + (size_t)t * tstride;
-            uint8_t *ts = s_sum + (size_t)t * tstride;
-            float *td = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(s_d8) + (size_t)t * tstride);
-            const uint4 *gq = reinterpret_cast<const uint4 *>(p.qs + t * K);
-            for (int64_t i = threadIdx.x; i < K / 16; i += 256) reinterpret_cast<uint4 *>(tq)[i] = gq[i];
-            if constexpr (PAIRS) {
-                // sum of each 32-element sub-block = two consecutive bsums
-                const int *gb = reinterpret_cast<const int *>(p.bs + t * (K / 16));
-                for (int64_t i = threadIdx.x; i < K / 32; i += 256) {
-                    const int v = gb[i];
-                    reinterpret_cast<int *>(ts)[i] = (int)(int16_t)(v & 0xFFFF) + (v >> 16);
-                }
-            } else {
-                const uint4 *gb = reinterpret_cast<const uint4 *>(p.bs + t * (K / 16));
-                for (int64_t i = threadIdx.x; i < K / 128; i += 256) reinterpret_cast<uint4 *>(ts)[i] = gb[i];
-            }
-            for (int64_t i = threadIdx.x; i < nsb; i += 256) td[i] = p.d8[t * nsb + i];
-        }
-    }
+    stage_rows(need);
     __syncthreads();
 
     int rs = 0;
@@ -762,6 +801,13 @@ static int sm_count() {
 #define KQ_GEMV_TWO_BLOCKS_MAX_NSB 80
 #endif
 
+// Blocks per SM of a grouped-rows (MoE decode) launch: its weights are
+// known only after the wait, so nothing is prefetched beside the previous
+// kernel, and more warps folding is what counts.
+#ifndef KQ_GEMV_GR_BLOCKS_PER_SM
+#define KQ_GEMV_GR_BLOCKS_PER_SM 2
+#endif
+
 #ifndef KQ_GEMV_CUT_ITEMS
 #define KQ_GEMV_CUT_ITEMS 3
 #endif
@@ -790,11 +836,19 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     const int64_t G = p.gpre[p.nmat];
     if (G == 0) return cudaSuccess;
     p.items = G * p.nsb;
+    p.stage_stride = gemv_stage_stride(p.K);
+    if (T == 1 && !GR) p.ntok = 1;
+    // (a grouped launch stages its ntok activation rows; a pass of a few
+    // tokens keeps to half an SM while its rows leave room for a 3-stage ring)
+    const int64_t rows_bytes = (GR ? p.ntok : T) * gemv_stage_stride(p.K);
+    const bool wide = (GR && KQ_GEMV_GR_BLOCKS_PER_SM == 1) ||
+                      ((T > 1 || GR) && (GEMV_SMEM_BUDGET - rows_bytes) / (8 * GemvFmt<F>::SLOT) < 3);
     // one block per SM, each with an even share of the items; a row group
     // may then be cut between two blocks, which needs the workspace
     int64_t blocks = sm_count();
     if (T == 1 && !GR && p.items > (int64_t)KQ_GEMV_TWO_BLOCKS_ITEMS_PER_SM * blocks && p.nsb <= KQ_GEMV_TWO_BLOCKS_MAX_NSB)
         blocks *= 2;
+    if (GR && !wide) blocks *= KQ_GEMV_GR_BLOCKS_PER_SM;
     if (blocks > GEMV_MAX_BLOCKS) blocks = GEMV_MAX_BLOCKS;
     if (blocks > G) blocks = G;  // every row group spans at most two blocks
     // cut row groups between blocks only where whole row groups would leave
@@ -804,12 +858,6 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     p.split = T == 1 && !GR && ws != nullptr && ws_bytes >= GEMV_WORKSPACE_BYTES && blocks > 1 &&
               ((launch_flags() & LAUNCH_GEMV_SPLIT) || (whole + 7) / 8 - (even + 7) / 8 >= KQ_GEMV_CUT_ITEMS);
     p.ws = static_cast<unsigned long long *>(ws);
-    p.stage_stride = gemv_stage_stride(p.K);
-    if (T == 1 && !GR) p.ntok = 1;
-    // (a grouped launch stages its ntok activation rows; a pass of a few
-    // tokens keeps to half an SM while its rows leave room for a 3-stage ring)
-    const int64_t rows_bytes = (GR ? p.ntok : T) * gemv_stage_stride(p.K);
-    const bool wide = GR || (T > 1 && (GEMV_SMEM_BUDGET - rows_bytes) / (8 * GemvFmt<F>::SLOT) < 3);
     const int64_t budget = wide ? GEMV_BATCH_SMEM_BUDGET : GEMV_SMEM_BUDGET;
     const int64_t stage_bytes = (GR ? p.ntok : T) * p.stage_stride;
     int64_t D = (budget - stage_bytes) / (8 * GemvFmt<F>::SLOT);
