@@ -51,6 +51,8 @@
 // wait the block stages the activation row in shared memory (copied from
 // the Q8_K planes, or quantized from the fp32 row bit-identically to
 // kq_quantize_q8k) with the sums the fold needs.
+#include <type_traits>
+
 #include "kq_internal.h"
 #include "kq_sm100.cuh"
 
@@ -318,6 +320,187 @@ __device__ __forceinline__ float item_d(const ItemQ6 &w) { return half_lo(w.d); 
 __device__ __forceinline__ float item_dmin(const ItemQ4 &w) { return half_hi(w.hdr.x); }
 __device__ __forceinline__ float item_dmin(const ItemQ5 &w) { return half_hi(w.hdr.x); }
 __device__ __forceinline__ float item_dmin(const ItemQ6 &) { return 0.0f; }
+
+// ---------------------------------------------------------------------------
+// Tensor-core fold of one item for a pass of 8 tokens (T = 8, Q4_K and
+// Q6_K): the warp's 16 weight rows x the pass's token rows with the
+// integer warp MMA, u8 weights x s8 activations -> s32 (exact).  Q4_K takes
+// one m16n8k32 per 32-element sub-block (its scale and min are per row),
+// Q6_K one m16n8k16 per 16-element group.  Fragment ownership (PTX ISA,
+// m16n8k32 / m16n8k16 with 8-bit operands): lane (gq = lane / 4,
+// cq = lane % 4) holds A bytes 4cq..4cq+3 of rows gq and gq+8 (and 16 bytes
+// further for k32), B bytes 4cq..4cq+3 (and +16) of token column gq, and
+// the accumulators (row gq, tokens 2cq, 2cq+1) and (row gq+8, the same
+// tokens).  The weights come from the stage already in shared memory; the
+// reads of one item are all issued before the stage is handed back.
+// (Measured on GB300, the Qwen3-4B-shaped layer through kq_gemv_fused_batch:
+// M = 8 in 76.8 instead of 84.6 us; at M = 4, where half of each MMA's
+// token columns are empty, 62.7 instead of 51.9 us, so T = 4 keeps dp4a.)
+template <int F, int T> struct MmaFold {
+    static constexpr bool on = T >= 8 && (F == FMT_Q4_K || F == FMT_Q6_K);
+};
+
+__device__ __forceinline__ void mma_k32_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(0));
+}
+__device__ __forceinline__ void mma_k16_u8s8(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%7,%7,%7};"
+                 : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+                 : "r"(a0), "r"(a1), "r"(b0), "r"(0));
+}
+
+// the lane's raw share of a Q4_K item: [half][row gq / gq+8][piece] words
+// (bytes 4cq..4cq+3 of the row's 16-byte piece), and the two rows' headers
+struct MmaQ4 {
+    uint32_t q[2][2][4];
+    uint4 hdr[2];
+};
+struct MmaQ6 {
+    uint32_t ql[2][2][4];
+    uint32_t qh[2][2][2];
+    uint4 sc[2];     // the 16 int8 group scales of rows gq, gq+8
+    uint32_t d[2];   // their fp16 d
+};
+
+__device__ __forceinline__ void mma_read(MmaQ4 &w, uint32_t st, int gq, int cq) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc)
+                w.q[h2][rr][pc] = lds32(st + 16u * (gq + 8 * rr + 16 * h2) + 512u * pc + 4u * cq);
+    w.hdr[0] = lds128(st + 2048u + 16u * gq);
+    w.hdr[1] = lds128(st + 2048u + 16u * (gq + 8));
+}
+__device__ __forceinline__ void mma_read(MmaQ6 &w, uint32_t st, int gq, int cq) {
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const uint32_t r = gq + 8 * rr + 16 * h2;
+#pragma unroll
+            for (int pc = 0; pc < 4; ++pc) w.ql[h2][rr][pc] = lds32(st + 16u * r + 512u * pc + 4u * cq);
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) w.qh[h2][rr][pc] = lds32(st + 2048u + 512u * pc + 16u * r + 4u * cq);
+        }
+    w.sc[0] = lds128(st + 3072u + 16u * gq);
+    w.sc[1] = lds128(st + 3072u + 16u * (gq + 8));
+    w.d[0] = lds16(st + 3328u + 2u * gq);
+    w.d[1] = lds16(st + 3328u + 2u * (gq + 8));
+}
+
+// Fold of one item for the pass: acc[rr * 2 + k] (row gq + 8 rr, token
+// 2cq + k) += d * d8 * isum - dmin * d8 * msum.  act = shared address of
+// token 0's activation superblock, sums / d8s of its sums and scale; tokens
+// are tstride apart; tokens at or past ntok are not read (their columns are
+// zero and their accumulators unused).
+__device__ __forceinline__ void mma_fold(const MmaQ4 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
+                                         uint32_t d8s, uint32_t tstride, float (&acc)[4]) {
+    constexpr uint32_t LO = 0x0F0F0F0Fu;
+    const bool bt = gq < ntok;
+    const uint32_t ab = act + (uint32_t)gq * tstride + 4u * cq;
+    int isum[4] = {0, 0, 0, 0};
+    uint32_t scw[2][2], mw[2][2];  // [row][half]
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        scale_words(w.hdr[rr], 0, scw[rr][0], mw[rr][0]);
+        scale_words(w.hdr[rr], 1, scw[rr][1], mw[rr][1]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int h2 = j >> 2, jj = j & 3, pp = (jj >> 1) * 2, sh = 4 * (jj & 1);
+        const uint32_t a0 = (w.q[h2][0][pp] >> sh) & LO, a1 = (w.q[h2][1][pp] >> sh) & LO;
+        const uint32_t a2 = (w.q[h2][0][pp + 1] >> sh) & LO, a3 = (w.q[h2][1][pp + 1] >> sh) & LO;
+        const uint32_t b0 = bt ? lds32(ab + 32u * j) : 0u, b1 = bt ? lds32(ab + 32u * j + 16u) : 0u;
+        int dd[4];
+        mma_k32_u8s8(dd, a0, a1, a2, a3, b0, b1);
+        const int s0 = byte_u(scw[0][h2], jj), s1 = byte_u(scw[1][h2], jj);
+        isum[0] += s0 * dd[0];
+        isum[1] += s0 * dd[1];
+        isum[2] += s1 * dd[2];
+        isum[3] += s1 * dd[3];
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int t = 2 * cq + k;
+        if (t < ntok) {
+            const uint32_t so = sums + (uint32_t)t * tstride;
+            const uint4 S0 = lds128(so), S1 = lds128(so + 16u);  // the 8 sub-block sums
+            const int Sv[8] = {(int)S0.x, (int)S0.y, (int)S0.z, (int)S0.w, (int)S1.x, (int)S1.y, (int)S1.z, (int)S1.w};
+            const float d8 = __uint_as_float(lds32(d8s + (uint32_t)t * tstride));
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                int msum = 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) msum += byte_u(mw[rr][j >> 2], j & 3) * Sv[j];
+                const float dw = half_lo(w.hdr[rr].x), dmw = half_hi(w.hdr[rr].x);
+                float a = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k]), acc[rr * 2 + k]);
+                acc[rr * 2 + k] = fmaf(-(dmw * d8), static_cast<float>(msum), a);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void mma_fold(const MmaQ6 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
+                                         uint32_t d8s, uint32_t tstride, float (&acc)[4]) {
+    constexpr uint32_t LO = 0x0F0F0F0Fu, HB = 0x30303030u;
+    const bool bt = gq < ntok;
+    const uint32_t ab = act + (uint32_t)gq * tstride + 4u * cq;
+    int isum[4] = {0, 0, 0, 0};
+    const uint32_t scv[2][4] = {{w.sc[0].x, w.sc[0].y, w.sc[0].z, w.sc[0].w},
+                                {w.sc[1].x, w.sc[1].y, w.sc[1].z, w.sc[1].w}};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            // group t of the half: piece t % 4 (low nibbles for t < 4), high
+            // bits from qh piece t % 2 at bit 2 (t / 2 % 2) + 4 (t / 4)
+            const int pc = t & 3, pq = t & 1, ns = t < 4 ? 0 : 4;
+            uint32_t a[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const uint32_t lo = (w.ql[h2][rr][pc] >> ns) & LO;
+                const uint32_t qh = w.qh[h2][rr][pq];
+                const int sel = t >> 1;  // 0: << 4, 1: << 2, 2: as is, 3: >> 2
+                const uint32_t hb = sel == 0 ? (qh << 4) : (sel == 1 ? (qh << 2) : (sel == 2 ? qh : (qh >> 2)));
+                a[rr] = lo | (hb & HB);
+            }
+            const uint32_t b0 = bt ? lds32(ab + 128u * h2 + 16u * t) : 0u;
+            int dd[4];
+            mma_k16_u8s8(dd, a[0], a[1], b0);
+            const int grp = 8 * h2 + t;
+            const int s0 = byte_s(scv[0][grp >> 2], grp & 3), s1 = byte_s(scv[1][grp >> 2], grp & 3);
+            isum[0] += s0 * dd[0];
+            isum[1] += s0 * dd[1];
+            isum[2] += s1 * dd[2];
+            isum[3] += s1 * dd[3];
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int t = 2 * cq + k;
+        if (t < ntok) {
+            const uint32_t so = sums + (uint32_t)t * tstride;
+            const uint4 B0 = lds128(so), B1 = lds128(so + 16u);  // the 16 int16 bsums
+            const uint32_t bw[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
+            const float d8 = __uint_as_float(lds32(d8s + (uint32_t)t * tstride));
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                int bacc = 0;
+#pragma unroll
+                for (int grp = 0; grp < 16; ++grp)
+                    bacc += byte_s(scv[rr][grp >> 2], grp & 3) * half_s(bw[grp >> 1], grp & 1);
+                const float dw = half_lo(w.d[rr]);
+                acc[rr * 2 + k] = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k] - 32 * bacc), acc[rr * 2 + k]);
+            }
+        }
+    }
+}
 
 // ---------------------------------------------------------------------------
 // ---------------------------------------------------------------------------
@@ -653,12 +836,18 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
     float acc[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) acc[t] = 0.0f;
+    constexpr bool MMA = MmaFold<F, T>::on;
+    using MItem = typename std::conditional<F == FMT_Q6_K, MmaQ6, MmaQ4>::type;
+    const int gq = lane >> 2, cq = lane & 3;
+    float macc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
     for (int64_t it = w0; it < w1; ++it) {
         stage_wait(&bars[rs], rph);
         const uint32_t st = ring_s + rs * SLOT;
         Item cur;
-        item_read(cur, st, lo, h);
+        MItem mcur;
+        if constexpr (MMA) mma_read(mcur, st, gq, cq);
+        else item_read(cur, st, lo, h);
         // every lane's reads of the stage are done before it is refilled
         __syncwarp();
         if (lane == 0 && iit < w1) sm100::fence_proxy_async_smem();
@@ -673,6 +862,8 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
             const float d8 = __uint_as_float(lds32(d_cur));
             acc[0] = fmaf(item_d(cur) * d8, static_cast<float>(isum), acc[0]);
             if constexpr (F != FMT_Q6_K) acc[0] = fmaf(-(item_dmin(cur) * d8), static_cast<float>(msum), acc[0]);
+        } else if constexpr (MMA) {
+            mma_fold(mcur, gq, cq, ntok, a_cur - 128u * h, s_cur - 16u * h, d_cur, tstride, macc);
         } else {
             const float dw = item_d(cur), dmw = item_dmin(cur);
 #pragma unroll
@@ -700,6 +891,22 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                     if (h == 0 && n < s_n[m]) s_y[m][n] = v;
                 } else if (h == 0) {
                     s_rec[warp][g * nsb < w0 ? 0 : 1][0][r16] = v;
+                }
+            } else if constexpr (MMA) {
+                // each (row, token) sum is one lane's: no halves to add
+                const bool whole = g * nsb >= w0 && (g + 1) * nsb <= w1;
+                const int64_t nb = (g - s_gpre[m]) * GROUP_ROWS;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int row = gq + 8 * (q >> 1), t = 2 * cq + (q & 1);
+                    if (t < ntok) {
+                        if (whole) {
+                            if (nb + row < s_n[m]) s_y[m][t * s_n[m] + nb + row] = macc[q];
+                        } else {
+                            s_rec[warp][g * nsb < w0 ? 0 : 1][t][row] = macc[q];
+                        }
+                    }
+                    macc[q] = 0.0f;
                 }
             } else {
                 const bool whole = g * nsb >= w0 && (g + 1) * nsb <= w1;
