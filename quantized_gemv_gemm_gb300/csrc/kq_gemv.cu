@@ -459,7 +459,7 @@ __device__ __forceinline__ void mma_fold(const MmaQ6 &w, int gq, int cq, int nto
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
             // group t of the half: piece t % 4 (low nibbles for t < 4), high
-            // bits from qh piece t % 2 at bit 2 (t / 2 % 2) + 4 (t / 4)
+            // bits from qh piece t % 2 at bits 2 (t / 2), +1 of each byte
             const int pc = t & 3, pq = t & 1, ns = t < 4 ? 0 : 4;
             uint32_t a[2];
 #pragma unroll
