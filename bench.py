@@ -357,52 +357,29 @@ def run_ours(args, world, rank, local):
                   for names, t, b in zip(layers.GROUPS, mean_ms, alg)]
     traffic = recorded_traffic("gemv_decode_layer")
 
-    # end to end through the public API: every step copies its activations in
-    # from pinned host memory, runs the layer and copies all its outputs back.
-    # The copies run on their own streams into NBUF rotating device rows, so
-    # step l's inputs arrive while earlier steps compute and its outputs leave
-    # while later steps compute (the copy into a buffer waits for the step
-    # that last used it); replayed from a graph
+    # end to end through the public API: every step copies its four input
+    # rows in from pinned host memory (kq_copy_in: a kernel of the launch
+    # chain that reads the host rows before its dependency wait) and the four
+    # GEMV launches store all seven outputs straight into pinned host memory.
+    # Two rotating input/output buffers, so a step's host outputs are never
+    # overwritten while an earlier step may still be writing them; replayed
+    # from a graph.  (Copy-engine copies on side streams with event waits
+    # measured 2.31 TB/s: each cross-stream wait breaks the early launch.)
     x_host = torch.from_numpy(np.concatenate(
         [synth.activations(1, k, synth.rng_for(1, 7000 + j))[0] for j, (_, k) in enumerate(LAYER_INPUTS)])).pin_memory()
-    NBUF = 2    # (3 or 4 measured no faster: the waits on the copies, not their slack, cost the time)
+    NBUF = 2
     y_host = [torch.empty(layers.y_total, dtype=torch.float32).pin_memory() for _ in range(NBUF)]
     x_dev = [torch.empty(layers.x_total, dtype=torch.float32, device="cuda") for _ in range(NBUF)]
-    y_dev = [torch.empty(layers.y_total, dtype=torch.float32, device="cuda") for _ in range(NBUF)]
     xo = np.cumsum([0] + [k for _, k in LAYER_INPUTS])
     yo = np.cumsum([0] + [m.N for m in layers.mats])
     x_views = [[xd[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))] for xd in x_dev]
-    y_views = [[yd[yo[i]:yo[i + 1]] for i in range(len(layers.mats))] for yd in y_dev]
-    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+    y_views = [[yh[yo[i]:yo[i + 1]] for i in range(len(layers.mats))] for yh in y_host]
 
     def e2e_rot():
-        cur = torch.cuda.current_stream()
-        fork = torch.cuda.Event()
-        fork.record(cur)
-        h2d_s.wait_event(fork)
-        d2h_s.wait_event(fork)
-        done_c, done_d = {}, {}
         for l in range(G):
             b = l % NBUF
-            if l >= NBUF:
-                h2d_s.wait_event(done_c[l - NBUF])    # step l-NBUF has read x_dev[b]
-            with torch.cuda.stream(h2d_s):
-                x_dev[b].copy_(x_host, non_blocking=True)
-            arrived = torch.cuda.Event()
-            arrived.record(h2d_s)
-            cur.wait_event(arrived)
-            if l >= NBUF:
-                cur.wait_event(done_d[l - NBUF])      # y_dev[b] of step l-NBUF is back on the host
+            kq.kq_copy_in(x_host, x_dev[b])
             layers.step(l % L, x_override=x_views[b], y_override=y_views[b])
-            done_c[l] = torch.cuda.Event()
-            done_c[l].record(cur)
-            d2h_s.wait_event(done_c[l])
-            with torch.cuda.stream(d2h_s):
-                y_host[b].copy_(y_dev[b], non_blocking=True)
-            done_d[l] = torch.cuda.Event()
-            done_d[l].record(d2h_s)
-        cur.wait_stream(h2d_s)
-        cur.wait_stream(d2h_s)
 
     g_e2e = graph_of(torch, e2e_rot)
     for _ in range(warm_reps):
@@ -461,9 +438,10 @@ def run_ours(args, world, rank, local):
                               "how": "4 kq_quantize_q8k + 7 kq_gemv launches per step"},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": 4 * layers.x_total, "d2h_bytes_per_step": 4 * layers.y_total,
-                    "how": "graph replay of, every step: H2D of the 4 fp32 inputs from pinned memory, 4 "
-                           "kq_gemv_fused launches, D2H of all 7 outputs; the copies on their own streams into "
-                           f"{NBUF} rotating device buffers, overlapping the neighbouring steps' compute"},
+                    "how": "graph replay of, every step: kq_copy_in of the 4 fp32 input rows from pinned host "
+                           "memory (a kernel in the launch chain, reading the host rows before its dependency "
+                           "wait), 4 kq_gemv_fused launches storing all 7 outputs straight into pinned host "
+                           f"memory; {NBUF} rotating input/output buffers"},
             "gpu_launches": layers.launches_per_step() * steps,
             "clocks": clocks,
             "cpu_baseline": cpu,

@@ -189,7 +189,8 @@ int kq_gemv(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const 
  *           a matrix with N = 0 is skipped)
  *   K       shared inner dimension: a multiple of 256, at most 40960
  *   x       device float32 [K], 16-byte aligned, finite values
- *   y       host array of n_mats device pointers, y[m] float32 [N[m]]
+ *   y       host array of n_mats pointers, y[m] float32 [N[m]] in device
+ *           memory or in mapped pinned host memory (see kq_copy_in)
  *   workspace  NULL, or KQ_GEMV_WORKSPACE_BYTES as for kq_gemv
  * The host arrays are read during the call only.
  * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (n_mats out of range, null, K), KQ_ERR_ALIGN,
@@ -365,6 +366,25 @@ int kq_debug_wait_timeout(uint64_t limit_ns, cudaStream_t s);
  * Errors: KQ_ERR_ARG for blocks < 0, iters < 0 or a null out; KQ_ERR_LAUNCH.
  */
 int kq_measure_mma_s8(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s);
+
+/*
+ * Transport, not part of the method: copy a step's input rows from pinned
+ * host memory into device memory with a kernel in the stream's launch chain,
+ * so that under KQ_LAUNCH_PDL the copy needs no copy engine and no
+ * cross-stream event (either breaks the chain's early launch).  The kernel
+ * reads src BEFORE its dependency wait and writes dst after it: src must
+ * not be written by earlier kernels in the stream (host-produced data,
+ * ready when the call is made), while dst may still be read by them.
+ *   src    pinned host memory mapped into the device address space (page-
+ *          locked by cudaHostAlloc or cudaHostRegister on a system with
+ *          unified addressing), or device memory; 16-byte aligned
+ *   dst    device memory, 16-byte aligned, not overlapping src
+ *   bytes  a multiple of 16 (at most 2^40)
+ * The outputs of the GEMV entry points may likewise be pinned host memory:
+ * the kernels store the results there directly.
+ * Errors: KQ_ERR_ARG (bytes, null), KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ */
+int kq_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s);
 
 /*
  * Launch options, process-wide (a plain atomic word; the new value applies

@@ -287,6 +287,14 @@ int kq_measure_mma_s8(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t 
     return launch_status(launch_mma_s8_rate(blocks, iters, out, s));
 }
 
+int kq_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s) {
+    if (bytes % 16 != 0 || bytes > ((size_t)1 << 40)) return KQ_ERR_ARG;
+    if (bytes == 0) return KQ_OK;
+    if (!src || !dst) return KQ_ERR_ARG;
+    if (!aligned(src, 16) || !aligned(dst, 16)) return KQ_ERR_ALIGN;
+    return launch_status(launch_copy_in(src, dst, bytes, s));
+}
+
 unsigned kq_set_launch_flags(unsigned flags) {
     return g_launch_flags.exchange(flags & (KQ_LAUNCH_PDL | KQ_LAUNCH_GEMV_SPLIT), std::memory_order_relaxed);
 }

@@ -84,6 +84,7 @@ cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_mma_s8_rate(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s);
+cudaError_t launch_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s);
 cudaError_t launch_debug_decode(int f, const void *packed, int64_t N, int64_t K, int32_t *q,
                                 int32_t *sc, int32_t *mn, float *d, float *dmin, cudaStream_t s);
 

@@ -55,6 +55,7 @@ _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
 _lib.kq_measure_mma_s8.argtypes = [_I64, _I64, _P, _P]
+_lib.kq_copy_in.argtypes = [_P, _P, _SZ, _P]
 _lib.kq_debug_wait_timeout.argtypes = [ctypes.c_uint64, _P]
 _lib.kq_quantize_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_gemv_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
@@ -66,7 +67,7 @@ _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
            "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout",
-           "kq_gemv_q8_0_fused"):
+           "kq_gemv_q8_0_fused", "kq_copy_in"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -111,6 +112,14 @@ def _need_cuda(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError("libkq takes contiguous CUDA tensors")
+
+
+def _need_out(*ts):
+    """Outputs: contiguous CUDA tensors, or pinned host tensors (the kernel
+    stores into the mapped host memory)."""
+    for t in ts:
+        if t is not None and (not t.is_contiguous() or not (t.is_cuda or (t.device.type == "cpu" and t.is_pinned()))):
+            raise ValueError("libkq outputs are contiguous CUDA or pinned host tensors")
 
 
 def kq_block_bytes(fmt: int) -> int:
@@ -203,7 +212,7 @@ def kq_gemv_fused(fmt: int, packed_list, N_list, K: int, x: torch.Tensor, y_list
         raise ValueError("x must be float32")
     if y_list is None:
         y_list = [torch.empty(int(N), dtype=torch.float32, device=x.device) for N in N_list]
-    _need_cuda(*y_list)
+    _need_out(*y_list)
     pk = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in packed_list])
     nn = (ctypes.c_int64 * max(n, 1))(*[int(v) for v in N_list])
     yy = (ctypes.c_void_p * max(n, 1))(*[t.data_ptr() for t in y_list])
@@ -415,3 +424,16 @@ def kq_get_launch_flags() -> int:
 def raw():
     """The ctypes handle of libkq.so, for callers that pass raw pointers."""
     return _lib
+
+
+def kq_copy_in(src: torch.Tensor, dst: torch.Tensor, stream=None) -> torch.Tensor:
+    """Copy the pinned host tensor src into the device tensor dst (same number
+    of bytes, a multiple of 16) with a kernel of the stream's launch chain."""
+    if src.device.type != "cpu" or not src.is_pinned() or not src.is_contiguous():
+        raise ValueError("src must be a contiguous pinned host tensor")
+    _need_cuda(dst)
+    n = src.numel() * src.element_size()
+    if not dst.is_contiguous() or dst.numel() * dst.element_size() != n:
+        raise ValueError("dst must be a contiguous device tensor of the same size")
+    _check(_lib.kq_copy_in(_ptr(src), _ptr(dst), n, _stream(stream)), "kq_copy_in")
+    return dst

@@ -895,3 +895,68 @@ def test_gemv_fused_batch_layer_shapes(K, M):
         planes = oracle_q8k(x)
         for m, d, y in zip(ms, disks, ys):
             assert_row_tol(y.cpu().numpy(), oracle.gemm(m.fmt, d, *planes))
+
+
+# ---------------------------------------------------------------- host transport
+def test_copy_in_from_pinned_host(K):
+    """kq_copy_in moves pinned host bytes into device memory exactly, for
+    sizes that leave partial blocks and partial vectors of the copy grid."""
+    g = torch.Generator().manual_seed(7)
+    for n in (4, 516, 4096 + 12, 18944):
+        src = torch.randint(-2**31, 2**31 - 1, (n,), dtype=torch.int32, generator=g).pin_memory()
+        full, dst = poisoned((n,))
+        K.kq_copy_in(src, dst.view(torch.int32))
+        torch.cuda.synchronize()
+        assert torch.equal(dst.view(torch.int32).cpu(), src)
+        check_guard(full, n)  # nothing written past the end
+
+
+def test_copy_in_chain_under_pdl(K):
+    """Under programmatic dependent launch kq_copy_in reads the host rows
+    early but overwrites the device row only after the GEMV before it (which
+    reads that row) has finished: every output equals the plain launches',
+    and each against the oracle on its own row."""
+    fmt, N, Kdim = synth.Q4_K, 300, 2560
+    rng = synth.rng_for(131, 0)
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    packed = pack(K, fmt, disk)
+    rows = synth.activations(4, Kdim, rng, outliers=True)
+    hosts = [torch.from_numpy(rows[i].copy()).pin_memory() for i in range(4)]
+    x_dev = torch.empty(Kdim, dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+
+    def chain():
+        outs = []
+        for i in range(4):
+            K.kq_copy_in(hosts[i], x_dev)
+            outs.append(K.kq_gemv_fused(fmt, [packed], [N], Kdim, x_dev)[0])
+        torch.cuda.synchronize()
+        return torch.stack(outs).cpu().numpy()
+
+    old = K.kq_set_launch_flags(0)
+    try:
+        plain = chain()
+        K.kq_set_launch_flags(K.KQ_LAUNCH_PDL)
+        pdl = chain()
+    finally:
+        K.kq_set_launch_flags(old)
+    np.testing.assert_array_equal(pdl, plain)
+    planes = oracle_q8k(rows)
+    assert_row_tol(pdl, oracle.gemm(fmt, disk, *planes))
+
+
+def test_gemv_fused_writes_pinned_host_outputs(K):
+    """The fused GEMV stores into pinned host outputs directly: the same bits
+    as device outputs, nothing written past the rows."""
+    fmt, Kdim, Ns = synth.Q6_K, 9728, [2560]
+    rng = synth.rng_for(132, 0)
+    disk = synth.disk_weights(fmt, Ns[0], Kdim, rng)
+    packed = pack(K, fmt, disk)
+    x = to_dev(synth.activations(1, Kdim, rng)[0])
+    y_dev = K.kq_gemv_fused(fmt, [packed], Ns, Kdim, x)[0]
+    y_host = torch.full((Ns[0] + 16,), float("nan"), dtype=torch.float32).pin_memory()
+    K.kq_gemv_fused(fmt, [packed], Ns, Kdim, x, [y_host[:Ns[0]]])
+    torch.cuda.synchronize()
+    assert torch.equal(y_host[:Ns[0]], y_dev.cpu())
+    assert bool(torch.isnan(y_host[Ns[0]:]).all())
+

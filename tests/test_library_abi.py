@@ -80,6 +80,11 @@ def test_host_argument_checks(kq):
     assert lib.kq_gemv_q8_0(None, 8, 256, fake, fake, fake, None) == ARG
     assert lib.kq_gemv_q8_0(odd, 8, 256, fake, fake, fake, None) == ALIGN
     assert lib.kq_gemv_q8_0(fake, 8, 256, fake, odd, fake, None) == ALIGN
+    assert lib.kq_copy_in(fake, fake, 24, None) == ARG
+    assert lib.kq_copy_in(None, None, 0, None) == 0
+    assert lib.kq_copy_in(None, fake, 32, None) == ARG
+    assert lib.kq_copy_in(odd, fake, 32, None) == ALIGN
+    assert lib.kq_copy_in(fake, odd, 32, None) == ALIGN
     assert lib.kq_gemv_q8_0_fused(fake, 8, 200, fake, fake, None) == ARG
     assert lib.kq_gemv_q8_0_fused(fake, 8, 256 * 161, fake, fake, None) == ARG
     assert lib.kq_gemv_q8_0_fused(None, 0, 256, None, None, None) == 0
