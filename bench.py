@@ -7,9 +7,9 @@ Q8_K quantization of the layer's four GEMV inputs, then the seven GEMVs.
 Steps rotate over L distinct copies of the layer's weights (8 by default,
 505 MB, about 4x the 126 MB L2) so that every step streams its weights from
 HBM, as consecutive layers of a model do.  `value` = weight bytes streamed
-per second (GB/s), timed on the device with CUDA events around K steps
-replayed from CUDA graphs of 32 layer steps (about one decode pass of a
-36-layer model).
+per second (GB/s), timed on the device with CUDA events around regions of
+exactly K steps replayed from CUDA graphs, repeated until the regions cover
+at least 100 ms; the median region gives the value.
 
 Also reported: the same metric end to end (activations copied in from pinned
 host memory and outputs copied back every step), the roofline of the GEMV
@@ -158,6 +158,23 @@ LAYER_INPUTS = [("x_attn", 2560), ("x_o", 4096), ("x_ffn", 2560), ("x_down", 972
 # rotations of the layer copies captured in one CUDA graph (4 x 8 = 32 layer
 # steps, about one decode pass of a 36-layer model)
 GRAPH_ROTATIONS = 4
+# largest graph of headline steps (a region of K steps replays it K // G
+# times, then a graph of the remainder)
+GRAPH_MAX_STEPS = 256
+DEFAULT_LAYER_COPIES = 8
+
+
+def headline_config(world: int, layer_copies: int = DEFAULT_LAYER_COPIES):
+    """The headline workload, shared by both arms' JSON lines."""
+    mats = synth.configs()[1].matrices
+    wb = sum(m.weight_bytes for m in mats)
+    return {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
+            "M": 1, "hidden": 2560,
+            "matrices": [f"{m.name} {synth.FORMAT_NAMES[m.fmt]} {m.N}x{m.K}" for m in mats],
+            "weight_bytes_per_step": wb, "layer_copies": layer_copies,
+            "l2": f"inputs larger than L2: step i reads layer copy i % {layer_copies}, "
+                  f"{wb * layer_copies / 1e6:.1f} MB of weights in all",
+            "parallelism": f"replicas x{world}"}
 # matrix -> index of its input
 LAYER_USES = {"wq": 0, "wk": 0, "wv": 0, "wo": 1, "gate": 2, "up": 2, "down": 3}
 
@@ -246,6 +263,45 @@ def job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
     return units_per_rank * world / (ms_max * 1e-3)
 
 
+# timed regions: each holds exactly the work asked for (K steps for the
+# headline); a region is repeated until the regions together cover at least
+# MIN_TIMED_MS, and the median region is reported
+MIN_TIMED_MS = 100.0
+MIN_REGIONS = 5
+MAX_REGIONS = 5000
+SPIN_CYCLES = 100_000   # ~50 us spin before each start event
+
+
+def time_regions(torch, run, barrier=None, min_ms=MIN_TIMED_MS, min_regions=MIN_REGIONS):
+    """ms of each of R regions of `run()` (R >= min_regions, together >=
+    min_ms).  Per region: barrier, synchronize, a short spin kernel (so the
+    start event is recorded while the GPU is still busy and the submission of
+    the region's work is not inside it), events around run(), synchronize,
+    barrier.  Returns the list of region times."""
+    times = []
+    while True:
+        if barrier is not None:
+            barrier()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(SPIN_CYCLES)
+        a.record()
+        run()
+        b.record()
+        torch.cuda.synchronize()
+        if barrier is not None:
+            barrier()
+        times.append(a.elapsed_time(b))
+        if len(times) >= MAX_REGIONS or (len(times) >= min_regions and sum(times) >= min_ms):
+            return times
+
+
+def region_summary(times):
+    return {"regions": len(times), "median_ms": round(float(statistics.median(times)), 5),
+            "min_ms": round(float(min(times)), 5), "max_ms": round(float(max(times)), 5),
+            "total_ms": round(float(sum(times)), 3)}
+
+
 def graph_of(torch, fn):
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -277,11 +333,27 @@ def run_ours(args, world, rank, local):
     L = args.layers
     layers = DecodeLayers(kq, torch, L)
     NG = len(layers.GROUPS)
-    # one graph holds GRAPH_STEPS layer steps (the layer copies in rotation),
-    # as one decode pass of a 36-layer model is one graph
-    G = GRAPH_ROTATIONS * L
-    g_plain = graph_of(torch, lambda: [layers.step(l % L) for l in range(G)])
-    g_sep = graph_of(torch, lambda: [layers.step(l % L, fused=False) for l in range(G)])
+    # a timed region holds exactly K = args.steps layer steps (step i reads
+    # layer copy i % L), replayed from CUDA graphs of at most GRAPH_MAX_STEPS
+    # steps plus one graph of the remainder
+    K = args.steps
+    G = min(K, GRAPH_MAX_STEPS)
+    n_full, rem = divmod(K, G)
+
+    def region_graphs(step_fn):
+        gs = [graph_of(torch, lambda: [step_fn(l % L) for l in range(G)])]
+        if rem:
+            gs.append(graph_of(torch, lambda: [step_fn((n_full * G + l) % L) for l in range(rem)]))
+        return gs
+
+    def replay_region(gs):
+        for _ in range(n_full):
+            gs[0].replay()
+        if rem:
+            gs[1].replay()
+
+    g_plain = region_graphs(lambda l: layers.step(l))
+    g_sep = region_graphs(lambda l: layers.step(l, fused=False))
 
     # events around every launch of every step of one rotation
     def timing_event():
@@ -298,37 +370,24 @@ def run_ours(args, world, rank, local):
         ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in range(NG)] for _ in range(L)]
 
-    reps = max(1, args.steps // G)
-    steps = reps * G
-    warm_reps = max(1, -(-args.warmup // G))
-    for _ in range(warm_reps):
-        g_plain.replay()
-        g_sep.replay()
+    # W untimed warm-up steps (after the graphs' own set-up passes)
+    for l in range(args.warmup):
+        layers.step(l % L)
     torch.cuda.synchronize()
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    def timed(graph, n):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        torch.cuda.synchronize()
-        a.record()
-        for _ in range(n):
-            graph.replay()
-        b.record()
-        torch.cuda.synchronize()
-        barrier()
-        return a.elapsed_time(b)
-
     with ClockSampler(local) as clk:
-        ms = timed(g_plain, reps)
-        ms_sep = timed(g_sep, max(1, reps // 2))
+        regions = time_regions(torch, lambda: replay_region(g_plain), barrier)
+        regions_sep = time_regions(torch, lambda: replay_region(g_sep), barrier, min_ms=MIN_TIMED_MS / 2)
+        ms = float(statistics.median(regions))
+        ms_sep = float(statistics.median(regions_sep))
         # kernel-timing pass: event nodes around each launch; the times of the
         # last rotation are read after each of a few replays
         kt = {j: [] for j in range(NG)}
-        for _ in range(max(3, min(50, reps // 4))):
+        for _ in range(10):
             if graph_events:
                 g_timed.replay()
             else:
@@ -342,9 +401,10 @@ def run_ours(args, world, rank, local):
 
     ms_max = max_over_ranks(torch, ms, world)
     ms_sep = max_over_ranks(torch, ms_sep, world)
+    steps = K
     bytes_per_step = layers.weight_bytes
     value = job_rate(bytes_per_step * steps, world, ms_max) / 1e9
-    value_sep = bytes_per_step * max(1, reps // 2) * G * world / (ms_sep * 1e-3) / 1e9
+    value_sep = job_rate(bytes_per_step * steps, world, ms_sep) / 1e9
 
     # roofline of the GEMV kernel: the timed region holds nothing but its
     # launches (4 per step), so its average launch duration is the region's
@@ -375,26 +435,18 @@ def run_ours(args, world, rank, local):
     x_views = [[xd[xo[j]:xo[j + 1]].view(1, -1) for j in range(len(LAYER_INPUTS))] for xd in x_dev]
     y_views = [[yh[yo[i]:yo[i + 1]] for i in range(len(layers.mats))] for yh in y_host]
 
-    def e2e_rot():
-        for l in range(G):
-            b = l % NBUF
-            kq.kq_copy_in(x_host, x_dev[b])
-            layers.step(l % L, x_override=x_views[b], y_override=y_views[b])
+    def e2e_step(i):
+        b = i % NBUF
+        kq.kq_copy_in(x_host, x_dev[b])
+        layers.step(i % L, x_override=x_views[b], y_override=y_views[b])
 
-    g_e2e = graph_of(torch, e2e_rot)
-    for _ in range(warm_reps):
-        g_e2e.replay()
+    g_e2e = region_graphs(e2e_step)
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_reps = max(1, reps // 2)
-    barrier()
-    e0.record()
-    for _ in range(e_reps):
-        g_e2e.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    e_ms = max_over_ranks(torch, e0.elapsed_time(e1), world)
-    e2e_value = job_rate(bytes_per_step * e_reps * G, world, e_ms) / 1e9
+    e_regions = time_regions(torch, lambda: replay_region(g_e2e), barrier, min_ms=MIN_TIMED_MS / 2)
+    e_ms = max_over_ranks(torch, float(statistics.median(e_regions)), world)
+    e2e_value = job_rate(bytes_per_step * steps, world, e_ms) / 1e9
     y_check = np.concatenate([yh.numpy() for yh in y_host])
     assert np.isfinite(y_check).all()
 
@@ -411,20 +463,18 @@ def run_ours(args, world, rank, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-            "steps": steps, "warmup": warm_reps * G, "ms_per_step": round(ms_max / steps, 6),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_max / steps, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic (seeded random K-quant superblocks and N(0,1) activations)",
-            "config": {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
-                       "M": 1, "hidden": 2560,
-                       "matrices": [f"{m.name} {synth.FORMAT_NAMES[m.fmt]} {m.N}x{m.K}" for m in layers.mats],
-                       "weight_bytes_per_step": bytes_per_step, "layer_copies": L,
-                       "l2": f"inputs larger than L2: {L} rotating layer copies, "
-                             f"{bytes_per_step * L / 1e6:.1f} MB of weights",
-                       "timing": f"CUDA events around graph replays of {G} layer steps each, K steps in all",
-                       "pdl": not args.no_pdl,
-                       "parallelism": f"replicas x{world}"},
+            "config": headline_config(world, L),
+            "timing": {"how": f"each timed region is exactly K = {steps} layer steps, replayed from CUDA graphs "
+                              f"(of at most {GRAPH_MAX_STEPS} steps) with programmatic dependent launch "
+                              f"{'on' if not args.no_pdl else 'off'}; CUDA events on the launching stream, a "
+                              f"short spin kernel before each start event; regions repeated until they cover "
+                              f">= {MIN_TIMED_MS:.0f} ms; value and ms_per_step from the median region",
+                       **region_summary(regions)},
             "roofline": {"bound": "hbm", "kernel": "kq gemv_kernel (fused quantize + GEMV, 4 launches per step)",
-                         "timing": "CUDA events around the K graph-replayed steps (only gemv_kernel launches)",
+                         "timing": "the headline's median region of K steps (only gemv_kernel launches in it)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4),
                          "peak_source": f"{peaks['source']} hbm_gbs (STREAM-style copy)",
@@ -441,7 +491,8 @@ def run_ours(args, world, rank, local):
                     "how": "graph replay of, every step: kq_copy_in of the 4 fp32 input rows from pinned host "
                            "memory (a kernel in the launch chain, reading the host rows before its dependency "
                            "wait), 4 kq_gemv_fused launches storing all 7 outputs straight into pinned host "
-                           f"memory; {NBUF} rotating input/output buffers"},
+                           f"memory; {NBUF} rotating input/output buffers; regions of exactly K steps as for "
+                           f"the headline, median of {len(e_regions)}"},
             "gpu_launches": layers.launches_per_step() * steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -485,14 +536,7 @@ def bench_small_batch(kq, torch, layers, peaks, args):
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        reps = max(3, min(100, args.steps // (8 * G)))
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) * 1e3 / (reps * G)
+        us = statistics.median(time_regions(torch, g.replay, min_ms=50)) * 1e3 / G
         gbs = layers.weight_bytes / (us * 1e-6) / 1e9
         out.append({"M": M, "us_per_step": round(us, 3), "weight_gbs": round(gbs, 1),
                     "frac_of_hbm": round(gbs / hbm, 4), "tokens_per_s": round(M / (us * 1e-6), 1),
@@ -546,14 +590,8 @@ def bench_moe_decode(kq, torch, peaks, args):
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    reps = max(3, min(100, args.steps // (4 * S)))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / (reps * S)
+    times = time_regions(torch, g.replay, min_ms=50)
+    us = statistics.median(times) * 1e3 / S
     step_bytes = topk * sum(per)
     gbs = step_bytes / (us * 1e-6) / 1e9
     hbm = float(peaks["hbm_gbs"])
@@ -563,7 +601,7 @@ def bench_moe_decode(kq, torch, peaks, args):
                         "down Q6_K 2048x768 (2 kq_gemv_grouped_fused launches per step)",
             "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
             "expert_bytes_per_step": step_bytes,
-            "timing": f"CUDA events around {reps} graph replays of {S} steps, each step routed to 8 fresh experts "
+            "timing": f"median of {len(times)} timed graph replays of {S} steps, each step routed to 8 fresh experts "
                       f"(experts {E * sum(per) / 1e6:.0f} MB)"}
 
 
@@ -603,21 +641,14 @@ def bench_q8_0(kq, torch, peaks, args):
             kq.kq_quantize_q8_0(h, d=dh, qs=qh)
             kq.kq_gemv_q8_0(c[2], 5120, 17408, dh, qh, y=ys[2])
 
-    reps = max(3, min(200, args.steps // (4 * C)))
-
     def timed(rot):
         g = graph_of(torch, rot)
         for _ in range(3):
             g.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            g.replay()
-        b.record()
-        torch.cuda.synchronize()
+        times = time_regions(torch, g.replay, min_ms=50)
         del g
-        return a.elapsed_time(b) * 1e3 / (reps * C)
+        return statistics.median(times) * 1e3 / C
 
     us = timed(rot_fused)
     us_split = timed(rot_split)
@@ -630,7 +661,8 @@ def bench_q8_0(kq, torch, peaks, args):
             "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
             "split_quantize_us_per_step": round(us_split, 3),
             "weight_bytes_per_step": step_bytes, "copies": C,
-            "timing": f"CUDA events around {reps} graph replays of {C} steps (weights {C * step_bytes / 1e6:.0f} MB)"}
+            "timing": f"median of >= {MIN_REGIONS} timed graph replays of {C} steps covering >= 50 ms "
+                      f"(weights {C * step_bytes / 1e6:.0f} MB)"}
 
 
 def bench_gemv_27b(kq, torch, peaks, args):
@@ -661,14 +693,8 @@ def bench_gemv_27b(kq, torch, peaks, args):
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    reps = max(3, min(200, args.steps // (4 * C)))
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(reps):
-        g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    us = a.elapsed_time(b) * 1e3 / (reps * C)
+    times = time_regions(torch, g.replay, min_ms=50)
+    us = statistics.median(times) * 1e3 / C
     gbs = step_bytes / (us * 1e-6) / 1e9
     hbm = float(peaks["hbm_gbs"])
     del copies, base, g
@@ -676,7 +702,8 @@ def bench_gemv_27b(kq, torch, peaks, args):
     return {"workload": "27B-shaped dense FFN at M=1 (Q4_K gate/up 17408x5120, down 5120x17408), 2 launches",
             "us_per_step": round(us, 3), "value": round(gbs, 1), "unit": "GB/s", "frac_of_hbm": round(gbs / hbm, 4),
             "weight_bytes_per_step": step_bytes, "copies": C,
-            "timing": f"CUDA events around {reps} graph replays of {C} steps (weights {C * step_bytes / 1e6:.0f} MB)"}
+            "timing": f"median of {len(times)} timed graph replays of {C} steps "
+                      f"(weights {C * step_bytes / 1e6:.0f} MB)"}
 
 
 # --------------------------------------------------------------------------
@@ -751,23 +778,16 @@ def bench_gemm(kq, torch, peaks, args):
 
     def time_it(fn, reps):
         """ms per call of fn(r): calls r = 0..reps-1 captured in one CUDA graph
-        (with the launch flags the headline uses), replayed three times; the
-        median replay."""
+        (with the launch flags the headline uses), replayed in timed regions
+        covering >= 100 ms; the median replay."""
         fn(0)
         torch.cuda.synchronize()
         g = graph_of(torch, lambda: [fn(r) for r in range(reps)])
         g.replay()
         torch.cuda.synchronize()
-        times = []
-        for _ in range(3):
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            g.replay()
-            b.record()
-            torch.cuda.synchronize()
-            times.append(a.elapsed_time(b) / reps)
+        times = time_regions(torch, g.replay, min_ms=100)
         del g
-        return float(statistics.median(times))
+        return float(statistics.median(times)) / reps
 
     def dense(name, cfg_index, mats, outliers):
         M = 512
@@ -795,7 +815,8 @@ def bench_gemm(kq, torch, peaks, args):
         ops = sum(2 * M * m.N * m.K for m in mats)
         tops = ops / (ms * 1e-3) / 1e12
         out.append({"workload": name, "M": M, "ms": round(ms, 4), "tops": round(tops, 2),
-                    "timing": f"median of 3 graph replays of {args.gemm_reps} steps, {copies} rotating weight copies",
+                    "timing": f"median of timed graph replays of {args.gemm_reps} steps (>= 100 ms in all), "
+                              f"{copies} rotating weight copies",
                     "frac_of_fp16_tensor_peak": round(tops / tc_peak, 4),
                     "frac_of_int8_tensor_peak": None if i8_peak is None else round(tops / i8_peak, 4),
                     "weight_gbs": round(sum(m.weight_bytes for m in mats) / (ms * 1e-3) / 1e9, 1)})
@@ -850,63 +871,88 @@ def bench_gemm(kq, torch, peaks, args):
 # --------------------------------------------------------------------------
 # CPU oracle (baseline / reference arm)
 
-def cpu_oracle_layer_rate(seconds: float, threads: int | None = None):
-    """GB/s of the oracle on the decode layer: repeat the full 7-matrix layer
-    (every output) until `seconds` of wall time have passed."""
-    import oracle
-    if threads:
-        oracle.set_num_threads(threads)
-    cfg = synth.configs()[1]
-    mats = []
-    for i, m in enumerate(cfg.matrices):
-        disk = synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(1, i))
-        x = synth.activations(1, m.K, synth.rng_for(1, 100 + i))
-        mats.append((m, disk, x))
-    layer_bytes = sum(m.weight_bytes for m in cfg.matrices)
-    t0 = time.perf_counter()
-    passes = 0
+REF_MIN_SECONDS = 10.0
+REF_MAX_SECONDS = 60.0
+
+
+class OracleLayers:
+    """The headline workload for the CPU oracle: the same seeded layer copies
+    (weights and input rows) as the GPU arm's DecodeLayers, in disk form."""
+
+    def __init__(self, n_copies: int = DEFAULT_LAYER_COPIES, seed_cfg: int = 1):
+        self.mats = synth.configs()[1].matrices
+        self.copies = []
+        for l in range(n_copies):
+            disks = [synth.disk_weights(m.fmt, m.N, m.K, synth.rng_for(seed_cfg, 1000 * l + i))
+                     for i, m in enumerate(self.mats)]
+            xs = [synth.activations(1, k, synth.rng_for(seed_cfg, 1000 * l + 100 + j))
+                  for j, (_, k) in enumerate(LAYER_INPUTS)]
+            self.copies.append((disks, xs))
+        self.weight_bytes = sum(m.weight_bytes for m in self.mats)
+
+    def step(self, i: int):
+        """One layer step with the oracle: quantize the four inputs, then the
+        seven products (every output)."""
+        import oracle
+        disks, xs = self.copies[i % len(self.copies)]
+        q = [oracle.quantize_q8k(x) for x in xs]
+        for m, disk in zip(self.mats, disks):
+            oracle.gemm(m.fmt, disk, *q[LAYER_USES[m.name]])
+
+
+def cpu_oracle_regions(layers: OracleLayers, steps: int, warmup: int, min_seconds: float, max_seconds: float):
+    """Times of regions of exactly `steps` oracle layer steps (after `warmup`
+    untimed steps), repeated until they cover min_seconds (at least 3
+    regions) or max_seconds has passed."""
+    for i in range(warmup):
+        layers.step(i)
+    times, i0, t_start = [], warmup, time.perf_counter()
     while True:
-        for m, disk, x in mats:
-            d8, q8, bs = oracle.quantize_q8k(x)
-            oracle.gemm(m.fmt, disk, d8, q8, bs)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    return layer_bytes * passes / el / 1e9, passes, el
+        t0 = time.perf_counter()
+        for i in range(steps):
+            layers.step(i0 + i)
+        times.append(time.perf_counter() - t0)
+        i0 += steps
+        if (len(times) >= 3 and sum(times) >= min_seconds) or time.perf_counter() - t_start >= max_seconds:
+            return times
 
 
 def cpu_baseline(seconds):
     import oracle
-    v, passes, el = cpu_oracle_layer_rate(seconds)
-    return {"value": round(v, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "host_cpus": os.cpu_count(),
-            "sample": f"{passes} full passes of the Qwen3-4B-shaped decode layer (7 matrices, every output), "
-                      f"{el:.1f} s wall, OpenMP over weight rows"}
+    layers = OracleLayers()
+    times = cpu_oracle_regions(layers, 32, 2, seconds, 3 * seconds)
+    el = float(statistics.median(times))
+    return {"value": round(layers.weight_bytes * 32 / el / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "host_cpus": os.cpu_count(),
+            "sample": f"{len(times)} regions of 32 layer steps of the headline workload (7 matrices, every output, "
+                      f"rotating over the same {len(layers.copies)} layer copies), {sum(times):.1f} s wall, median "
+                      f"region, OpenMP over weight rows"}
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
-    per_step = max(0.5, min(5.0, 60.0 / max(1, args.steps + args.warmup)))
-    for _ in range(args.warmup):
-        cpu_oracle_layer_rate(per_step)
-    vals, passes_total, el_total = [], 0, 0.0
-    for _ in range(args.steps):
-        v, p, el = cpu_oracle_layer_rate(per_step)
-        vals.append(v)
-        passes_total += p
-        el_total += el
-    value = sum(synth.configs()[1].matrices[i].weight_bytes for i in range(7)) * passes_total / el_total / 1e9
+    layers = OracleLayers()
+    steps = args.steps
+    # bounded: regions of exactly K steps until REF_MIN_SECONDS are covered
+    # (at least 3 regions), at most ~REF_MAX_SECONDS
+    times = cpu_oracle_regions(layers, steps, args.warmup, REF_MIN_SECONDS, REF_MAX_SECONDS)
+    el = float(statistics.median(times))
+    value = layers.weight_bytes * steps / el / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el_total / max(1, passes_total) * 1e3, 3),
+            "steps": steps, "warmup": args.warmup, "ms_per_step": round(el / steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
             "data": "synthetic (seeded random K-quant superblocks and N(0,1) activations)",
-            "config": {"workload": "Qwen3-4B-shaped decode layer, M=1 (Q4_K q/k/v/o/gate/up, Q6_K down)",
-                       "M": 1, "hidden": 2560, "step": "full layer passes of the CPU oracle for ~%.1f s" % per_step},
+            "config": headline_config(world),
+            "timing": {"how": "the CPU oracle (scalar C, OpenMP over weight rows) on the host cores: regions of "
+                              "exactly K layer steps after W untimed ones, repeated until "
+                              f"{REF_MIN_SECONDS:.0f} s are covered; "
+                              "value and ms_per_step from the median region",
+                       "regions": len(times), "median_ms": round(el * 1e3, 3), "total_s": round(sum(times), 2)},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-                             "sample": f"{passes_total} full layer passes over {args.steps} steps"},
+                             "sample": f"{len(times)} regions of {steps} layer steps (the headline workload, every "
+                                       f"output)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -914,10 +960,10 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=80000)
+    ap.add_argument("--steps", type=int, default=2048)
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--layers", type=int, default=8, help="rotating layer copies (weights > L2)")
+    ap.add_argument("--layers", type=int, default=DEFAULT_LAYER_COPIES, help="rotating layer copies (weights > L2)")
     ap.add_argument("--gemm-reps", type=int, default=20)
     ap.add_argument("--no-gemm", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -436,11 +436,14 @@ unsigned kq_get_launch_flags(void);
  * Limits and behaviour:
  *   - The scratch needed, kq_gemm_workspace_bytes(f, M, N, K), must not
  *     exceed KQ_NOALLOC_SCRATCH_BYTES; larger problems return
- *     KQ_ERR_TOO_LARGE before anything is enqueued (M*K up to about 15.9
- *     million activations, e.g. 512 tokens x K = 31744).
+ *     KQ_ERR_TOO_LARGE before anything is enqueued.  The scratch is about
+ *     2.14 bytes per activation, so M*K up to about 15.6 million
+ *     activations fit (e.g. 512 tokens x K = 30464; K = 30720 is refused).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept for the life of the
+ *     process: after a cudaDeviceReset the next call would reuse the old
+ *     one, so do not call it on a device that has been reset.
  *   - Every call on a device shares the one array, and the array keeps what
  *     the last call wrote; each call rewrites every scratch byte it reads,
  *     so nothing needs clearing.  Calls whose work may overlap on the GPU

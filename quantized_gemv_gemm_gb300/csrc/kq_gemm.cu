@@ -43,6 +43,7 @@
 
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
+#include <atomic>
 #include <mutex>
 
 namespace kq {
@@ -1139,13 +1140,17 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     if (!make_map_2d(&mb, b16, (uint64_t)(K / 16), (uint64_t)M, (uint64_t)(K / 16) * 2, 16, BT,
                      CU_TENSOR_MAP_SWIZZLE_32B))
         return cudaErrorInvalidValue;
-    static bool attr_set[4] = {false, false, false, false};
-    if (!attr_set[F]) {
+    // the shared-memory limit is a per-device attribute of the kernel: set it
+    // once on every device the process launches on
+    static std::atomic<bool> attr_set[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set[F] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     GemmParams p{};
     p.packed = static_cast<const uint8_t *>(packed);
@@ -1170,12 +1175,13 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     if (offsets && E > MAX_GROUPED_E) return cudaErrorNotSupported;
     int64_t blocks = tiles;
     if (offsets) {
-        static int sms[64] = {0};
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-        int &n_sm = sms[dev & 63];
-        if (!n_sm && cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return cudaErrorInvalidDevice;
+        static std::atomic<int> sms[64];
+        int n_sm = sms[dev].load(std::memory_order_relaxed);
+        if (!n_sm) {
+            if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sm <= 0)
+                return cudaErrorInvalidDevice;
+            sms[dev].store(n_sm, std::memory_order_relaxed);
+        }
         const int64_t need = (tiles + TILE_CAP - 3) / (TILE_CAP - 2);
         blocks = tiles < n_sm ? tiles : n_sm;
         if (blocks < need) blocks = need;

@@ -51,6 +51,7 @@
 // wait the block stages the activation row in shared memory (copied from
 // the Q8_K planes, or quantized from the fp32 row bit-identically to
 // kq_quantize_q8k) with the sums the fold needs.
+#include <atomic>
 #include <type_traits>
 
 #include "kq_internal.h"
@@ -985,15 +986,15 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
 }
 
 static int sm_count() {
-    static int cached[64] = {0};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
-    if (!cached[dev]) {
-        int v = 0;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (!v) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
-        cached[dev] = v;
+        cached[dev].store(v, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return v;
 }
 
 // Above this many items per SM a launch takes two blocks per SM (more warps
@@ -1072,10 +1073,11 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
     if (D < 2) D = 2;
     p.D = (int)D;
     const size_t smem = (size_t)(8 * D * GemvFmt<F>::SLOT + stage_bytes);
-    static bool attr_set[64][4][9][2] = {};
+    // per-device attributes of this instantiation, set once on every device
+    static std::atomic<bool> attr_set[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
-    if (!attr_set[dev][F][T][GR]) {
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         // the largest this instantiation may ask for (a launch asks for what it uses)
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)((T > 1 || GR) ? GEMV_BATCH_MAX_SMEM : GEMV_SMEM_BUDGET));
@@ -1083,7 +1085,7 @@ static cudaError_t launch_gemv_t(GemvParams p, void *ws, size_t ws_bytes, cudaSt
         e = cudaFuncSetAttribute(gemv_kernel<F, T, GR>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        attr_set[dev][F][T][GR] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);

@@ -4,6 +4,8 @@
 // source pages have no counterpart of this entry point.
 #include "kq_internal.h"
 
+#include <atomic>
+
 namespace {
 
 // The scratch: reserved on every GPU that loads the library, until exit.
@@ -12,22 +14,23 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[KQ_NOALLOC_SCRATCH_BY
 
 // Device address of g_noalloc_scratch, looked up once per device with that
 // device current (in host code the symbol's name is only a host-side handle,
-// not a device address).
+// not a device address).  Host threads making their first call on a device
+// at the same time may both look it up; they store the same address.
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_ptr[MAX_DEVICES] = {};
+std::atomic<void *> g_scratch_ptr[MAX_DEVICES];
 
 int scratch_of_current_device(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KQ_ERR_DEVICE;
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
             cudaGetLastError();
             return KQ_ERR_LAUNCH;
         }
-        g_scratch_ptr[dev] = p;
+        g_scratch_ptr[dev].store(p, std::memory_order_relaxed);
     }
-    *ptr = g_scratch_ptr[dev];
+    *ptr = p;
     return KQ_OK;
 }
 

@@ -58,3 +58,44 @@ def test_noalloc_rejects_problems_beyond_its_scratch(K):
     rc = K.raw().kq_gemm_noalloc(synth.Q4_K, 0x10000, 4096, Kdim, q, M, 0x10000, None)
     assert rc == -8
     assert "scratch" in K.kq_strerror(rc)
+
+
+def test_noalloc_size_limit_boundary(K):
+    """The documented largest shape (512 tokens x K = 30464) fits the fixed
+    array and the next step of K (30720) is refused before anything runs."""
+    fits = K.kq_gemm_workspace_bytes(synth.Q4_K, 512, 4096, 30464)
+    over = K.kq_gemm_workspace_bytes(synth.Q4_K, 512, 4096, 30720)
+    assert fits <= K.KQ_NOALLOC_SCRATCH_BYTES < over
+    q = K._Q8KConst(0x10000, 0x10000, 0x10000)   # never dereferenced: the size check comes first
+    rc = K.raw().kq_gemm_noalloc(synth.Q4_K, 0x10000, 4096, 30720, q, 512, 0x10000, None)
+    assert rc == -8
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.Q6_K])
+def test_noalloc_back_to_back_under_pdl(K, fmt):
+    """Two calls enqueued on one stream with no synchronisation between them
+    and programmatic dependent launch on: the second call's pre-pass rewrites
+    the shared scratch while the first call's GEMM may still be running, so
+    it must wait for it.  The second call has fewer tokens (301, not a
+    multiple of 4), so a stale padded tail of the first call's scales would
+    show.  Both outputs must equal kq_gemm's."""
+    N, Kdim = 200, 1024
+    rng = synth.rng_for(121, fmt)
+    packed = pack(K, fmt, synth.disk_weights(fmt, N, Kdim, rng))
+    cases = []
+    for M in (512, 301):
+        a = q8k_to_dev(K, oracle_q8k(synth.activations(M, Kdim, rng)))
+        cases.append((M, a, torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")))
+    refs = [K.kq_gemm(fmt, packed, N, Kdim, a) for _, a, _ in cases]
+    torch.cuda.synchronize()
+    old = K.kq_set_launch_flags(K.KQ_LAUNCH_PDL)
+    try:
+        for M, a, y in cases:
+            rc = K.raw().kq_gemm_noalloc(fmt, packed.data_ptr(), N, Kdim, K._q8k_struct(a), M, y.data_ptr(),
+                                         K._stream())
+            assert rc == 0, K.kq_strerror(rc)
+        torch.cuda.synchronize()
+    finally:
+        K.kq_set_launch_flags(old)
+    for (_, _, y), y_ref in zip(cases, refs):
+        assert_row_tol(y.cpu().numpy(), y_ref.cpu().numpy().astype(np.float64))
