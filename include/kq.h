@@ -118,9 +118,15 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
  * Inside a chunk, row r's 16-byte piece i (disk bytes 16i .. 16i+15 of that
  * field) sits at: qs/ql 512*(i%4) + 16*(r + 16*(i/4)); Q6_K qh
  * 512*(i%2) + 16*(r + 16*(i/2)); Q5_K qh 256*i + 16*r; hdr/sc 16*r; d 2*r.
- * Every byte of the disk superblock is kept once, so the image is the disk
- * size of the rows padded to a multiple of 16, plus at most 3 x 255 bytes
- * of plane padding.
+ * Every byte of the disk superblock is kept once.  A last plane holds data
+ * derived at repack time for the tensor-core GEMM: per (row group,
+ * superblock), two uint32, for each half of the superblock the largest
+ * over the group's rows of W1 = sum |w'| (w' = sub-scale * q, Q6_K
+ * q - 32), which bounds every partial sum of the half's integer dot
+ * (|a8| <= 128) and so tells the GEMM how long its fp32 accumulators may
+ * run exactly.  The image is the disk size of the rows padded to a multiple
+ * of 16, plus 8 bytes per (row group, superblock), plus at most 4 x 255
+ * bytes of plane padding.
  */
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K);
 /*
@@ -292,6 +298,27 @@ int kq_gemv_grouped_fused(kq_format f, int n_sets, const void *const *packed, co
  */
 int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a,
                       int64_t M, int32_t *isum, int32_t *msum, cudaStream_t s);
+
+/*
+ * Test hook: the same int32 partials from the tensor-core GEMM ([kq-arc],
+ * kq v3 panel-scratch commit: the tile must equal the GEMV bit for bit,
+ * unpack included).  It runs the kq_gemm / kq_gemm_grouped kernel with its
+ * epilogue switched from the float fold to integers: each fp32 accumulator
+ * unit the tensor pipe produced (an exact integer below 2^24) is converted
+ * to int32 and the units of a superblock are added, so isum and msum are
+ * what the GEMM's contraction computed, bit for bit.
+ *   E, row_offsets  1 and NULL for the dense GEMM; else as kq_gemm_grouped
+ *   M           token rows, >= 16 (the tensor-core path)
+ *   isum, msum  device int32 [M][N][K/256]; for Q6_K isum = iacc - 32*bacc,
+ *               msum = 0; rows outside every expert range are left 0
+ *   workspace   as kq_gemm (kq_gemm_workspace_bytes(f, M, N, K) bytes)
+ * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (M < 16, null, E > 1 without offsets, a
+ * grouped shape the tensor-core kernel does not take), KQ_ERR_ALIGN,
+ * KQ_ERR_WORKSPACE, KQ_ERR_LAUNCH.
+ */
+int kq_debug_gemm_partials(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets, int64_t N,
+                           int64_t K, kq_q8k_const a, int64_t M, int32_t *isum, int32_t *msum, void *workspace,
+                           size_t workspace_bytes, cudaStream_t s);
 
 /*
  * Test hook: decode the packed image back to stored quants and scales with

@@ -105,9 +105,9 @@ int kq_quantize_q8k(const float *x, int64_t M, int64_t K, kq_q8k out, cudaStream
 size_t kq_repack_bytes(kq_format f, int64_t N, int64_t K) {
     if (f == KQ_Q8_0) return check_shape(N, K) ? 0 : (size_t)q8_0_image_bytes(N, K);
     if (!fmt_ok(f) || check_shape(N, K)) return 0;
-    uint64_t off[5];
+    uint64_t off[6];
     plane_offsets(f, N, K / QK, off);
-    return (size_t)off[4];
+    return (size_t)off[5];
 }
 
 int kq_repack(kq_format f, const void *disk, int64_t N, int64_t K, void *packed, cudaStream_t s) {
@@ -263,6 +263,29 @@ int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_
     if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
     if (!aligned(packed, 256) || !aligned(isum, 4) || !aligned(msum, 4)) return KQ_ERR_ALIGN;
     return launch_status(launch_partials(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, M, isum, msum, s));
+}
+
+int kq_debug_gemm_partials(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets, int64_t N,
+                           int64_t K, kq_q8k_const a, int64_t M, int32_t *isum, int32_t *msum, void *workspace,
+                           size_t workspace_bytes, cudaStream_t s) {
+    if (!fmt_ok(f)) return KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (M < GEMM_TC_MIN_M || E < 1 || (E > 1 && !row_offsets)) return KQ_ERR_ARG;
+    if (N == 0) return KQ_OK;
+    if (!packed || !isum || !msum) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(isum, 4) || !aligned(msum, 4)) return KQ_ERR_ALIGN;
+    const size_t need = gemm_workspace_bytes(f, M, N, K);
+    if (!workspace || workspace_bytes < need) return KQ_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return KQ_ERR_ALIGN;
+    const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
+    cudaError_t e = launch_gemm_tc_partials(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, M, row_offsets, E, expert_bytes,
+                                            isum, msum, workspace, workspace_bytes, s);
+    if (e == cudaErrorNotSupported) {
+        cudaGetLastError();
+        return KQ_ERR_ARG;
+    }
+    return launch_status(e);
 }
 
 int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32_t *q, int32_t *sc, int32_t *mn,

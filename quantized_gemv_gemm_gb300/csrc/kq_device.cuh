@@ -51,7 +51,8 @@ __host__ __device__ inline uint64_t align256(uint64_t x) { return (x + 255) & ~u
 // So every chunk is contiguous and 16-byte aligned (one bulk copy), a warp
 // serving 16 rows x one superblock reads consecutive 16-byte pieces, and a
 // row's next superblock is one chunk further on in every plane.  Every disk
-// byte is kept as it is; only its place changes.
+// byte is kept as it is; only its place changes.  A small bounds plane
+// (below) follows the data planes.
 constexpr int GROUP_ROWS = 16;
 
 __host__ __device__ inline int64_t row_groups(int64_t N) { return (N + GROUP_ROWS - 1) / GROUP_ROWS; }
@@ -64,25 +65,36 @@ __host__ __device__ inline void plane_unit_bytes(int f, int u[4]) {
     else if (f == FMT_Q6_K) { u[1] = 64; u[2] = 16; u[3] = 2; }
 }
 
-// Offsets of the planes of an [N][K] image; off[4] = total bytes.
-__host__ __device__ inline void plane_offsets(int f, int64_t N, int64_t nsb, uint64_t off[5]) {
+// Bounds plane (derived at repack time, read by the tensor-core GEMM only):
+// per (row group g, superblock sb), in the order g * nsb + sb, two uint32:
+// for each half of the superblock (K 0..127, 128..255) the largest over the
+// group's 16 rows of W1 = sum |w'| = sum over the half's sub-blocks of
+// |sub-scale| * sum |q| (Q4_K/Q5_K q, Q6_K q - 32).  Any partial sum of
+// w' * a8 over a row's half is at most 128 * W1 in magnitude (|a8| <= 128),
+// so an fp32 accumulator over it stays exact while 128 * W1 <= 2^24.
+constexpr int BOUND_BYTES = 8;
+
+// Offsets of the planes of an [N][K] image: the data planes 0..3, the
+// bounds plane at off[4]; off[5] = total bytes.
+__host__ __device__ inline void plane_offsets(int f, int64_t N, int64_t nsb, uint64_t off[6]) {
     int u[4];
     plane_unit_bytes(f, u);
     const uint64_t units = (uint64_t)row_groups(N) * GROUP_ROWS * (uint64_t)nsb;
     off[0] = 0;
     for (int i = 0; i < 4; ++i) off[i + 1] = off[i] + align256(units * (uint64_t)u[i]);
+    off[5] = off[4] + align256((uint64_t)row_groups(N) * (uint64_t)nsb * BOUND_BYTES);
 }
 
-// Plane base pointers of one packed matrix.
+// Plane base pointers of one packed matrix (p4: the bounds plane).
 struct Planes {
-    const uint8_t *p0, *p1, *p2, *p3;
+    const uint8_t *p0, *p1, *p2, *p3, *p4;
 };
 
 __host__ __device__ inline Planes make_planes(int f, const void *base, int64_t N, int64_t nsb) {
-    uint64_t off[5];
+    uint64_t off[6];
     plane_offsets(f, N, nsb, off);
     const uint8_t *b = static_cast<const uint8_t *>(base);
-    return Planes{b + off[0], b + off[1], b + off[2], b + off[3]};
+    return Planes{b + off[0], b + off[1], b + off[2], b + off[3], b + off[4]};
 }
 
 // Chunk index of (row n, superblock sb): the chunk of n's row group at sb.
@@ -463,6 +475,10 @@ __device__ __forceinline__ void cp_async16_if(uint32_t dst_smem, const void *src
         "{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p cp.async.cg.shared.global [%0], [%1], 16;\n}\n" ::"r"(dst_smem),
         "l"(src), "r"(pred)
         : "memory");
+}
+// an 8-byte copy (both addresses 8-byte aligned), through L1
+__device__ __forceinline__ void cp_async8(uint32_t dst_smem, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst_smem), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 

@@ -16,28 +16,37 @@
 //     larger sub-scale the weight is split into two exact planes,
 //     sc*(v - (v&1)) (even, |.| <= 4096) and sc*(v&1), both multiplied into
 //     the same accumulator;
-//   - tcgen05.mma kind::f16 accumulates I = sum w'*q8 (the page's isum, or
-//     iacc - 32*bacc for Q6_K) in fp32 TMEM; for Q4_K/Q5_K a second K=16 MMA
-//     of the sub-mins (duplicated per 16) against the bsums gives msum;
-//   - the epilogue folds once per superblock, y += d8*(d*I - dmin*msum), in
-//     fp32 registers ([kq-arc], "The pieces": one float fold per superblock).
+//   - tcgen05.mma kind::f16 accumulates the page's integer sums in fp32
+//     TMEM in "units" short enough that every partial sum stays an integer
+//     below 2^24, where fp32 is exact: a unit is K = 128 for Q4_K
+//     (128 * 945 * 127 < 2^24), K = 64 for Q5_K (64 * 1953 * 127 < 2^24);
+//     for Q6_K it is chosen per tile half from the largest |sub-scale| in it:
+//     K = 128 up to 32 (|w'| <= 1024), K = 64 up to 62 (|w'| <= 1984) and
+//     K = 32 beyond (split planes of the same sign, |w'| <= 4096).  The
+//     superblock's integer sum I (the page's isum, or iacc - 32*bacc for
+//     Q6_K) is the exact sum of its units; for Q4_K/Q5_K a K=16 MMA of the
+//     sub-mins (duplicated per 16) against the bsums gives msum
+//     (16 * 63 * 2032 < 2^24);
+//   - the epilogue folds each pair of units as d8*d*(Ua + Ub), and msum as
+//     -d8*dmin*msum, in fp32 ([kq-arc], "The pieces": the float work is per
+//     superblock, not per sub-block).  A debug variant of the same kernel
+//     (kq_debug_gemm_partials) converts each unit to int32 instead and adds
+//     them, giving I and msum bit for bit.
 // The grouped (MoE) form runs one block per SM over a list of tiles (see the
 // tile comment below), so short expert tiles do not pay a block's start-up
 // and drain each.
-// The fp32 accumulator is exact while every partial sum stays below 2^24 in
-// magnitude (true for realistic activations; at adversarial extremes the
-// sum is rounded like the fold's own float(isum)).
 //
 // Warp roles (14 warps): 0 TMA producer of the activation tiles, 1 MMA issuer
 // (and TMEM owner); Q4_K/Q5_K: 2..5 weight unpack (thread = weight row),
 // 6..13 epilogue (thread = row x 64 token columns, y in registers); Q6_K,
 // whose unpack is the longer chain: 2..9 weight unpack (two threads per row,
 // one 64-wide K sub-tile each), 10..13 epilogue (thread = row x every token
-// column, y accumulated in TMEM columns 128..255, which Q6_K's missing mins
-// leave free).  TMEM lane quadrant = warp % 4.  Stages are half superblocks (K = 128): an A ring of 2 slots,
-// a B ring of 3 (Q6_K: 2); accumulators I and msum double-buffered by
-// superblock parity.  Every mbarrier wait is bounded; on timeout the block
-// records KQ_ERR_TIMEOUT in the device status word and winds down.
+// column, y accumulated in TMEM).  TMEM lane quadrant = warp % 4.  Stages
+// are half superblocks (K = 128): an A ring of 2 slots, a B ring of 3
+// (Q6_K: 2).  TMEM (512 columns) holds a ring of 3 unit accumulators and,
+// in its last 128 columns, msum (Q4_K/Q5_K) or y (Q6_K).  Every mbarrier
+// wait is bounded; on timeout the block records KQ_ERR_TIMEOUT in the
+// device status word and winds down.
 #include "kq_internal.h"
 #include "kq_sm100.cuh"
 
@@ -78,7 +87,7 @@ struct Cfg {
     static constexpr int OFF_D8 = OFF_SD + 2 * 2 * BM * 4;        // per epilogue warp [64] floats
     static constexpr int OFF_BAR = OFF_D8 + 8 * 64 * 4;
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
-    static constexpr int OFF_TILES = OFF_MISC + 128;              // grouped: the block's tile list
+    static constexpr int OFF_TILES = OFF_MISC + 256;              // grouped: the block's tile list
     static constexpr int OFF_OFFS = OFF_TILES + TILE_CAP * 16;    // grouped: the row offsets [E + 1]
     // grouped Q4_K: each unpack thread's row bytes for a half superblock (4
     // qs pieces + the scale block, 16 B each) staged by cp.async RS - 1 halves
@@ -86,7 +95,8 @@ struct Cfg {
     // bank conflicts)
     static constexpr int RS = F == FMT_Q4_K ? 3 : 0, RCH = 5;
     static constexpr int OFF_RAW = OFF_OFFS + (MAX_GROUPED_E + 4) * 4;
-    static constexpr int SMEM = OFF_RAW + RS * RCH * BM * 16 + 1024;  // + alignment slack
+    static constexpr int OFF_RBND = OFF_RAW + RS * RCH * BM * 16;     // and its W1 bounds, [RS][BM] x 8 B
+    static constexpr int SMEM = OFF_RBND + RS * BM * 8 + 1024;        // + alignment slack
     static constexpr int SMEM_DENSE = OFF_RAW + 1024;                  // the dense kernel stages no rows
     static_assert(SMEM <= 232448, "shared memory per block");
     static_assert(OFF_RAW % 16 == 0, "cp.async needs 16-byte aligned destinations");
@@ -94,9 +104,80 @@ struct Cfg {
     static_assert(B_SLOT % 1024 == 0, "B slots need 1024-byte alignment");
 };
 
-// barrier indices
-enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_ACC_FULL = 10, BAR_ACC_EMPTY = 12,
-       BAR_SD_FULL = 14, BAR_MMA_DONE = 16, BAR_TILES = 17 };
+// barrier indices: A and B operand rings, the ring of unit accumulators
+// (U), the two msum accumulators (M), the per-superblock weight scales and
+// unit plans (SD, by superblock parity), MMA completion, the tile list
+enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
+       BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25 };
+
+// TMEM (512 columns) in slots of 128 columns: a ring of unit accumulators
+// from column 0 (Q4_K/Q5_K 2 slots, Q6_K 3), then msum by superblock parity
+// (Q4_K/Q5_K, columns 256 and 384) or y (Q6_K, column 384).
+template <int F> constexpr int n_units() { return F == FMT_Q6_K ? 3 : 2; }
+constexpr uint32_t COL_M = 256, COL_Y = 384;
+
+// ---------------------------------------------------------------------------
+// Accumulator units.  The fp32 TMEM accumulator is exact while every partial
+// sum is an integer of magnitude <= 2^24.  With |a8| <= 128 a partial sum
+// of w' * a8 over a set of weights is at most 128 * sum |w'| over them, so:
+//   - a half superblock (K = 128) is always one unit for Q4_K
+//     (128 * 945 * 128 < 2^24); for Q5_K when its rows' W1 (sum |w'|, from
+//     the image's bounds plane) is <= 2^24 / 128, else two units of K = 64
+//     (64 * 1953 * 128 < 2^24); for Q6_K when W1 allows it or every
+//     |sub-scale| <= 32 (128 * 32 * 32 * 128 = 2^24), else two units of
+//     K = 64 while every |sub-scale| <= 62, else four of K = 32 (split
+//     planes of the same sign, 32 * 4096 * 128 = 2^24);
+//   - a whole superblock is one unit when both halves are single units and
+//     the rows' W1 over the superblock is <= 2^24 / 128 (the common case).
+// Each unpack warp publishes, per half, a flag byte for its rows: bits 0..1
+// the half's category (units 1, 2, 4), bit 2 (second half only) the whole-
+// superblock bound, bit 3 (Q6_K) split planes.  The MMA issuer and the
+// epilogue derive the same plan from these flags.
+constexpr uint32_t W1_LIMIT = 1u << 17;  // 2^24 / 128
+__host__ __device__ constexpr int units_of_cat(int cat) { return cat == 0 ? 1 : (cat == 1 ? 2 : 4); }
+
+struct SbPlan {
+    int cat[2];     // per half: 0, 1, 2
+    bool split[2];  // Q6_K: two A planes in the half
+    bool whole;     // one unit for the superblock
+    int n;          // units of the superblock
+};
+// A half's flags: one byte per unpack warp (8 bytes; the bytes of absent
+// warps hold FLAG_NEUTRAL), read as one 64-bit shared-memory load.
+constexpr uint8_t FLAG_NEUTRAL = 4;
+constexpr uint64_t BYTES_1 = 0x0101010101010101ull;
+__device__ __forceinline__ uint64_t ld_flags(uint32_t saddr) {
+    uint64_t v;
+    asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(saddr) : "memory");
+    return v;
+}
+__device__ __forceinline__ int half_cat(uint64_t f) {
+    return (f & (2 * BYTES_1)) ? 2 : ((f & BYTES_1) ? 1 : 0);
+}
+__device__ __forceinline__ bool half_split(uint64_t f) { return (f & (8 * BYTES_1)) != 0; }
+// The plan of a superblock from its two halves' flags.
+__device__ __forceinline__ SbPlan sb_plan(uint64_t f0, uint64_t f1) {
+    SbPlan pl;
+    pl.cat[0] = half_cat(f0);
+    pl.cat[1] = half_cat(f1);
+    pl.split[0] = half_split(f0);
+    pl.split[1] = half_split(f1);
+    pl.whole = pl.cat[0] == 0 && pl.cat[1] == 0 && (f1 & (4 * BYTES_1)) == 4 * BYTES_1;
+    pl.n = pl.whole ? 1 : units_of_cat(pl.cat[0]) + units_of_cat(pl.cat[1]);
+    return pl;
+}
+// An unpack warp's flag for half h: w1 = its rows' W1 bound of the half,
+// w1sb of the superblock (h = 1), maxsc the largest |sub-scale| (Q6_K).
+template <int F>
+__device__ __forceinline__ int unit_flag(int h, uint32_t w1, uint32_t w1sb, int maxsc) {
+    int cat = 0;
+    if constexpr (F == FMT_Q5_K) cat = w1 <= W1_LIMIT ? 0 : 1;
+    if constexpr (F == FMT_Q6_K) cat = (w1 <= W1_LIMIT || maxsc <= 32) ? 0 : (maxsc <= 62 ? 1 : 2);
+    int f = cat;
+    if (h == 1 && w1sb <= W1_LIMIT) f |= 4;
+    if (F == FMT_Q6_K && maxsc > 62) f |= 8;
+    return f;
+}
 
 struct GemmParams {
     const uint8_t *packed;
@@ -107,6 +188,9 @@ struct GemmParams {
     const float *d8t;        // workspace: d8 transposed [nsb][Mp]
     int64_t Mp;
     float *y;
+    // debug: instead of y, the superblock integer sums, [M][N][nsb] each
+    // (isum_out zero-filled before the launch; it is accumulated per unit pair)
+    int32_t *isum_out, *msum_out;
 };
 
 __device__ __forceinline__ void set_timeout() { atomicExch(&g_status, 1); }
@@ -194,21 +278,26 @@ __device__ __forceinline__ void unpack_q45(uint32_t a_tile, int r, const uint32_
 // q of four elements is assembled in one word, then spread into fp16 lanes
 // 1024 + q.  v = q - 32: P1 = v*sc = (1024 + q)*sc - 1056*sc in one fp16 FMA,
 // exact for |sc| <= 62 (1056*sc and the result are exact fp16 integers); with
-// `split` (some |sc| > 62), P1 = (v - (v&1))*sc and P2 = (v&1)*sc, each exact.
-// `zero2` writes zeros to this thread's P2 rows instead.
+// `split` (some |sc| > 62), sc = sa + sb with sa = floor(sc / 2), sb = sc - sa
+// (same sign, |sa|, |sb| <= 64): P1 = v*sa and P2 = v*sb, each an exact fp16
+// integer (|.| <= 2048), of the same sign, summing to v*sc.  `zero2` writes
+// zeros to this thread's P2 rows instead.
 __device__ __forceinline__ void unpack_q6(uint32_t a_tile, uint32_t a2_tile, int r, const uint32_t (&ql)[16],
                                           const uint32_t (&qh)[8], uint32_t scw, int j, bool split, bool zero2) {
     const uint32_t off1056 = h2_splat(1056.0f);
 #pragma unroll
     for (int tt = 0; tt < 2; ++tt) {
         const int t = 2 * j + tt;
-        // the group's two sub-scales (l < 16, l >= 16) and -1056 * each
-        uint32_t s2v[2], c2v[2];
+        // the group's two sub-scales (l < 16, l >= 16): sc, -1056 * sc, and the halves sa, sb
+        uint32_t s2v[2], c2v[2], sav[2], sbv[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int scv = (int)(int8_t)((scw >> (8 * (2 * tt + u))) & 0xFF);
+            const int sa = scv >> 1;
             s2v[u] = h2_splat((float)scv);
             c2v[u] = h2_splat(-1056.0f * (float)scv);
+            sav[u] = h2_splat((float)sa);
+            sbv[u] = h2_splat((float)(scv - sa));
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {  // K 32tt + 8q .. +7: l = 8q .. 8q+7
@@ -223,9 +312,9 @@ __device__ __forceinline__ void unpack_q6(uint32_t a_tile, uint32_t a2_tile, int
                 for (int pr = 0; pr < 2; ++pr) {
                     const uint32_t x = prmt(q6, MAGIC, pr ? SEL_23 : SEL_01);  // fp16 1024 + q
                     if (split) {
-                        const uint32_t odd = x & 0x00010001u;
-                        p1[2 * w + pr] = h2_mul(h2_sub(x ^ odd, off1056), s2);
-                        p2[2 * w + pr] = h2_mul(odd * 0x3C00u, s2);     // fp16 1.0 in each odd lane
+                        const uint32_t v = h2_sub(x, off1056);                 // q - 32, exact
+                        p1[2 * w + pr] = h2_mul(v, sav[q >> 1]);
+                        p2[2 * w + pr] = h2_mul(v, sbv[q >> 1]);
                     } else {
                         p1[2 * w + pr] = h2_fma(x, s2, c2);
                         p2[2 * w + pr] = 0u;
@@ -240,9 +329,10 @@ __device__ __forceinline__ void unpack_q6(uint32_t a_tile, uint32_t a2_tile, int
 
 // Raw packed bytes one unpack thread (one weight row) converts for one half
 // superblock (K 128h .. 128h + 127).
-struct RawQ4 { uint32_t qs[16]; uint4 hdr; };              // qs[64h .. 64h+64)
-struct RawQ5 { uint32_t qs[16]; uint32_t qh[8]; uint4 hdr; };
-struct RawQ6 { uint32_t ql[16]; uint32_t qh[8]; uint32_t sc[2]; uint32_t d; };  // ql/qh/sc of half h
+// bnd: the row group's W1 bounds of the superblock's two halves.
+struct RawQ4 { uint32_t qs[16]; uint4 hdr; uint2 bnd; };              // qs[64h .. 64h+64)
+struct RawQ5 { uint32_t qs[16]; uint32_t qh[8]; uint4 hdr; uint2 bnd; };
+struct RawQ6 { uint32_t ql[16]; uint32_t qh[8]; uint32_t sc[2]; uint32_t d; uint2 bnd; };  // ql/qh/sc of half h
 template <int F> struct RawOf;
 template <> struct RawOf<FMT_Q4_K> { using T = RawQ4; };
 template <> struct RawOf<FMT_Q5_K> { using T = RawQ5; };
@@ -260,6 +350,7 @@ __device__ __forceinline__ void load_raw(RawQ4 &r, const Planes &P, int64_t n, i
 #pragma unroll
     for (int i = 0; i < 4; ++i) ld16w(r.qs + 4 * i, q + 512 * i);
     r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p1 + ch * 256 + 16 * rr));
+    r.bnd = __ldg(reinterpret_cast<const uint2 *>(P.p4) + ch);
 }
 __device__ __forceinline__ void load_raw(RawQ5 &r, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int h) {
     const uint64_t ch = chunk_of(n, sb, nsb);
@@ -270,6 +361,7 @@ __device__ __forceinline__ void load_raw(RawQ5 &r, const Planes &P, int64_t n, i
     ld16w(r.qh, P.p1 + ch * 512 + 16 * rr);
     ld16w(r.qh + 4, P.p1 + ch * 512 + 256 + 16 * rr);
     r.hdr = __ldg(reinterpret_cast<const uint4 *>(P.p2 + ch * 256 + 16 * rr));
+    r.bnd = __ldg(reinterpret_cast<const uint2 *>(P.p4) + ch);
 }
 __device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, int64_t n, int64_t sb, int64_t nsb, int h) {
     const uint64_t ch = chunk_of(n, sb, nsb);
@@ -283,6 +375,7 @@ __device__ __forceinline__ void load_raw(RawQ6 &r, const Planes &P, int64_t n, i
     r.sc[0] = sc.x;
     r.sc[1] = sc.y;
     r.d = __ldg(reinterpret_cast<const unsigned short *>(P.p3 + ch * 32) + rr);
+    r.bnd = __ldg(reinterpret_cast<const uint2 *>(P.p4) + ch);
 }
 
 // ---------------------------------------------------------------------------
@@ -436,18 +529,96 @@ __device__ __forceinline__ void prefetch_tile(const GemmParams &p, const Tile &t
         if (u[q] && r1 > n0) prefetch_l2_bulk(base[q] + (uint64_t)n0 * p.nsb * u[q], (uint64_t)(r1 - n0) * p.nsb * u[q]);
 }
 
-template <int F, bool G>
+// ---------------------------------------------------------------------------
+// Epilogue helpers.  TMEM addresses are of this warp's lane quadrant; a
+// thread holds one weight row.
+
+// Q4_K/Q5_K: y[64] (64 token columns, in registers) += d8 * (d * U - dmin *
+// msum) for one unit U, CW (8 or 16) columns per TMEM load round trip
+template <int CW>
+__device__ __forceinline__ void fold_unit_q45(float (&y)[64], uint32_t xu, uint32_t xm, float dd, float dm,
+                                              const float *s_d8) {
+#pragma unroll
+    for (int cc = 0; cc < 64 / CW; ++cc) {
+        uint32_t vu[CW], vm[CW];
+        if constexpr (CW == 16) {
+            tmem_ld16(xu + 16 * cc, vu);
+            tmem_ld16(xm + 16 * cc, vm);
+        } else {
+            tmem_ld8(xu + 8 * cc, vu);
+            tmem_ld8(xm + 8 * cc, vm);
+        }
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < CW; ++i) {
+            const float tv = fmaf(-dm, __uint_as_float(vm[i]), dd * __uint_as_float(vu[i]));
+            y[CW * cc + i] = fmaf(s_d8[CW * cc + i], tv, y[CW * cc + i]);
+        }
+    }
+}
+
+// Q6_K: y (in TMEM at yt) += d8 * d * (Ua [+ Ub]) over nc chunks of 16
+// columns; FIRST: y starts from zero
+template <bool PAIR, bool FIRST>
+__device__ __forceinline__ void fold_units_q6(uint32_t xa, uint32_t xb, uint32_t yt, int nc, float dd,
+                                              const float *s_d8) {
+    for (int c = 0; c < nc; ++c) {
+        uint32_t va[16], vb[PAIR ? 16 : 1], vy[16];
+        tmem_ld16(xa + 16 * c, va);
+        if constexpr (PAIR) tmem_ld16(xb + 16 * c, vb);
+        if constexpr (!FIRST) tmem_ld16(yt + 16 * c, vy);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float sum = __uint_as_float(va[i]);
+            if constexpr (PAIR) sum += __uint_as_float(vb[i]);
+            const float yo = FIRST ? 0.0f : __uint_as_float(vy[i]);
+            vy[i] = __float_as_uint(fmaf(s_d8[16 * c + i] * dd, sum, yo));
+        }
+        tmem_st16(yt + 16 * c, vy);
+    }
+}
+
+// Debug epilogue (kq_debug_gemm_partials): the units' exact integers added
+// into isum, msum stored, for `ncols` token columns from tok0 (16 at a
+// time); has_b: a second unit at xb, has_m: msum at xm.
+__device__ __forceinline__ void debug_units(int32_t *isum_out, int32_t *msum_out, int64_t N, int64_t nsb, uint32_t xa,
+                                            bool has_b, uint32_t xb, bool has_m, uint32_t xm, int ncols, int64_t tok0,
+                                            int64_t t_end, int64_t n, int64_t sb) {
+    for (int c = 0; c < ncols; c += 16) {
+        uint32_t va[16], vb[16], vm[16];
+        tmem_ld16(xa + c, va);
+        if (has_b) tmem_ld16(xb + c, vb);
+        if (has_m) tmem_ld16(xm + c, vm);
+        tmem_wait_ld();
+        if (n >= N) continue;
+        for (int i = 0; i < 16; ++i) {
+            const int64_t tt = tok0 + c + i;
+            if (tt >= t_end) break;
+            int iv = __float2int_rn(__uint_as_float(va[i]));
+            if (has_b) iv += __float2int_rn(__uint_as_float(vb[i]));
+            const int64_t o = (tt * N + n) * nsb + sb;
+            atomicAdd(isum_out + o, iv);
+            if (has_m) msum_out[o] = __float2int_rn(__uint_as_float(vm[i]));
+        }
+    }
+}
+
+template <int F, bool G, bool DBG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a16, const __grid_constant__ CUtensorMap map_b16,
                 const GemmParams p) {
     using C = Cfg<F>;
+    constexpr int NU = n_units<F>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     float *s_d = reinterpret_cast<float *>(smem + C::OFF_SD);
     float *s_dmin = s_d + 2 * BM;
     uint32_t *misc = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);  // [0] tmem base, [1] tile count
-    int *s_flag = reinterpret_cast<int *>(misc + 8);                     // Q6_K split flags [2 halves][8 warps]
+    // each unpack warp's unit flag byte, [superblock parity][half][8 warps]
+    uint8_t *s_flag = reinterpret_cast<uint8_t *>(misc + 16);
+    const uint32_t flag_sa = smem_u32(s_flag);  // the same, as a shared-memory address
     int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_TILES);        // grouped tile list
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -472,15 +643,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bar[BAR_FULL_B + i], 1);
             mbar_init(&bar[BAR_EMPTY_B + i], 1);
         }
-        mbar_init(&bar[BAR_ACC_FULL + 0], 1);
-        mbar_init(&bar[BAR_ACC_FULL + 1], 1);
-        mbar_init(&bar[BAR_ACC_EMPTY + 0], n_epi<F>());
-        mbar_init(&bar[BAR_ACC_EMPTY + 1], n_epi<F>());
-        mbar_init(&bar[BAR_SD_FULL + 0], 4);
-        mbar_init(&bar[BAR_SD_FULL + 1], 4);
+        for (int i = 0; i < NU; ++i) {
+            mbar_init(&bar[BAR_U_FULL + i], 1);
+            mbar_init(&bar[BAR_U_EMPTY + i], n_epi<F>());
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[BAR_M_FULL + i], 1);
+            mbar_init(&bar[BAR_M_EMPTY + i], n_epi<F>());
+        }
+        // every unpack warp arrives once the scales and both halves' unit
+        // flags of the superblock are written
+        mbar_init(&bar[BAR_SD_FULL + 0], n_unpack<F>());
+        mbar_init(&bar[BAR_SD_FULL + 1], n_unpack<F>());
+        mbar_init(&bar[BAR_SD_EMPTY + 0], n_epi<F>());
+        mbar_init(&bar[BAR_SD_EMPTY + 1], n_epi<F>());
         mbar_init(&bar[BAR_MMA_DONE], 1);
         mbar_init(&bar[BAR_TILES], 1);
         mbar_fence_init();
+        for (int i = 0; i < 32; ++i) s_flag[i] = FLAG_NEUTRAL;
     }
     if (warp == W_MMA) {
         tmem_alloc(&misc[0], 512);
@@ -490,8 +670,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns: I[b] at 256b, msum[b] at 256b + 128.  Buffer b and the
-    // phases follow g, the block's count of superblock steps over all tiles.
+    // TMEM columns: unit accumulator i at 128i (i < NU), msum at COL_M, y at COL_Y.
+    // The unit ring's slots and phases follow u, the block's count of units
+    // over all tiles; msum's phase the count of non-empty superblocks; the
+    // SD barriers' the block's count g of superblock steps over all tiles.
     bool ok = true;
 
     if (warp == W_TMA) {
@@ -543,21 +725,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
         const uint32_t b_base = smem_u32(smem + C::OFF_B);
-        int64_t g = 0, use = 0;
+        int64_t g = 0, use = 0, u = 0, mc = 0;
         if (lane == 0) {
             int ntiles = 1;
             if constexpr (G) {
                 ok = mbar_wait(&bar[BAR_TILES], 0);
                 ntiles = ok ? (int)misc[1] : 0;
             }
+            // issue the K16 steps [s0, s1) of the half in slot a_slot / b_slot
+            // into accumulator acc; `fresh`: the first overwrites it
+            auto issue = [&](uint32_t acc, uint32_t a_slot, uint32_t b_slot, int s0, int s1, int planes, bool fresh,
+                             uint32_t idesc) {
+                for (int st = s0; st < s1; ++st) {
+                    const int j = st >> 2, kk = st & 3;
+                    const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * kk, 16, 1024, SWZ_128B);
+                    for (int pl = 0; pl < planes; ++pl) {
+                        const uint64_t ad = smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * kk, 16, 1024, SWZ_128B);
+                        umma_f16(acc, ad, bd, idesc, fresh ? 0u : 1u);
+                        fresh = false;
+                    }
+                }
+            };
             for (int k = 0; k < ntiles && ok; ++k) {
                 const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
                 const uint32_t idesc = idesc_f16_f32(BM, t.n_mma > 0 ? t.n_mma : 16);
                 for (int64_t sb = 0; sb < nsb && ok; ++sb, ++g) {
-                    const int b = (int)(g & 1);
-                    const uint32_t acc_i = tmem + 256 * b, acc_m = tmem + 256 * b + 128;
-                    if (!mbar_wait(&bar[BAR_ACC_EMPTY + b], (uint32_t)(((g >> 1) & 1) ^ 1))) { ok = false; break; }
-                    tc_fence_after();
+                    bool open = false;  // a unit begun in the first half, still accumulating
                     for (int h = 0; h < 2; ++h) {
                         const int slot = (int)(use % C::NB);
                         if (!mbar_wait(&bar[BAR_FULL_A + h], (uint32_t)(g & 1)) ||
@@ -572,34 +765,66 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                         const uint32_t a_slot = a_base + h * C::A_SLOT;
                         const uint32_t b_slot = b_base + slot * C::B_SLOT;
-                        int planes = 1;
-                        if constexpr (F == FMT_Q6_K) {
-                            int any = 0;
-                            for (int w = 0; w < n_unpack<F>(); ++w) any |= s_flag[8 * h + w];
-                            planes = any ? 2 : 1;
+                        // this half's flags are in (the second half's are written after FULL_A[1])
+                        const uint32_t fl = flag_sa + 16 * (uint32_t)(g & 1);
+                        SbPlan pl;
+                        if (h == 0) {
+                            const uint64_t f0 = ld_flags(fl);
+                            pl.cat[0] = half_cat(f0);
+                            pl.split[0] = half_split(f0);
+                            pl.whole = false;
+                        } else {
+                            pl = sb_plan(ld_flags(fl), ld_flags(fl + 8));
                         }
-                        for (int pl = 0; pl < planes; ++pl) {
-                            for (int j = 0; j < 2; ++j) {
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t ad =
-                                        smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * kk, 16, 1024, SWZ_128B);
-                                    const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * kk, 16, 1024, SWZ_128B);
-                                    umma_f16(acc_i, ad, bd, idesc, (h | j | kk | pl) != 0);
+                        const int planes = (F == FMT_Q6_K && pl.split[h]) ? 2 : 1;
+                        if (h == 1 && open && pl.whole) {
+                            // the superblock is one unit: the second half goes on into it
+                            issue(tmem + 128 * (uint32_t)(u % NU), a_slot, b_slot, 0, 8, planes, false, idesc);
+                            umma_commit(&bar[BAR_U_FULL + (int)(u % NU)]);
+                            ++u;
+                            open = false;
+                        } else {
+                            if (open) {  // the first half's unit ends there
+                                umma_commit(&bar[BAR_U_FULL + (int)(u % NU)]);
+                                ++u;
+                                open = false;
+                            }
+                            const int U = units_of_cat(pl.cat[h]);
+                            for (int v = 0; v < U && ok; ++v) {
+                                const int us = (int)(u % NU);
+                                if (!mbar_wait(&bar[BAR_U_EMPTY + us], (uint32_t)(((u / NU) & 1) ^ 1))) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+                                issue(tmem + 128 * (uint32_t)us, a_slot, b_slot, v * 8 / U, (v + 1) * 8 / U, planes, true,
+                                      idesc);
+                                if (h == 0 && U == 1) {
+                                    open = true;  // committed with the second half, or before it
+                                } else {
+                                    umma_commit(&bar[BAR_U_FULL + us]);
+                                    ++u;
                                 }
                             }
                         }
+                        if (!ok) break;
                         if (C::kMins && h == 0) {
+                            const int mb = (int)(mc & 1);
+                            if (!mbar_wait(&bar[BAR_M_EMPTY + mb], (uint32_t)(((mc >> 1) & 1) ^ 1))) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                             const uint64_t ad = smem_desc(amin, 16, 256, SWZ_32B);
                             const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
-                            umma_f16(acc_m, ad, bd, idesc, 0);
+                            umma_f16(tmem + COL_M + 128 * (uint32_t)mb, ad, bd, idesc, 0);
+                            umma_commit(&bar[BAR_M_FULL + mb]);
+                            ++mc;
                         }
                         umma_commit(&bar[BAR_EMPTY_A + h]);
                         umma_commit(&bar[BAR_EMPTY_B + slot]);
                         ++use;
                     }
-                    if (!ok) break;
-                    if (t.ntok > 0) umma_commit(&bar[BAR_ACC_FULL + b]);
-                    else mbar_arrive(&bar[BAR_ACC_FULL + b]);
                 }
             }
             // all MMAs issued by this thread complete before TMEM is released
@@ -650,7 +875,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // copy cursor: tile kc, half-stage hc of it, this row's plane pointers
         int kc = 0, hc = 0;
         bool c_on = false;
-        const uint8_t *cq = nullptr, *chd = nullptr;
+        const uint8_t *cq = nullptr, *chd = nullptr, *cbd = nullptr;
+        const uint32_t rbnd = smem_u32(smem + C::OFF_RBND);  // the W1 bounds ring, [RS][BM] x 8 B
         auto enter_tile = [&](int k) {
             int e, n0;
             c_on = tile_rows(k, e, n0);
@@ -661,6 +887,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const int rr = (int)(row % GROUP_ROWS);
             cq = P.p0 + ch0 * 2048 + 16 * rr;
             chd = P.p1 + ch0 * 256 + 16 * rr;
+            cbd = P.p4 + ch0 * BOUND_BYTES;
         };
         auto issue = [&](int cs) {
             if (c_on) {
@@ -669,6 +896,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) cp_async16(slot_addr(slot, i), q + 512 * i);
                 cp_async16(slot_addr(slot, 4), chd + (uint64_t)sb * 256);
+                cp_async8(rbnd + (uint32_t)((slot * BM + r) * 8), cbd + (uint64_t)sb * BOUND_BYTES);
                 if (++hc == nstage) {
                     hc = 0;
                     enter_tile(++kc);
@@ -697,8 +925,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     qs[4 * i + 3] = v.w;
                 }
                 const uint4 hdr = lds128(slot_addr(slot, 4));
+                uint2 bnd;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(bnd.x), "=r"(bnd.y) : "r"(rbnd + (uint32_t)((slot * BM + r) * 8)));
                 bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
-                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_ACC_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
+                // the epilogue has read the scales of superblock gg - 2
+                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_SD_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
                 if (!__all_sync(0xFFFFFFFFu, w_ok)) {
                     ok = false;
                     break;
@@ -729,11 +960,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     s_d[(gg & 1) * BM + r] = half_lo(hdr.x);
                     s_dmin[(gg & 1) * BM + r] = half_hi(hdr.x);
                 }
+                {
+                    const uint32_t w1 = __reduce_max_sync(0xFFFFFFFFu, h ? bnd.y : bnd.x);
+                    const uint32_t w1sb = h ? __reduce_max_sync(0xFFFFFFFFu, bnd.x + bnd.y) : 0u;
+                    if (lane == 0) s_flag[16 * (gg & 1) + 8 * h + uw] = (uint8_t)unit_flag<F>(h, w1, w1sb, 0);
+                }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bar[BAR_FULL_A + h]);
-                    if (h == 0) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
+                    // the scales and both halves' unit flags are written
+                    if (h == 1) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
                 }
             }
             g += (int)nsb;
@@ -790,29 +1027,35 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         n0_nxt = v.y;
                         // the next tile's planes: this expert's, shifted by whole expert images
                         const int64_t delta = (int64_t)(e_nxt - e_cur) * (int64_t)p.expert_bytes;
-                        const Planes Q{P.p0 + delta, P.p1 + delta, P.p2 + delta, P.p3 + delta};
+                        const Planes Q{P.p0 + delta, P.p1 + delta, P.p2 + delta, P.p3 + delta, P.p4 + delta};
                         const int rn = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
                         load_raw(nxt, Q, rn, 0, nsb, 0);
                     }
                 }
                 bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
-                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_ACC_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
+                // the epilogue has read the scales (and Q6_K categories) of superblock gg - 2
+                if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_SD_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
                 if (!__all_sync(0xFFFFFFFFu, w_ok)) {
                     ok = false;
                     break;
                 }
                 const uint32_t a_slot = a_base + h * C::A_SLOT;
                 float d = 0.0f, dmin = 0.0f;
+                // this warp's unit flag for the half: its rows' W1 bounds and
+                // (Q6_K) the largest |sub-scale| of its rows' K sub-tile
+                const uint32_t w1 = __reduce_max_sync(0xFFFFFFFFu, h ? cur.bnd.y : cur.bnd.x);
+                const uint32_t w1sb = h ? __reduce_max_sync(0xFFFFFFFFu, cur.bnd.x + cur.bnd.y) : 0u;
                 if constexpr (F == FMT_Q6_K) {
                     const uint32_t scj = my_jj ? cur.sc[1] : cur.sc[0];
-                    bool big = false;
+                    int amax = 0;
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int v = (int)(int8_t)((scj >> (8 * i)) & 0xFF);
-                        big |= (v > 62 || v < -62);
+                        amax = max(amax, v < 0 ? -v : v);
                     }
-                    const unsigned any = __ballot_sync(0xFFFFFFFFu, big);
-                    if (lane == 0) s_flag[8 * h + uw] = any ? 1 : 0;
+                    const int wmax = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)amax);
+                    if (lane == 0) s_flag[16 * (gg & 1) + 8 * h + uw] = (uint8_t)unit_flag<F>(h, w1, w1sb, wmax);
+                    const bool big = wmax > 62;
                     const uint32_t a_tile = a_slot + my_jj * 16384;
                     const bool dirty = h ? p2_dirty1 : p2_dirty0;
                     unpack_q6(a_tile, a_tile + 32768, r, cur.ql, cur.qh, scj, my_jj, big, !big && dirty);
@@ -848,6 +1091,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     }
                     d = half_lo(cur.hdr.x);
                     dmin = half_hi(cur.hdr.x);
+                    if (lane == 0) s_flag[16 * (gg & 1) + 8 * h + uw] = (uint8_t)unit_flag<F>(h, w1, w1sb, 0);
                 }
                 if (h == 0 && my_jj == 0) {
                     s_d[(gg & 1) * BM + r] = d;
@@ -857,7 +1101,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&bar[BAR_FULL_A + h]);
-                    if (h == 0 && my_jj == 0) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
+                    // the scales and both halves' unit flags are written
+                    if (h == 1) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
                 }
                 cur = nxt;
             }
@@ -872,71 +1117,117 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if constexpr (F == FMT_Q6_K) {
         // ------------------------------------------------ epilogue, Q6_K
         // 4 warps, thread = weight row x every token column; y accumulates
-        // in TMEM columns 128..255 (the mins slot of buffer 0, which Q6_K
-        // does not use), read back once at the end of each tile
+        // in TMEM columns COL_Y.. (Q6_K has no mins), read back once at the
+        // end of each tile.  TMEM is read 16 columns at a time.
         const int ew = warp - w_epi<F>();    // 0..3
         const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
         const int r = 32 * quad + lane;
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 128 * ew;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
-        const uint32_t y_tm = lane_addr + 128;
+        const uint32_t y_tm = lane_addr + COL_Y;
+        constexpr bool dbg = DBG;
         griddep_wait();  // the scales are written by the kernels before this one
         int ntiles = 1;
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
         }
-        int64_t g = 0;
+        int64_t g = 0, u = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
             const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
             const int64_t n = t.n0 + r;
-            const int nchunk = t.n_mma / 8;
+            const int nc = t.n_mma / 16;
+            bool first = true;
+            // the token scales d8 of the next superblock, loaded one superblock ahead
+            float d8n[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t tc = t.t0 + 32 * q + lane;
+                d8n[q] = tc < t.t_end ? __ldg(p.d8t + tc) : 0.0f;
+            }
             for (int64_t sb = 0; sb < nsb; ++sb) {
                 const int64_t gg = g + sb;
                 const int b = (int)(gg & 1);
-                // the 128 token scales d8 of the superblock
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int64_t tc = t.t0 + 32 * q + lane;
-                    s_d8[32 * q + lane] = tc < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
-                }
+                for (int q = 0; q < 4; ++q) s_d8[32 * q + lane] = d8n[q];
                 __syncwarp();
-                bool w_ok = mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1));
-                if (w_ok) w_ok = mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((gg >> 1) & 1));
-                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                if (sb + 1 < nsb) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int64_t tc = t.t0 + 32 * q + lane;
+                        d8n[q] = tc < t.t_end ? __ldg(p.d8t + (sb + 1) * p.Mp + tc) : 0.0f;
+                    }
+                }
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1)))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const float dd = s_d[b * BM + r];
-                for (int c = 0; c < nchunk; ++c) {
-                    uint32_t vi[8], vy[8];
-                    tmem_ld8(lane_addr + 256 * b + 8 * c, vi);
-                    if (sb > 0) tmem_ld8(y_tm + 8 * c, vy);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float yo = sb > 0 ? __uint_as_float(vy[i]) : 0.0f;
-                        vy[i] = __float_as_uint(fmaf(s_d8[8 * c + i], dd * __uint_as_float(vi[i]), yo));
-                    }
-                    tmem_st8(y_tm + 8 * c, vy);
-                }
-                tmem_wait_st();
-                tc_fence_before();
+                const int nu = sb_plan(ld_flags(flag_sa + 16 * b), ld_flags(flag_sa + 16 * b + 8)).n;
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+                if (lane == 0) mbar_arrive(&bar[BAR_SD_EMPTY + b]);
+                if (t.ntok == 0) continue;
+                if (nu == 1) {
+                    // one unit for the superblock (the common case)
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (uint32_t)((u / NU) & 1)))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = lane_addr + 128 * (uint32_t)(u % NU);
+                    if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xa, false, 0u, false, 0u, t.n_mma, t.t0, t.t_end, n, sb);
+                    else if (first) fold_units_q6<false, true>(xa, 0u, y_tm, nc, dd, s_d8);
+                    else fold_units_q6<false, false>(xa, 0u, y_tm, nc, dd, s_d8);
+                    if (!dbg) tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[BAR_U_EMPTY + (int)(u % NU)]);
+                    ++u;
+                    first = false;
+                    continue;
+                }
+                // several units, two at a time: y += d8 * d * (Ua + Ub)
+                for (int left = nu; left > 0 && ok;) {
+                    const int m = left >= 2 ? 2 : 1;
+                    bool w_ok = mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (uint32_t)((u / NU) & 1));
+                    if (w_ok && m == 2) w_ok = mbar_wait(&bar[BAR_U_FULL + (int)((u + 1) % NU)], (uint32_t)(((u + 1) / NU) & 1));
+                    if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xa = lane_addr + 128 * (uint32_t)(u % NU), xb = lane_addr + 128 * (uint32_t)((u + 1) % NU);
+                    if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xa, m == 2, xb, false, 0u, t.n_mma, t.t0, t.t_end, n, sb);
+                    else if (m == 2 && first) fold_units_q6<true, true>(xa, xb, y_tm, nc, dd, s_d8);
+                    else if (m == 2) fold_units_q6<true, false>(xa, xb, y_tm, nc, dd, s_d8);
+                    else if (first) fold_units_q6<false, true>(xa, xb, y_tm, nc, dd, s_d8);
+                    else fold_units_q6<false, false>(xa, xb, y_tm, nc, dd, s_d8);
+                    if (!dbg) tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bar[BAR_U_EMPTY + (int)(u % NU)]);
+                        if (m == 2) mbar_arrive(&bar[BAR_U_EMPTY + (int)((u + 1) % NU)]);
+                    }
+                    u += m;
+                    left -= m;
+                    first = false;
+                }
+                if (!ok) break;
             }
             if (!ok) break;
-            tc_fence_after();
-            for (int c = 0; c < nchunk; ++c) {
-                uint32_t vy[8];
-                tmem_ld8(y_tm + 8 * c, vy);
-                tmem_wait_ld();
-                if (n < p.N) {
+            if (!dbg && t.ntok > 0) {
+                tc_fence_after();
+                for (int c = 0; c < nc; ++c) {
+                    uint32_t vy[16];
+                    tmem_ld16(y_tm + 16 * c, vy);
+                    tmem_wait_ld();
+                    if (n < p.N) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int64_t tt = t.t0 + 8 * c + i;
-                        if (tt < t.t_end) p.y[tt * p.N + n] = __uint_as_float(vy[i]);
+                        for (int i = 0; i < 16; ++i) {
+                            const int64_t tt = t.t0 + 16 * c + i;
+                            if (tt < t.t_end) p.y[tt * p.N + n] = __uint_as_float(vy[i]);
+                        }
                     }
                 }
             }
@@ -944,74 +1235,98 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         if (!ok && lane == 0) set_timeout();
     } else {
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue, Q4_K / Q5_K
+        // 8 warps, thread = weight row x 64 token columns, y in registers.
+        // Each unit is folded as it lands, the first of a superblock with
+        // msum: y += d8 * (d * U0 - dmin * msum), then y += d8 * d * Uk.
         const int ew = warp - w_epi<F>();    // 0..7
         const int quad = warp & 3;           // TMEM lanes 32*quad .. +31
         const int ch = ew >> 2;              // token columns 64*ch .. +63
         const int r = 32 * quad + lane;
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 64 * ew;
-        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16);
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16) + 64 * ch;
         griddep_wait();  // the scales are written by the kernels before this one
         int ntiles = 1;
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
         }
-        int64_t g = 0;
+        // 32-bit counters: a block runs at most TILE_CAP tiles of at most 2^22 superblocks
+        uint32_t g = 0, u = 0, mc = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
             const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+            const int n = t.n0 + r;
             float y[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) y[i] = 0.0f;
             const bool cols = 64 * ch < t.n_mma;
-            for (int64_t sb = 0; sb < nsb; ++sb) {
-                const int64_t gg = g + sb;
+            // this warp's 64 token scales d8 of the next superblock, loaded one superblock ahead
+            const int tc = t.t0 + 64 * ch + lane;
+            const float *d8col = p.d8t + tc;
+            float d8n0 = tc < t.t_end ? __ldg(d8col) : 0.0f;
+            float d8n1 = (tc + 32) < t.t_end ? __ldg(d8col + 32) : 0.0f;
+            for (int sb = 0; sb < (int)nsb; ++sb) {
+                const uint32_t gg = g + (uint32_t)sb;
                 const int b = (int)(gg & 1);
-                // this warp's 64 token scales d8 for the superblock
-                {
-                    const int64_t tc = t.t0 + 64 * ch + lane;
-                    s_d8[lane] = tc < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc) : 0.0f;
-                    s_d8[lane + 32] = (tc + 32) < t.t_end ? __ldg(p.d8t + sb * p.Mp + tc + 32) : 0.0f;
-                    __syncwarp();
+                s_d8[lane] = d8n0;
+                s_d8[lane + 32] = d8n1;
+                __syncwarp();
+                if (sb + 1 < (int)nsb) {
+                    const float *d8p = d8col + (int64_t)(sb + 1) * p.Mp;
+                    d8n0 = tc < t.t_end ? __ldg(d8p) : 0.0f;
+                    d8n1 = (tc + 32) < t.t_end ? __ldg(d8p + 32) : 0.0f;
                 }
-                bool w_ok = mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1));
-                if (w_ok) w_ok = mbar_wait(&bar[BAR_ACC_FULL + b], (uint32_t)((gg >> 1) & 1));
-                if (!__all_sync(0xFFFFFFFFu, w_ok)) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_SD_FULL + b], (uint32_t)((gg >> 1) & 1)))) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const float dd = s_d[b * BM + r], dm = s_dmin[b * BM + r];
-                if (cols) {
-#pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        uint32_t vi[16], vm[16];
-                        tmem_ld16(lane_addr + 256 * b + 64 * ch + 16 * cc, vi);
-                        if (C::kMins) tmem_ld16(lane_addr + 256 * b + 128 + 64 * ch + 16 * cc, vm);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float iv = __uint_as_float(vi[i]);
-                            float tv = dd * iv;
-                            if (C::kMins) tv = fmaf(-dm, __uint_as_float(vm[i]), tv);
-                            y[16 * cc + i] = fmaf(s_d8[16 * cc + i], tv, y[16 * cc + i]);
-                        }
+                const int nu = sb_plan(ld_flags(flag_sa + 16 * b), ld_flags(flag_sa + 16 * b + 8)).n;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[BAR_SD_EMPTY + b]);
+                if (t.ntok == 0) continue;
+                // the superblock's units; msum is folded with the first (and
+                // multiplied by 0 with the others, so one fold serves all: its
+                // slot is held until the last unit)
+                const int mb = (int)(mc & 1);
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_M_FULL + mb], (mc >> 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t xm = lane_addr + COL_M + 128 * (uint32_t)mb;
+#pragma unroll 1
+                for (int v = 0; v < nu; ++v, ++u) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (u / NU) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xu = lane_addr + 128 * (u % NU);
+                    if (cols) {
+                        // 8 columns a TMEM round trip: with y[64] and the loop's
+                        // state live, 16 would spill
+                        if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xu, false, 0u, v == 0, xm, 64, t.t0 + 64 * ch, t.t_end, n, sb);
+                        else fold_unit_q45<8>(y, xu, xm, dd, v == 0 ? dm : 0.0f, s_d8);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&bar[BAR_U_EMPTY + (int)(u % NU)]);
+                        if (v == nu - 1) mbar_arrive(&bar[BAR_M_EMPTY + mb]);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[BAR_ACC_EMPTY + b]);
+                ++mc;
+                if (!ok) break;
             }
             if (!ok) break;
-            const int n = t.n0 + r;
-            if (n < p.N && cols) {
+            if (!DBG && n < p.N && cols) {
                 const int c0 = t.t0 + 64 * ch, lim = t.t_end - c0;
                 float *yp = p.y + (int64_t)c0 * p.N + n;
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
                     if (i < lim) yp[(int64_t)i * p.N] = y[i];
             }
-            g += nsb;
+            g += (uint32_t)nsb;
         }
         if (!ok && lane == 0) set_timeout();
     }
@@ -1114,7 +1429,8 @@ size_t gemm_workspace_bytes(int, int64_t M, int64_t, int64_t K) {
 
 template <int F>
 static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
-                                 int64_t E, uint64_t expert_bytes, float *y, uint8_t *ws, cudaStream_t s) {
+                                 int64_t E, uint64_t expert_bytes, float *y, uint8_t *ws, cudaStream_t s,
+                                 int32_t *isum_out = nullptr, int32_t *msum_out = nullptr) {
     using Cf = Cfg<F>;
     const WsLayout L = ws_layout(M, K);
     __half *a16 = reinterpret_cast<__half *>(ws + L.a16);
@@ -1146,10 +1462,12 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_kernel<F, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemm_kernel<F, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
-        if (e != cudaSuccess) return e;
+        const void *fns[4] = {(const void *)gemm_kernel<F, false, false>, (const void *)gemm_kernel<F, true, false>,
+                              (const void *)gemm_kernel<F, false, true>, (const void *)gemm_kernel<F, true, true>};
+        for (const void *fn : fns) {
+            const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
+            if (e != cudaSuccess) return e;
+        }
         attr_set[dev].store(true, std::memory_order_release);
     }
     GemmParams p{};
@@ -1164,6 +1482,14 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     p.d8t = d8t;
     p.Mp = L.Mp;
     p.y = y;
+    p.isum_out = isum_out;
+    p.msum_out = msum_out;
+    if (isum_out) {
+        const size_t bytes = (size_t)M * (size_t)N * (size_t)(K / QK) * sizeof(int32_t);
+        cudaError_t e = cudaMemsetAsync(isum_out, 0, bytes, s);
+        if (e == cudaSuccess) e = cudaMemsetAsync(msum_out, 0, bytes, s);
+        if (e != cudaSuccess) return e;
+    }
     // dense: one block per tile; grouped: a block per SM walking a list of
     // tiles (the experts' first token tiles, plus at most M / BT later ones),
     // with enough blocks that no list exceeds TILE_CAP
@@ -1196,8 +1522,12 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-    if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true>, ma, mb, p);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false>, ma, mb, p);
+    if (isum_out) {
+        if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, true>, ma, mb, p);
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, true>, ma, mb, p);
+    }
+    if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, false>, ma, mb, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, false>, ma, mb, p);
 }
 
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
@@ -1210,6 +1540,20 @@ cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K 
     if (f == FMT_Q4_K) return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
     if (f == FMT_Q5_K) return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
     return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
+}
+
+cudaError_t launch_gemm_tc_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
+                                    const int32_t *offsets, int64_t E, uint64_t expert_bytes, int32_t *isum,
+                                    int32_t *msum, void *workspace, size_t workspace_bytes, cudaStream_t s) {
+    if (M < GEMM_TC_MIN_M || !workspace) return cudaErrorNotSupported;
+    if (workspace_bytes < ws_layout(M, K).total) return cudaErrorInvalidValue;
+    if (M > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX / 2) return cudaErrorNotSupported;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (f == FMT_Q4_K)
+        return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
+    if (f == FMT_Q5_K)
+        return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
+    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
 }
 
 // Test hook: one block whose single bounded wait is never satisfied, so the

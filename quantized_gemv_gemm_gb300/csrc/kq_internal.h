@@ -95,6 +95,13 @@ cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K 
                            const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
                            void *workspace, size_t workspace_bytes, cudaStream_t s);
 
+// The same kernel with the debug epilogue: per (row, weight row, superblock)
+// the int32 sums isum / msum [M][N][K/256] (zero-filled here, then
+// accumulated) instead of y.
+cudaError_t launch_gemm_tc_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
+                                    const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, int32_t *isum,
+                                    int32_t *msum, void *workspace, size_t workspace_bytes, cudaStream_t s);
+
 // The C-ABI body of the three GEMM entry points (kq_api.cu).
 int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offsets, int64_t N, int64_t K,
                 kq_q8k_const a, int64_t M, float *y, void *ws, size_t ws_bytes, cudaStream_t s);

@@ -58,6 +58,41 @@ __device__ __forceinline__ uint4 piece16(const uint16_t *src) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// W1 of half h of one disk superblock: the sum over its 128 weights of
+// |sub-scale| * |q| (Q4_K/Q5_K: q with its fifth bit; Q6_K: q - 32), in the
+// GGUF element order (the same order the kernels unpack).
+template <int F>
+__device__ uint32_t half_l1(const uint8_t *blk, int h) {
+    uint32_t w1 = 0;
+    if constexpr (F == FMT_Q4_K || F == FMT_Q5_K) {
+        const uint8_t *sc = blk + 4;
+        const uint8_t *qh = blk + 16;
+        const uint8_t *qs = blk + (F == FMT_Q5_K ? 48 : 16);
+        for (int j = 4 * h; j < 4 * h + 4; ++j) {
+            const uint32_t s = j < 4 ? (sc[j] & 63u) : ((sc[j + 4] & 15u) | ((uint32_t)(sc[j - 4] >> 6) << 4));
+            uint32_t sum = 0;
+            for (int l = 0; l < 32; ++l) {
+                const uint8_t b = qs[32 * (j >> 1) + l];
+                uint32_t q = (j & 1) ? (b >> 4) : (b & 15u);
+                if constexpr (F == FMT_Q5_K) q += 16u * ((qh[l] >> j) & 1u);
+                sum += q;
+            }
+            w1 += s * sum;
+        }
+    } else {
+        const uint8_t *ql = blk + 64 * h, *qh = blk + 128 + 32 * h;
+        const int8_t *sc = reinterpret_cast<const int8_t *>(blk + 192);
+        for (int t = 0; t < 4; ++t)
+            for (int l = 0; l < 32; ++l) {
+                const uint8_t b = ql[32 * (t & 1) + l];
+                const int q = (int)((t < 2 ? (b & 15u) : (b >> 4)) | (((qh[l] >> (2 * t)) & 3u) << 4));
+                const int s = sc[8 * h + 2 * t + l / 16];
+                w1 += (uint32_t)((s < 0 ? -s : s) * (q < 32 ? 32 - q : q - 32));
+            }
+    }
+    return w1;
+}
+
 template <int F>
 __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__ disk, int64_t N, int64_t nsb,
                                                      int64_t units, Planes P) {
@@ -86,6 +121,14 @@ __global__ void __launch_bounds__(256) repack_kernel(const uint8_t *__restrict__
         put(p2 + ch * 256 + 16 * r, piece(96));                                    // scales (int8)
         reinterpret_cast<uint16_t *>(p3 + ch * 32)[r] = real ? b[104] : uint16_t(0);  // d
     }
+    // the group's bounds: the largest W1 of each half over its rows (the
+    // plane is zero-filled before this kernel)
+    if (real) {
+        const uint8_t *blk = reinterpret_cast<const uint8_t *>(b);
+        uint32_t *bound = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(P.p4)) + 2 * (int64_t)ch;
+        atomicMax(bound, half_l1<F>(blk, 0));
+        atomicMax(bound + 1, half_l1<F>(blk, 1));
+    }
 }
 
 cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,
@@ -94,6 +137,8 @@ cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint
     const int64_t units = row_groups(N) * GROUP_ROWS * nsb;
     if (units == 0) return cudaSuccess;
     const Planes P = make_planes(f, packed, N, nsb);
+    cudaError_t e = cudaMemsetAsync(const_cast<uint8_t *>(P.p4), 0, (size_t)row_groups(N) * nsb * BOUND_BYTES, s);
+    if (e != cudaSuccess) return e;
     const unsigned grid = (unsigned)((units + 255) / 256);
     if (f == FMT_Q4_K) repack_kernel<FMT_Q4_K><<<grid, 256, 0, s>>>(disk, N, nsb, units, P);
     else if (f == FMT_Q5_K) repack_kernel<FMT_Q5_K><<<grid, 256, 0, s>>>(disk, N, nsb, units, P);

@@ -47,7 +47,8 @@ def assert_row_tol(y_gpu: np.ndarray, y_ref: np.ndarray, rel: float = 1e-3, row_
         i, j = np.argwhere(bad)[0]
         raise AssertionError(f"{bad.sum()} outputs off; first at {i},{j}: gpu {y_gpu[i, j]} ref {y_ref[i, j]} "
                              f"tol {rel * scale[i, 0]}; max err/scale {float((err / scale).max()):.3e}")
-    return float((err / scale).max())
+    with np.errstate(divide="ignore", invalid="ignore"):
+        return float(np.nanmax(np.where(scale > 0, err / np.where(scale > 0, scale, 1.0), 0.0)))
 
 
 def poisoned(shape, guard=64):

@@ -42,7 +42,8 @@ def test_sizes_and_names(kq):
             assert nb % 256 == 0
             disk = N * (K // 256) * per_sb
             padded = -(-N // 16) * 16 * (K // 256) * per_sb   # rows padded to groups of 16
-            assert disk <= nb <= padded + 4 * 255
+            bounds = -(-N // 16) * (K // 256) * 8             # the bounds plane: 8 B per (row group, superblock)
+            assert disk + bounds <= nb <= padded + bounds + 5 * 255
     assert kq.kq_repack_bytes(1, 10, 100) == 0
     assert kq.kq_repack_bytes(1, -1, 256) == 0
     assert kq.kq_repack_bytes(5, 10, 256) == 0
