@@ -300,6 +300,19 @@ int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_
                       int64_t M, int32_t *isum, int32_t *msum, cudaStream_t s);
 
 /*
+ * Test hook: the same int32 partials from the small-batch passes' integer
+ * warp-MMA fold (the 8-token passes of kq_gemm / kq_gemv_fused_batch for
+ * Q4_K and Q6_K; the other passes fold with the GEMV's dp4a code above),
+ * run by the same device functions on M <= 8 token rows ([kq-arc], kq v3
+ * panel-scratch commit: every tile form must equal the GEMV bit for bit).
+ *   f           KQ_Q4_K or KQ_Q6_K (KQ_Q5_K: KQ_ERR_ARG, it has no such fold)
+ *   isum, msum  device int32 [M][N][K/256], as kq_debug_partials
+ * Errors: KQ_ERR_FORMAT, KQ_ERR_ARG (M > 8, null), KQ_ERR_ALIGN, KQ_ERR_LAUNCH.
+ */
+int kq_debug_batch_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M,
+                            int32_t *isum, int32_t *msum, cudaStream_t s);
+
+/*
  * Test hook: the same int32 partials from the tensor-core GEMM ([kq-arc],
  * kq v3 panel-scratch commit: the tile must equal the GEMV bit for bit,
  * unpack included).  It runs the kq_gemm / kq_gemm_grouped kernel with its

@@ -265,6 +265,18 @@ int kq_debug_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_
     return launch_status(launch_partials(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, M, isum, msum, s));
 }
 
+int kq_debug_batch_partials(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M,
+                            int32_t *isum, int32_t *msum, cudaStream_t s) {
+    if (f != KQ_Q4_K && f != KQ_Q6_K) return fmt_ok(f) ? KQ_ERR_ARG : KQ_ERR_FORMAT;
+    if (int r = check_shape(N, K)) return r;
+    if (M < 0 || M > 8) return KQ_ERR_ARG;
+    if (M == 0 || N == 0) return KQ_OK;
+    if (!packed || !isum || !msum) return KQ_ERR_ARG;
+    if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
+    if (!aligned(packed, 256) || !aligned(isum, 4) || !aligned(msum, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_mma_partials(f, packed, N, K, Q8K{a.d, a.qs, a.bsums}, M, isum, msum, s));
+}
+
 int kq_debug_gemm_partials(kq_format f, const void *packed, int64_t E, const int32_t *row_offsets, int64_t N,
                            int64_t K, kq_q8k_const a, int64_t M, int32_t *isum, int32_t *msum, void *workspace,
                            size_t workspace_bytes, cudaStream_t s) {

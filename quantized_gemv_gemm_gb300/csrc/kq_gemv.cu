@@ -395,23 +395,25 @@ __device__ __forceinline__ void mma_read(MmaQ6 &w, uint32_t st, int gq, int cq) 
     w.d[1] = lds16(st + 3328u + 2u * (gq + 8));
 }
 
-// Fold of one item for the pass: acc[rr * 2 + k] (row gq + 8 rr, token
-// 2cq + k) += d * d8 * isum - dmin * d8 * msum.  act = shared address of
-// token 0's activation superblock, sums / d8s of its sums and scale; tokens
-// are tstride apart; tokens at or past ntok are not read (their columns are
-// zero and their accumulators unused).
-__device__ __forceinline__ void mma_fold(const MmaQ4 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
-                                         uint32_t d8s, uint32_t tstride, float (&acc)[4]) {
+// Integer sums of one item for the pass: isum[rr * 2 + k], msum[rr * 2 + k]
+// (row gq + 8 rr, token 2cq + k) -- Q4_K isum = sum_j sc_j * dot32_j and
+// msum = sum_j m_j * (bs_2j + bs_2j+1); Q6_K isum = iacc - 32 * bacc and
+// msum = 0.  act = shared address of token 0's activation superblock, sums
+// of its sums; tokens are tstride apart; tokens at or past ntok are not read
+// (their columns are zero and their sums left 0).
+__device__ __forceinline__ void mma_isums(const MmaQ4 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
+                                          uint32_t tstride, int (&isum)[4], int (&msum)[4]) {
     constexpr uint32_t LO = 0x0F0F0F0Fu;
     const bool bt = gq < ntok;
     const uint32_t ab = act + (uint32_t)gq * tstride + 4u * cq;
-    int isum[4] = {0, 0, 0, 0};
     uint32_t scw[2][2], mw[2][2];  // [row][half]
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         scale_words(w.hdr[rr], 0, scw[rr][0], mw[rr][0]);
         scale_words(w.hdr[rr], 1, scw[rr][1], mw[rr][1]);
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) isum[i] = msum[i] = 0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int h2 = j >> 2, jj = j & 3, pp = (jj >> 1) * 2, sh = 4 * (jj & 1);
@@ -433,26 +435,23 @@ __device__ __forceinline__ void mma_fold(const MmaQ4 &w, int gq, int cq, int nto
             const uint32_t so = sums + (uint32_t)t * tstride;
             const uint4 S0 = lds128(so), S1 = lds128(so + 16u);  // the 8 sub-block sums
             const int Sv[8] = {(int)S0.x, (int)S0.y, (int)S0.z, (int)S0.w, (int)S1.x, (int)S1.y, (int)S1.z, (int)S1.w};
-            const float d8 = __uint_as_float(lds32(d8s + (uint32_t)t * tstride));
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                int msum = 0;
+                int m = 0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) msum += byte_u(mw[rr][j >> 2], j & 3) * Sv[j];
-                const float dw = half_lo(w.hdr[rr].x), dmw = half_hi(w.hdr[rr].x);
-                float a = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k]), acc[rr * 2 + k]);
-                acc[rr * 2 + k] = fmaf(-(dmw * d8), static_cast<float>(msum), a);
+                for (int j = 0; j < 8; ++j) m += byte_u(mw[rr][j >> 2], j & 3) * Sv[j];
+                msum[rr * 2 + k] = m;
             }
         }
     }
 }
 
-__device__ __forceinline__ void mma_fold(const MmaQ6 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
-                                         uint32_t d8s, uint32_t tstride, float (&acc)[4]) {
+__device__ __forceinline__ void mma_isums(const MmaQ6 &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
+                                          uint32_t tstride, int (&isum)[4], int (&msum)[4]) {
     constexpr uint32_t LO = 0x0F0F0F0Fu, HB = 0x30303030u;
     const bool bt = gq < ntok;
     const uint32_t ab = act + (uint32_t)gq * tstride + 4u * cq;
-    int isum[4] = {0, 0, 0, 0};
+    int iacc[4] = {0, 0, 0, 0};
     const uint32_t scv[2][4] = {{w.sc[0].x, w.sc[0].y, w.sc[0].z, w.sc[0].w},
                                 {w.sc[1].x, w.sc[1].y, w.sc[1].z, w.sc[1].w}};
 #pragma unroll
@@ -476,12 +475,14 @@ __device__ __forceinline__ void mma_fold(const MmaQ6 &w, int gq, int cq, int nto
             mma_k16_u8s8(dd, a[0], a[1], b0);
             const int grp = 8 * h2 + t;
             const int s0 = byte_s(scv[0][grp >> 2], grp & 3), s1 = byte_s(scv[1][grp >> 2], grp & 3);
-            isum[0] += s0 * dd[0];
-            isum[1] += s0 * dd[1];
-            isum[2] += s1 * dd[2];
-            isum[3] += s1 * dd[3];
+            iacc[0] += s0 * dd[0];
+            iacc[1] += s0 * dd[1];
+            iacc[2] += s1 * dd[2];
+            iacc[3] += s1 * dd[3];
         }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) isum[i] = msum[i] = 0;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         const int t = 2 * cq + k;
@@ -489,15 +490,41 @@ __device__ __forceinline__ void mma_fold(const MmaQ6 &w, int gq, int cq, int nto
             const uint32_t so = sums + (uint32_t)t * tstride;
             const uint4 B0 = lds128(so), B1 = lds128(so + 16u);  // the 16 int16 bsums
             const uint32_t bw[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
-            const float d8 = __uint_as_float(lds32(d8s + (uint32_t)t * tstride));
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 int bacc = 0;
 #pragma unroll
                 for (int grp = 0; grp < 16; ++grp)
                     bacc += byte_s(scv[rr][grp >> 2], grp & 3) * half_s(bw[grp >> 1], grp & 1);
-                const float dw = half_lo(w.d[rr]);
-                acc[rr * 2 + k] = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k] - 32 * bacc), acc[rr * 2 + k]);
+                isum[rr * 2 + k] = iacc[rr * 2 + k] - 32 * bacc;
+            }
+        }
+    }
+}
+
+// Fold of one item for the pass: acc[rr * 2 + k] (row gq + 8 rr, token
+// 2cq + k) += d * d8 * isum - dmin * d8 * msum, from the integer sums
+// above; d8s = shared address of token 0's scale (tokens tstride apart).
+template <typename MItem>
+__device__ __forceinline__ void mma_fold(const MItem &w, int gq, int cq, int ntok, uint32_t act, uint32_t sums,
+                                         uint32_t d8s, uint32_t tstride, float (&acc)[4]) {
+    int isum[4], msum[4];
+    mma_isums(w, gq, cq, ntok, act, sums, tstride, isum, msum);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int t = 2 * cq + k;
+        if (t < ntok) {
+            const float d8 = __uint_as_float(lds32(d8s + (uint32_t)t * tstride));
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                if constexpr (std::is_same<MItem, MmaQ4>::value) {
+                    const float dw = half_lo(w.hdr[rr].x), dmw = half_hi(w.hdr[rr].x);
+                    const float a = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k]), acc[rr * 2 + k]);
+                    acc[rr * 2 + k] = fmaf(-(dmw * d8), static_cast<float>(msum[rr * 2 + k]), a);
+                } else {
+                    const float dw = half_lo(w.d[rr]);
+                    acc[rr * 2 + k] = fmaf(dw * d8, static_cast<float>(isum[rr * 2 + k]), acc[rr * 2 + k]);
+                }
             }
         }
     }
@@ -1286,6 +1313,72 @@ __global__ void __launch_bounds__(256) partials_kernel(const uint8_t *packed, in
         isum_out[o] = isum;
         msum_out[o] = msum;
     }
+}
+
+// Test hook: the integer sums of the 8-token passes' integer-MMA fold
+// (MmaFold, Q4_K and Q6_K), per (token, row, superblock).  One warp per
+// (row group, superblock): the item is fetched with item_issue, the M <= 8
+// token rows' superblock staged side by side as the batch kernel stages
+// them (quants, then the sums the fold needs), and mma_read + mma_isums
+// run on them as in the batch kernel.
+template <int F>
+__global__ void __launch_bounds__(32) mma_partials_kernel(const uint8_t *packed, int64_t N, int64_t nsb, int64_t K,
+                                                          Q8K a, int ntok, int32_t *isum_out, int32_t *msum_out) {
+    constexpr int SLOT = GemvFmt<F>::SLOT;
+    constexpr uint32_t TSTRIDE = 304;  // 256 quants + 32 bytes of sums + d8, 16-byte aligned
+    __shared__ __align__(128) uint8_t s_item[SLOT];
+    __shared__ __align__(16) uint8_t s_tok[8 * TSTRIDE];
+    __shared__ uint64_t s_bar;
+    const int lane = threadIdx.x;
+    const int64_t g = blockIdx.x, sb = blockIdx.y;
+    for (int t = 0; t < ntok; ++t) {
+        reinterpret_cast<uint2 *>(s_tok + t * TSTRIDE)[lane] =
+            reinterpret_cast<const uint2 *>(a.qs + t * K + sb * QK)[lane];
+        const int16_t *gb = a.bsums + (t * nsb + sb) * 16;
+        if constexpr (F != FMT_Q6_K) {
+            if (lane < 8) reinterpret_cast<int *>(s_tok + t * TSTRIDE + 256)[lane] = (int)gb[2 * lane] + (int)gb[2 * lane + 1];
+        } else {
+            if (lane < 16) reinterpret_cast<int16_t *>(s_tok + t * TSTRIDE + 256)[lane] = gb[lane];
+        }
+    }
+    if (lane == 0) {
+        sm100::mbar_init(&s_bar, 1);
+        sm100::mbar_fence_init();
+    }
+    __syncwarp();
+    const Planes P = make_planes(F, packed, N, nsb);
+    ChunkPtr cp = chunk_ptr<F>(P, (uint64_t)g * nsb + sb);
+    if (lane == 0) item_issue<F>(cp, smem_addr(s_item), smem_addr(&s_bar), true, weight_stream_policy());
+    stage_wait(&s_bar, 0);
+    using MItem = typename std::conditional<F == FMT_Q6_K, MmaQ6, MmaQ4>::type;
+    const int gq = lane >> 2, cq = lane & 3;
+    MItem w;
+    mma_read(w, smem_addr(s_item), gq, cq);
+    int isum[4], msum[4];
+    mma_isums(w, gq, cq, ntok, smem_addr(s_tok), smem_addr(s_tok) + 256u, TSTRIDE, isum, msum);
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int t = 2 * cq + k;
+            const int64_t n = g * GROUP_ROWS + gq + 8 * rr;
+            if (t < ntok && n < N) {
+                const int64_t o = ((int64_t)t * N + n) * nsb + sb;
+                isum_out[o] = isum[rr * 2 + k];
+                msum_out[o] = msum[rr * 2 + k];
+            }
+        }
+}
+
+cudaError_t launch_mma_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, int32_t *isum,
+                                int32_t *msum, cudaStream_t s) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    const int64_t nsb = K / QK;
+    dim3 grid((unsigned)row_groups(N), (unsigned)nsb);
+    const uint8_t *pk = static_cast<const uint8_t *>(packed);
+    if (f == FMT_Q4_K) mma_partials_kernel<FMT_Q4_K><<<grid, 32, 0, s>>>(pk, N, nsb, K, a, (int)M, isum, msum);
+    else mma_partials_kernel<FMT_Q6_K><<<grid, 32, 0, s>>>(pk, N, nsb, K, a, (int)M, isum, msum);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,

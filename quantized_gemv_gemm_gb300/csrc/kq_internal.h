@@ -81,6 +81,9 @@ cudaError_t launch_gemv_grouped(int f, int sets, const void *const *packed, cons
 
 cudaError_t launch_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                             int32_t *isum, int32_t *msum, cudaStream_t s);
+// the same from the small-batch passes' integer-MMA fold (Q4_K, Q6_K; M <= 8)
+cudaError_t launch_mma_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, int32_t *isum,
+                                int32_t *msum, cudaStream_t s);
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t s);
 cudaError_t launch_mma_s8_rate(int64_t blocks, int64_t iters, int32_t *out, cudaStream_t s);

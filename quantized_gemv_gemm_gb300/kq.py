@@ -52,6 +52,7 @@ _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_grouped.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_noalloc.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P]
 _lib.kq_debug_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
+_lib.kq_debug_batch_partials.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P]
 _lib.kq_debug_gemm_partials.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _P, _SZ, _P]
 _lib.kq_debug_decode.argtypes = [_INT, _P, _I64, _I64, _P, _P, _P, _P, _P, _P]
 _lib.kq_device_status.argtypes = [_P]
@@ -66,7 +67,7 @@ _lib.kq_set_launch_flags.restype = ctypes.c_uint
 _lib.kq_get_launch_flags.argtypes = []
 _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
-           "kq_debug_partials", "kq_debug_gemm_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
+           "kq_debug_partials", "kq_debug_gemm_partials", "kq_debug_batch_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
            "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout",
            "kq_gemv_q8_0_fused", "kq_copy_in"):
     getattr(_lib, _f).restype = _INT
@@ -331,6 +332,18 @@ def kq_debug_partials(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, st
     msum = torch.zeros_like(isum)
     _check(_lib.kq_debug_partials(int(fmt), _ptr(packed), N, K, _q8k_struct(a), M, _ptr(isum), _ptr(msum),
                                   _stream(stream)), "kq_debug_partials")
+    return isum, msum
+
+
+def kq_debug_batch_partials(fmt: int, packed: torch.Tensor, N: int, K: int, a: Q8K, stream=None):
+    """int32 (isum, msum) [M, N, K/256] from the 8-token passes' integer-MMA
+    fold (Q4_K, Q6_K; M <= 8)."""
+    _need_cuda(packed, *a)
+    M = a.qs.shape[0]
+    isum = torch.zeros((M, N, K // QK), dtype=torch.int32, device=packed.device)
+    msum = torch.zeros_like(isum)
+    _check(_lib.kq_debug_batch_partials(int(fmt), _ptr(packed), N, K, _q8k_struct(a), M, _ptr(isum), _ptr(msum),
+                                        _stream(stream)), "kq_debug_batch_partials")
     return isum, msum
 
 

@@ -196,3 +196,20 @@ def test_repack_bounds_plane(K, fmt):
             for h in range(2):
                 want[n // 16, s, h] = max(want[n // 16, s, h], w[128 * h:128 * (h + 1)].sum())
     np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", [synth.Q4_K, synth.Q6_K])
+@pytest.mark.parametrize("M", [8, 5])
+def test_batch_mma_partials_bit_exact(K, fmt, M):
+    """The 8-token passes' integer warp-MMA fold: int32 partials per (token,
+    row, superblock) equal the oracle's and the GEMV's, on random fields and
+    on every field at its extreme (a ragged row group, fewer tokens than 8)."""
+    rng = synth.rng_for(145, fmt * 10 + M)
+    N, Kdim = 200, 768
+    disk = synth.disk_weights(fmt, N, Kdim, rng)
+    disk[16:48] = extreme_weights(fmt, 32, Kdim, rng)
+    for planes in (oracle_q8k(synth.activations(M, Kdim, rng)), extreme_tokens(max(M, 3), Kdim, rng)):
+        planes = tuple(p_[:M] for p_ in planes)
+        got_i, got_m = K.kq_debug_batch_partials(fmt, pack(K, fmt, disk), N, Kdim, q8k_to_dev(K, planes))
+        torch.cuda.synchronize()
+        check_against_oracle_and_gemv(K, fmt, disk, planes, got_i.cpu().numpy(), got_m.cpu().numpy())
