@@ -78,6 +78,7 @@ def lib():
             L.ko_quantize_q8_0.argtypes = [P, i64, i64, P, P]
             L.ko_quantize_q8_0.restype = None
             L.ko_gemv_q8_0.argtypes = [P, i64, i64, P, P, i64, P]
+            L.ko_partials_q8_0.argtypes = [P, i64, i64, P, i64, P]
             L.ko_bruteforce_q8_0.argtypes = [P, i64, P, P]
             L.ko_bruteforce_q8_0.restype = ctypes.c_double
             L.ko_num_threads.argtypes = []
@@ -209,6 +210,26 @@ def quantize_q8_0(x: np.ndarray):
     q = np.zeros((M, K), np.int8)
     lib().ko_quantize_q8_0(_p(x), M, K, _p(d), _p(q))
     return d, q
+
+
+def partials_q8_0(disk: np.ndarray, q_a: np.ndarray) -> np.ndarray:
+    """int32 per-block dots [M, N, K/32] of disk Q8_0 weights [N, K/32, 34] and M activation rows."""
+    disk = np.ascontiguousarray(disk, dtype=np.uint8)
+    q_a = np.ascontiguousarray(np.atleast_2d(q_a), dtype=np.int8)
+    N, nb, bb = disk.shape
+    assert bb == Q8_0_BLOCK
+    M, K = q_a.shape
+    assert K == nb * QK8_0
+    isum = np.zeros((M, N, nb), np.int32)
+    if lib().ko_partials_q8_0(_p(disk), N, K, _p(q_a), M, _p(isum)):
+        raise ValueError("ko_partials_q8_0 rejected its arguments")
+    return isum
+
+
+def gemm_q8_0(disk: np.ndarray, d_a: np.ndarray, q_a: np.ndarray) -> np.ndarray:
+    """Y[M, N] in float64: the Q8_0 product for M activation rows (the same
+    definition as gemv_q8_0, which takes any number of rows)."""
+    return gemv_q8_0(disk, d_a, q_a)
 
 
 def gemv_q8_0(disk: np.ndarray, d_a: np.ndarray, q_a: np.ndarray) -> np.ndarray:

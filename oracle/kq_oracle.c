@@ -376,6 +376,22 @@ int ko_gemv_q8_0(const uint8_t *disk, int64_t N, int64_t K, const float *d_a,
     return 0;
 }
 
+/* The integer dot of every 32-block, per (activation row m, weight row n,
+ * block b): isum[(m * N + n) * nb + b] = sum_k q_w * q_a over the block. */
+int ko_partials_q8_0(const uint8_t *disk, int64_t N, int64_t K, const int8_t *q_a, int64_t M, int32_t *isum) {
+    if (K % KO_QK8_0 || N < 0 || M < 0) return -1;
+    const int64_t nb = K / KO_QK8_0;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *blk = disk + (n * nb + b) * KO_Q8_0_BLOCK;
+                int32_t acc = 0;
+                for (int k = 0; k < KO_QK8_0; ++k) acc += (int32_t)(int8_t)blk[2 + k] * (int32_t)q_a[m * K + b * KO_QK8_0 + k];
+                isum[(m * N + n) * nb + b] = acc;
+            }
+    return 0;
+}
+
 double ko_bruteforce_q8_0(const uint8_t *row, int64_t nblk, const float *d_a, const int8_t *q_a) {
     double acc = 0.0;
     for (int64_t b = 0; b < nblk; ++b) {

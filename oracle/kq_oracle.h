@@ -111,6 +111,9 @@ int ko_gemv_q8_0(const uint8_t *disk, int64_t N, int64_t K, const float *d_a,
 
 /* Brute force for one row and one activation row: both dequantized to
  * double (d * q), plain dot product.  Independent of the fold. */
+/* Per-block int32 dots of Q8_0 weights [N][K/32] and M activation rows:
+ * isum [M][N][K/32].  Returns 0, or -1 for bad sizes. */
+int ko_partials_q8_0(const uint8_t *disk, int64_t N, int64_t K, const int8_t *q_a, int64_t M, int32_t *isum);
 double ko_bruteforce_q8_0(const uint8_t *row, int64_t nblk, const float *d_a,
                           const int8_t *q_a);
 

@@ -244,3 +244,43 @@ def test_q8_0_fold_matches_fp64_bruteforce(K):
     d2 = disk.copy()
     d2[0, 0, 2:] = disk[0, 0, 2:][::-1]
     assert oracle.gemv_q8_0(d2, d_a, q_a)[0, 0] != Y[0, 0]
+
+
+def test_q8_0_partials_closed_forms():
+    """Per-block int32 dots of the Q8_0 product: all ones against +127 tokens
+    gives 32 * 127 per block; alternating signs cancel to 0; the extremes
+    (+127 weights, -127 tokens) give -32 * 127 * 127; a weight nonzero in
+    one block only contributes to that block; each token row is its own."""
+    K = 256
+    one = 0x3C00
+    rows = np.stack([
+        _q8_0_row([one] * 8, np.ones(K)),
+        _q8_0_row([one] * 8, np.tile([1, -1], K // 2)),
+        _q8_0_row([one] * 8, np.full(K, 127)),
+        _q8_0_row([one] * 8, np.where(np.arange(K) // 32 == 5, np.arange(K) % 32 - 16, 0)),
+    ])
+    q_a = np.stack([np.full(K, 127), np.full(K, -127), np.tile([3, 3], K // 2)]).astype(np.int8)
+    p = oracle.partials_q8_0(rows, q_a)
+    assert p.shape == (3, 4, 8)
+    assert (p[0, 0] == 32 * 127).all() and (p[1, 0] == -32 * 127).all()
+    assert (p[:, 1] == 0).all()
+    assert (p[1, 2] == -32 * 127 * 127).all()
+    want5 = int((np.arange(32) - 16).sum()) * 3
+    assert p[2, 3, 5] == want5 and (np.delete(p[2, 3], 5) == 0).all()
+
+
+@pytest.mark.parametrize("M,K", [(3, 256), (4, 1024)])
+def test_q8_0_gemm_rows_from_partials_and_bruteforce(M, K):
+    """The M-row product: each output equals the fp64 brute force of its own
+    row, and folding the per-block partials by d_w * d_a reproduces it."""
+    rng = synth.rng_for(901, M * K)
+    disk = synth.disk_weights_q8_0(6, K, rng)
+    d_a, q_a = oracle.quantize_q8_0(synth.activations(M, K, rng, outliers=True))
+    Y = oracle.gemm_q8_0(disk, d_a, q_a)
+    P = oracle.partials_q8_0(disk, q_a)
+    d_w = disk[:, :, :2].copy().view(np.float16)[..., 0].astype(np.float64)
+    for m in range(M):
+        for n in range(6):
+            assert Y[m, n] == pytest.approx(oracle.bruteforce_q8_0(disk[n], d_a[m], q_a[m]), rel=1e-12, abs=1e-12)
+            fold = float((d_w[n] * d_a[m].astype(np.float64) * P[m, n]).sum())
+            assert Y[m, n] == pytest.approx(fold, rel=1e-12, abs=1e-12)
