@@ -828,6 +828,43 @@ def bench_gemm(kq, torch, peaks, args):
     dense("Qwen3-4B prefill pp512 all-Q5_K", 2, cfgs[2].matrices[:7], False)
     dense("Qwen3-4B prefill pp512 all-Q6_K", 2, cfgs[2].matrices[7:], False)
 
+    # Q8_0 rail at M = 512: the 27B-shaped FFN in Q8_0 (gate, up, down), each
+    # step quantizing its activations (kq_quantize_q8_0) and running the GEMM
+    M = 512
+    shapes = [(17408, 5120), (17408, 5120), (5120, 17408)]
+    wbytes = sum(N * Kd * 34 // 32 for N, Kd in shapes)
+    copies = max(1, -(-260_000_000 // wbytes))
+    items = []
+    for i, (N, Kd) in enumerate(shapes):
+        disk = torch.from_numpy(synth.disk_weights_q8_0(N, Kd, synth.rng_for(3, 60 + i)).reshape(-1)).cuda()
+        p0 = kq.kq_repack(synth.Q8_0, disk, N, Kd)
+        del disk
+        packed = [p0] + [p0.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(synth.activations(M, Kd, synth.rng_for(3, 160 + i), outliers=True)).cuda()
+        dq = torch.empty((M, Kd // 32), dtype=torch.float32, device="cuda")
+        qq = torch.empty((M, Kd), dtype=torch.int8, device="cuda")
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        items.append((N, Kd, packed, x, dq, qq, y))
+    torch.cuda.synchronize()
+
+    def q8_step(r):
+        for N, Kd, packed, x, dq, qq, y in items:
+            kq.kq_quantize_q8_0(x, d=dq, qs=qq)
+            kq.kq_gemm_q8_0(packed[r % copies], N, Kd, dq, qq, y=y)
+
+    ms = time_it(q8_step, args.gemm_reps)
+    ops = sum(2 * M * N * Kd for N, Kd in shapes)
+    tops = ops / (ms * 1e-3) / 1e12
+    out.append({"workload": "27B-shaped dense FFN in Q8_0, M=512 (kq_quantize_q8_0 + kq_gemm_q8_0 per matrix)",
+                "M": M, "ms": round(ms, 4), "tops": round(tops, 2),
+                "timing": f"median of timed graph replays of {args.gemm_reps} steps (>= 100 ms in all), "
+                          f"{copies} rotating weight copies",
+                "frac_of_fp16_tensor_peak": round(tops / tc_peak, 4),
+                "frac_of_int8_tensor_peak": None if i8_peak is None else round(tops / i8_peak, 4),
+                "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1)})
+    del items
+    torch.cuda.empty_cache()
+
     # MoE grouped
     cfg = cfgs[4]
     T, E = cfg.M, cfg.experts

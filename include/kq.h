@@ -360,6 +360,23 @@ int kq_debug_decode(kq_format f, const void *packed, int64_t N, int64_t K, int32
 int kq_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *qs, cudaStream_t s);
 
 /*
+ * Q8_0 GEMM (prefill, any M >= 1): y[m][n] = sum over the 32-blocks b of
+ * d_w(n, b) * d(m, b) * isum(m, n, b), isum the int32 dot of the block's
+ * weight quants and token m's activation quants, one float fold per block
+ * ([kq-arc], MoE prefill fix: the Q8_0 GEMMs read the Q8_0-form batch
+ * image).  Each block's dot is one warp-level integer MMA, exact in int32.
+ *   packed  device KQ_Q8_0 image from kq_repack (256-byte aligned)
+ *   d       device float32 [M][K/32] from kq_quantize_q8_0, 16-byte aligned
+ *   qs      device int8 [M][K], 16-byte aligned
+ *   y       device float32 [M][N] row-major
+ *   K       a positive multiple of 256
+ * The result is independent of scheduling (fixed summation order).
+ * Errors: KQ_ERR_ARG, KQ_ERR_ALIGN, KQ_ERR_LAUNCH.  M == 0 or N == 0 is a no-op.
+ */
+int kq_gemm_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, int64_t M, float *y,
+                 cudaStream_t s);
+
+/*
  * Q8_0 GEMV (M = 1): y[n] = sum over the 32-blocks b of row n of
  * d_w(n, b) * d(b) * isum_b, isum_b the int32 dot of the block's weight and
  * activation quants (one float fold per block).  Reads every packed byte once.

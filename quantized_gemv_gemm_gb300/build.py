@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkq.so")
 SOURCES = ["kq_api.cu", "kq_quant.cu", "kq_gemv.cu", "kq_mv.cu", "kq_gemm.cu", "kq_noalloc.cu", "kq_peak.cu",
-           "kq_q8_0.cu"]
+           "kq_q8_0.cu", "kq_q8_0_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -129,6 +129,15 @@ int kq_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d, int8_t *qs,
     return launch_status(launch_quantize_q8_0(x, M, K, d, qs, s));
 }
 
+int kq_gemm_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, int64_t M, float *y,
+                 cudaStream_t s) {
+    if (N < 0 || M < 0 || K <= 0 || K % QK != 0) return KQ_ERR_ARG;
+    if (M == 0 || N == 0) return KQ_OK;
+    if (!packed || !d || !qs || !y) return KQ_ERR_ARG;
+    if (!aligned(packed, 256) || !aligned(d, 16) || !aligned(qs, 16) || !aligned(y, 4)) return KQ_ERR_ALIGN;
+    return launch_status(launch_gemm_q8_0(packed, N, K, d, qs, M, y, s));
+}
+
 int kq_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs, float *y,
                  cudaStream_t s) {
     if (int r = check_shape(N, K)) return r;

@@ -34,6 +34,11 @@ cudaError_t launch_quantize_q8_0(const float *x, int64_t M, int64_t K, float *d,
 cudaError_t launch_gemv_q8_0(const void *packed, int64_t N, int64_t K, const float *d, const int8_t *qs,
                              const float *x, float *y, cudaStream_t s);
 
+// Q8_0 prefill GEMM (kq_q8_0_gemm.cu): y [M][N] from the image and M
+// Q8_0-form activation rows.
+cudaError_t launch_gemm_q8_0(const void *packed, int64_t N, int64_t K, const float *d_a, const int8_t *q_a, int64_t M,
+                             float *y, cudaStream_t s);
+
 // Disk superblocks -> packed image.
 cudaError_t launch_repack(int f, const uint8_t *disk, int64_t N, int64_t K, uint8_t *packed,
                           cudaStream_t s);

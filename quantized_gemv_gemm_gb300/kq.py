@@ -61,6 +61,7 @@ _lib.kq_copy_in.argtypes = [_P, _P, _SZ, _P]
 _lib.kq_debug_wait_timeout.argtypes = [ctypes.c_uint64, _P]
 _lib.kq_quantize_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_gemv_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _P, _P]
+_lib.kq_gemm_q8_0.argtypes = [_P, _I64, _I64, _P, _P, _I64, _P, _P]
 _lib.kq_gemv_q8_0_fused.argtypes = [_P, _I64, _I64, _P, _P, _P]
 _lib.kq_set_launch_flags.argtypes = [ctypes.c_uint]
 _lib.kq_set_launch_flags.restype = ctypes.c_uint
@@ -69,7 +70,7 @@ _lib.kq_get_launch_flags.restype = ctypes.c_uint
 for _f in ("kq_quantize_q8k", "kq_repack", "kq_gemv", "kq_gemv_fused", "kq_gemv_fused_batch", "kq_gemm", "kq_gemm_grouped", "kq_gemm_noalloc",
            "kq_debug_partials", "kq_debug_gemm_partials", "kq_debug_batch_partials", "kq_debug_decode", "kq_device_status", "kq_measure_mma_s8",
            "kq_quantize_q8_0", "kq_gemv_q8_0", "kq_gemv_grouped_fused", "kq_debug_wait_timeout",
-           "kq_gemv_q8_0_fused", "kq_copy_in"):
+           "kq_gemv_q8_0_fused", "kq_copy_in", "kq_gemm_q8_0"):
     getattr(_lib, _f).restype = _INT
 
 LIB_PATH = _LIB_PATH
@@ -405,6 +406,18 @@ def kq_gemv_q8_0(packed: torch.Tensor, N: int, K: int, d: torch.Tensor, qs: torc
         y = torch.empty(N, dtype=torch.float32, device=packed.device)
     _check(_lib.kq_gemv_q8_0(_ptr(packed), int(N), int(K), _ptr(d), _ptr(qs), _ptr(y), _stream(stream)),
            "kq_gemv_q8_0")
+    return y
+
+
+def kq_gemm_q8_0(packed: torch.Tensor, N: int, K: int, d: torch.Tensor, qs: torch.Tensor,
+                 y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Q8_0 GEMM: y [M, N] from a KQ_Q8_0 image and Q8_0-form activations d [M, K/32], qs [M, K]."""
+    _need_cuda(packed, d, qs)
+    M = qs.shape[0] if qs.dim() == 2 else 1
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.float32, device=packed.device)
+    _need_cuda(y)
+    _check(_lib.kq_gemm_q8_0(_ptr(packed), N, K, _ptr(d), _ptr(qs), M, _ptr(y), _stream(stream)), "kq_gemm_q8_0")
     return y
 
 
