@@ -604,6 +604,53 @@ __device__ __forceinline__ void debug_units(int32_t *isum_out, int32_t *msum_out
     }
 }
 
+// MMA issue of the K16 steps [S0, S1) of one half (A slot a_slot, B slot
+// b_slot) into accumulator acc; `fresh`: the first step overwrites it.
+// Straight-line: one tcgen05.mma per step and plane.  The two base
+// descriptors are pinned in registers (the empty asm keeps the compiler from
+// re-deriving them per step) and each step adds its compile-time offset to the
+// 14-bit address field, which cannot carry: shared memory ends below 256 KB.
+// A build that derived every step's descriptor from the slot address instead
+// fed one step the operand address of the step before it (one K16 slice of
+// the second half counted twice and the next one dropped, the same in every
+// superblock), which the bit-exact partials tests caught.
+template <int B_SUB, int S0, int S1, int PLANES>
+__device__ __forceinline__ void issue_steps(uint32_t acc, uint32_t a_slot, uint32_t b_slot, bool fresh,
+                                            uint32_t idesc) {
+    uint64_t a0 = smem_desc(a_slot, 16, 1024, SWZ_128B), b0 = smem_desc(b_slot, 16, 1024, SWZ_128B);
+    asm volatile("mov.b64 %0, %0;" : "+l"(a0));
+    asm volatile("mov.b64 %0, %0;" : "+l"(b0));
+#pragma unroll
+    for (int st = S0; st < S1; ++st) {
+        const int j = st >> 2, kk = st & 3;
+        const uint64_t bd = b0 + (uint64_t)((j * B_SUB + 32 * kk) >> 4);
+#pragma unroll
+        for (int pl = 0; pl < PLANES; ++pl) {
+            const uint64_t ad = a0 + (uint64_t)((pl * 32768 + j * 16384 + 32 * kk) >> 4);
+            umma_f16(acc, ad, bd, idesc, (fresh && st == S0 && pl == 0) ? 0u : 1u);
+        }
+    }
+}
+
+// unit v of the U (1, 2 or 4) units a half is cut into: steps [8v/U, 8(v+1)/U)
+template <int B_SUB, int PLANES>
+__device__ __forceinline__ void issue_unit(int U, int v, uint32_t acc, uint32_t a_slot, uint32_t b_slot, bool fresh,
+                                           uint32_t idesc) {
+    if (U == 1) {
+        issue_steps<B_SUB, 0, 8, PLANES>(acc, a_slot, b_slot, fresh, idesc);
+    } else if (U == 2) {
+        if (v == 0) issue_steps<B_SUB, 0, 4, PLANES>(acc, a_slot, b_slot, fresh, idesc);
+        else issue_steps<B_SUB, 4, 8, PLANES>(acc, a_slot, b_slot, fresh, idesc);
+    } else {
+        switch (v) {
+        case 0: issue_steps<B_SUB, 0, 2, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
+        case 1: issue_steps<B_SUB, 2, 4, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
+        case 2: issue_steps<B_SUB, 4, 6, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
+        default: issue_steps<B_SUB, 6, 8, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
+        }
+    }
+}
+
 template <int F, bool G, bool DBG>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a16, const __grid_constant__ CUtensorMap map_b16,
@@ -732,19 +779,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ok = mbar_wait(&bar[BAR_TILES], 0);
                 ntiles = ok ? (int)misc[1] : 0;
             }
-            // issue the K16 steps [s0, s1) of the half in slot a_slot / b_slot
-            // into accumulator acc; `fresh`: the first overwrites it
-            auto issue = [&](uint32_t acc, uint32_t a_slot, uint32_t b_slot, int s0, int s1, int planes, bool fresh,
+            // unit v of U of the half in slot a_slot / b_slot into accumulator
+            // acc (Q6_K split halves: both planes per step)
+            auto issue = [&](int U, int v, uint32_t acc, uint32_t a_slot, uint32_t b_slot, int planes, bool fresh,
                              uint32_t idesc) {
-                for (int st = s0; st < s1; ++st) {
-                    const int j = st >> 2, kk = st & 3;
-                    const uint64_t bd = smem_desc(b_slot + j * C::B_SUB + 32 * kk, 16, 1024, SWZ_128B);
-                    for (int pl = 0; pl < planes; ++pl) {
-                        const uint64_t ad = smem_desc(a_slot + pl * 32768 + j * 16384 + 32 * kk, 16, 1024, SWZ_128B);
-                        umma_f16(acc, ad, bd, idesc, fresh ? 0u : 1u);
-                        fresh = false;
-                    }
-                }
+                if (F == FMT_Q6_K && planes == 2) issue_unit<C::B_SUB, 2>(U, v, acc, a_slot, b_slot, fresh, idesc);
+                else issue_unit<C::B_SUB, 1>(U, v, acc, a_slot, b_slot, fresh, idesc);
             };
             for (int k = 0; k < ntiles && ok; ++k) {
                 const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
@@ -779,7 +819,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int planes = (F == FMT_Q6_K && pl.split[h]) ? 2 : 1;
                         if (h == 1 && open && pl.whole) {
                             // the superblock is one unit: the second half goes on into it
-                            issue(tmem + 128 * (uint32_t)(u % NU), a_slot, b_slot, 0, 8, planes, false, idesc);
+                            issue(1, 0, tmem + 128 * (uint32_t)(u % NU), a_slot, b_slot, planes, false, idesc);
                             umma_commit(&bar[BAR_U_FULL + (int)(u % NU)]);
                             ++u;
                             open = false;
@@ -797,8 +837,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                     break;
                                 }
                                 tc_fence_after();
-                                issue(tmem + 128 * (uint32_t)us, a_slot, b_slot, v * 8 / U, (v + 1) * 8 / U, planes, true,
-                                      idesc);
+                                issue(U, v, tmem + 128 * (uint32_t)us, a_slot, b_slot, planes, true, idesc);
                                 if (h == 0 && U == 1) {
                                     open = true;  // committed with the second half, or before it
                                 } else {
