@@ -554,6 +554,71 @@ __device__ __forceinline__ void stage_block_from_x(float4 v0, float4 v1, int lan
     if (lane == 0) *db = d8;
 }
 
+// The same for the J blocks b0, b0 + 8, ..., b0 + 8(J-1) of the row x (those
+// below nsb are stored), one warp, with the blocks' steps interleaved: each
+// block's chain (max, divide, round, sums) is independent of the others', so
+// J blocks take about the latency of one.  Every step is q8k_lane's (an all-
+// zero block gets iscale 0, hence every q = 0, as q8k_lane gives it).
+template <bool PAIRS, int J>
+__device__ __forceinline__ void stage_blocks_from_x(const float *x, int64_t nsb, int64_t b0, int lane, int8_t *qs,
+                                                    uint8_t *sums, float *d8s) {
+    float4 v0[J], v1[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int64_t b = b0 + 8 * j;
+        if (b < nsb) {
+            const float4 *xp = reinterpret_cast<const float4 *>(x + b * QK + 8 * lane);
+            v0[j] = xp[0];
+            v1[j] = xp[1];
+        } else {
+            v0[j] = v1[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+    }
+    float amax[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        float ax = fmaxf(fmaxf(fabsf(v0[j].x), fabsf(v0[j].y)), fmaxf(fabsf(v0[j].z), fabsf(v0[j].w)));
+        ax = fmaxf(ax, fmaxf(fmaxf(fabsf(v1[j].x), fabsf(v1[j].y)), fmaxf(fabsf(v1[j].z), fabsf(v1[j].w))));
+        amax[j] = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(ax)));
+    }
+    float iscale[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) iscale[j] = amax[j] == 0.0f ? 0.0f : __fdiv_rn(127.0f, amax[j]);
+    int part[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const float v[8] = {v0[j].x, v0[j].y, v0[j].z, v0[j].w, v1[j].x, v1[j].y, v1[j].z, v1[j].w};
+        uint32_t lo = 0, hi = 0;
+        int sum = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int q = max(-127, min(127, __float2int_rn(__fmul_rn(v[i], iscale[j]))));
+            sum += q;
+            if (i < 4) lo |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * i);
+            else hi |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (i - 4));
+        }
+        part[j] = sum;
+        const int64_t b = b0 + 8 * j;
+        if (b < nsb) *reinterpret_cast<uint2 *>(qs + b * QK + 8 * lane) = make_uint2(lo, hi);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        part[j] += __shfl_xor_sync(0xFFFFFFFFu, part[j], 1);        // 16-element sums
+        if constexpr (PAIRS) part[j] += __shfl_xor_sync(0xFFFFFFFFu, part[j], 2);  // 32-element sums
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int64_t b = b0 + 8 * j;
+        if (b >= nsb) continue;
+        if constexpr (PAIRS) {
+            if ((lane & 3) == 0) reinterpret_cast<int *>(sums + b * 32)[lane >> 2] = part[j];
+        } else {
+            if ((lane & 1) == 0) reinterpret_cast<int16_t *>(sums + b * 32)[lane >> 1] = static_cast<int16_t>(part[j]);
+        }
+        if (lane == 0) d8s[b] = amax[j] == 0.0f ? 0.0f : __fdiv_rn(amax[j], 127.0f);
+    }
+}
+
 struct GemvParams {
     int nmat;
     const uint8_t *packed[GEMV_MAX_MATRICES];
@@ -686,23 +751,14 @@ __global__ void __launch_bounds__(256, 2) gemv_kernel(const GemvParams p) {
                 }
             }
         } else if (p.x) {
-            // up to eight blocks per warp per round, all loads issued first
-            for (int64_t b0 = warp; b0 < nsb; b0 += 64) {
-                float4 v[8][2];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int64_t b = b0 + 8 * j;
-                    if (b < nsb) {
-                        const float4 *xp = reinterpret_cast<const float4 *>(p.x + b * QK + 8 * lane);
-                        v[j][0] = xp[0];
-                        v[j][1] = xp[1];
-                    }
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int64_t b = b0 + 8 * j;
-                    if (b < nsb) stage_block_from_x<PAIRS>(v[j][0], v[j][1], lane, s_qs + b * QK, s_sum + b * 32, s_d8 + b);
-                }
+            // up to four blocks per warp per round (warp w: blocks w, w + 8,
+            // ...), quantized together (measured: five or eight at once are
+            // slower -- the registers run out)
+            for (int64_t b0 = warp; b0 < nsb; b0 += 32) {
+                const int64_t mine = (nsb - b0 + 7) / 8;  // this warp's blocks in the round
+                if (mine > 2) stage_blocks_from_x<PAIRS, 4>(p.x, nsb, b0, lane, s_qs, s_sum, s_d8);
+                else if (mine > 1) stage_blocks_from_x<PAIRS, 2>(p.x, nsb, b0, lane, s_qs, s_sum, s_d8);
+                else stage_blocks_from_x<PAIRS, 1>(p.x, nsb, b0, lane, s_qs, s_sum, s_d8);
             }
         } else {
             for (int t = 0; t < ntok; ++t) {
