@@ -9,9 +9,12 @@
 //     image of q8 (exact, |q8| <= 127), of the per-16 bsums (exact, <= 2032)
 //     and a transposed copy of d8, in the caller's workspace;
 //   - each block owns 128 weight rows x up to 128 tokens; per superblock its
-//     unpack warps expand the packed weights once into shared memory as fp16
-//     w' = sc*q with the sub-scale folded in (Q4_K <= 945, Q5_K <= 1953:
-//     exact): the kq v3 panel scratch, unpacked once per token block;
+//     unpack warps expand the packed weights once as fp16 w' = sc*q with the
+//     sub-scale folded in (Q4_K <= 945, Q5_K <= 1953: exact): the kq v3 panel
+//     scratch, unpacked once per token block.  Q4_K/Q5_K write it into TMEM
+//     (thread = weight row = TMEM lane, tcgen05.st) and the MMA reads its A
+//     operand from there, so the tensor pipe's shared-memory reads are the
+//     token tiles alone; Q6_K writes it into shared memory;
 //     Q6_K's w' = sc*(q-32) is one exact fp16 FMA for |sc| <= 62, and when a tile holds a
 //     larger sub-scale the weight is split into two exact planes,
 //     sc*(v - (v&1)) (even, |.| <= 4096) and sc*(v&1), both multiplied into
@@ -43,8 +46,9 @@
 // one 64-wide K sub-tile each), 10..13 epilogue (thread = row x every token
 // column, y accumulated in TMEM).  TMEM lane quadrant = warp % 4.  Stages
 // are half superblocks (K = 128): an A ring of 2 slots, a B ring of 3
-// (Q6_K: 2).  TMEM (512 columns) holds a ring of 3 unit accumulators and,
-// in its last 128 columns, msum (Q4_K/Q5_K) or y (Q6_K).  Every mbarrier
+// (Q6_K: 2).  TMEM (512 columns): Q4_K/Q5_K a ring of 2 unit accumulators,
+// one msum (issued after the superblock's last unit, folded with it) and
+// the two A slots; Q6_K a ring of 3 units and y.  Every mbarrier
 // wait is bounded; on timeout the block records KQ_ERR_TIMEOUT in the
 // device status word and winds down.
 #include "kq_internal.h"
@@ -76,13 +80,17 @@ template <int F> constexpr int n_epi() { return NTHREADS / 32 - w_epi<F>(); }
 template <int F>
 struct Cfg {
     static constexpr bool kMins = F != FMT_Q6_K;
+    // Q4_K/Q5_K keep the unpacked weights (the A operand) in TMEM, Q6_K (two
+    // planes, no room beside its y) in shared memory
+    static constexpr bool kTmemA = F != FMT_Q6_K;
     static constexpr int NB = F == FMT_Q6_K ? 2 : 3;              // B ring slots
-    static constexpr int A_SLOT = F == FMT_Q6_K ? 65536 : 32768;  // 2 sub-tiles (x2 planes for Q6_K)
+    static constexpr int A_SLOT = kTmemA ? 0 : 65536;             // Q6_K: 2 sub-tiles x 2 planes
     static constexpr int B_SUB = BT * 128;                         // one 64-wide K sub-tile of tokens
     static constexpr int B_SLOT = 2 * B_SUB + (kMins ? BT * 32 : 0);
+    static constexpr int AMIN_BYTES = BM * 32;                     // one superblock's sub-mins operand
     static constexpr int OFF_A = 0;
-    static constexpr int OFF_AMIN = 2 * A_SLOT;
-    static constexpr int OFF_B = OFF_AMIN + (kMins ? BM * 32 : 0);
+    static constexpr int OFF_AMIN = 2 * A_SLOT;                    // by superblock parity
+    static constexpr int OFF_B = OFF_AMIN + (kMins ? 2 * AMIN_BYTES : 0);
     static constexpr int OFF_SD = OFF_B + NB * B_SLOT;            // s_d, s_dmin [2][BM]
     static constexpr int OFF_D8 = OFF_SD + 2 * 2 * BM * 4;        // per epilogue warp [64] floats
     static constexpr int OFF_BAR = OFF_D8 + 8 * 64 * 4;
@@ -110,11 +118,11 @@ struct Cfg {
 enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
        BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25 };
 
-// TMEM (512 columns) in slots of 128 columns: a ring of unit accumulators
-// from column 0 (Q4_K/Q5_K 2 slots, Q6_K 3), then msum by superblock parity
-// (Q4_K/Q5_K, columns 256 and 384) or y (Q6_K, column 384).
+// TMEM (512 columns): a ring of unit accumulators of 128 columns from column
+// 0 (Q4_K/Q5_K 2 slots, Q6_K 3); Q4_K/Q5_K then msum (columns 256..383) and
+// the A operand, 64 columns per half superblock (384..511); Q6_K y (384..511).
 template <int F> constexpr int n_units() { return F == FMT_Q6_K ? 3 : 2; }
-constexpr uint32_t COL_M = 256, COL_Y = 384;
+constexpr uint32_t COL_M = 256, COL_Y = 384, COL_A = 384;
 
 // ---------------------------------------------------------------------------
 // Accumulator units.  The fp32 TMEM accumulator is exact while every partial
@@ -230,18 +238,18 @@ constexpr uint32_t MAGIC = 0x64646464u;
 
 // ---------------------------------------------------------------------------
 // Unpack of one weight row x one 64-wide K sub-tile of a half superblock into
-// the A operand (128-byte swizzled K-major fp16 rows).  `a_row` is the shared
-// address of the sub-tile base; the row's 8 chunks of 8 fp16 are written at
-// sw128_offset(r, 8q).
+// the A operand.
 
-// Q4_K/Q5_K: sub-tile = chunk c of the superblock (64 elements): elements
+// Q4_K/Q5_K, into TMEM: the row is the thread's lane, `a_tm` the TMEM address
+// of the sub-tile (32 columns, two fp16 per column, the lower K in the low
+// half).  Sub-tile = chunk c of the superblock (64 elements): elements
 // 64c + l (low nibbles of qs[32c + l], sub-scale sc_2c) at K 0..31 and
 // 64c + 32 + l (high nibbles, sc_2c+1) at K 32..63; Q5_K ORs bit 2c / 2c+1 of
 // qh[l] in as value 16.  w' = q*sc is built exactly in fp16 as
 // (1024 + q)*sc - 1024*sc (low) and (1024 + 16q)*(sc/16) - 64*sc (high).
 template <int F>
-__device__ __forceinline__ void unpack_q45(uint32_t a_tile, int r, const uint32_t (&qs)[8], const uint32_t (&qh)[8],
-                                           int c, int sc_lo, int sc_hi) {
+__device__ __forceinline__ void unpack_q45(uint32_t a_tm, const uint32_t (&qs)[8], const uint32_t (&qh)[8], int c,
+                                           int sc_lo, int sc_hi) {
     const uint32_t s_lo = h2_splat((float)sc_lo), o_lo = h2_splat(-1024.0f * sc_lo);
     const uint32_t s_hi = h2_splat(sc_hi * 0.0625f), o_hi = h2_splat(-64.0f * sc_hi);
 #pragma unroll
@@ -266,12 +274,14 @@ __device__ __forceinline__ void unpack_q45(uint32_t a_tile, int r, const uint32_
                 hi[2 * w + pr] = h2_fma(h, s_hi, o_hi);
             }
         }
-        sts128(a_tile + sw128_offset(r, 8 * q), lo[0], lo[1], lo[2], lo[3]);
-        sts128(a_tile + sw128_offset(r, 32 + 8 * q), hi[0], hi[1], hi[2], hi[3]);
+        tmem_st4(a_tm + 4 * q, lo[0], lo[1], lo[2], lo[3]);        // K 8q .. 8q+7
+        tmem_st4(a_tm + 16 + 4 * q, hi[0], hi[1], hi[2], hi[3]);   // K 32 + 8q ..
     }
 }
 
-// Q6_K: sub-tile j of half h holds groups t = 2j (K 0..31) and 2j+1 (K 32..63)
+// Q6_K, into shared memory (128-byte swizzled K-major fp16 rows; `a_tile` is
+// the sub-tile base, the row's 8 chunks of 8 fp16 at sw128_offset(r, 8q)):
+// sub-tile j of half h holds groups t = 2j (K 0..31) and 2j+1 (K 32..63)
 // of the half: element 128h + 32t + l is the low (t < 2) or high (t >= 2)
 // nibble of ql[64h + 32(t&1) + l] with bits 2t..2t+1 of qh[32h + l] on top,
 // sub-scale sc[8h + 2t + l/16] (byte 2(t - 2j) + l/16 of `scw`).  The 6-bit
@@ -535,7 +545,7 @@ __device__ __forceinline__ void prefetch_tile(const GemmParams &p, const Tile &t
 
 // Q4_K/Q5_K: y[64] (64 token columns, in registers) += d8 * (d * U - dmin *
 // msum) for one unit U, CW (8 or 16) columns per TMEM load round trip
-template <int CW>
+template <int CW, bool WM>
 __device__ __forceinline__ void fold_unit_q45(float (&y)[64], uint32_t xu, uint32_t xm, float dd, float dm,
                                               const float *s_d8) {
 #pragma unroll
@@ -543,15 +553,16 @@ __device__ __forceinline__ void fold_unit_q45(float (&y)[64], uint32_t xu, uint3
         uint32_t vu[CW], vm[CW];
         if constexpr (CW == 16) {
             tmem_ld16(xu + 16 * cc, vu);
-            tmem_ld16(xm + 16 * cc, vm);
+            if constexpr (WM) tmem_ld16(xm + 16 * cc, vm);
         } else {
             tmem_ld8(xu + 8 * cc, vu);
-            tmem_ld8(xm + 8 * cc, vm);
+            if constexpr (WM) tmem_ld8(xm + 8 * cc, vm);
         }
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < CW; ++i) {
-            const float tv = fmaf(-dm, __uint_as_float(vm[i]), dd * __uint_as_float(vu[i]));
+            const float tv = WM ? fmaf(-dm, __uint_as_float(vm[i]), dd * __uint_as_float(vu[i]))
+                                : dd * __uint_as_float(vu[i]);
             y[CW * cc + i] = fmaf(s_d8[CW * cc + i], tv, y[CW * cc + i]);
         }
     }
@@ -632,6 +643,21 @@ __device__ __forceinline__ void issue_steps(uint32_t acc, uint32_t a_slot, uint3
     }
 }
 
+// The same with A in TMEM (Q4_K/Q5_K): step st reads the 8 columns a_tm + 8st.
+template <int B_SUB, int S0, int S1>
+__device__ __forceinline__ void issue_steps_ts(uint32_t acc, uint32_t a_tm, uint32_t b_slot, bool fresh,
+                                               uint32_t idesc) {
+    uint64_t b0 = smem_desc(b_slot, 16, 1024, SWZ_128B);
+    asm volatile("mov.b64 %0, %0;" : "+l"(b0));
+    asm volatile("mov.b32 %0, %0;" : "+r"(a_tm));
+#pragma unroll
+    for (int st = S0; st < S1; ++st) {
+        const int j = st >> 2, kk = st & 3;
+        const uint64_t bd = b0 + (uint64_t)((j * B_SUB + 32 * kk) >> 4);
+        umma_f16_ts(acc, a_tm + 8u * st, bd, idesc, (fresh && st == S0) ? 0u : 1u);
+    }
+}
+
 // unit v of the U (1, 2 or 4) units a half is cut into: steps [8v/U, 8(v+1)/U)
 template <int B_SUB, int PLANES>
 __device__ __forceinline__ void issue_unit(int U, int v, uint32_t acc, uint32_t a_slot, uint32_t b_slot, bool fresh,
@@ -647,6 +673,23 @@ __device__ __forceinline__ void issue_unit(int U, int v, uint32_t acc, uint32_t 
         case 1: issue_steps<B_SUB, 2, 4, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
         case 2: issue_steps<B_SUB, 4, 6, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
         default: issue_steps<B_SUB, 6, 8, PLANES>(acc, a_slot, b_slot, fresh, idesc); break;
+        }
+    }
+}
+template <int B_SUB>
+__device__ __forceinline__ void issue_unit_ts(int U, int v, uint32_t acc, uint32_t a_tm, uint32_t b_slot, bool fresh,
+                                              uint32_t idesc) {
+    if (U == 1) {
+        issue_steps_ts<B_SUB, 0, 8>(acc, a_tm, b_slot, fresh, idesc);
+    } else if (U == 2) {
+        if (v == 0) issue_steps_ts<B_SUB, 0, 4>(acc, a_tm, b_slot, fresh, idesc);
+        else issue_steps_ts<B_SUB, 4, 8>(acc, a_tm, b_slot, fresh, idesc);
+    } else {
+        switch (v) {
+        case 0: issue_steps_ts<B_SUB, 0, 2>(acc, a_tm, b_slot, fresh, idesc); break;
+        case 1: issue_steps_ts<B_SUB, 2, 4>(acc, a_tm, b_slot, fresh, idesc); break;
+        case 2: issue_steps_ts<B_SUB, 4, 6>(acc, a_tm, b_slot, fresh, idesc); break;
+        default: issue_steps_ts<B_SUB, 6, 8>(acc, a_tm, b_slot, fresh, idesc); break;
         }
     }
 }
@@ -717,7 +760,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = misc[0];
-    // TMEM columns: unit accumulator i at 128i (i < NU), msum at COL_M, y at COL_Y.
+    // TMEM columns: unit accumulator i at 128i (i < NU), msum at COL_M, A at COL_A (Q4_K/Q5_K), y at COL_Y (Q6_K).
     // The unit ring's slots and phases follow u, the block's count of units
     // over all tiles; msum's phase the count of non-empty superblocks; the
     // SD barriers' the block's count g of superblock steps over all tiles.
@@ -751,7 +794,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const uint32_t par = (uint32_t)((use / C::NB) & 1);
                         if (!mbar_wait(&bar[BAR_EMPTY_B + slot], par ^ 1)) { ok = false; break; }
                         uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
-                        const bool mins = C::kMins && h == 0;
+                        // the token bsums (msum's operand) come with the second half,
+                        // after whose units msum is issued
+                        const bool mins = C::kMins && h == 1;
                         mbar_arrive_expect_tx(&bar[BAR_FULL_B + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
                         const int k0 = (int)(sb * QK + 128 * h);
                         tma_load_2d(bs, &map_a16, k0, t.t0, &bar[BAR_FULL_B + slot]);
@@ -779,11 +824,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ok = mbar_wait(&bar[BAR_TILES], 0);
                 ntiles = ok ? (int)misc[1] : 0;
             }
-            // unit v of U of the half in slot a_slot / b_slot into accumulator
-            // acc (Q6_K split halves: both planes per step)
-            auto issue = [&](int U, int v, uint32_t acc, uint32_t a_slot, uint32_t b_slot, int planes, bool fresh,
-                             uint32_t idesc) {
-                if (F == FMT_Q6_K && planes == 2) issue_unit<C::B_SUB, 2>(U, v, acc, a_slot, b_slot, fresh, idesc);
+            // unit v of U of half h (A: TMEM columns a_tm, or shared-memory slot
+            // a_slot; B: slot b_slot) into accumulator acc (Q6_K split halves:
+            // both planes per step)
+            auto issue = [&](int U, int v, uint32_t acc, uint32_t a_slot, uint32_t a_tm, uint32_t b_slot, int planes,
+                             bool fresh, uint32_t idesc) {
+                if constexpr (C::kTmemA) issue_unit_ts<C::B_SUB>(U, v, acc, a_tm, b_slot, fresh, idesc);
+                else if (planes == 2) issue_unit<C::B_SUB, 2>(U, v, acc, a_slot, b_slot, fresh, idesc);
                 else issue_unit<C::B_SUB, 1>(U, v, acc, a_slot, b_slot, fresh, idesc);
             };
             for (int k = 0; k < ntiles && ok; ++k) {
@@ -804,6 +851,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             continue;
                         }
                         const uint32_t a_slot = a_base + h * C::A_SLOT;
+                        const uint32_t a_tm = tmem + COL_A + 64 * (uint32_t)h;
                         const uint32_t b_slot = b_base + slot * C::B_SLOT;
                         // this half's flags are in (the second half's are written after FULL_A[1])
                         const uint32_t fl = flag_sa + 16 * (uint32_t)(g & 1);
@@ -819,7 +867,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         const int planes = (F == FMT_Q6_K && pl.split[h]) ? 2 : 1;
                         if (h == 1 && open && pl.whole) {
                             // the superblock is one unit: the second half goes on into it
-                            issue(1, 0, tmem + 128 * (uint32_t)(u % NU), a_slot, b_slot, planes, false, idesc);
+                            issue(1, 0, tmem + 128 * (uint32_t)(u % NU), a_slot, a_tm, b_slot, planes, false, idesc);
                             umma_commit(&bar[BAR_U_FULL + (int)(u % NU)]);
                             ++u;
                             open = false;
@@ -837,7 +885,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                     break;
                                 }
                                 tc_fence_after();
-                                issue(U, v, tmem + 128 * (uint32_t)us, a_slot, b_slot, planes, true, idesc);
+                                issue(U, v, tmem + 128 * (uint32_t)us, a_slot, a_tm, b_slot, planes, true, idesc);
                                 if (h == 0 && U == 1) {
                                     open = true;  // committed with the second half, or before it
                                 } else {
@@ -847,17 +895,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             }
                         }
                         if (!ok) break;
-                        if (C::kMins && h == 0) {
-                            const int mb = (int)(mc & 1);
-                            if (!mbar_wait(&bar[BAR_M_EMPTY + mb], (uint32_t)(((mc >> 1) & 1) ^ 1))) {
+                        if (C::kMins && h == 1) {
+                            // msum after the superblock's last unit (the epilogue folds
+                            // it with that unit): the sub-mins of the superblock's
+                            // parity against the token bsums of this slot; one slot
+                            if (!mbar_wait(&bar[BAR_M_EMPTY], (uint32_t)((mc & 1) ^ 1))) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint64_t ad = smem_desc(amin, 16, 256, SWZ_32B);
+                            const uint64_t ad = smem_desc(amin + (uint32_t)((g & 1) * C::AMIN_BYTES), 16, 256, SWZ_32B);
                             const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
-                            umma_f16(tmem + COL_M + 128 * (uint32_t)mb, ad, bd, idesc, 0);
-                            umma_commit(&bar[BAR_M_FULL + mb]);
+                            umma_f16(tmem + COL_M, ad, bd, idesc, 0);
+                            umma_commit(&bar[BAR_M_FULL]);
                             ++mc;
                         }
                         umma_commit(&bar[BAR_EMPTY_A + h]);
@@ -874,9 +924,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     } else if (warp < w_epi<F>()) {
         // ------------------------------------------------ weight unpack
         const int uw = warp - W_UNPACK;          // 0..3 (Q6_K 0..7)
-        const int r = 32 * (uw & 3) + lane;      // tile row
+        // tile row: Q4_K/Q5_K write it into TMEM lane r, in the warp's quadrant
+        const int r = C::kTmemA ? 32 * (warp & 3) + lane : 32 * (uw & 3) + lane;
         const int my_jj = uw >> 2;               // Q6_K: this thread's K sub-tile of each half
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
+        const uint32_t a_tm0 = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + COL_A;  // Q4_K/Q5_K A, half 0
         if constexpr (F == FMT_Q4_K && G) {
         // ---- grouped Q4_K: the row's bytes of each half superblock arrive by
         // cp.async in this thread's shared-memory ring, RS - 1 halves ahead:
@@ -973,7 +1025,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ok = false;
                     break;
                 }
-                const uint32_t a_slot = a_base + h * C::A_SLOT;
+                tc_fence_after();  // the MMAs that read this half's A columns are complete
                 const ScaleMin sm = unpack_scale_min(hdr);
                 uint32_t qh0[8];
 #pragma unroll
@@ -986,11 +1038,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     uint32_t qsc[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) qsc[i] = qs[8 * jj + i];
-                    unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                    unpack_q45<F>(a_tm0 + 64 * h + 32 * jj, qsc, qh0, cch, sc_lo, sc_hi);
                 }
                 if (h == 0) {
                     // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
-                    const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+                    const uint32_t amin = smem_u32(smem + C::OFF_AMIN) + (uint32_t)((gg & 1) * C::AMIN_BYTES);
                     uint32_t mw[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
@@ -1004,6 +1056,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const uint32_t w1sb = h ? __reduce_max_sync(0xFFFFFFFFu, bnd.x + bnd.y) : 0u;
                     if (lane == 0) s_flag[16 * (gg & 1) + 8 * h + uw] = (uint8_t)unit_flag<F>(h, w1, w1sb, 0);
                 }
+                tmem_wait_st();
+                tc_fence_before();
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -1078,6 +1132,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     ok = false;
                     break;
                 }
+                if constexpr (C::kTmemA) tc_fence_after();  // the MMAs that read this half's A columns are complete
                 const uint32_t a_slot = a_base + h * C::A_SLOT;
                 float d = 0.0f, dmin = 0.0f;
                 // this warp's unit flag for the half: its rows' W1 bounds and
@@ -1117,11 +1172,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         uint32_t qsc[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) qsc[i] = cur.qs[8 * jj + i];
-                        unpack_q45<F>(a_slot + jj * 16384, r, qsc, qh0, cch, sc_lo, sc_hi);
+                        unpack_q45<F>(a_tm0 + 64 * h + 32 * jj, qsc, qh0, cch, sc_lo, sc_hi);
                     }
                     if (h == 0) {
                         // sub-mins duplicated per 16: K i of the mins operand holds m_{i/2}
-                        const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
+                        const uint32_t amin = smem_u32(smem + C::OFF_AMIN) + (uint32_t)((gg & 1) * C::AMIN_BYTES);
                         uint32_t mw[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) mw[i] = h2_splat((float)byte_of(i < 4 ? sm.m_lo : sm.m_hi, i & 3));
@@ -1135,6 +1190,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (h == 0 && my_jj == 0) {
                     s_d[(gg & 1) * BM + r] = d;
                     s_dmin[(gg & 1) * BM + r] = dmin;
+                }
+                if constexpr (C::kTmemA) {
+                    tmem_wait_st();
+                    tc_fence_before();
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -1324,18 +1383,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[BAR_SD_EMPTY + b]);
                 if (t.ntok == 0) continue;
-                // the superblock's units; msum is folded with the first (and
-                // multiplied by 0 with the others, so one fold serves all: its
-                // slot is held until the last unit)
-                const int mb = (int)(mc & 1);
-                if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_M_FULL + mb], (mc >> 1) & 1))) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t xm = lane_addr + COL_M + 128 * (uint32_t)mb;
+                // the superblock's units, folded as they land; msum, issued
+                // after the last unit into its one slot, is folded with the
+                // last (the units before it never wait for it)
+                const uint32_t xm = lane_addr + COL_M;
 #pragma unroll 1
                 for (int v = 0; v < nu; ++v, ++u) {
-                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (u / NU) & 1))) {
+                    const bool last = v == nu - 1;
+                    bool w_ok = mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (u / NU) & 1);
+                    if (w_ok && last) w_ok = mbar_wait(&bar[BAR_M_FULL], mc & 1);
+                    if (!__all_sync(0xFFFFFFFFu, w_ok)) {
                         ok = false;
                         break;
                     }
@@ -1344,14 +1401,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (cols) {
                         // 8 columns a TMEM round trip: with y[64] and the loop's
                         // state live, 16 would spill
-                        if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xu, false, 0u, v == 0, xm, 64, t.t0 + 64 * ch, t.t_end, n, sb);
-                        else fold_unit_q45<8>(y, xu, xm, dd, v == 0 ? dm : 0.0f, s_d8);
+                        if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xu, false, 0u, last, xm, 64, t.t0 + 64 * ch, t.t_end, n, sb);
+                        else if (last) fold_unit_q45<8, true>(y, xu, xm, dd, dm, s_d8);
+                        else fold_unit_q45<8, false>(y, xu, xm, dd, 0.0f, s_d8);
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&bar[BAR_U_EMPTY + (int)(u % NU)]);
-                        if (v == nu - 1) mbar_arrive(&bar[BAR_M_EMPTY + mb]);
+                        if (last) mbar_arrive(&bar[BAR_M_EMPTY]);
                     }
                 }
                 ++mc;
