@@ -224,11 +224,24 @@ int kq_gemv_fused_batch(kq_format f, int n_mats, const void *const *packed, cons
                         size_t workspace_bytes, cudaStream_t s);
 
 /*
- * Size of the device workspace kq_gemm / kq_gemm_grouped need for M token
- * rows of K (an fp16 image of the activation quants and bsums, plus tile
- * bookkeeping).  0 means no workspace is needed for this shape.
+ * Size of the device workspace kq_gemm / kq_gemm_grouped use for M token
+ * rows of K and N weight rows: an fp16 image of the activation quants and
+ * bsums with the transposed scales, then room for the dense GEMM's split-
+ * tile schedule (two fp32 128 x 128 partial tiles per SM and a counter per
+ * 128 x 128 output tile).  With it, kq_gemm runs one block per SM, each an
+ * even share of the tiles x superblocks steps, so no wave of tiles runs
+ * part-empty; a tile cut between blocks is added up, in block order, by the
+ * last of them.  0 means no workspace is needed for this shape.
  */
 size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K);
+
+/*
+ * The least workspace kq_gemm / kq_gemm_grouped accept for this shape: the
+ * activation image alone (about 2.14 bytes per activation).  With less than
+ * kq_gemm_workspace_bytes, kq_gemm runs one block per output tile instead
+ * of the split-tile schedule (same results up to float rounding order).
+ */
+size_t kq_gemm_min_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K);
 
 /*
  * Prefill GEMM ([kq-arc], "The pieces", kq v3: each weight panel is unpacked
@@ -237,7 +250,8 @@ size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K);
  * token row m of a.
  *   a          device Q8_K planes of M rows
  *   y          device float32 [M][N]
- *   workspace  device, >= kq_gemm_workspace_bytes(f, M, N, K) bytes,
+ *   workspace  device, >= kq_gemm_min_workspace_bytes(f, M, N, K) bytes
+ *              (kq_gemm_workspace_bytes for the split-tile schedule),
  *              256-byte aligned (may be NULL when that size is 0)
  * Calls that share a workspace must not overlap on the GPU.
  * Errors: KQ_ERR_ARG, KQ_ERR_FORMAT, KQ_ERR_ALIGN, KQ_ERR_WORKSPACE,
@@ -471,6 +485,16 @@ int kq_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s);
  * rounding.
  */
 #define KQ_LAUNCH_GEMV_SPLIT 2u
+/*
+ * KQ_LAUNCH_GEMM_SPLIT: a dense kq_gemm given kq_gemm_workspace_bytes always
+ * runs the split-tile schedule (one block per SM, an even share of the
+ * tiles x superblocks steps each, tiles cut between blocks finished from
+ * their partial tiles in block order).  Without it the schedule is chosen
+ * by shape: where a block per tile would leave the last wave of tiles
+ * mostly empty and every block still gets 16 superblock steps or more.
+ * Results of the two schedules differ only in float rounding order.
+ */
+#define KQ_LAUNCH_GEMM_SPLIT 4u
 unsigned kq_set_launch_flags(unsigned flags);
 unsigned kq_get_launch_flags(void);
 
@@ -491,11 +515,13 @@ unsigned kq_get_launch_flags(void);
  *
  *   arguments  as kq_gemm, without workspace / workspace_bytes
  * Limits and behaviour:
- *   - The scratch needed, kq_gemm_workspace_bytes(f, M, N, K), must not
- *     exceed KQ_NOALLOC_SCRATCH_BYTES; larger problems return
+ *   - The scratch needed, kq_gemm_min_workspace_bytes(f, M, N, K), must
+ *     not exceed KQ_NOALLOC_SCRATCH_BYTES; larger problems return
  *     KQ_ERR_TOO_LARGE before anything is enqueued.  The scratch is about
  *     2.14 bytes per activation, so M*K up to about 15.6 million
  *     activations fit (e.g. 512 tokens x K = 30464; K = 30720 is refused).
+ *     When kq_gemm_workspace_bytes(f, M, N, K) fits as well, the call runs
+ *     the split-tile schedule, else one block per output tile.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.  The address is kept for the life of the

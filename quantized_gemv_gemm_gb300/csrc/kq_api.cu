@@ -51,7 +51,7 @@ int gemm_common(kq_format f, const void *packed, int64_t E, const int32_t *offse
     if (!packed || !y) return KQ_ERR_ARG;
     if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
     if (!aligned(packed, 256) || !aligned(y, 4)) return KQ_ERR_ALIGN;
-    const size_t need = gemm_workspace_bytes(f, M, N, K);
+    const size_t need = gemm_workspace_min_bytes(f, M, N, K);
     if (need && (!ws || ws_bytes < need)) return KQ_ERR_WORKSPACE;
     if (ws && !aligned(ws, 256)) return KQ_ERR_ALIGN;
     const Q8K q{a.d, a.qs, a.bsums};
@@ -230,6 +230,11 @@ size_t kq_gemm_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
     return gemm_workspace_bytes(f, M, N, K);
 }
 
+size_t kq_gemm_min_workspace_bytes(kq_format f, int64_t M, int64_t N, int64_t K) {
+    if (!fmt_ok(f) || M < 0 || check_shape(N, K)) return 0;
+    return gemm_workspace_min_bytes(f, M, N, K);
+}
+
 int kq_gemm(kq_format f, const void *packed, int64_t N, int64_t K, kq_q8k_const a, int64_t M, float *y,
             void *workspace, size_t workspace_bytes, cudaStream_t s) {
     return gemm_common(f, packed, 1, nullptr, N, K, a, M, y, workspace, workspace_bytes, s);
@@ -296,7 +301,7 @@ int kq_debug_gemm_partials(kq_format f, const void *packed, int64_t E, const int
     if (!packed || !isum || !msum) return KQ_ERR_ARG;
     if (int r = check_q8k(a.d, a.qs, a.bsums)) return r;
     if (!aligned(packed, 256) || !aligned(isum, 4) || !aligned(msum, 4)) return KQ_ERR_ALIGN;
-    const size_t need = gemm_workspace_bytes(f, M, N, K);
+    const size_t need = gemm_workspace_min_bytes(f, M, N, K);
     if (!workspace || workspace_bytes < need) return KQ_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return KQ_ERR_ALIGN;
     const uint64_t expert_bytes = kq_repack_bytes(f, N, K);
@@ -340,7 +345,8 @@ int kq_copy_in(const void *src, void *dst, size_t bytes, cudaStream_t s) {
 }
 
 unsigned kq_set_launch_flags(unsigned flags) {
-    return g_launch_flags.exchange(flags & (KQ_LAUNCH_PDL | KQ_LAUNCH_GEMV_SPLIT), std::memory_order_relaxed);
+    return g_launch_flags.exchange(flags & (KQ_LAUNCH_PDL | KQ_LAUNCH_GEMV_SPLIT | KQ_LAUNCH_GEMM_SPLIT),
+                                   std::memory_order_relaxed);
 }
 
 unsigned kq_get_launch_flags(void) { return launch_flags(); }

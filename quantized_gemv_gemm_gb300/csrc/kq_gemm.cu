@@ -116,7 +116,8 @@ struct Cfg {
 // (U), the two msum accumulators (M), the per-superblock weight scales and
 // unit plans (SD, by superblock parity), MMA completion, the tile list
 enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
-       BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25 };
+       BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25,
+       BAR_EPI = 26, BAR_END = 27 };
 
 // TMEM (512 columns): a ring of unit accumulators of 128 columns from column
 // 0 (Q4_K/Q5_K 2 slots, Q6_K 3); Q4_K/Q5_K then msum (columns 256..383) and
@@ -199,6 +200,14 @@ struct GemmParams {
     // debug: instead of y, the superblock integer sums, [M][N][nsb] each
     // (isum_out zero-filled before the launch; it is accumulated per unit pair)
     int32_t *isum_out, *msum_out;
+    // dense: block b runs the steps [b * units / grid, (b + 1) * units / grid)
+    // of the tiles x superblocks grid, in pieces of one tile each; a tile cut
+    // between blocks is finished from their fp32 partial tiles (part: two
+    // slots per block, [BT][BM] each) by the last of them to count itself in
+    // tile_cnt (zeroed by the pre-pass)
+    int64_t units;
+    float *part;
+    int *tile_cnt;
 };
 
 __device__ __forceinline__ void set_timeout() { atomicExch(&g_status, 1); }
@@ -419,17 +428,50 @@ __device__ __forceinline__ void finish_tile(Tile &t) {
     t.n_mma = (t.ntok + 15) & ~15;
 }
 
-// Dense tile of this block.
-__device__ __forceinline__ Tile dense_tile(const GemmParams &p) {
+// Dense tile i: the token tiles of a weight row tile are adjacent, so
+// consecutive tiles share that weight panel in L2.
+__device__ __forceinline__ Tile tile_at(const GemmParams &p, int64_t i) {
     const int t_tiles = (int)((p.M + BT - 1) / BT);
-    const int i = (int)blockIdx.x;
     Tile t;
     t.e = 0;
-    t.n0 = (i / t_tiles) * BM;
-    t.t0 = (i % t_tiles) * BT;
+    t.n0 = (int)(i / t_tiles) * BM;
+    t.t0 = (int)(i % t_tiles) * BT;
     t.t_end = (t.t0 + BT < p.M) ? t.t0 + BT : (int)p.M;
     finish_tile(t);
     return t;
+}
+
+// A block's work item: tile t, superblocks [sb0, sb1) of it (dense: one
+// piece of the block's share of the steps; grouped: a whole list tile).
+struct Piece {
+    Tile t;
+    int64_t tile;  // dense: the tile's index
+    int sb0, sb1;
+};
+// first step of block b's share (dense)
+__device__ __forceinline__ int64_t dense_step_of(int64_t b, int64_t units) { return b * units / (int64_t)gridDim.x; }
+__device__ __forceinline__ int64_t dense_step(const GemmParams &p, int64_t b) { return dense_step_of(b, p.units); }
+__device__ __forceinline__ int dense_pieces(const GemmParams &p) {
+    const int64_t u0 = dense_step(p, blockIdx.x), u1 = dense_step(p, blockIdx.x + 1);
+    return u0 < u1 ? (int)((u1 - 1) / p.nsb - u0 / p.nsb + 1) : 0;
+}
+__device__ __forceinline__ Piece dense_piece(const GemmParams &p, int k) {
+    const int64_t u0 = dense_step(p, blockIdx.x), u1 = dense_step(p, blockIdx.x + 1);
+    const int64_t i = u0 / p.nsb + k, lo = i * p.nsb, hi = lo + p.nsb;
+    Piece q;
+    q.t = tile_at(p, i);
+    q.tile = i;
+    q.sb0 = (int)((u0 > lo ? u0 : lo) - lo);
+    q.sb1 = (int)((u1 < hi ? u1 : hi) - lo);
+    return q;
+}
+// the block whose share holds step x (dense)
+__device__ __forceinline__ int64_t dense_block_of(int64_t x, int64_t units) {
+    const int64_t B = gridDim.x;
+    int64_t b = x * B / units;
+    while (b + 1 < B && dense_step_of(b + 1, units) <= x) ++b;
+    while (b > 0 && dense_step_of(b, units) > x) --b;
+    return b;
 }
 
 // Grouped list entry k (written by build_tile_list).
@@ -442,6 +484,29 @@ __device__ __forceinline__ Tile list_tile(const int4 *list, int k) {
     t.t_end = v.w;
     finish_tile(t);
     return t;
+}
+
+// work item k of the block: grouped, list tile k; dense with the split-tile
+// schedule (SK), piece k of the block's share; dense without it, the block's
+// tile, whole
+template <bool G, bool SK>
+__device__ __forceinline__ Piece work_piece(const GemmParams &p, const int4 *list, int k) {
+    if constexpr (!G && SK) {
+        return dense_piece(p, k);
+    } else {
+        Piece q;
+        q.t = G ? list_tile(list, k) : tile_at(p, blockIdx.x);
+        q.tile = G ? -1 : (int64_t)blockIdx.x;
+        q.sb0 = 0;
+        q.sb1 = (int)p.nsb;
+        return q;
+    }
+}
+// dense: the block's work items
+template <bool SK>
+__device__ __forceinline__ int dense_items(const GemmParams &p) {
+    if constexpr (SK) return dense_pieces(p);
+    else return 1;
 }
 
 // Rows [a, b) of expert e from the staged offsets, clamped to [0, M].
@@ -694,7 +759,66 @@ __device__ __forceinline__ void issue_unit_ts(int U, int v, uint32_t acc, uint32
     }
 }
 
-template <int F, bool G, bool DBG>
+// Dense split tiles: this block's partial tile for its k-th piece (slot 0
+// for its first piece, 1 for its last: the pieces between are whole tiles).
+__device__ __forceinline__ float *own_slot(const GemmParams &p, int k) {
+    return p.part + (size_t)(2 * blockIdx.x + (k == 0 ? 0 : 1)) * (BT * BM);
+}
+
+// After every epilogue thread has written its part of this block's partial
+// tile for tile `tile`: the block counts itself in, and the last of the
+// tile's blocks adds their partial tiles in block order (a fixed sum, so
+// the result does not depend on timing) and writes this thread's row n of
+// y, token columns [t0 + cbeg, t0 + cbeg + ncol) below t_end (`act`: the
+// thread has such a row and columns).  The epilogue warps meet twice on the
+// BAR_EPI mbarrier (bounded waits; its phase counted in *phase).  Out of
+// line: it runs once per split tile, and inline its registers would crowd
+// the epilogue's loop.  False on a timeout.
+__device__ __noinline__ bool split_finish(float *part, int *tile_cnt, int64_t units, int64_t nsb, int64_t tile,
+                                          float *y, int64_t N, int64_t n, int t0, int t_end, int cbeg, int ncol,
+                                          bool act, bool leader, int lane, uint32_t *phase, uint64_t *bar,
+                                          uint32_t *misc) {
+    __threadfence();  // the partial sums are visible before the count
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[BAR_EPI]);
+    bool w = mbar_wait(&bar[BAR_EPI], *phase & 1u);
+    ++*phase;
+    if (!__all_sync(0xFFFFFFFFu, w)) return false;
+    const int64_t b_lo = dense_block_of(tile * nsb, units), b_hi = dense_block_of((tile + 1) * nsb - 1, units);
+    if (leader) {
+        const int before = atomicAdd(&tile_cnt[tile], 1);
+        const bool is_last = before == (int)(b_hi - b_lo);
+        if (is_last) tile_cnt[tile] = 0;  // every block of the tile has counted
+        misc[2] = is_last ? 1u : 0u;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar[BAR_EPI]);
+    w = mbar_wait(&bar[BAR_EPI], *phase & 1u);
+    ++*phase;
+    if (!__all_sync(0xFFFFFFFFu, w)) return false;
+    if (*reinterpret_cast<volatile uint32_t *>(&misc[2]) == 0u || !act) return true;
+    __threadfence();  // the other blocks' partial sums are read after their counts
+    for (int c = 0; c < ncol; c += 16) {
+        float acc[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int64_t b = b_lo; b <= b_hi; ++b) {
+            // block b's slot for this tile: its first piece's when that piece is this tile
+            const int which = dense_step_of(b, units) / nsb == tile ? 0 : 1;
+            const float *src = part + (size_t)(2 * b + which) * (BT * BM) + (size_t)(cbeg + c) * BM + (n % BM);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] += __ldcg(src + i * BM);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int64_t tt = (int64_t)t0 + cbeg + c + i;
+            if (tt < t_end) y[tt * N + n] = acc[i];
+        }
+    }
+    return true;
+}
+
+template <int F, bool G, bool DBG, bool SK>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap map_a16, const __grid_constant__ CUtensorMap map_b16,
                 const GemmParams p) {
@@ -749,6 +873,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(&bar[BAR_SD_EMPTY + 1], n_epi<F>());
         mbar_init(&bar[BAR_MMA_DONE], 1);
         mbar_init(&bar[BAR_TILES], 1);
+        mbar_init(&bar[BAR_EPI], n_epi<F>());  // the epilogue warps' split-tile handshake
+        mbar_init(&bar[BAR_END], NTHREADS / 32);  // every warp is done with TMEM
         mbar_fence_init();
         for (int i = 0; i < 32; ++i) s_flag[i] = FLAG_NEUTRAL;
     }
@@ -769,7 +895,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == W_TMA) {
         // ------------------------------------------------ activation tiles
         griddep_wait();
-        int ntiles = 1;
+        int ntiles = G ? 0 : dense_items<SK>(p);
         if constexpr (G) {
             ntiles = build_tile_list(p, reinterpret_cast<int *>(smem + C::OFF_OFFS), s_list, lane);
             __threadfence_block();
@@ -783,12 +909,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             tma_prefetch_desc(&map_a16);
             if (C::kMins) tma_prefetch_desc(&map_b16);
-            if (ntiles > 0) prefetch_tile<F>(p, G ? list_tile(s_list, 0) : dense_tile(p));
+            if (ntiles > 0) prefetch_tile<F>(p, work_piece<G, SK>(p, s_list, 0).t);
             for (int k = 0; k < ntiles && ok; ++k) {
-                const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+                const Piece q = work_piece<G, SK>(p, s_list, k);
+                const Tile t = q.t;
                 // the next tile's weights stream into L2 while this one runs
-                if (k + 1 < ntiles) prefetch_tile<F>(p, list_tile(s_list, k + 1));
-                for (int64_t sb = 0; sb < nsb && ok && t.ntok > 0; ++sb) {
+                if (k + 1 < ntiles) prefetch_tile<F>(p, work_piece<G, SK>(p, s_list, k + 1).t);
+                for (int64_t sb = q.sb0; sb < q.sb1 && ok && t.ntok > 0; ++sb) {
                     for (int h = 0; h < 2 && ok; ++h, ++use) {
                         const int slot = (int)(use % C::NB);
                         const uint32_t par = (uint32_t)((use / C::NB) & 1);
@@ -819,7 +946,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t b_base = smem_u32(smem + C::OFF_B);
         int64_t g = 0, use = 0, u = 0, mc = 0;
         if (lane == 0) {
-            int ntiles = 1;
+            int ntiles = G ? 0 : dense_items<SK>(p);
             if constexpr (G) {
                 ok = mbar_wait(&bar[BAR_TILES], 0);
                 ntiles = ok ? (int)misc[1] : 0;
@@ -834,9 +961,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 else issue_unit<C::B_SUB, 1>(U, v, acc, a_slot, b_slot, fresh, idesc);
             };
             for (int k = 0; k < ntiles && ok; ++k) {
-                const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+                const Piece q = work_piece<G, SK>(p, s_list, k);
+                const Tile t = q.t;
                 const uint32_t idesc = idesc_f16_f32(BM, t.n_mma > 0 ? t.n_mma : 16);
-                for (int64_t sb = 0; sb < nsb && ok; ++sb, ++g) {
+                for (int64_t sb = q.sb0; sb < q.sb1 && ok; ++sb, ++g) {
                     bool open = false;  // a unit begun in the first half, still accumulating
                     for (int h = 0; h < 2; ++h) {
                         const int slot = (int)(use % C::NB);
@@ -1079,8 +1207,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int k = 0, g = 0, ntiles = -1;  // ntiles: grouped list length, read once it is needed
         Tile t;
         bool have = true;
+        // the piece's half-stages [hs0, hs1) (grouped: the whole tile)
+        int hs0 = 0, hs1 = nstage;
+        int dn = 0;  // dense: the block's pieces
         if constexpr (!G) {
-            t = dense_tile(p);
+            dn = dense_items<SK>(p);
+            have = dn > 0;
+            if (have) {
+                const Piece q = work_piece<G, SK>(p, s_list, 0);
+                t = q.t;
+                hs0 = 2 * q.sb0;
+                hs1 = 2 * q.sb1;
+            }
         } else if (static_first) {
             const int w_tiles = w_tiles_of(p);
             t.e = (int)(blockIdx.x / w_tiles);
@@ -1093,18 +1231,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         // this thread's weight row of the tile
         int e_cur = t.e, row = t.n0 + r < p.N ? t.n0 + r : (int)p.N - 1;
-        if (have) load_raw(cur, make_planes(F, p.packed + (uint64_t)e_cur * p.expert_bytes, p.N, nsb), row, 0, nsb, 0);
+        if (have) load_raw(cur, make_planes(F, p.packed + (uint64_t)e_cur * p.expert_bytes, p.N, nsb), row, hs0 >> 1, nsb, 0);
         while (have && ok) {
             bool have_n = false;
             int e_nxt = e_cur, n0_nxt = 0;
+            int hs0_n = 0, hs1_n = nstage;
             const Planes P = make_planes(F, p.packed + (uint64_t)e_cur * p.expert_bytes, p.N, nsb);
-            for (int hs = 0; hs < nstage; ++hs) {
-                const int sb = hs >> 1, gg = g + sb;
+            for (int hs = hs0; hs < hs1; ++hs) {
+                const int gg = g + ((hs - hs0) >> 1);  // the block's superblock step
                 const int h = hs & 1;
-                // the next half's bytes (the next tile's first half at the
-                // end of a tile) are in flight while this one is converted
-                if (hs + 1 < nstage) {
+                // the next half's bytes (the next piece's first half at the
+                // end of a piece) are in flight while this one is converted
+                if (hs + 1 < hs1) {
                     load_raw(nxt, P, row, (hs + 1) >> 1, nsb, (hs + 1) & 1);
+                } else if constexpr (!G && SK) {
+                    have_n = k + 1 < dn;
+                    if (have_n) {
+                        const Piece q = dense_piece(p, k + 1);
+                        n0_nxt = q.t.n0;
+                        hs0_n = 2 * q.sb0;
+                        hs1_n = 2 * q.sb1;
+                        const int rn = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
+                        load_raw(nxt, P, rn, q.sb0, nsb, 0);
+                    }
                 } else if constexpr (G) {
                     if (ntiles < 0) {
                         if (!__all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0))) {
@@ -1204,11 +1353,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 cur = nxt;
             }
-            g += (int)nsb;
+            g += (hs1 - hs0) >> 1;
             ++k;
             have = have_n;
             e_cur = e_nxt;
             row = n0_nxt + r < p.N ? n0_nxt + r : (int)p.N - 1;
+            hs0 = hs0_n;
+            hs1 = hs1_n;
         }
         if (!ok && lane == 0) set_timeout();
         }
@@ -1225,14 +1376,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t y_tm = lane_addr + COL_Y;
         constexpr bool dbg = DBG;
         griddep_wait();  // the scales are written by the kernels before this one
-        int ntiles = 1;
+        int ntiles = G ? 0 : dense_items<SK>(p);
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
         }
         int64_t g = 0, u = 0;
+        uint32_t epi_phase = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
-            const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+            const Piece pc = work_piece<G, SK>(p, s_list, k);
+            const Tile t = pc.t;
             const int64_t n = t.n0 + r;
             const int nc = t.n_mma / 16;
             bool first = true;
@@ -1241,15 +1394,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int64_t tc = t.t0 + 32 * q + lane;
-                d8n[q] = tc < t.t_end ? __ldg(p.d8t + tc) : 0.0f;
+                d8n[q] = tc < t.t_end ? __ldg(p.d8t + pc.sb0 * p.Mp + tc) : 0.0f;
             }
-            for (int64_t sb = 0; sb < nsb; ++sb) {
-                const int64_t gg = g + sb;
+            for (int64_t sb = pc.sb0; sb < pc.sb1; ++sb) {
+                const int64_t gg = g + sb - pc.sb0;
                 const int b = (int)(gg & 1);
 #pragma unroll
                 for (int q = 0; q < 4; ++q) s_d8[32 * q + lane] = d8n[q];
                 __syncwarp();
-                if (sb + 1 < nsb) {
+                if (sb + 1 < pc.sb1) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const int64_t tc = t.t0 + 32 * q + lane;
@@ -1316,11 +1469,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             if (!ok) break;
             if (!dbg && t.ntok > 0) {
                 tc_fence_after();
+                const bool whole = G || !SK || (pc.sb0 == 0 && pc.sb1 == (int)nsb);
+                float *mine = own_slot(p, k);
                 for (int c = 0; c < nc; ++c) {
                     uint32_t vy[16];
                     tmem_ld16(y_tm + 16 * c, vy);
                     tmem_wait_ld();
-                    if (n < p.N) {
+                    if (!whole) {
+                        // a tile split between blocks: this block's partial sums
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) mine[(16 * c + i) * BM + r] = __uint_as_float(vy[i]);
+                    } else if (n < p.N) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int64_t tt = t.t0 + 16 * c + i;
@@ -1328,8 +1487,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         }
                     }
                 }
+                if (!whole && !split_finish(p.part, p.tile_cnt, p.units, nsb, pc.tile, p.y, p.N, n, t.t0, t.t_end, 0,
+                                            16 * nc, n < p.N, ew == 0 && lane == 0, lane, &epi_phase, bar, misc)) {
+                    ok = false;
+                    break;
+                }
             }
-            g += nsb;
+            g += pc.sb1 - pc.sb0;
         }
         if (!ok && lane == 0) set_timeout();
     } else {
@@ -1344,15 +1508,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 64 * ew;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16) + 64 * ch;
         griddep_wait();  // the scales are written by the kernels before this one
-        int ntiles = 1;
+        int ntiles = G ? 0 : dense_items<SK>(p);
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
         }
         // 32-bit counters: a block runs at most TILE_CAP tiles of at most 2^22 superblocks
-        uint32_t g = 0, u = 0, mc = 0;
+        uint32_t g = 0, u = 0, mc = 0, epi_phase = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
-            const Tile t = G ? list_tile(s_list, k) : dense_tile(p);
+            const Piece pc = work_piece<G, SK>(p, s_list, k);
+            const Tile t = pc.t;
             const int n = t.n0 + r;
             float y[64];
 #pragma unroll
@@ -1361,15 +1526,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // this warp's 64 token scales d8 of the next superblock, loaded one superblock ahead
             const int tc = t.t0 + 64 * ch + lane;
             const float *d8col = p.d8t + tc;
-            float d8n0 = tc < t.t_end ? __ldg(d8col) : 0.0f;
-            float d8n1 = (tc + 32) < t.t_end ? __ldg(d8col + 32) : 0.0f;
-            for (int sb = 0; sb < (int)nsb; ++sb) {
-                const uint32_t gg = g + (uint32_t)sb;
+            float d8n0 = tc < t.t_end ? __ldg(d8col + (int64_t)pc.sb0 * p.Mp) : 0.0f;
+            float d8n1 = (tc + 32) < t.t_end ? __ldg(d8col + (int64_t)pc.sb0 * p.Mp + 32) : 0.0f;
+            for (int sb = pc.sb0; sb < pc.sb1; ++sb) {
+                const uint32_t gg = g + (uint32_t)(sb - pc.sb0);
                 const int b = (int)(gg & 1);
                 s_d8[lane] = d8n0;
                 s_d8[lane + 32] = d8n1;
                 __syncwarp();
-                if (sb + 1 < (int)nsb) {
+                if (sb + 1 < pc.sb1) {
                     const float *d8p = d8col + (int64_t)(sb + 1) * p.Mp;
                     d8n0 = tc < t.t_end ? __ldg(d8p) : 0.0f;
                     d8n1 = (tc + 32) < t.t_end ? __ldg(d8p + 32) : 0.0f;
@@ -1416,21 +1581,41 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (!ok) break;
             }
             if (!ok) break;
-            if (!DBG && n < p.N && cols) {
-                const int c0 = t.t0 + 64 * ch, lim = t.t_end - c0;
-                float *yp = p.y + (int64_t)c0 * p.N + n;
+            if constexpr (!DBG) {
+                // a whole tile goes to y; a tile split between blocks to this
+                // block's partial slot, finished by the last of its blocks
+                const bool whole = G || !SK || (pc.sb0 == 0 && pc.sb1 == (int)nsb);
+                const int c0 = t.t0 + 64 * ch;
+                const int lim = whole ? t.t_end - c0 : 64;
+                float *yp = whole ? p.y + (int64_t)c0 * p.N + n : own_slot(p, k) + 64 * ch * BM + r;
+                const int64_t ys = whole ? p.N : BM;
+                if (cols && (n < p.N || !whole)) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    if (i < lim) yp[(int64_t)i * p.N] = y[i];
+                    for (int i = 0; i < 64; ++i)
+                        if (i < lim) yp[(int64_t)i * ys] = y[i];
+                }
+                if (!whole && !split_finish(p.part, p.tile_cnt, p.units, nsb, pc.tile, p.y, p.N, n, t.t0, t.t_end,
+                                            64 * ch, 64, n < p.N && cols, ew == 0 && lane == 0, lane, &epi_phase,
+                                            bar, misc)) {
+                    ok = false;
+                    break;
+                }
             }
-            g += (uint32_t)nsb;
+            g += (uint32_t)(pc.sb1 - pc.sb0);
         }
         if (!ok && lane == 0) set_timeout();
     }
 
+    // TMEM is released once every warp is done with it.  An explicit
+    // mbarrier, not __syncthreads: the roles reach the end at different
+    // times on diverged lanes (the TMA and MMA roles run on lane 0), and a
+    // block barrier reached that way was measured to let the MMA warp pass
+    // while the epilogue warps were still at work.
+    __syncwarp();
     tc_fence_before();
-    __syncthreads();
+    if (lane == 0) mbar_arrive(&bar[BAR_END]);
     if (warp == W_MMA) {
+        if (!mbar_wait(&bar[BAR_END], 0) && lane == 0) set_timeout();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -1442,10 +1627,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 __global__ void __launch_bounds__(256) act_image_kernel(const int8_t *__restrict__ qs, const int16_t *__restrict__ bs,
                                                         const float *__restrict__ d8, int64_t M, int64_t K,
                                                         int64_t Mp, __half *__restrict__ a16,
-                                                        __half *__restrict__ b16, float *__restrict__ d8t) {
+                                                        __half *__restrict__ b16, float *__restrict__ d8t,
+                                                        int *__restrict__ tile_cnt, int64_t n_cnt) {
     griddep_launch_dependents();
     griddep_wait();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // group of 8 quants
+    // the GEMM's split-tile counters start from zero (the image has at least as many threads)
+    if (i < n_cnt) tile_cnt[i] = 0;
     const int64_t groups = M * K / 8;
     if (i < groups) {
         const uint2 v = __ldg(reinterpret_cast<const uint2 *>(qs) + i);
@@ -1502,37 +1690,77 @@ static bool make_map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The workspace: the activation image (a16, b16, d8t: all a launch needs),
+// then, for the dense split-tile schedule, two fp32 partial tiles per SM and
+// a counter per tile.
 struct WsLayout {
     uint64_t a16, b16, d8t, total;
-    int64_t Mp;
+    uint64_t part, cnt, total_split;
+    int64_t Mp, tiles;
 };
 
-static WsLayout ws_layout(int64_t M, int64_t K) {
+static int device_sms() {
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (!v) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+        cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+static WsLayout ws_layout(int64_t M, int64_t N, int64_t K) {
     WsLayout w;
     w.Mp = (M + 3) & ~int64_t(3);
     w.a16 = 0;
     w.b16 = align256((uint64_t)M * K * 2);
     w.d8t = w.b16 + align256((uint64_t)M * (K / 16) * 2);
     w.total = w.d8t + align256((uint64_t)(K / QK) * w.Mp * 4);
+    w.tiles = ((N + BM - 1) / BM) * ((M + BT - 1) / BT);
+    w.part = w.total;
+    w.cnt = w.part + (uint64_t)2 * device_sms() * BT * BM * 4;
+    w.total_split = w.cnt + align256((uint64_t)w.tiles * 4);
     return w;
 }
 
 // M below which the CUDA-core token-group kernel is used instead
 
-size_t gemm_workspace_bytes(int, int64_t M, int64_t, int64_t K) {
+size_t gemm_workspace_bytes(int, int64_t M, int64_t N, int64_t K) {
     if (M < GEMM_TC_MIN_M) return 0;
-    return (size_t)ws_layout(M, K).total;
+    return (size_t)ws_layout(M, N, K).total_split;
+}
+
+size_t gemm_workspace_min_bytes(int, int64_t M, int64_t N, int64_t K) {
+    if (M < GEMM_TC_MIN_M) return 0;
+    return (size_t)ws_layout(M, N, K).total;
 }
 
 template <int F>
 static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
-                                 int64_t E, uint64_t expert_bytes, float *y, uint8_t *ws, cudaStream_t s,
-                                 int32_t *isum_out = nullptr, int32_t *msum_out = nullptr) {
+                                 int64_t E, uint64_t expert_bytes, float *y, uint8_t *ws, size_t ws_bytes,
+                                 cudaStream_t s, int32_t *isum_out = nullptr, int32_t *msum_out = nullptr) {
     using Cf = Cfg<F>;
-    const WsLayout L = ws_layout(M, K);
+    const WsLayout L = ws_layout(M, N, K);
     __half *a16 = reinterpret_cast<__half *>(ws + L.a16);
     __half *b16 = reinterpret_cast<__half *>(ws + L.b16);
     float *d8t = reinterpret_cast<float *>(ws + L.d8t);
+    // dense: the split-tile schedule (one block per SM, each an even share of
+    // the tiles x superblocks steps) where a block per tile would leave the
+    // last wave of tiles mostly empty and every block still gets 16
+    // superblock steps or more (fewer: its start-up and the partial tiles'
+    // handoff cost more than the wave saves; measured on GB300), and the
+    // workspace has its room
+    bool split = false;
+    if (!offsets && ws_bytes >= L.total_split) {
+        const int64_t n_sm = device_sms(), nsb = K / QK;
+        const int64_t waves = (L.tiles + n_sm - 1) / n_sm;
+        const bool ragged = 4 * L.tiles < 3 * waves * n_sm;  // the tiles fill under 3/4 of their waves
+        split = (ragged && L.tiles * nsb >= 16 * n_sm) || (launch_flags() & LAUNCH_GEMM_SPLIT);
+    }
+    int *tile_cnt = split ? reinterpret_cast<int *>(ws + L.cnt) : nullptr;
+    const int64_t n_cnt = split ? L.tiles : 0;
     {
         const int64_t groups = M * K / 8;
         cudaLaunchConfig_t cfg = {};
@@ -1544,7 +1772,8 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, act_image_kernel, a.qs, a.bsums, a.d, M, K, L.Mp, a16, b16, d8t);
+        cudaError_t e = cudaLaunchKernelEx(&cfg, act_image_kernel, a.qs, a.bsums, a.d, M, K, L.Mp, a16, b16, d8t,
+                                           tile_cnt, n_cnt);
         if (e != cudaSuccess) return e;
     }
     CUtensorMap ma, mb;
@@ -1559,8 +1788,12 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_acquire)) {
-        const void *fns[4] = {(const void *)gemm_kernel<F, false, false>, (const void *)gemm_kernel<F, true, false>,
-                              (const void *)gemm_kernel<F, false, true>, (const void *)gemm_kernel<F, true, true>};
+        const void *fns[6] = {(const void *)gemm_kernel<F, false, false, false>,
+                              (const void *)gemm_kernel<F, false, false, true>,
+                              (const void *)gemm_kernel<F, true, false, false>,
+                              (const void *)gemm_kernel<F, false, true, false>,
+                              (const void *)gemm_kernel<F, false, true, true>,
+                              (const void *)gemm_kernel<F, true, true, false>};
         for (const void *fn : fns) {
             const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, Cf::SMEM);
             if (e != cudaSuccess) return e;
@@ -1581,6 +1814,8 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     p.y = y;
     p.isum_out = isum_out;
     p.msum_out = msum_out;
+    p.part = split ? reinterpret_cast<float *>(ws + L.part) : nullptr;
+    p.tile_cnt = tile_cnt;
     if (isum_out) {
         const size_t bytes = (size_t)M * (size_t)N * (size_t)(K / QK) * sizeof(int32_t);
         cudaError_t e = cudaMemsetAsync(isum_out, 0, bytes, s);
@@ -1597,6 +1832,13 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     if (tiles > (int64_t)INT32_MAX || N > (int64_t)INT32_MAX - BM) return cudaErrorNotSupported;
     if (offsets && E > MAX_GROUPED_E) return cudaErrorNotSupported;
     int64_t blocks = tiles;
+    if (!offsets) {
+        p.units = tiles * p.nsb;
+        if (split) {
+            const int64_t n_sm = device_sms();
+            blocks = p.units < n_sm ? p.units : n_sm;
+        }
+    }
     if (offsets) {
         static std::atomic<int> sms[64];
         int n_sm = sms[dev].load(std::memory_order_relaxed);
@@ -1620,37 +1862,41 @@ static cudaError_t launch_gemm_f(const void *packed, int64_t N, int64_t K, Q8K a
     cfg.attrs = attr;
     cfg.numAttrs = (launch_flags() & LAUNCH_PDL) ? 1 : 0;
     if (isum_out) {
-        if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, true>, ma, mb, p);
-        return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, true>, ma, mb, p);
+        if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, true, false>, ma, mb, p);
+        if (split) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, true, true>, ma, mb, p);
+        return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, true, false>, ma, mb, p);
     }
-    if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, false>, ma, mb, p);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, false>, ma, mb, p);
+    if (offsets) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, true, false, false>, ma, mb, p);
+    if (split) return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, false, true>, ma, mb, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<F, false, false, false>, ma, mb, p);
 }
 
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M, const int32_t *offsets,
                            int64_t E, uint64_t expert_bytes, float *y, void *workspace, size_t workspace_bytes,
                            cudaStream_t s) {
     if (M < GEMM_TC_MIN_M || !workspace) return cudaErrorNotSupported;
-    if (workspace_bytes < ws_layout(M, K).total) return cudaErrorInvalidValue;
+    if (workspace_bytes < ws_layout(M, N, K).total) return cudaErrorInvalidValue;
     if (M > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX / 2) return cudaErrorNotSupported;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    if (f == FMT_Q4_K) return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
-    if (f == FMT_Q5_K) return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
-    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, s);
+    const size_t wb = workspace_bytes;
+    if (f == FMT_Q4_K) return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, wb, s);
+    if (f == FMT_Q5_K) return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, wb, s);
+    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, y, ws, wb, s);
 }
 
 cudaError_t launch_gemm_tc_partials(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                                     const int32_t *offsets, int64_t E, uint64_t expert_bytes, int32_t *isum,
                                     int32_t *msum, void *workspace, size_t workspace_bytes, cudaStream_t s) {
     if (M < GEMM_TC_MIN_M || !workspace) return cudaErrorNotSupported;
-    if (workspace_bytes < ws_layout(M, K).total) return cudaErrorInvalidValue;
+    if (workspace_bytes < ws_layout(M, N, K).total) return cudaErrorInvalidValue;
     if (M > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX / 2) return cudaErrorNotSupported;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const size_t wb = workspace_bytes;
     if (f == FMT_Q4_K)
-        return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
+        return launch_gemm_f<FMT_Q4_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, wb, s, isum, msum);
     if (f == FMT_Q5_K)
-        return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
-    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, s, isum, msum);
+        return launch_gemm_f<FMT_Q5_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, wb, s, isum, msum);
+    return launch_gemm_f<FMT_Q6_K>(packed, N, K, a, M, offsets, E, expert_bytes, nullptr, ws, wb, s, isum, msum);
 }
 
 // Test hook: one block whose single bounded wait is never satisfied, so the

@@ -14,6 +14,7 @@ namespace kq {
 // Library-wide launch options (kq_set_launch_flags).
 constexpr unsigned LAUNCH_PDL = 1u;
 constexpr unsigned LAUNCH_GEMV_SPLIT = 2u;
+constexpr unsigned LAUNCH_GEMM_SPLIT = 4u;
 unsigned launch_flags();
 
 struct Q8K {
@@ -98,7 +99,12 @@ cudaError_t launch_debug_decode(int f, const void *packed, int64_t N, int64_t K,
 
 // Tensor-core GEMM (tcgen05).  Returns cudaErrorNotSupported when the shape
 // or device is not handled, so the caller can fall back to launch_mv.
+// gemm_workspace_bytes: the workspace with room for the dense split-tile
+// schedule (what kq_gemm_workspace_bytes reports); gemm_workspace_min_bytes:
+// the least a launch accepts (the activation image alone; the dense GEMM then
+// runs a block per tile).
 size_t gemm_workspace_bytes(int f, int64_t M, int64_t N, int64_t K);
+size_t gemm_workspace_min_bytes(int f, int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_tc(int f, const void *packed, int64_t N, int64_t K, Q8K a, int64_t M,
                            const int32_t *row_offsets, int64_t E, uint64_t expert_bytes, float *y,
                            void *workspace, size_t workspace_bytes, cudaStream_t s);

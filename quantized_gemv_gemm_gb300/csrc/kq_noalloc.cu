@@ -40,11 +40,12 @@ extern "C" int kq_gemm_noalloc(kq_format f, const void *packed, int64_t N, int64
                                float *y, cudaStream_t s) {
     if (f != KQ_Q4_K && f != KQ_Q5_K && f != KQ_Q6_K) return KQ_ERR_FORMAT;
     if (N < 0 || M < 0 || K <= 0 || K % kq::QK != 0) return KQ_ERR_ARG;
-    const size_t need = kq_gemm_workspace_bytes(f, M, N, K);
+    // the activation image must fit; the split-tile room is used when it fits too
+    const size_t need = kq::gemm_workspace_min_bytes(f, M, N, K);
     if (need > KQ_NOALLOC_SCRATCH_BYTES) return KQ_ERR_TOO_LARGE;
     void *ws = nullptr;
     if (need > 0 && M > 0 && N > 0) {
         if (int r = scratch_of_current_device(&ws)) return r;
     }
-    return kq::gemm_common(f, packed, 1, nullptr, N, K, a, M, y, ws, need, s);
+    return kq::gemm_common(f, packed, 1, nullptr, N, K, a, M, y, ws, need ? KQ_NOALLOC_SCRATCH_BYTES : 0, s);
 }

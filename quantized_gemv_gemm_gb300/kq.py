@@ -48,6 +48,8 @@ _lib.kq_gemv_fused_batch.argtypes = [_INT, _INT, _P, _P, _I64, _P, _I64, _P, _P,
 _lib.kq_gemv_grouped_fused.argtypes = [_INT, _INT, _P, _P, _I64, _I64, _P, _P, _I64, _P, _P]
 _lib.kq_gemm_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
 _lib.kq_gemm_workspace_bytes.restype = _SZ
+_lib.kq_gemm_min_workspace_bytes.argtypes = [_INT, _I64, _I64, _I64]
+_lib.kq_gemm_min_workspace_bytes.restype = _SZ
 _lib.kq_gemm.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_grouped.argtypes = [_INT, _P, _I64, _P, _I64, _I64, _Q8KConst, _I64, _P, _P, _SZ, _P]
 _lib.kq_gemm_noalloc.argtypes = [_INT, _P, _I64, _I64, _Q8KConst, _I64, _P, _P]
@@ -272,6 +274,10 @@ def kq_gemm_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
     return int(_lib.kq_gemm_workspace_bytes(int(fmt), int(M), int(N), int(K)))
 
 
+def kq_gemm_min_workspace_bytes(fmt: int, M: int, N: int, K: int) -> int:
+    return int(_lib.kq_gemm_min_workspace_bytes(int(fmt), int(M), int(N), int(K)))
+
+
 def _workspace(fmt, M, N, K, workspace, device):
     need = kq_gemm_workspace_bytes(fmt, M, N, K)
     if workspace is None and need:
@@ -456,10 +462,12 @@ def kq_device_status(stream=None) -> int:
 
 KQ_LAUNCH_PDL = 1
 KQ_LAUNCH_GEMV_SPLIT = 2
+KQ_LAUNCH_GEMM_SPLIT = 4
 
 
 def kq_set_launch_flags(flags: int) -> int:
-    """Set the process-wide launch flags (KQ_LAUNCH_PDL, KQ_LAUNCH_GEMV_SPLIT); returns the old ones."""
+    """Set the process-wide launch flags (KQ_LAUNCH_PDL, KQ_LAUNCH_GEMV_SPLIT, KQ_LAUNCH_GEMM_SPLIT); returns
+    the old ones."""
     return int(_lib.kq_set_launch_flags(int(flags)))
 
 

@@ -152,11 +152,11 @@ def test_host_argument_checks(kq):
 
 
 def test_launch_flags_mask(kq):
-    """Unknown flag bits are dropped; the two defined ones are kept."""
+    """Unknown flag bits are dropped; the three defined ones are kept."""
     old = kq.kq_set_launch_flags(0xFFFF)
     try:
-        assert kq.kq_get_launch_flags() == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT
-        assert kq.kq_set_launch_flags(0) == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT
+        assert kq.kq_get_launch_flags() == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT | kq.KQ_LAUNCH_GEMM_SPLIT
+        assert kq.kq_set_launch_flags(0) == kq.KQ_LAUNCH_PDL | kq.KQ_LAUNCH_GEMV_SPLIT | kq.KQ_LAUNCH_GEMM_SPLIT
         assert kq.kq_get_launch_flags() == 0
     finally:
         kq.kq_set_launch_flags(old)

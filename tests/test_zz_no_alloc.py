@@ -53,7 +53,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(K):
     """A problem whose scratch would exceed the fixed array is refused with
     KQ_ERR_TOO_LARGE before anything is enqueued."""
     M, Kdim = 4096, 8192                 # 64 MiB of fp16 activation image
-    assert K.kq_gemm_workspace_bytes(synth.Q4_K, M, 4096, Kdim) > K.KQ_NOALLOC_SCRATCH_BYTES
+    assert K.kq_gemm_min_workspace_bytes(synth.Q4_K, M, 4096, Kdim) > K.KQ_NOALLOC_SCRATCH_BYTES
     q = K._Q8KConst(0x10000, 0x10000, 0x10000)   # never dereferenced: the size check comes first
     rc = K.raw().kq_gemm_noalloc(synth.Q4_K, 0x10000, 4096, Kdim, q, M, 0x10000, None)
     assert rc == -8
@@ -63,8 +63,8 @@ def test_noalloc_rejects_problems_beyond_its_scratch(K):
 def test_noalloc_size_limit_boundary(K):
     """The documented largest shape (512 tokens x K = 30464) fits the fixed
     array and the next step of K (30720) is refused before anything runs."""
-    fits = K.kq_gemm_workspace_bytes(synth.Q4_K, 512, 4096, 30464)
-    over = K.kq_gemm_workspace_bytes(synth.Q4_K, 512, 4096, 30720)
+    fits = K.kq_gemm_min_workspace_bytes(synth.Q4_K, 512, 4096, 30464)
+    over = K.kq_gemm_min_workspace_bytes(synth.Q4_K, 512, 4096, 30720)
     assert fits <= K.KQ_NOALLOC_SCRATCH_BYTES < over
     q = K._Q8KConst(0x10000, 0x10000, 0x10000)   # never dereferenced: the size check comes first
     rc = K.raw().kq_gemm_noalloc(synth.Q4_K, 0x10000, 4096, 30720, q, 512, 0x10000, None)
