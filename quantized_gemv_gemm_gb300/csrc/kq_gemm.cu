@@ -609,12 +609,14 @@ __device__ __forceinline__ void prefetch_tile(const GemmParams &p, const Tile &t
 // thread holds one weight row.
 
 // Q4_K/Q5_K: y[64] (64 token columns, in registers) += d8 * (d * U - dmin *
-// msum) for one unit U, CW (8 or 16) columns per TMEM load round trip
+// msum) for one unit U, CW (8 or 16) columns per TMEM load round trip, over
+// the first nch such chunks (the tile's token columns; the rest are padding)
 template <int CW, bool WM>
 __device__ __forceinline__ void fold_unit_q45(float (&y)[64], uint32_t xu, uint32_t xm, float dd, float dm,
-                                              const float *s_d8) {
+                                              const float *s_d8, int nch) {
 #pragma unroll
     for (int cc = 0; cc < 64 / CW; ++cc) {
+        if (cc >= nch) break;
         uint32_t vu[CW], vm[CW];
         if constexpr (CW == 16) {
             tmem_ld16(xu + 16 * cc, vu);
@@ -1523,6 +1525,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int i = 0; i < 64; ++i) y[i] = 0.0f;
             const bool cols = 64 * ch < t.n_mma;
+            // this warp's 8-column chunks holding tokens of the tile
+            const int nch = cols ? (t.n_mma - 64 * ch >= 64 ? 8 : (t.n_mma - 64 * ch + 7) / 8) : 0;
             // this warp's 64 token scales d8 of the next superblock, loaded one superblock ahead
             const int tc = t.t0 + 64 * ch + lane;
             const float *d8col = p.d8t + tc;
@@ -1567,8 +1571,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         // 8 columns a TMEM round trip: with y[64] and the loop's
                         // state live, 16 would spill
                         if constexpr (DBG) debug_units(p.isum_out, p.msum_out, p.N, nsb, xu, false, 0u, last, xm, 64, t.t0 + 64 * ch, t.t_end, n, sb);
-                        else if (last) fold_unit_q45<8, true>(y, xu, xm, dd, dm, s_d8);
-                        else fold_unit_q45<8, false>(y, xu, xm, dd, 0.0f, s_d8);
+                        else if (last) fold_unit_q45<8, true>(y, xu, xm, dd, dm, s_d8, nch);
+                        else fold_unit_q45<8, false>(y, xu, xm, dd, 0.0f, s_d8, nch);
                     }
                     tc_fence_before();
                     __syncwarp();
