@@ -83,7 +83,10 @@ struct Cfg {
     // Q4_K/Q5_K keep the unpacked weights (the A operand) in TMEM, Q6_K (two
     // planes, no room beside its y) in shared memory
     static constexpr bool kTmemA = F != FMT_Q6_K;
-    static constexpr int NB = F == FMT_Q6_K ? 2 : 3;              // B ring slots
+    // the ring of half superblocks: NB token tiles in flight; the A operand
+    // has two half slots, A slot h of half i free once half i - 2 is empty
+    static constexpr int NB = F == FMT_Q6_K ? 2 : 3;
+    static_assert(NB >= 2 && NB <= 4, "ring of half superblocks");
     static constexpr int A_SLOT = kTmemA ? 0 : 65536;             // Q6_K: 2 sub-tiles x 2 planes
     static constexpr int B_SUB = BT * 128;                         // one 64-wide K sub-tile of tokens
     static constexpr int B_SLOT = 2 * B_SUB + (kMins ? BT * 32 : 0);
@@ -112,10 +115,13 @@ struct Cfg {
     static_assert(B_SLOT % 1024 == 0, "B slots need 1024-byte alignment");
 };
 
-// barrier indices: A and B operand rings, the ring of unit accumulators
-// (U), the two msum accumulators (M), the per-superblock weight scales and
-// unit plans (SD, by superblock parity), MMA completion, the tile list
-enum { BAR_FULL_A = 0, BAR_EMPTY_A = 2, BAR_FULL_B = 4, BAR_EMPTY_B = 7, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
+// barrier indices: the operand ring of half superblocks (FULL: the half's
+// A operand unpacked and its token tile landed; EMPTY: its MMAs complete,
+// so both its A slot and its B slot may be refilled), the ring of unit
+// accumulators (U), the msum accumulator (M), the per-superblock weight
+// scales and unit plans (SD, by superblock parity), MMA completion, the
+// tile list
+enum { BAR_FULL = 0, BAR_EMPTY = 4, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
        BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25,
        BAR_EPI = 26, BAR_END = 27 };
 
@@ -851,13 +857,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- setup
     if (threadIdx.x == 0) {
-        mbar_init(&bar[BAR_FULL_A + 0], n_unpack<F>());
-        mbar_init(&bar[BAR_FULL_A + 1], n_unpack<F>());
-        mbar_init(&bar[BAR_EMPTY_A + 0], 1);
-        mbar_init(&bar[BAR_EMPTY_A + 1], 1);
+        // a half is full once every unpack warp has written its A rows and
+        // the TMA thread's token tile has landed (its arrive carries the
+        // byte count); empty once the MMAs that read it are complete
         for (int i = 0; i < C::NB; ++i) {
-            mbar_init(&bar[BAR_FULL_B + i], 1);
-            mbar_init(&bar[BAR_EMPTY_B + i], 1);
+            mbar_init(&bar[BAR_FULL + i], n_unpack<F>() + 1);
+            mbar_init(&bar[BAR_EMPTY + i], 1);
         }
         for (int i = 0; i < NU; ++i) {
             mbar_init(&bar[BAR_U_FULL + i], 1);
@@ -907,7 +912,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 mbar_arrive(&bar[BAR_TILES]);
             }
         }
-        int64_t use = 0;
+        // ring position of the half: slot and the parity of its round
+        uint32_t slot = 0, round = 0, issued = 0;
         if (lane == 0) {
             tma_prefetch_desc(&map_a16);
             if (C::kMins) tma_prefetch_desc(&map_b16);
@@ -917,28 +923,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const Tile t = q.t;
                 // the next tile's weights stream into L2 while this one runs
                 if (k + 1 < ntiles) prefetch_tile<F>(p, work_piece<G, SK>(p, s_list, k + 1).t);
-                for (int64_t sb = q.sb0; sb < q.sb1 && ok && t.ntok > 0; ++sb) {
-                    for (int h = 0; h < 2 && ok; ++h, ++use) {
-                        const int slot = (int)(use % C::NB);
-                        const uint32_t par = (uint32_t)((use / C::NB) & 1);
-                        if (!mbar_wait(&bar[BAR_EMPTY_B + slot], par ^ 1)) { ok = false; break; }
-                        uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
-                        // the token bsums (msum's operand) come with the second half,
-                        // after whose units msum is issued
-                        const bool mins = C::kMins && h == 1;
-                        mbar_arrive_expect_tx(&bar[BAR_FULL_B + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
-                        const int k0 = (int)(sb * QK + 128 * h);
-                        tma_load_2d(bs, &map_a16, k0, t.t0, &bar[BAR_FULL_B + slot]);
-                        tma_load_2d(bs + C::B_SUB, &map_a16, k0 + 64, t.t0, &bar[BAR_FULL_B + slot]);
-                        if (mins) tma_load_2d(bs + 2 * C::B_SUB, &map_b16, (int)(sb * 16), t.t0, &bar[BAR_FULL_B + slot]);
+                for (int64_t sb = q.sb0; sb < q.sb1 && ok; ++sb) {
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        if (!mbar_wait(&bar[BAR_EMPTY + slot], (round & 1u) ^ 1u)) { ok = false; break; }
+                        if (t.ntok > 0) {
+                            uint8_t *bs = smem + C::OFF_B + slot * C::B_SLOT;
+                            // the token bsums (msum's operand) come with the second half,
+                            // after whose units msum is issued
+                            const bool mins = C::kMins && h == 1;
+                            mbar_arrive_expect_tx(&bar[BAR_FULL + slot], 2 * C::B_SUB + (mins ? BT * 32 : 0));
+                            const int k0 = (int)(sb * QK + 128 * h);
+                            tma_load_2d(bs, &map_a16, k0, t.t0, &bar[BAR_FULL + slot]);
+                            tma_load_2d(bs + C::B_SUB, &map_a16, k0 + 64, t.t0, &bar[BAR_FULL + slot]);
+                            if (mins) tma_load_2d(bs + 2 * C::B_SUB, &map_b16, (int)(sb * 16), t.t0, &bar[BAR_FULL + slot]);
+                            ++issued;
+                        } else {
+                            mbar_arrive(&bar[BAR_FULL + slot]);  // a tile without rows: nothing to load
+                        }
+                        if (++slot == C::NB) {
+                            slot = 0;
+                            ++round;
+                        }
                     }
                 }
             }
             if (!ok) {
                 set_timeout();
-                // let the copies already issued land before the block exits
-                for (int s = 0; s < C::NB; ++s)
-                    if (use > s) mbar_wait(&bar[BAR_FULL_B + ((use - 1 - s) % C::NB)], (uint32_t)(((use - 1 - s) / C::NB) & 1));
+                // let the copies already issued land before the block exits:
+                // the MMA thread, also winding down, has stopped consuming,
+                // so wait (bounded) for the last slots' phases
+                for (int s = 0; s < C::NB && (uint32_t)s < issued; ++s) {
+                    slot = slot == 0 ? C::NB - 1 : slot - 1;
+                    if (slot == C::NB - 1) --round;
+                    mbar_wait(&bar[BAR_FULL + slot], round & 1u, 20000000ull);
+                }
             }
         }
     } else if (warp == W_MMA) {
@@ -946,7 +964,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t a_base = smem_u32(smem + C::OFF_A);
         const uint32_t amin = smem_u32(smem + C::OFF_AMIN);
         const uint32_t b_base = smem_u32(smem + C::OFF_B);
-        int64_t g = 0, use = 0, u = 0, mc = 0;
+        // g: the block's superblock steps; slot/round: the ring position of the
+        // half; u: units issued; mc: msum issues (32 bits: a block runs at
+        // most TILE_CAP tiles of at most 2^22 superblocks)
+        uint32_t g = 0, slot = 0, round = 0, u = 0, mc = 0;
         if (lane == 0) {
             int ntiles = G ? 0 : dense_items<SK>(p);
             if constexpr (G) {
@@ -969,21 +990,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 for (int64_t sb = q.sb0; sb < q.sb1 && ok; ++sb, ++g) {
                     bool open = false;  // a unit begun in the first half, still accumulating
                     for (int h = 0; h < 2; ++h) {
-                        const int slot = (int)(use % C::NB);
-                        if (!mbar_wait(&bar[BAR_FULL_A + h], (uint32_t)(g & 1)) ||
-                            (t.ntok > 0 && !mbar_wait(&bar[BAR_FULL_B + slot], (uint32_t)((use / C::NB) & 1)))) {
+                        const uint32_t cur = slot, cur_par = round & 1u;
+                        if (++slot == C::NB) {
+                            slot = 0;
+                            ++round;
+                        }
+                        // the half's A operand and token tile
+                        if (!mbar_wait(&bar[BAR_FULL + cur], cur_par)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (t.ntok == 0) {  // a first tile without rows: release the A slot unread
-                            mbar_arrive(&bar[BAR_EMPTY_A + h]);
+                        if (t.ntok == 0) {  // a first tile without rows: release the half unread
+                            mbar_arrive(&bar[BAR_EMPTY + cur]);
                             continue;
                         }
                         const uint32_t a_slot = a_base + h * C::A_SLOT;
                         const uint32_t a_tm = tmem + COL_A + 64 * (uint32_t)h;
-                        const uint32_t b_slot = b_base + slot * C::B_SLOT;
-                        // this half's flags are in (the second half's are written after FULL_A[1])
+                        const uint32_t b_slot = b_base + cur * C::B_SLOT;
+                        // this half's flags are in (each unpack warp writes its byte before
+                        // it arrives on the half's FULL)
                         const uint32_t fl = flag_sa + 16 * (uint32_t)(g & 1);
                         SbPlan pl;
                         if (h == 0) {
@@ -1040,9 +1066,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             umma_commit(&bar[BAR_M_FULL]);
                             ++mc;
                         }
-                        umma_commit(&bar[BAR_EMPTY_A + h]);
-                        umma_commit(&bar[BAR_EMPTY_B + slot]);
-                        ++use;
+                        umma_commit(&bar[BAR_EMPTY + cur]);  // frees the half's A and B slots
                     }
                 }
             }
@@ -1148,7 +1172,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const uint4 hdr = lds128(slot_addr(slot, 4));
                 uint2 bnd;
                 asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(bnd.x), "=r"(bnd.y) : "r"(rbnd + (uint32_t)((slot * BM + r) * 8)));
-                bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
+                // A slot h: the MMAs of half 2 gg + h - 2 are complete
+                const uint32_t hu = 2u * (uint32_t)gg + (uint32_t)h;
+                bool w_ok = hu < 2 || mbar_wait(&bar[BAR_EMPTY + (hu - 2) % C::NB], ((hu - 2) / C::NB) & 1u);
                 // the epilogue has read the scales of superblock gg - 2
                 if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_SD_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
                 if (!__all_sync(0xFFFFFFFFu, w_ok)) {
@@ -1191,7 +1217,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&bar[BAR_FULL_A + h]);
+                    mbar_arrive(&bar[BAR_FULL + hu % C::NB]);
                     // the scales and both halves' unit flags are written
                     if (h == 1) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
                 }
@@ -1276,7 +1302,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         load_raw(nxt, Q, rn, 0, nsb, 0);
                     }
                 }
-                bool w_ok = mbar_wait(&bar[BAR_EMPTY_A + h], (uint32_t)((gg & 1) ^ 1));
+                // A slot h: the MMAs of half 2 gg + h - 2 are complete
+                const uint32_t hu = 2u * (uint32_t)gg + (uint32_t)h;
+                bool w_ok = hu < 2 || mbar_wait(&bar[BAR_EMPTY + (hu - 2) % C::NB], ((hu - 2) / C::NB) & 1u);
                 // the epilogue has read the scales (and Q6_K categories) of superblock gg - 2
                 if (h == 0 && w_ok) w_ok = mbar_wait(&bar[BAR_SD_EMPTY + (gg & 1)], (uint32_t)(((gg >> 1) & 1) ^ 1));
                 if (!__all_sync(0xFFFFFFFFu, w_ok)) {
@@ -1349,7 +1377,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&bar[BAR_FULL_A + h]);
+                    mbar_arrive(&bar[BAR_FULL + hu % C::NB]);
                     // the scales and both halves' unit flags are written
                     if (h == 1) mbar_arrive(&bar[BAR_SD_FULL + (gg & 1)]);
                 }
