@@ -279,9 +279,12 @@ __device__ __forceinline__ void unpack_q45(uint32_t a_tm, const uint32_t (&qs)[8
                 const uint32_t x = prmt(word, MAGIC, sel);
                 uint32_t l = x & 0xFF0FFF0Fu, h = x & 0xFFF0FFF0u;
                 if constexpr (F == FMT_Q5_K) {
-                    const uint32_t hb = prmt(qh[2 * q + w], 0u, pr ? 0x4342u : 0x4140u) & 0x00FF00FFu;
+                    // qh bytes 2pr, 2pr+1 in bytes 0 and 2 (bytes 1 and 3 from the zero operand)
+                    const uint32_t hb = prmt(qh[2 * q + w], 0u, pr ? 0x4342u : 0x4140u);
                     const int b = 2 * c;  // low nibble's fifth bit
-                    l |= (b <= 4 ? (hb << (4 - b)) : (hb >> (b - 4))) & 0x00100010u;
+                    // bit b of each byte to bit 4 of its 16-bit lane: a rotation by
+                    // 4 - b (the bits it wraps around fall outside the mask)
+                    l |= __funnelshift_r(hb, hb, (uint32_t)(b - 4) & 31u) & 0x00100010u;
                     // high nibble's fifth bit (2c+1) lands on bit 8: value 256 = 16 * 16
                     h |= (hb << (7 - b)) & 0x01000100u;
                 }
