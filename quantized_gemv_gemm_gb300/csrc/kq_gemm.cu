@@ -47,7 +47,8 @@
 // column, y accumulated in TMEM).  TMEM lane quadrant = warp % 4.  Stages
 // are half superblocks (K = 128): an A ring of 2 slots, a B ring of 3
 // (Q6_K: 2).  TMEM (512 columns): Q4_K/Q5_K a ring of 2 unit accumulators,
-// one msum (issued after the superblock's last unit, folded with it) and
+// one msum (issued after the superblock's last unit and before that unit's
+// commit, which covers both; folded with it) and
 // the two A slots; Q6_K a ring of 3 units and y.  Every mbarrier
 // wait is bounded; on timeout the block records KQ_ERR_TIMEOUT in the
 // device status word and winds down.
@@ -122,7 +123,7 @@ struct Cfg {
 // scales and unit plans (SD, by superblock parity), MMA completion, the
 // tile list
 enum { BAR_FULL = 0, BAR_EMPTY = 4, BAR_U_FULL = 10, BAR_U_EMPTY = 13,
-       BAR_M_FULL = 16, BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25,
+       BAR_M_EMPTY = 18, BAR_SD_FULL = 20, BAR_SD_EMPTY = 22, BAR_MMA_DONE = 24, BAR_TILES = 25,
        BAR_EPI = 26, BAR_END = 27 };
 
 // TMEM (512 columns): a ring of unit accumulators of 128 columns from column
@@ -871,10 +872,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bar[BAR_U_FULL + i], 1);
             mbar_init(&bar[BAR_U_EMPTY + i], n_epi<F>());
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bar[BAR_M_FULL + i], 1);
-            mbar_init(&bar[BAR_M_EMPTY + i], n_epi<F>());
-        }
+        mbar_init(&bar[BAR_M_EMPTY], n_epi<F>());
         // every unpack warp arrives once the scales and both halves' unit
         // flags of the superblock are written
         mbar_init(&bar[BAR_SD_FULL + 0], n_unpack<F>());
@@ -898,7 +896,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = misc[0];
     // TMEM columns: unit accumulator i at 128i (i < NU), msum at COL_M, A at COL_A (Q4_K/Q5_K), y at COL_Y (Q6_K).
     // The unit ring's slots and phases follow u, the block's count of units
-    // over all tiles; msum's phase the count of non-empty superblocks; the
+    // over all tiles; the msum slot's phase the count of non-empty superblocks; the
     // SD barriers' the block's count g of superblock steps over all tiles.
     bool ok = true;
 
@@ -1024,9 +1022,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             pl = sb_plan(ld_flags(fl), ld_flags(fl + 8));
                         }
                         const int planes = (F == FMT_Q6_K && pl.split[h]) ? 2 : 1;
+                        // msum, after the superblock's last unit and before that unit's
+                        // commit (which then covers both; the epilogue folds msum with
+                        // that unit): the sub-mins of the superblock's parity against the
+                        // token bsums of this slot, into its one slot
+                        auto issue_msum = [&]() -> bool {
+                            if (!mbar_wait(&bar[BAR_M_EMPTY], (uint32_t)((mc & 1) ^ 1))) return false;
+                            tc_fence_after();
+                            const uint64_t ad = smem_desc(amin + (uint32_t)((g & 1) * C::AMIN_BYTES), 16, 256, SWZ_32B);
+                            const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
+                            umma_f16(tmem + COL_M, ad, bd, idesc, 0);
+                            ++mc;
+                            return true;
+                        };
                         if (h == 1 && open && pl.whole) {
                             // the superblock is one unit: the second half goes on into it
                             issue(1, 0, tmem + 128 * (uint32_t)(u % NU), a_slot, a_tm, b_slot, planes, false, idesc);
+                            if (C::kMins && !issue_msum()) {
+                                ok = false;
+                                break;
+                            }
                             umma_commit(&bar[BAR_U_FULL + (int)(u % NU)]);
                             ++u;
                             open = false;
@@ -1048,27 +1063,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 if (h == 0 && U == 1) {
                                     open = true;  // committed with the second half, or before it
                                 } else {
+                                    if (C::kMins && h == 1 && v == U - 1 && !issue_msum()) {
+                                        ok = false;
+                                        break;
+                                    }
                                     umma_commit(&bar[BAR_U_FULL + us]);
                                     ++u;
                                 }
                             }
                         }
                         if (!ok) break;
-                        if (C::kMins && h == 1) {
-                            // msum after the superblock's last unit (the epilogue folds
-                            // it with that unit): the sub-mins of the superblock's
-                            // parity against the token bsums of this slot; one slot
-                            if (!mbar_wait(&bar[BAR_M_EMPTY], (uint32_t)((mc & 1) ^ 1))) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint64_t ad = smem_desc(amin + (uint32_t)((g & 1) * C::AMIN_BYTES), 16, 256, SWZ_32B);
-                            const uint64_t bd = smem_desc(b_slot + 2 * C::B_SUB, 16, 256, SWZ_32B);
-                            umma_f16(tmem + COL_M, ad, bd, idesc, 0);
-                            umma_commit(&bar[BAR_M_FULL]);
-                            ++mc;
-                        }
                         umma_commit(&bar[BAR_EMPTY + cur]);  // frees the half's A and B slots
                     }
                 }
@@ -1547,7 +1551,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             ntiles = ok ? (int)misc[1] : 0;
         }
         // 32-bit counters: a block runs at most TILE_CAP tiles of at most 2^22 superblocks
-        uint32_t g = 0, u = 0, mc = 0, epi_phase = 0;
+        uint32_t g = 0, u = 0, epi_phase = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
             const Piece pc = work_piece<G, SK>(p, s_list, k);
             const Tile t = pc.t;
@@ -1584,14 +1588,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (lane == 0) mbar_arrive(&bar[BAR_SD_EMPTY + b]);
                 if (t.ntok == 0) continue;
                 // the superblock's units, folded as they land; msum, issued
-                // after the last unit into its one slot, is folded with the
-                // last (the units before it never wait for it)
+                // after the last unit into its one slot and covered by that
+                // unit's commit, is folded with it (the units before it never
+                // wait for it)
                 const uint32_t xm = lane_addr + COL_M;
 #pragma unroll 1
                 for (int v = 0; v < nu; ++v, ++u) {
                     const bool last = v == nu - 1;
                     bool w_ok = mbar_wait(&bar[BAR_U_FULL + (int)(u % NU)], (u / NU) & 1);
-                    if (w_ok && last) w_ok = mbar_wait(&bar[BAR_M_FULL], mc & 1);
                     if (!__all_sync(0xFFFFFFFFu, w_ok)) {
                         ok = false;
                         break;
@@ -1612,7 +1616,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                         if (last) mbar_arrive(&bar[BAR_M_EMPTY]);
                     }
                 }
-                ++mc;
                 if (!ok) break;
             }
             if (!ok) break;
