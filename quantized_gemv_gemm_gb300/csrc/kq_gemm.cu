@@ -45,8 +45,12 @@
 // whose unpack is the longer chain: 2..9 weight unpack (two threads per row,
 // one 64-wide K sub-tile each), 10..13 epilogue (thread = row x every token
 // column, y accumulated in TMEM).  TMEM lane quadrant = warp % 4.  Stages
-// are half superblocks (K = 128): an A ring of 2 slots, a B ring of 3
-// (Q6_K: 2).  TMEM (512 columns): Q4_K/Q5_K a ring of 2 unit accumulators,
+// are half superblocks (K = 128): a ring of token tiles (3 slots, Q6_K 2)
+// with one full barrier per slot (every unpack warp's A rows of the half and
+// the TMA tile) and one empty barrier (the commit after the half's MMAs,
+// which frees both the tile and the half's A slot; A has 2 half slots, slot
+// h of half i written once half i - 2 is empty).  TMEM (512 columns):
+// Q4_K/Q5_K a ring of 2 unit accumulators,
 // one msum (issued after the superblock's last unit and before that unit's
 // commit, which covers both; folded with it) and
 // the two A slots; Q6_K a ring of 3 units and y.  Every mbarrier
