@@ -443,13 +443,23 @@ __device__ __forceinline__ void finish_tile(Tile &t) {
 }
 
 // Dense tile i: the token tiles of a weight row tile are adjacent, so
-// consecutive tiles share that weight panel in L2.
+// consecutive tiles share that weight panel in L2.  The index arithmetic is
+// 32-bit for Q4_K/Q5_K (the launcher takes at most INT32_MAX tiles) and
+// 64-bit for Q6_K: measured per format on GB300 (27B Q4_K FFN 574 -> 587
+// TOPS with 32 bits; the 4B Q6_K block-per-tile shapes 3-4 % slower).
+template <int F>
 __device__ __forceinline__ Tile tile_at(const GemmParams &p, int64_t i) {
-    const int t_tiles = (int)((p.M + BT - 1) / BT);
     Tile t;
     t.e = 0;
-    t.n0 = (int)(i / t_tiles) * BM;
-    t.t0 = (int)(i % t_tiles) * BT;
+    if constexpr (F == FMT_Q6_K) {
+        const int t_tiles = (int)((p.M + BT - 1) / BT);
+        t.n0 = (int)(i / t_tiles) * BM;
+        t.t0 = (int)(i % t_tiles) * BT;
+    } else {
+        const uint32_t t_tiles = (uint32_t)((p.M + BT - 1) / BT), ii = (uint32_t)i;
+        t.n0 = (int)(ii / t_tiles) * BM;
+        t.t0 = (int)(ii % t_tiles) * BT;
+    }
     t.t_end = (t.t0 + BT < p.M) ? t.t0 + BT : (int)p.M;
     finish_tile(t);
     return t;
@@ -465,18 +475,29 @@ struct Piece {
 // first step of block b's share (dense)
 __device__ __forceinline__ int64_t dense_step_of(int64_t b, int64_t units) { return b * units / (int64_t)gridDim.x; }
 __device__ __forceinline__ int64_t dense_step(const GemmParams &p, int64_t b) { return dense_step_of(b, p.units); }
-__device__ __forceinline__ int dense_pieces(const GemmParams &p) {
+// The block's share as pieces, worked out once by one thread at the start
+// (the 64-bit divisions stay out of every role's loop): plan[0] the first
+// tile, [1] the last, [2] the first piece's first superblock, [3] the last
+// piece's end, [4] the number of pieces.
+constexpr int MISC_PLAN = 4;
+__device__ __forceinline__ void dense_plan(const GemmParams &p, uint32_t *plan) {
     const int64_t u0 = dense_step(p, blockIdx.x), u1 = dense_step(p, blockIdx.x + 1);
-    return u0 < u1 ? (int)((u1 - 1) / p.nsb - u0 / p.nsb + 1) : 0;
+    const int64_t i0 = u0 / p.nsb, i1 = u1 > u0 ? (u1 - 1) / p.nsb : i0;
+    plan[0] = (uint32_t)i0;
+    plan[1] = (uint32_t)i1;
+    plan[2] = (uint32_t)(u0 - i0 * p.nsb);
+    plan[3] = (uint32_t)(u1 - i1 * p.nsb);
+    plan[4] = u0 < u1 ? (uint32_t)(i1 - i0 + 1) : 0u;
 }
-__device__ __forceinline__ Piece dense_piece(const GemmParams &p, int k) {
-    const int64_t u0 = dense_step(p, blockIdx.x), u1 = dense_step(p, blockIdx.x + 1);
-    const int64_t i = u0 / p.nsb + k, lo = i * p.nsb, hi = lo + p.nsb;
+__device__ __forceinline__ int dense_pieces(const uint32_t *plan) { return (int)plan[4]; }
+template <int F>
+__device__ __forceinline__ Piece dense_piece(const GemmParams &p, const uint32_t *plan, int k) {
+    const uint32_t i = plan[0] + (uint32_t)k;
     Piece q;
-    q.t = tile_at(p, i);
+    q.t = tile_at<F>(p, i);
     q.tile = i;
-    q.sb0 = (int)((u0 > lo ? u0 : lo) - lo);
-    q.sb1 = (int)((u1 < hi ? u1 : hi) - lo);
+    q.sb0 = k == 0 ? (int)plan[2] : 0;
+    q.sb1 = i == plan[1] ? (int)plan[3] : (int)p.nsb;
     return q;
 }
 // the block whose share holds step x (dense)
@@ -503,13 +524,13 @@ __device__ __forceinline__ Tile list_tile(const int4 *list, int k) {
 // work item k of the block: grouped, list tile k; dense with the split-tile
 // schedule (SK), piece k of the block's share; dense without it, the block's
 // tile, whole
-template <bool G, bool SK>
-__device__ __forceinline__ Piece work_piece(const GemmParams &p, const int4 *list, int k) {
+template <int F, bool G, bool SK>
+__device__ __forceinline__ Piece work_piece(const GemmParams &p, const int4 *list, const uint32_t *plan, int k) {
     if constexpr (!G && SK) {
-        return dense_piece(p, k);
+        return dense_piece<F>(p, plan, k);
     } else {
         Piece q;
-        q.t = G ? list_tile(list, k) : tile_at(p, blockIdx.x);
+        q.t = G ? list_tile(list, k) : tile_at<F>(p, blockIdx.x);
         q.tile = G ? -1 : (int64_t)blockIdx.x;
         q.sb0 = 0;
         q.sb1 = (int)p.nsb;
@@ -518,8 +539,8 @@ __device__ __forceinline__ Piece work_piece(const GemmParams &p, const int4 *lis
 }
 // dense: the block's work items
 template <bool SK>
-__device__ __forceinline__ int dense_items(const GemmParams &p) {
-    if constexpr (SK) return dense_pieces(p);
+__device__ __forceinline__ int dense_items(const uint32_t *plan) {
+    if constexpr (SK) return dense_pieces(plan);
     else return 1;
 }
 
@@ -849,6 +870,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // each unpack warp's unit flag byte, [superblock parity][half][8 warps]
     uint8_t *s_flag = reinterpret_cast<uint8_t *>(misc + 16);
     const uint32_t flag_sa = smem_u32(s_flag);  // the same, as a shared-memory address
+    const uint32_t *s_plan = misc + MISC_PLAN;    // dense split-tile: the block's pieces
     int4 *s_list = reinterpret_cast<int4 *>(smem + C::OFF_TILES);        // grouped tile list
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -887,6 +909,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(&bar[BAR_TILES], 1);
         mbar_init(&bar[BAR_EPI], n_epi<F>());  // the epilogue warps' split-tile handshake
         mbar_init(&bar[BAR_END], NTHREADS / 32);  // every warp is done with TMEM
+        if constexpr (!G && SK) dense_plan(p, misc + MISC_PLAN);
         mbar_fence_init();
         for (int i = 0; i < 32; ++i) s_flag[i] = FLAG_NEUTRAL;
     }
@@ -907,7 +930,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == W_TMA) {
         // ------------------------------------------------ activation tiles
         griddep_wait();
-        int ntiles = G ? 0 : dense_items<SK>(p);
+        int ntiles = G ? 0 : dense_items<SK>(s_plan);
         if constexpr (G) {
             ntiles = build_tile_list(p, reinterpret_cast<int *>(smem + C::OFF_OFFS), s_list, lane);
             __threadfence_block();
@@ -922,12 +945,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             tma_prefetch_desc(&map_a16);
             if (C::kMins) tma_prefetch_desc(&map_b16);
-            if (ntiles > 0) prefetch_tile<F>(p, work_piece<G, SK>(p, s_list, 0).t);
+            if (ntiles > 0) prefetch_tile<F>(p, work_piece<F, G, SK>(p, s_list, s_plan, 0).t);
             for (int k = 0; k < ntiles && ok; ++k) {
-                const Piece q = work_piece<G, SK>(p, s_list, k);
+                const Piece q = work_piece<F, G, SK>(p, s_list, s_plan, k);
                 const Tile t = q.t;
                 // the next tile's weights stream into L2 while this one runs
-                if (k + 1 < ntiles) prefetch_tile<F>(p, work_piece<G, SK>(p, s_list, k + 1).t);
+                if (k + 1 < ntiles) prefetch_tile<F>(p, work_piece<F, G, SK>(p, s_list, s_plan, k + 1).t);
                 for (int64_t sb = q.sb0; sb < q.sb1 && ok; ++sb) {
                     for (int h = 0; h < 2 && ok; ++h) {
                         if (!mbar_wait(&bar[BAR_EMPTY + slot], (round & 1u) ^ 1u)) { ok = false; break; }
@@ -974,7 +997,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // most TILE_CAP tiles of at most 2^22 superblocks)
         uint32_t g = 0, slot = 0, round = 0, u = 0, mc = 0;
         if (lane == 0) {
-            int ntiles = G ? 0 : dense_items<SK>(p);
+            int ntiles = G ? 0 : dense_items<SK>(s_plan);
             if constexpr (G) {
                 ok = mbar_wait(&bar[BAR_TILES], 0);
                 ntiles = ok ? (int)misc[1] : 0;
@@ -989,7 +1012,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 else issue_unit<C::B_SUB, 1>(U, v, acc, a_slot, b_slot, fresh, idesc);
             };
             for (int k = 0; k < ntiles && ok; ++k) {
-                const Piece q = work_piece<G, SK>(p, s_list, k);
+                const Piece q = work_piece<F, G, SK>(p, s_list, s_plan, k);
                 const Tile t = q.t;
                 const uint32_t idesc = idesc_f16_f32(BM, t.n_mma > 0 ? t.n_mma : 16);
                 for (int64_t sb = q.sb0; sb < q.sb1 && ok; ++sb, ++g) {
@@ -1250,10 +1273,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int hs0 = 0, hs1 = nstage;
         int dn = 0;  // dense: the block's pieces
         if constexpr (!G) {
-            dn = dense_items<SK>(p);
+            dn = dense_items<SK>(s_plan);
             have = dn > 0;
             if (have) {
-                const Piece q = work_piece<G, SK>(p, s_list, 0);
+                const Piece q = work_piece<F, G, SK>(p, s_list, s_plan, 0);
                 t = q.t;
                 hs0 = 2 * q.sb0;
                 hs1 = 2 * q.sb1;
@@ -1286,7 +1309,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 } else if constexpr (!G && SK) {
                     have_n = k + 1 < dn;
                     if (have_n) {
-                        const Piece q = dense_piece(p, k + 1);
+                        const Piece q = dense_piece<F>(p, s_plan, k + 1);
                         n0_nxt = q.t.n0;
                         hs0_n = 2 * q.sb0;
                         hs1_n = 2 * q.sb1;
@@ -1417,7 +1440,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const uint32_t y_tm = lane_addr + COL_Y;
         constexpr bool dbg = DBG;
         griddep_wait();  // the scales are written by the kernels before this one
-        int ntiles = G ? 0 : dense_items<SK>(p);
+        int ntiles = G ? 0 : dense_items<SK>(s_plan);
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
@@ -1425,7 +1448,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         int64_t g = 0, u = 0;
         uint32_t epi_phase = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
-            const Piece pc = work_piece<G, SK>(p, s_list, k);
+            const Piece pc = work_piece<F, G, SK>(p, s_list, s_plan, k);
             const Tile t = pc.t;
             const int64_t n = t.n0 + r;
             const int nc = t.n_mma / 16;
@@ -1549,7 +1572,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         float *s_d8 = reinterpret_cast<float *>(smem + C::OFF_D8) + 64 * ew;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * quad) << 16) + 64 * ch;
         griddep_wait();  // the scales are written by the kernels before this one
-        int ntiles = G ? 0 : dense_items<SK>(p);
+        int ntiles = G ? 0 : dense_items<SK>(s_plan);
         if constexpr (G) {
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(&bar[BAR_TILES], 0));
             ntiles = ok ? (int)misc[1] : 0;
@@ -1557,7 +1580,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // 32-bit counters: a block runs at most TILE_CAP tiles of at most 2^22 superblocks
         uint32_t g = 0, u = 0, epi_phase = 0;
         for (int k = 0; k < ntiles && ok; ++k) {
-            const Piece pc = work_piece<G, SK>(p, s_list, k);
+            const Piece pc = work_piece<F, G, SK>(p, s_list, s_plan, k);
             const Tile t = pc.t;
             const int n = t.n0 + r;
             float y[64];
